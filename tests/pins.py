@@ -1,0 +1,264 @@
+"""Checks that tie the CPU oracle to facts fixed outside the oracle itself.
+
+Each check takes the oracle module and raises AssertionError on a mismatch.
+tests/test_oracle_pins.py runs every check against the real oracle and
+against copies with a planted mistake (to show each check has teeth).
+Sources: the C2KV explainer (paper-daily.com) sections "C2 tokens",
+"structured information flow" and "positions at concatenation"; the Llama 3
+paragraph of the KV-cache essay (feinterview.poetries.top); textbook
+identities of rotations and of softmax.
+"""
+import math
+
+import numpy as np
+import torch
+from scipy.special import expit
+
+from conftest import read_golden
+
+
+# --------------------------------------------------------------- positions
+
+def check_blog_positions(o):
+    g = read_golden("positions_400tok_k4.txt")
+    k = g["k"][0]
+    n0, s0 = g["doc0_tokens"][0], g["doc0_slots"][0]
+    assert o.slot_count(n0, k) == s0
+    pos, l_tot = o.composed_positions([n0, 40], [s0, o.slot_count(40, k)], k)
+    want0 = np.arange(g["doc0_first"][0], g["doc0_last"][0] + 1, g["doc0_step"][0])
+    assert len(want0) == s0
+    assert np.array_equal(pos[:s0], want0), pos[:5]
+    assert pos[s0] == g["doc1_first"][0], pos[s0]
+    assert l_tot == n0 + 40
+    e = g["extraction_first_slots"]
+    assert [o.extraction_slot_position(j, n0, k) for j in range(len(e))] == e
+
+
+def check_slot_counts(o):
+    for n, k, s in read_golden("slot_counts.txt")["_rows"]:
+        assert o.slot_count(n, k) == s, (n, k)
+
+
+def _brute_positions(docs, k):
+    """Lay the original text out token by token and read each slot's position
+    off the last token of its block (independent of the oracle's formula)."""
+    out = []
+    cursor = 0
+    for n, s in docs:
+        global_pos = list(range(cursor, cursor + n))
+        blocks = {}
+        for t in range(n):
+            blocks[t // k] = global_pos[t]      # later tokens overwrite: last one wins
+        for j in range(s):
+            out.append(blocks[j])
+        cursor += n
+    return out
+
+
+def check_positions_bruteforce(o):
+    rng = np.random.default_rng(7)
+    for trial in range(40):
+        k = int(rng.choice([1, 2, 4, 8, 16]))
+        ndoc = int(rng.integers(1, 7))
+        lens = [int(rng.integers(1, 60)) for _ in range(ndoc)]
+        docs = [(n, o.slot_count(n, k)) for n in lens]
+        want = _brute_positions(docs, k)
+        assert [len({t // k for t in range(n)}) for n in lens] == [s for _, s in docs]
+        ids = list(range(ndoc))
+        order = [int(x) for x in rng.permutation(ndoc)]
+        seq = o.composed_order(ids, order)
+        assert seq == order
+        pos, l_tot = o.composed_positions([docs[i][0] for i in seq],
+                                          [docs[i][1] for i in seq], k)
+        assert pos.tolist() == _brute_positions([docs[i] for i in seq], k)
+        assert l_tot == sum(lens)
+        pos_id, _ = o.composed_positions(lens, [s for _, s in docs], k)
+        assert pos_id.tolist() == want
+
+
+# ------------------------------------------------------------------ mask
+
+def check_blog_mask(o):
+    g = read_golden("structured_mask_k4_12tok_3slot.txt")
+    k, n, m = g["k"][0], g["n_doc"][0], g["n_slot"][0]
+    M = o.structured_mask(n, m, k)
+    assert M.shape == (n + m, n + m)
+    slot_doc = M[n:, :n]
+    assert int(slot_doc.sum()) == g["c2kv_slot_doc_cells"][0]
+    assert m * n == g["plain_causal_slot_doc_cells"][0]
+    for i in range(m):
+        seen = [c + 1 for c in range(n) if slot_doc[i, c]]
+        assert seen == g["slot%d" % (i + 1)], (i, seen)
+    assert not M[:n, n:].any()                      # documents never see slots
+    assert np.array_equal(M[:n, :n], np.tril(np.ones((n, n), bool)))
+    assert np.array_equal(M[n:, n:], np.tril(np.ones((m, m), bool)))
+    assert int(M.sum()) == n * (n + 1) // 2 + 20 + m * (m + 1) // 2
+
+
+def check_extraction_positions(o):
+    g = read_golden("positions_400tok_k4.txt")
+    p = o.extraction_positions(12, 3, 4)
+    assert p[:12].tolist() == list(range(12))
+    assert p[12:14].tolist() == g["extraction_first_slots"]
+    assert p[14] == 11
+
+
+# ------------------------------------------------------------------ bf16
+
+def check_bf16_conversion(o):
+    rng = np.random.default_rng(3)
+    x32 = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32),
+        (rng.standard_normal(2000) * 1e-39).astype(np.float32),   # subnormals
+        (rng.standard_normal(2000) * 1e38).astype(np.float32),
+        np.array([0.0, -0.0, 1.0, -1.0, 3.3895314e38, 3.4e38], np.float32),
+    ])
+    ref = torch.from_numpy(x32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = o.f64_to_bf16(x32.astype(np.float64))
+    assert np.array_equal(got, ref)
+    # ties to even, and no double rounding through fp32
+    one = 1.0
+    assert o.f64_to_bf16(np.array([one + 2.0 ** -8]))[0] == 0x3F80
+    assert o.f64_to_bf16(np.array([one + 3 * 2.0 ** -8]))[0] == 0x3F82
+    assert o.f64_to_bf16(np.array([one + 2.0 ** -8 + 2.0 ** -40]))[0] == 0x3F81
+    assert o.f64_to_bf16(np.array([np.inf, -np.inf]))[0] == 0x7F80
+    bits = rng.integers(0, 0x7F80, 5000).astype(np.uint16)
+    assert np.array_equal(o.f64_to_bf16(o.bf16_to_f64(bits)), bits)
+    assert o.bf16_to_f64(np.array([0x3F80, 0xC000], np.uint16)).tolist() == [1.0, -2.0]
+
+
+# ------------------------------------------------------------------ RoPE
+
+def check_rope(o):
+    rng = np.random.default_rng(11)
+    d, theta = 8, 1.0e4
+    inv = o.rope_inv_freq(theta, d)
+    assert inv[0] == 1.0
+    assert np.allclose(inv[1:] / inv[:-1], theta ** (-2.0 / d), rtol=1e-14)
+    x = rng.standard_normal((3, 5, d))
+    assert np.array_equal(o.rope_rotate(x, np.zeros(5, np.int64), theta), x)
+    pos = rng.integers(0, 200000, 5)
+    y = o.rope_rotate(x, pos, theta)
+    # rotate-half pairing (i, i+d/2) equals multiplying z_i = x_i + 1j x_{i+d/2}
+    # by exp(1j * pos * inv_freq_i)
+    h = d // 2
+    z = (x[..., :h] + 1j * x[..., h:]) * np.exp(1j * pos[:, None] * inv[None, :])
+    assert np.allclose(y[..., :h], z.real, atol=1e-9)
+    assert np.allclose(y[..., h:], z.imag, atol=1e-9)
+    # composition of rotations, and the relative-position property
+    a, b = rng.integers(0, 5000, 5), rng.integers(0, 5000, 5)
+    assert np.allclose(o.rope_rotate(o.rope_rotate(x, a, theta), b, theta),
+                       o.rope_rotate(x, a + b, theta), atol=1e-9)
+    q, kk = rng.standard_normal(d), rng.standard_normal(d)
+    dots = []
+    for shift in (0, 17, 123456):
+        pq = np.array([shift + 40]); pk = np.array([shift + 3])
+        dots.append(float(o.rope_rotate(q[None], pq, theta)[0] @ o.rope_rotate(kk[None], pk, theta)[0]))
+    assert np.allclose(dots, dots[0], atol=1e-9)
+
+
+# ------------------------------------------------------------- attention
+
+def _bits(rng, shape, scale=1.0):
+    x = (rng.standard_normal(shape) * scale).astype(np.float32)
+    return torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def check_attention_special_cases(o):
+    rng = np.random.default_rng(5)
+    d = 16
+    q = rng.standard_normal((3, d))
+    V = rng.standard_normal((6, d))
+    K = rng.standard_normal((6, d))
+    # one visible key -> its value
+    mask = np.zeros((3, 6), bool); mask[:, 2] = True
+    assert np.allclose(o.masked_softmax_attention(q, K, V, mask), V[[2, 2, 2]])
+    # identical keys -> mean of the values
+    Ks = np.repeat(K[:1], 6, axis=0)
+    full = np.ones((3, 6), bool)
+    assert np.allclose(o.masked_softmax_attention(q, Ks, V, full), V.mean(0)[None].repeat(3, 0))
+    # two keys: closed form through the logistic function, scale 1/sqrt(d)
+    a, b = 1.7, -0.4
+    q1 = np.zeros((1, d)); q1[0, 0] = 1.0
+    K2 = np.zeros((2, d)); K2[0, 0] = a; K2[1, 0] = b
+    V2 = rng.standard_normal((2, d))
+    w = expit((a - b) / math.sqrt(d))
+    want = V2[1] + w * (V2[0] - V2[1])
+    assert np.allclose(o.masked_softmax_attention(q1, K2, V2, np.ones((1, 2), bool))[0], want)
+    # one dominant logit -> that value
+    Kd = K.copy(); Kd[4] = q[0] * 400.0
+    out = o.masked_softmax_attention(q[:1], Kd, V, np.ones((1, 6), bool))
+    assert np.allclose(out[0], V[4], atol=1e-9)
+    # convex combination, invariant to a permutation of the keys
+    out = o.masked_softmax_attention(q, K, V, full)
+    assert np.all(out <= V.max(0) + 1e-12) and np.all(out >= V.min(0) - 1e-12)
+    perm = rng.permutation(6)
+    assert np.allclose(o.masked_softmax_attention(q, K[perm], V[perm], full), out)
+
+
+def check_gqa_and_causality(o):
+    rng = np.random.default_rng(9)
+    hq, hkv, d, n, t, theta = 6, 2, 16, 7, 4, 1.0e4
+    g = hq // hkv
+    q = _bits(rng, (t, hq, d)); kn = _bits(rng, (t, hkv, d))
+    kc = _bits(rng, (hkv, n, d))
+    # every value of kv head j is the constant j+1 -> output head h reads h//g + 1
+    vc = np.zeros((hkv, n, d), np.uint16); vn = np.zeros((t, hkv, d), np.uint16)
+    for j in range(hkv):
+        c = o.f64_to_bf16(np.array([j + 1.0]))[0]
+        vc[j] = c; vn[:, j] = c
+    out, _ = o.attend_new_tokens(q, kn, vn, kc, vc, 1000, theta)
+    for h in range(hq):
+        assert np.allclose(out[:, h, :], h // g + 1), h
+    # causal: changing new token 3 leaves rows 0..2 unchanged, changes row 3
+    vr = _bits(rng, (hkv, n, d)); vnr = _bits(rng, (t, hkv, d))
+    o1, _ = o.attend_new_tokens(q, kn, vnr, kc, vr, 50, theta)
+    vn2 = vnr.copy(); vn2[3] = _bits(rng, (hkv, d))
+    kn2 = kn.copy(); kn2[3] = _bits(rng, (hkv, d))
+    o2, _ = o.attend_new_tokens(q, kn2, vn2, kc, vr, 50, theta)
+    assert np.array_equal(o1[:3], o2[:3])
+    assert not np.allclose(o1[3], o2[3])
+    # a decode step is the last row of the same tokens prefilled together
+    od, _, _ = o.decode_sequence(q, kn, vnr, kc, vr, 50, theta)
+    assert np.allclose(od, o1, atol=1e-12)
+
+
+def check_k1_equals_uncompressed(o):
+    """k=1: every token is its own slot, so the composed cache must be the
+    plain RoPE cache of the concatenated documents at positions 0..L_tot-1."""
+    rng = np.random.default_rng(13)
+    L, hkv, d, theta = 2, 2, 16, 5.0e5
+    lens = [5, 1, 9, 3]
+    store = {}
+    for i, n in enumerate(lens):
+        store[10 + i] = (n, n, _bits(rng, (L, hkv, n, d)), _bits(rng, (L, hkv, n, d)))
+    ids = [10, 11, 12, 13]
+    order = [2, 0, 3, 1]
+    pos, l_tot, krot, vcat = o.compose(store, ids, order, 1, theta)
+    seq = [ids[i] for i in order]
+    raw_k = np.concatenate([store[s][2] for s in seq], axis=2)
+    raw_v = np.concatenate([store[s][3] for s in seq], axis=2)
+    assert pos.tolist() == list(range(sum(lens))) and l_tot == sum(lens)
+    x = o.bf16_to_f64(raw_k)
+    want = np.empty_like(x)
+    inv = o.rope_inv_freq(theta, d)
+    for p in range(l_tot):   # rotate token by token via complex numbers
+        h = d // 2
+        z = (x[..., p, :h] + 1j * x[..., p, h:]) * np.exp(1j * p * inv)
+        want[..., p, :h], want[..., p, h:] = z.real, z.imag
+    assert np.all(o.bf16_ulp_distance(krot, o.f64_to_bf16(want)) <= 1)
+    assert np.array_equal(vcat, raw_v)
+
+
+def check_llama3_bytes(o):
+    g = read_golden("kv_bytes_llama3.txt")
+    assert o.kv_bytes_per_slot(g["n_layers"][0], g["n_kv_heads"][0],
+                               g["head_dim"][0]) == g["bytes_per_token"][0]
+
+
+ALL_CHECKS = [
+    check_blog_positions, check_slot_counts, check_positions_bruteforce,
+    check_blog_mask, check_extraction_positions, check_bf16_conversion,
+    check_rope, check_attention_special_cases, check_gqa_and_causality,
+    check_k1_equals_uncompressed, check_llama3_bytes,
+]

@@ -1,0 +1,130 @@
+"""The CPU oracle against its pins, and each pin against a planted mistake.
+
+A planted mistake is a plausible bug put into the oracle on the CPU (via
+monkeypatch, undone after the test); the matching pin must then fail.
+"""
+import numpy as np
+import pytest
+
+import oracle.c2kv_oracle as O
+import pins
+
+
+@pytest.mark.parametrize("check", pins.ALL_CHECKS, ids=lambda c: c.__name__)
+def test_pin(check):
+    check(O)
+
+
+def _positions_no_minus_one(n_tokens, n_slots, k):
+    pos, off = [], 0
+    for n, s in zip(n_tokens, n_slots):
+        pos += [off + min((j + 1) * k, n) for j in range(s)]
+        off += n
+    return np.asarray(pos, np.int64), off
+
+
+def _positions_offset_by_slots(n_tokens, n_slots, k):
+    pos, off = [], 0
+    for n, s in zip(n_tokens, n_slots):
+        pos += [off + min((j + 1) * k, n) - 1 for j in range(s)]
+        off += s
+    return np.asarray(pos, np.int64), off
+
+
+def _rope_sign_flipped(x, pos, theta):
+    d = x.shape[-1]; h = d // 2
+    a = np.asarray(pos, np.float64)[:, None] * O.rope_inv_freq(theta, d)[None, :]
+    c, s = np.cos(a), np.sin(a)
+    return np.concatenate([x[..., :h] * c + x[..., h:] * s,
+                           x[..., h:] * c - x[..., :h] * s], axis=-1)
+
+
+def _rope_interleaved(x, pos, theta):
+    d = x.shape[-1]
+    a = np.asarray(pos, np.float64)[:, None] * O.rope_inv_freq(theta, d)[None, :]
+    c, s = np.cos(a), np.sin(a)
+    y = x.copy()
+    y[..., 0::2] = x[..., 0::2] * c - x[..., 1::2] * s
+    y[..., 1::2] = x[..., 1::2] * c + x[..., 0::2] * s
+    return y
+
+
+def _inv_freq_wrong_exponent(theta, d):
+    return np.power(float(theta), -np.arange(d // 2, dtype=np.float64) / d)
+
+
+def _mask_no_sink(n_doc, n_slot, k):
+    m = np.zeros((n_doc + n_slot,) * 2, bool)
+    for r in range(n_doc):
+        m[r, :r + 1] = True
+    for i in range(n_slot):
+        m[n_doc + i, i * k:min((i + 1) * k, n_doc)] = True
+        m[n_doc + i, n_doc:n_doc + i + 1] = True
+    return m
+
+
+def _mask_block_shifted(n_doc, n_slot, k):
+    m = np.zeros((n_doc + n_slot,) * 2, bool)
+    for r in range(n_doc):
+        m[r, :r + 1] = True
+    for i in range(n_slot):
+        m[n_doc + i, :min(k, n_doc)] = True
+        m[n_doc + i, i * k:min((i + 1) * k + 1, n_doc)] = True
+        m[n_doc + i, n_doc:n_doc + i + 1] = True
+    return m
+
+
+def _softmax_no_scale(q, K, V, mask):
+    s = np.where(mask, q @ K.T, -np.inf)
+    p = np.exp(s - s.max(1, keepdims=True))
+    return (p / p.sum(1, keepdims=True)) @ V
+
+
+def _bf16_truncate(x):
+    x = np.asarray(x, np.float64)
+    return (x.astype(np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def _bf16_double_round(x):
+    x32 = np.asarray(x, np.float64).astype(np.float32)
+    import torch
+    return torch.from_numpy(x32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+MUTATIONS = [
+    ("composed_positions", _positions_no_minus_one, pins.check_blog_positions),
+    ("composed_positions", _positions_offset_by_slots, pins.check_blog_positions),
+    ("rope_rotate", _rope_sign_flipped, pins.check_rope),
+    ("rope_rotate", _rope_interleaved, pins.check_rope),
+    ("rope_inv_freq", _inv_freq_wrong_exponent, pins.check_rope),
+    ("structured_mask", _mask_no_sink, pins.check_blog_mask),
+    ("structured_mask", _mask_block_shifted, pins.check_blog_mask),
+    ("masked_softmax_attention", _softmax_no_scale, pins.check_attention_special_cases),
+    ("f64_to_bf16", _bf16_truncate, pins.check_bf16_conversion),
+    ("f64_to_bf16", _bf16_double_round, pins.check_bf16_conversion),
+]
+
+
+@pytest.mark.parametrize("name,bad,check", MUTATIONS,
+                         ids=[f"{m[0]}:{m[1].__name__}" for m in MUTATIONS])
+def test_planted_mistake_is_caught(monkeypatch, name, bad, check):
+    monkeypatch.setattr(O, name, bad)
+    with pytest.raises(AssertionError):
+        check(O)
+
+
+def test_gqa_mapping_mistake_is_caught(monkeypatch):
+    """q head h must read kv head h // G, not h % G."""
+    real = O.attend_new_tokens
+
+    def modulo_mapping(q_pre, k_new_pre, v_new, k_cache, v_cache, start_pos, theta):
+        t, hq, d = q_pre.shape
+        hkv = k_new_pre.shape[1]
+        perm = [h % hkv * (hq // hkv) + h // hkv for h in range(hq)]
+        out, kr = real(q_pre[:, perm], k_new_pre, v_new, k_cache, v_cache, start_pos, theta)
+        inv = np.argsort(perm)
+        return out[:, inv], kr
+
+    monkeypatch.setattr(O, "attend_new_tokens", modulo_mapping)
+    with pytest.raises(AssertionError):
+        pins.check_gqa_and_causality(O)
