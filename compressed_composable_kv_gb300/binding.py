@@ -1,0 +1,268 @@
+"""ctypes binding of libc2kv.so: same names as the C ABI (include/c2kv.h).
+
+Argument marshalling only -- every step of the path runs in the CUDA
+library.  Device tensors are torch CUDA tensors (their data pointers are
+passed through); host inputs are numpy arrays or CPU tensors.  A missing
+library raises ImportError: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from .build import LIB
+
+C2KV_OK, C2KV_EINVAL, C2KV_ENOMEM, C2KV_ENOTFOUND = 0, 1, 2, 3
+C2KV_ECAPACITY, C2KV_ECUDA, C2KV_ETIMEOUT, C2KV_EDEVICE = 4, 5, 6, 7
+C2KV_MASK_CAUSAL, C2KV_MASK_STRUCTURED = 0, 1
+
+STATUS_NAMES = {0: "C2KV_OK", 1: "C2KV_EINVAL", 2: "C2KV_ENOMEM", 3: "C2KV_ENOTFOUND",
+                4: "C2KV_ECAPACITY", 5: "C2KV_ECUDA", 6: "C2KV_ETIMEOUT", 7: "C2KV_EDEVICE"}
+
+
+class C2KVError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+        self.message = message
+
+
+class c2kv_geometry(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("rope_theta", ctypes.c_double)]
+
+
+_i32, _sz, _vp = ctypes.c_int32, ctypes.c_size_t, ctypes.c_void_p
+_pi32 = ctypes.POINTER(ctypes.c_int32)
+_pvp = ctypes.POINTER(ctypes.c_void_p)
+_pg = ctypes.POINTER(c2kv_geometry)
+
+_SIGNATURES = {
+    "c2kv_last_error": (ctypes.c_char_p, []),
+    "c2kv_version": (ctypes.c_char_p, []),
+    "c2kv_store_create": (_i32, [_pg, _sz, ctypes.POINTER(_vp)]),
+    "c2kv_store_destroy": (None, [_vp]),
+    "c2kv_store_segments": (_i32, [_vp, _i32, _pi32, _pi32, _pi32, _i32, _pvp, _pvp]),
+    "c2kv_store_lookup": (_i32, [_vp, _i32, _pi32, _pi32, _pi32]),
+    "c2kv_plan": (_i32, [_i32, _pi32, _pi32, _pi32, _pi32, _pi32, _pi32, _pi32]),
+    "c2kv_compose": (_i32, [_vp, _i32, _pi32, _pi32, _i32, _vp, _vp, _i32, _vp, _pi32, _pi32, _vp]),
+    "c2kv_attend_workspace_size": (_sz, [_pg, _i32, _i32, _i32]),
+    "c2kv_masked_extra_bytes": (_sz, [_pg, _i32]),
+    "c2kv_workspace_init": (_i32, [_vp, _sz, _vp]),
+    "c2kv_attend_prefill": (_i32, [_pg, _i32, _i32, _pvp, _pvp, _i32, _pi32, _pi32, _i32,
+                                   _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "c2kv_attend_decode": (_i32, [_pg, _i32, _i32, _pvp, _pvp, _i32, _vp, _vp, _i32,
+                                  _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "c2kv_seq_advance": (_i32, [_i32, _vp, _vp, _i32, _vp]),
+    "c2kv_attend_masked": (_i32, [_pg, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "c2kv_device_error": (_i32, [_pi32]),
+}
+
+_lib = None
+
+
+def load_library(path: str = LIB) -> ctypes.CDLL:
+    """Load libc2kv.so (built by build.build_library) and declare signatures."""
+    global _lib
+    if _lib is not None and path == LIB:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"libc2kv.so is not built ({path}); run "
+                          "compressed_composable_kv_gb300.build.build_library()")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path == LIB:
+        _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != C2KV_OK:
+        raise C2KVError(status, load_library().c2kv_last_error().decode())
+
+
+def as_geometry(g) -> c2kv_geometry:
+    if isinstance(g, c2kv_geometry):
+        return g
+    return c2kv_geometry(g.n_layers, g.n_q_heads, g.n_kv_heads, g.head_dim, float(g.rope_theta))
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(t: Optional[torch.Tensor], dtype=None, name="tensor") -> int:
+    if t is None:
+        return 0
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _i32arr(vals) -> ctypes.Array:
+    vals = [int(v) for v in vals]
+    return (ctypes.c_int32 * max(1, len(vals)))(*vals)
+
+
+def _host_ptr(a) -> int:
+    if isinstance(a, torch.Tensor):
+        if a.is_cuda or not a.is_contiguous():
+            raise ValueError("host segment must be a contiguous CPU tensor")
+        return a.data_ptr()
+    a = np.asarray(a)
+    if not a.flags.c_contiguous:
+        raise ValueError("host segment must be C-contiguous")
+    return a.ctypes.data
+
+
+# --------------------------------------------------------------------- API
+
+def c2kv_last_error() -> str:
+    return load_library().c2kv_last_error().decode()
+
+
+def c2kv_version() -> str:
+    return load_library().c2kv_version().decode()
+
+
+def c2kv_store_create(geom, pinned_bytes: int) -> int:
+    g = as_geometry(geom)
+    h = ctypes.c_void_p()
+    _check(load_library().c2kv_store_create(ctypes.byref(g), int(pinned_bytes), ctypes.byref(h)))
+    return h.value
+
+
+def c2kv_store_destroy(store: int) -> None:
+    load_library().c2kv_store_destroy(store)
+
+
+def c2kv_store_segments(store: int, doc_ids, n_tokens, n_slots, k: int, k_pre, v) -> None:
+    n = len(doc_ids)
+    keep = list(k_pre) + list(v)   # keep the arrays alive through the call
+    kp = (ctypes.c_void_p * max(1, n))(*[_host_ptr(a) for a in k_pre])
+    vp = (ctypes.c_void_p * max(1, n))(*[_host_ptr(a) for a in v])
+    _check(load_library().c2kv_store_segments(store, n, _i32arr(doc_ids), _i32arr(n_tokens),
+                                              _i32arr(n_slots), int(k), kp, vp))
+    del keep
+
+
+def c2kv_store_lookup(store: int, doc_id: int):
+    nt, ns, k = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    _check(load_library().c2kv_store_lookup(store, int(doc_id), ctypes.byref(nt), ctypes.byref(ns),
+                                            ctypes.byref(k)))
+    return nt.value, ns.value, k.value
+
+
+def c2kv_plan(n_tokens: Sequence[int], n_slots: Sequence[int], order: Optional[Sequence[int]] = None):
+    """Returns (slot_start[c], pos_offset[c], total_slots, total_tokens)."""
+    n = len(n_tokens)
+    ss, po = _i32arr([0] * n), _i32arr([0] * n)
+    ts, tt = ctypes.c_int32(), ctypes.c_int32()
+    _check(load_library().c2kv_plan(n, _i32arr(n_tokens), _i32arr(n_slots),
+                                    None if order is None else _i32arr(order), ss, po,
+                                    ctypes.byref(ts), ctypes.byref(tt)))
+    return list(ss)[:n], list(po)[:n], ts.value, tt.value
+
+
+def c2kv_compose(store: int, doc_ids, order, k: int, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                 cap: int, pos_dev_out: Optional[torch.Tensor] = None, stream=None):
+    """Returns (n_slots, next_pos)."""
+    ns, nxt = ctypes.c_int32(), ctypes.c_int32()
+    _check(load_library().c2kv_compose(
+        store, len(doc_ids), _i32arr(doc_ids), None if order is None else _i32arr(order), int(k),
+        _dev(k_cache, torch.bfloat16, "k_cache"), _dev(v_cache, torch.bfloat16, "v_cache"), int(cap),
+        _dev(pos_dev_out, torch.int32, "pos_dev_out"), ctypes.byref(ns), ctypes.byref(nxt),
+        _stream(stream)))
+    return ns.value, nxt.value
+
+
+def c2kv_attend_workspace_size(geom, batch: int, t_len: int, max_keys: int) -> int:
+    g = as_geometry(geom)
+    return int(load_library().c2kv_attend_workspace_size(ctypes.byref(g), batch, t_len, max_keys))
+
+
+def c2kv_masked_extra_bytes(geom, n_tokens: int) -> int:
+    g = as_geometry(geom)
+    return int(load_library().c2kv_masked_extra_bytes(ctypes.byref(g), n_tokens))
+
+
+def c2kv_workspace_init(workspace: torch.Tensor, stream=None) -> None:
+    _check(load_library().c2kv_workspace_init(_dev(workspace, None, "workspace"),
+                                              workspace.numel() * workspace.element_size(),
+                                              _stream(stream)))
+
+
+def _ptrs(ts, name):
+    return (ctypes.c_void_p * len(ts))(*[_dev(t, torch.bfloat16, name) for t in ts])
+
+
+def c2kv_attend_prefill(geom, layer: int, k_caches, v_caches, cap: int, n_cached, start_pos,
+                        q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, out: torch.Tensor,
+                        workspace: Optional[torch.Tensor], stream=None) -> None:
+    g = as_geometry(geom)
+    B = len(k_caches)
+    q_len = q.shape[1]
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().c2kv_attend_prefill(
+        ctypes.byref(g), int(layer), B, _ptrs(k_caches, "k_cache"), _ptrs(v_caches, "v_cache"), int(cap),
+        _i32arr(n_cached), _i32arr(start_pos), int(q_len), _dev(q, torch.bfloat16, "q"),
+        _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
+        _dev(out, torch.bfloat16, "out"), _dev(workspace, None, "workspace"), ws, _stream(stream)))
+
+
+def c2kv_attend_decode(geom, layer: int, k_caches, v_caches, cap: int, n_cached_dev: torch.Tensor,
+                       pos_dev: torch.Tensor, max_keys: int, q: torch.Tensor, k_new: torch.Tensor,
+                       v_new: torch.Tensor, out: torch.Tensor, workspace: Optional[torch.Tensor],
+                       stream=None) -> None:
+    g = as_geometry(geom)
+    B = len(k_caches)
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().c2kv_attend_decode(
+        ctypes.byref(g), int(layer), B, _ptrs(k_caches, "k_cache"), _ptrs(v_caches, "v_cache"), int(cap),
+        _dev(n_cached_dev, torch.int32, "n_cached_dev"), _dev(pos_dev, torch.int32, "pos_dev"),
+        int(max_keys), _dev(q, torch.bfloat16, "q"), _dev(k_new, torch.bfloat16, "k_new"),
+        _dev(v_new, torch.bfloat16, "v_new"), _dev(out, torch.bfloat16, "out"),
+        _dev(workspace, None, "workspace"), ws, _stream(stream)))
+
+
+def c2kv_seq_advance(n_cached_dev: torch.Tensor, pos_dev: torch.Tensor, delta: int = 1, stream=None) -> None:
+    _check(load_library().c2kv_seq_advance(n_cached_dev.numel(), _dev(n_cached_dev, torch.int32),
+                                           _dev(pos_dev, torch.int32), int(delta), _stream(stream)))
+
+
+def c2kv_attend_masked(geom, mask: int, n_doc: int, n_slot: int, k: int, q: torch.Tensor,
+                       kk: torch.Tensor, v: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor,
+                       stream=None) -> None:
+    g = as_geometry(geom)
+    _check(load_library().c2kv_attend_masked(
+        ctypes.byref(g), int(mask), int(n_doc), int(n_slot), int(k), _dev(q, torch.bfloat16, "q"),
+        _dev(kk, torch.bfloat16, "kk"), _dev(v, torch.bfloat16, "v"), _dev(out, torch.bfloat16, "out"),
+        _dev(workspace, None, "workspace"), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def masked_workspace_bytes(geom, n_tokens: int) -> int:
+    """Scratch bytes c2kv_attend_masked needs for one n_tokens sequence."""
+    a = c2kv_attend_workspace_size(geom, 1, n_tokens, n_tokens)
+    return ((a + 255) // 256) * 256 + c2kv_masked_extra_bytes(geom, n_tokens)
+
+
+def c2kv_device_error() -> int:
+    code = ctypes.c_int32()
+    _check(load_library().c2kv_device_error(ctypes.byref(code)))
+    return code.value

@@ -1,0 +1,599 @@
+// C ABI of the C2KV composed-cache path: pinned segment store, composition
+// (host->device streaming + re-rotation), and the attention entry points.
+// Every argument check happens here, on the host, before anything is
+// enqueued.  See include/c2kv.h for the contract of each call.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <unordered_map>
+#include <unordered_set>
+#include <vector>
+
+#include "c2kv_internal.h"
+
+using namespace c2kv;
+
+namespace {
+
+thread_local std::string g_err;
+
+c2kv_status fail(c2kv_status st, const std::string& msg) {
+  g_err = msg;
+  return st;
+}
+
+#define C2KV_CUDA(call)                                                                   \
+  do {                                                                                    \
+    cudaError_t e_ = (call);                                                              \
+    if (e_ != cudaSuccess)                                                                \
+      return fail(C2KV_ECUDA, std::string(#call) + ": " + cudaGetErrorString(e_));        \
+  } while (0)
+
+// Device error word, one per device that loads the library.
+__device__ unsigned int g_error_word = 0;
+
+constexpr int kMaxDevices = 64;
+unsigned* g_err_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+std::mutex g_dev_mu;
+
+c2kv_status device_state(unsigned** err, int* num_sms) {
+  int dev = 0;
+  C2KV_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return fail(C2KV_EINVAL, "device index out of range");
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_err_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    C2KV_CUDA(cudaGetSymbolAddress(&ptr, g_error_word));
+    int sms = 0;
+    C2KV_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    g_err_ptr[dev] = static_cast<unsigned*>(ptr);
+    g_num_sms[dev] = sms;
+  }
+  if (err) *err = g_err_ptr[dev];
+  if (num_sms) *num_sms = g_num_sms[dev];
+  return C2KV_OK;
+}
+
+// SM count for sizing (no GPU needed: falls back to a GB300's 152 SMs).
+int sm_count_for_sizing() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0)
+    return sms;
+  cudaGetLastError();
+  return 152;
+}
+
+c2kv_status check_geom(const c2kv_geometry* g) {
+  if (g == nullptr) return fail(C2KV_EINVAL, "geometry is null");
+  if (g->n_layers < 1 || g->n_q_heads < 1 || g->n_kv_heads < 1)
+    return fail(C2KV_EINVAL, "geometry: layer and head counts must be >= 1");
+  if (g->n_q_heads % g->n_kv_heads != 0)
+    return fail(C2KV_EINVAL, "geometry: n_kv_heads must divide n_q_heads");
+  const int grp = g->n_q_heads / g->n_kv_heads;
+  if (grp != 1 && grp != 2 && grp != 4 && grp != 5 && grp != 8)
+    return fail(C2KV_EINVAL, "geometry: q heads per kv head must be 1, 2, 4, 5 or 8");
+  if (g->head_dim != 64 && g->head_dim != 128)
+    return fail(C2KV_EINVAL, "geometry: head_dim must be 64 or 128");
+  if (!(g->rope_theta > 1.0) || !std::isfinite(g->rope_theta))
+    return fail(C2KV_EINVAL, "geometry: rope_theta must be finite and > 1");
+  if (g->n_kv_heads * (g->head_dim / 16) > 1024)
+    return fail(C2KV_EINVAL, "geometry: too many kv heads");
+  return C2KV_OK;
+}
+
+void fill_inv_freq(const c2kv_geometry* g, double* out) {
+  for (int i = 0; i < g->head_dim / 2; ++i) out[i] = std::pow(g->rope_theta, -2.0 * i / g->head_dim);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Seg {
+  size_t k_off, v_off;
+  int32_t n_tokens, n_slots, k;
+};
+
+}  // namespace
+
+struct c2kv_store_s {
+  c2kv_geometry g{};
+  int device = 0;
+  uint8_t* pool = nullptr;
+  size_t pool_bytes = 0, used = 0;
+  std::unordered_map<int32_t, Seg> docs;
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr;
+  std::vector<cudaEvent_t> ev;
+  std::mutex mu;
+};
+
+namespace {
+constexpr int kLayerGroups = 4;   // copy/rotate pipeline depth of one compose
+
+// Composition plan shared by c2kv_plan and c2kv_compose.
+c2kv_status plan_impl(int32_t n_docs, const int32_t* n_tokens, const int32_t* n_slots,
+                      const int32_t* order, int32_t* slot_start, int32_t* pos_offset,
+                      int32_t* total_slots, int32_t* total_tokens) {
+  if (n_docs < 0) return fail(C2KV_EINVAL, "n_docs < 0");
+  if (n_docs > 0 && (n_tokens == nullptr || n_slots == nullptr))
+    return fail(C2KV_EINVAL, "n_tokens / n_slots is null");
+  if (order != nullptr) {
+    std::vector<char> seen(n_docs, 0);
+    for (int c = 0; c < n_docs; ++c) {
+      const int o = order[c];
+      if (o < 0 || o >= n_docs || seen[o]) return fail(C2KV_EINVAL, "order is not a permutation of 0..n_docs-1");
+      seen[o] = 1;
+    }
+  }
+  int64_t slots = 0, toks = 0;
+  for (int c = 0; c < n_docs; ++c) {
+    const int d = order ? order[c] : c;
+    if (n_tokens[d] < 1) return fail(C2KV_EINVAL, "document with n_tokens < 1");
+    if (n_slots[d] < 1 || n_slots[d] > n_tokens[d]) return fail(C2KV_EINVAL, "n_slots must be in [1, n_tokens]");
+    if (slot_start) slot_start[c] = (int32_t)slots;
+    if (pos_offset) pos_offset[c] = (int32_t)toks;
+    slots += n_slots[d];
+    toks += n_tokens[d];
+    if (slots > INT32_MAX / 2 || toks > INT32_MAX / 2) return fail(C2KV_EINVAL, "composed length overflows int32");
+  }
+  if (total_slots) *total_slots = (int32_t)slots;
+  if (total_tokens) *total_tokens = (int32_t)toks;
+  return C2KV_OK;
+}
+
+struct AttnWs {
+  int n_tb, num_splits, split_keys;
+  size_t counters_off, ml_off, o_off, total;
+};
+
+AttnWs attn_workspace(const c2kv_geometry* g, int batch, int t_len, int max_keys, int num_sms) {
+  AttnWs w{};
+  const int tpc = attn_tokens_per_cta(t_len);
+  w.n_tb = (t_len + tpc - 1) / tpc;
+  attn_plan_splits(batch * w.n_tb * g->n_kv_heads, max_keys, num_sms, &w.num_splits, &w.split_keys);
+  const int grp = g->n_q_heads / g->n_kv_heads;
+  const size_t rows = (size_t)batch * t_len * g->n_kv_heads * w.num_splits * grp;
+  w.counters_off = 0;
+  w.ml_off = align256((size_t)batch * w.n_tb * g->n_kv_heads * sizeof(int32_t));
+  w.o_off = w.ml_off + align256(rows * 2 * sizeof(float));
+  w.total = w.num_splits > 1 ? w.o_off + align256(rows * g->head_dim * sizeof(float)) : 0;
+  return w;
+}
+
+c2kv_status run_attention(const c2kv_geometry* g, int batch, const __nv_bfloat16* const* kb,
+                          const __nv_bfloat16* const* vb, const int32_t* n_cached_h, const int32_t* pos_h,
+                          const int32_t* n_cached_d, const int32_t* pos_d, int cap, int max_keys, int t_len,
+                          int pos_mode, int mask_mode, int n_doc, int kblk, const void* q, void* out,
+                          void* workspace, size_t workspace_bytes, cudaStream_t st) {
+  unsigned* err = nullptr;
+  int sms = 0;
+  c2kv_status s = device_state(&err, &sms);
+  if (s != C2KV_OK) return s;
+  const AttnWs w = attn_workspace(g, batch, t_len, max_keys, sms);
+  if (w.total > 0 && (workspace == nullptr || workspace_bytes < w.total))
+    return fail(C2KV_EINVAL, "workspace too small: need " + std::to_string(w.total) + " bytes");
+  AttnParams p;
+  std::memset(&p, 0, sizeof(p));
+  for (int b = 0; b < batch; ++b) {
+    p.k_base[b] = kb[b];
+    p.v_base[b] = vb[b];
+    p.n_cached_h[b] = n_cached_h ? n_cached_h[b] : 0;
+    p.pos_h[b] = pos_h ? pos_h[b] : 0;
+  }
+  p.n_cached_d = n_cached_d;
+  p.pos_d = pos_d;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.counters = w.total ? reinterpret_cast<int32_t*>(ws + w.counters_off) : nullptr;
+  p.part_ml = w.total ? reinterpret_cast<float*>(ws + w.ml_off) : nullptr;
+  p.part_o = w.total ? reinterpret_cast<float*>(ws + w.o_off) : nullptr;
+  p.err = err;
+  p.batch = batch;
+  p.t_len = t_len;
+  p.n_q = g->n_q_heads;
+  p.n_kv = g->n_kv_heads;
+  p.cap = cap;
+  p.max_keys = max_keys;
+  p.num_splits = w.num_splits;
+  p.split_keys = w.split_keys;
+  p.pos_mode = pos_mode;
+  p.mask_mode = mask_mode;
+  p.n_doc = n_doc;
+  p.kblk = kblk;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)g->head_dim));
+  fill_inv_freq(g, p.inv_freq);
+  C2KV_CUDA(launch_attention(p, g->head_dim, g->n_q_heads / g->n_kv_heads, st));
+  return C2KV_OK;
+}
+
+c2kv_status run_append(const c2kv_geometry* g, int batch, __nv_bfloat16* const* kd, __nv_bfloat16* const* vd,
+                       const int32_t* row_h, const int32_t* pos_h, const int32_t* row_d, const int32_t* pos_d,
+                       int cap, int t_len, int pos_mode, int n_doc, int kblk, const void* k_src,
+                       const void* v_src, cudaStream_t st) {
+  unsigned* err = nullptr;
+  c2kv_status s = device_state(&err, nullptr);
+  if (s != C2KV_OK) return s;
+  AppendParams p;
+  std::memset(&p, 0, sizeof(p));
+  for (int b = 0; b < batch; ++b) {
+    p.k_dst[b] = kd[b];
+    p.v_dst[b] = vd[b];
+    p.row_h[b] = row_h ? row_h[b] : 0;
+    p.pos_h[b] = pos_h ? pos_h[b] : 0;
+  }
+  p.row_d = row_d;
+  p.pos_d = pos_d;
+  p.k_src = static_cast<const __nv_bfloat16*>(k_src);
+  p.v_src = static_cast<const __nv_bfloat16*>(v_src);
+  p.err = err;
+  p.t_len = t_len;
+  p.n_kv = g->n_kv_heads;
+  p.cap = cap;
+  p.pos_mode = pos_mode;
+  p.n_doc = n_doc;
+  p.kblk = kblk;
+  fill_inv_freq(g, p.inv_freq);
+  C2KV_CUDA(launch_append(p, g->head_dim, batch, st));
+  return C2KV_OK;
+}
+
+c2kv_status check_caches(int batch, void* const* kc, void* const* vc, int cap) {
+  if (batch < 1 || batch > kMaxBatch) return fail(C2KV_EINVAL, "batch must be in [1, 16]");
+  if (kc == nullptr || vc == nullptr) return fail(C2KV_EINVAL, "cache pointer arrays are null");
+  if (cap < 1) return fail(C2KV_EINVAL, "cap must be >= 1");
+  for (int b = 0; b < batch; ++b) {
+    if (kc[b] == nullptr || vc[b] == nullptr) return fail(C2KV_EINVAL, "a cache pointer is null");
+    if ((reinterpret_cast<uintptr_t>(kc[b]) | reinterpret_cast<uintptr_t>(vc[b])) & 15)
+      return fail(C2KV_EINVAL, "cache pointers must be 16-byte aligned");
+  }
+  return C2KV_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* c2kv_last_error(void) { return g_err.c_str(); }
+
+const char* c2kv_version(void) { return "c2kv-gb300 0.1 (sm_103a)"; }
+
+c2kv_status c2kv_store_create(const c2kv_geometry* geom, size_t pinned_bytes, c2kv_store* out) {
+  c2kv_status s = check_geom(geom);
+  if (s != C2KV_OK) return s;
+  if (out == nullptr) return fail(C2KV_EINVAL, "out is null");
+  *out = nullptr;
+  c2kv_store st = new (std::nothrow) c2kv_store_s();
+  if (st == nullptr) return fail(C2KV_ENOMEM, "host allocation failed");
+  st->g = *geom;
+  cudaError_t e = cudaGetDevice(&st->device);
+  if (e == cudaSuccess && pinned_bytes > 0) {
+    e = cudaHostAlloc(reinterpret_cast<void**>(&st->pool), pinned_bytes, cudaHostAllocDefault);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      delete st;
+      return fail(C2KV_ENOMEM, std::string("cudaHostAlloc of the pinned pool failed: ") + cudaGetErrorString(e));
+    }
+    st->pool_bytes = pinned_bytes;
+  }
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&st->side, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st->fork, cudaEventDisableTiming);
+  for (int i = 0; e == cudaSuccess && i < kLayerGroups; ++i) {
+    cudaEvent_t ev;
+    e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (e == cudaSuccess) st->ev.push_back(ev);
+  }
+  if (e != cudaSuccess) {
+    c2kv_store_destroy(st);
+    return fail(C2KV_ECUDA, std::string("store setup failed: ") + cudaGetErrorString(e));
+  }
+  *out = st;
+  return C2KV_OK;
+}
+
+void c2kv_store_destroy(c2kv_store st) {
+  if (st == nullptr) return;
+  if (st->side) {
+    cudaStreamSynchronize(st->side);
+    cudaStreamDestroy(st->side);
+  }
+  if (st->fork) cudaEventDestroy(st->fork);
+  for (cudaEvent_t ev : st->ev) cudaEventDestroy(ev);
+  if (st->pool) cudaFreeHost(st->pool);
+  delete st;
+}
+
+c2kv_status c2kv_store_segments(c2kv_store st, int32_t n_docs, const int32_t* doc_ids,
+                                const int32_t* n_tokens, const int32_t* n_slots, int32_t k,
+                                const void* const* k_pre, const void* const* v) {
+  if (st == nullptr) return fail(C2KV_EINVAL, "store is null");
+  if (n_docs < 0) return fail(C2KV_EINVAL, "n_docs < 0");
+  if (n_docs == 0) return C2KV_OK;
+  if (!doc_ids || !n_tokens || !n_slots || !k_pre || !v) return fail(C2KV_EINVAL, "null argument");
+  if (k < 1) return fail(C2KV_EINVAL, "k must be >= 1");
+  std::lock_guard<std::mutex> lk(st->mu);
+  const c2kv_geometry& g = st->g;
+  const size_t row = (size_t)g.n_layers * g.n_kv_heads * g.head_dim * 2;   // bytes per slot (K or V)
+  size_t need = 0;
+  std::unordered_set<int32_t> ids;
+  for (int i = 0; i < n_docs; ++i) {
+    if (n_tokens[i] < 1) return fail(C2KV_EINVAL, "n_tokens must be >= 1");
+    if (n_slots[i] < 1 || n_slots[i] > n_tokens[i]) return fail(C2KV_EINVAL, "n_slots must be in [1, n_tokens]");
+    if (!k_pre[i] || !v[i]) return fail(C2KV_EINVAL, "segment pointer is null");
+    if (st->docs.count(doc_ids[i]) || !ids.insert(doc_ids[i]).second)
+      return fail(C2KV_EINVAL, "document id " + std::to_string(doc_ids[i]) + " is already stored");
+    need += 2 * align256(row * n_slots[i]);
+  }
+  if (st->used + need > st->pool_bytes)
+    return fail(C2KV_ENOMEM, "pinned pool full: need " + std::to_string(need) + " more bytes");
+  for (int i = 0; i < n_docs; ++i) {
+    const size_t bytes = row * n_slots[i];
+    Seg sg;
+    sg.k_off = st->used;
+    std::memcpy(st->pool + sg.k_off, k_pre[i], bytes);
+    st->used += align256(bytes);
+    sg.v_off = st->used;
+    std::memcpy(st->pool + sg.v_off, v[i], bytes);
+    st->used += align256(bytes);
+    sg.n_tokens = n_tokens[i];
+    sg.n_slots = n_slots[i];
+    sg.k = k;
+    st->docs[doc_ids[i]] = sg;
+  }
+  return C2KV_OK;
+}
+
+c2kv_status c2kv_store_lookup(c2kv_store st, int32_t doc_id, int32_t* n_tokens, int32_t* n_slots, int32_t* k) {
+  if (st == nullptr) return fail(C2KV_EINVAL, "store is null");
+  std::lock_guard<std::mutex> lk(st->mu);
+  auto it = st->docs.find(doc_id);
+  if (it == st->docs.end()) return fail(C2KV_ENOTFOUND, "unknown document id " + std::to_string(doc_id));
+  if (n_tokens) *n_tokens = it->second.n_tokens;
+  if (n_slots) *n_slots = it->second.n_slots;
+  if (k) *k = it->second.k;
+  return C2KV_OK;
+}
+
+c2kv_status c2kv_plan(int32_t n_docs, const int32_t* n_tokens, const int32_t* n_slots, const int32_t* order,
+                      int32_t* slot_start, int32_t* pos_offset, int32_t* total_slots, int32_t* total_tokens) {
+  return plan_impl(n_docs, n_tokens, n_slots, order, slot_start, pos_offset, total_slots, total_tokens);
+}
+
+c2kv_status c2kv_compose(c2kv_store st, int32_t n_docs, const int32_t* doc_ids, const int32_t* order, int32_t k,
+                         void* k_cache, void* v_cache, int32_t cap, int32_t* pos_dev_out, int32_t* n_slots_out,
+                         int32_t* next_pos_out, void* stream) {
+  if (st == nullptr) return fail(C2KV_EINVAL, "store is null");
+  if (n_docs < 0 || n_docs > kMaxDocsPerCompose)
+    return fail(C2KV_EINVAL, "n_docs must be in [0, " + std::to_string(kMaxDocsPerCompose) + "]");
+  if (n_docs > 0 && doc_ids == nullptr) return fail(C2KV_EINVAL, "doc_ids is null");
+  if (k < 1) return fail(C2KV_EINVAL, "k must be >= 1");
+  if (cap < 0) return fail(C2KV_EINVAL, "cap < 0");
+  std::lock_guard<std::mutex> lk(st->mu);
+  const c2kv_geometry& g = st->g;
+  std::vector<Seg> segs(n_docs);
+  std::vector<int32_t> ntok(n_docs), nsl(n_docs);
+  for (int i = 0; i < n_docs; ++i) {
+    auto it = st->docs.find(doc_ids[i]);
+    if (it == st->docs.end()) return fail(C2KV_ENOTFOUND, "unknown document id " + std::to_string(doc_ids[i]));
+    if (it->second.k != k)
+      return fail(C2KV_EINVAL, "document " + std::to_string(doc_ids[i]) + " was stored with k=" +
+                                   std::to_string(it->second.k));
+    segs[i] = it->second;
+    ntok[i] = segs[i].n_tokens;
+    nsl[i] = segs[i].n_slots;
+  }
+  std::vector<int32_t> slot0(n_docs), off(n_docs);
+  int32_t total = 0, l_tot = 0;
+  c2kv_status s = plan_impl(n_docs, ntok.data(), nsl.data(), order, slot0.data(), off.data(), &total, &l_tot);
+  if (s != C2KV_OK) return s;
+  if (total > cap)
+    return fail(C2KV_ECAPACITY, "composed slots " + std::to_string(total) + " exceed cap " + std::to_string(cap));
+  if (n_slots_out) *n_slots_out = total;
+  if (next_pos_out) *next_pos_out = l_tot;
+  if (total == 0) return C2KV_OK;
+  if (k_cache == nullptr || v_cache == nullptr) return fail(C2KV_EINVAL, "cache pointer is null");
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return fail(C2KV_EINVAL, "cache pointers must be 16-byte aligned");
+  int dev = -1;
+  C2KV_CUDA(cudaGetDevice(&dev));
+  if (dev != st->device) return fail(C2KV_EINVAL, "current device differs from the store's device");
+  unsigned* err = nullptr;
+  s = device_state(&err, nullptr);
+  if (s != C2KV_OK) return s;
+
+  cudaStream_t us = static_cast<cudaStream_t>(stream);
+  const int D = g.head_dim, H = g.n_kv_heads, L = g.n_layers;
+  const size_t elem = 2;
+  RopeParams rp;
+  std::memset(&rp, 0, sizeof(rp));
+  rp.k_cache = static_cast<__nv_bfloat16*>(k_cache);
+  rp.pos_out = pos_dev_out;
+  rp.err = err;
+  rp.cap = cap;
+  rp.n_kv = H;
+  rp.n_total = total;
+  rp.k = k;
+  rp.n_docs = n_docs;
+  fill_inv_freq(&g, rp.inv_freq);
+  for (int c = 0; c < n_docs; ++c) {
+    const int d = order ? order[c] : c;
+    rp.seg[c].slot0 = slot0[c];
+    rp.seg[c].n_slots = nsl[d];
+    rp.seg[c].off = off[c];
+    rp.seg[c].n_tokens = ntok[d];
+  }
+
+  // Copies run on the store's stream after the caller's earlier work; each
+  // layer group's re-rotation runs on the caller's stream once it has landed.
+  C2KV_CUDA(cudaEventRecord(st->fork, us));
+  C2KV_CUDA(cudaStreamWaitEvent(st->side, st->fork, 0));
+  const int ngroups = std::min(L, kLayerGroups);
+  uint8_t* kc = static_cast<uint8_t*>(k_cache);
+  uint8_t* vc = static_cast<uint8_t*>(v_cache);
+  for (int gi = 0; gi < ngroups; ++gi) {
+    const int l0 = gi * L / ngroups, l1 = (gi + 1) * L / ngroups;
+    for (int c = 0; c < n_docs; ++c) {
+      const int d = order ? order[c] : c;
+      const Seg& sg = segs[d];
+      const size_t spitch = (size_t)sg.n_slots * D * elem;          // one (layer, head) run in the store
+      const size_t dpitch = (size_t)cap * D * elem;                  // one (layer, head) run in the cache
+      const size_t src_off = (size_t)l0 * H * spitch;
+      const size_t dst_off = ((size_t)l0 * H * cap + slot0[c]) * D * elem;
+      const size_t height = (size_t)(l1 - l0) * H;
+      C2KV_CUDA(cudaMemcpy2DAsync(kc + dst_off, dpitch, st->pool + sg.k_off + src_off, spitch, spitch, height,
+                                  cudaMemcpyHostToDevice, st->side));
+      C2KV_CUDA(cudaMemcpy2DAsync(vc + dst_off, dpitch, st->pool + sg.v_off + src_off, spitch, spitch, height,
+                                  cudaMemcpyHostToDevice, st->side));
+    }
+    C2KV_CUDA(cudaEventRecord(st->ev[gi], st->side));
+    C2KV_CUDA(cudaStreamWaitEvent(us, st->ev[gi], 0));
+    rp.layer0 = l0;
+    rp.layer1 = l1;
+    C2KV_CUDA(launch_rerope(rp, D, us));
+  }
+  return C2KV_OK;
+}
+
+size_t c2kv_attend_workspace_size(const c2kv_geometry* geom, int32_t batch, int32_t t_len, int32_t max_keys) {
+  if (check_geom(geom) != C2KV_OK || batch < 1 || t_len < 1 || max_keys < 1) return 0;
+  const AttnWs w = attn_workspace(geom, batch, t_len, max_keys, sm_count_for_sizing());
+  return w.total > 0 ? w.total : 256;
+}
+
+size_t c2kv_masked_extra_bytes(const c2kv_geometry* geom, int32_t n_tokens) {
+  if (check_geom(geom) != C2KV_OK || n_tokens < 1) return 0;
+  return 2 * align256((size_t)geom->n_kv_heads * n_tokens * geom->head_dim * 2);
+}
+
+c2kv_status c2kv_workspace_init(void* workspace, size_t bytes, void* stream) {
+  if (bytes == 0) return C2KV_OK;
+  if (workspace == nullptr) return fail(C2KV_EINVAL, "workspace is null");
+  C2KV_CUDA(cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream)));
+  return C2KV_OK;
+}
+
+c2kv_status c2kv_attend_prefill(const c2kv_geometry* geom, int32_t layer, int32_t batch, void* const* k_caches,
+                                void* const* v_caches, int32_t cap, const int32_t* n_cached,
+                                const int32_t* start_pos, int32_t q_len, const void* q, const void* k_new,
+                                const void* v_new, void* out, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  c2kv_status s = check_geom(geom);
+  if (s != C2KV_OK) return s;
+  if (layer < 0 || layer >= geom->n_layers) return fail(C2KV_EINVAL, "layer out of range");
+  s = check_caches(batch, k_caches, v_caches, cap);
+  if (s != C2KV_OK) return s;
+  if (q_len < 1) return fail(C2KV_EINVAL, "q_len must be >= 1");
+  if (!n_cached || !start_pos) return fail(C2KV_EINVAL, "n_cached / start_pos is null");
+  if (!q || !k_new || !v_new || !out) return fail(C2KV_EINVAL, "null tensor pointer");
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new))
+    return fail(C2KV_EINVAL, "q / k_new / v_new must be 16-byte aligned");
+  int max_keys = 0;
+  for (int b = 0; b < batch; ++b) {
+    if (n_cached[b] < 0 || start_pos[b] < 0) return fail(C2KV_EINVAL, "negative n_cached / start_pos");
+    if ((int64_t)n_cached[b] + q_len > cap)
+      return fail(C2KV_ECAPACITY, "n_cached + q_len exceeds cap for sequence " + std::to_string(b));
+    if ((int64_t)start_pos[b] + q_len > INT32_MAX / 2) return fail(C2KV_EINVAL, "position overflows int32");
+    max_keys = std::max(max_keys, n_cached[b] + q_len);
+  }
+  const size_t lstride = (size_t)geom->n_kv_heads * cap * geom->head_dim;
+  __nv_bfloat16* kb[kMaxBatch];
+  __nv_bfloat16* vb[kMaxBatch];
+  for (int b = 0; b < batch; ++b) {
+    kb[b] = static_cast<__nv_bfloat16*>(k_caches[b]) + layer * lstride;
+    vb[b] = static_cast<__nv_bfloat16*>(v_caches[b]) + layer * lstride;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  s = run_append(geom, batch, kb, vb, n_cached, start_pos, nullptr, nullptr, cap, q_len, kPosSequential, 0, 0,
+                 k_new, v_new, st);
+  if (s != C2KV_OK) return s;
+  return run_attention(geom, batch, kb, vb, n_cached, start_pos, nullptr, nullptr, cap, max_keys, q_len,
+                       kPosSequential, kMaskCausal, 0, 0, q, out, workspace, workspace_bytes, st);
+}
+
+c2kv_status c2kv_attend_decode(const c2kv_geometry* geom, int32_t layer, int32_t batch, void* const* k_caches,
+                               void* const* v_caches, int32_t cap, const int32_t* n_cached_dev,
+                               const int32_t* pos_dev, int32_t max_keys, const void* q, const void* k_new,
+                               const void* v_new, void* out, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  c2kv_status s = check_geom(geom);
+  if (s != C2KV_OK) return s;
+  if (layer < 0 || layer >= geom->n_layers) return fail(C2KV_EINVAL, "layer out of range");
+  s = check_caches(batch, k_caches, v_caches, cap);
+  if (s != C2KV_OK) return s;
+  if (!n_cached_dev || !pos_dev) return fail(C2KV_EINVAL, "device length arrays are null");
+  if (max_keys < 1 || max_keys > cap) return fail(C2KV_EINVAL, "max_keys must be in [1, cap]");
+  if (!q || !k_new || !v_new || !out) return fail(C2KV_EINVAL, "null tensor pointer");
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new))
+    return fail(C2KV_EINVAL, "q / k_new / v_new must be 16-byte aligned");
+  const size_t lstride = (size_t)geom->n_kv_heads * cap * geom->head_dim;
+  __nv_bfloat16* kb[kMaxBatch];
+  __nv_bfloat16* vb[kMaxBatch];
+  for (int b = 0; b < batch; ++b) {
+    kb[b] = static_cast<__nv_bfloat16*>(k_caches[b]) + layer * lstride;
+    vb[b] = static_cast<__nv_bfloat16*>(v_caches[b]) + layer * lstride;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  s = run_append(geom, batch, kb, vb, nullptr, nullptr, n_cached_dev, pos_dev, cap, 1, kPosSequential, 0, 0,
+                 k_new, v_new, st);
+  if (s != C2KV_OK) return s;
+  return run_attention(geom, batch, kb, vb, nullptr, nullptr, n_cached_dev, pos_dev, cap, max_keys, 1,
+                       kPosSequential, kMaskCausal, 0, 0, q, out, workspace, workspace_bytes, st);
+}
+
+c2kv_status c2kv_seq_advance(int32_t batch, int32_t* n_cached_dev, int32_t* pos_dev, int32_t delta, void* stream) {
+  if (batch < 1 || batch > 32) return fail(C2KV_EINVAL, "batch must be in [1, 32]");
+  if (!n_cached_dev || !pos_dev) return fail(C2KV_EINVAL, "null device array");
+  C2KV_CUDA(launch_advance(batch, n_cached_dev, pos_dev, delta, static_cast<cudaStream_t>(stream)));
+  return C2KV_OK;
+}
+
+c2kv_status c2kv_attend_masked(const c2kv_geometry* geom, int32_t mask, int32_t n_doc, int32_t n_slot, int32_t k,
+                               const void* q, const void* kk, const void* v, void* out, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  c2kv_status s = check_geom(geom);
+  if (s != C2KV_OK) return s;
+  if (mask != C2KV_MASK_CAUSAL && mask != C2KV_MASK_STRUCTURED) return fail(C2KV_EINVAL, "unknown mask");
+  if (n_doc < 1 || n_slot < 0) return fail(C2KV_EINVAL, "need n_doc >= 1 and n_slot >= 0");
+  if (mask == C2KV_MASK_CAUSAL && n_slot != 0) return fail(C2KV_EINVAL, "causal mask takes n_slot = 0");
+  if (mask == C2KV_MASK_STRUCTURED && k < 1) return fail(C2KV_EINVAL, "k must be >= 1");
+  if ((int64_t)n_doc + n_slot > (1 << 24)) return fail(C2KV_EINVAL, "sequence too long");
+  if (!q || !kk || !v || !out || !workspace) return fail(C2KV_EINVAL, "null pointer");
+  if (!aligned16(q) || !aligned16(kk) || !aligned16(v) || !aligned16(workspace))
+    return fail(C2KV_EINVAL, "pointers must be 16-byte aligned");
+  const int N = n_doc + n_slot;
+  const size_t attn_bytes = c2kv_attend_workspace_size(geom, 1, N, N);
+  const size_t extra = c2kv_masked_extra_bytes(geom, N);
+  if (workspace_bytes < align256(attn_bytes) + extra)
+    return fail(C2KV_EINVAL, "workspace too small: need " + std::to_string(align256(attn_bytes) + extra));
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  __nv_bfloat16* krot = reinterpret_cast<__nv_bfloat16*>(ws + align256(attn_bytes));
+  __nv_bfloat16* vt = reinterpret_cast<__nv_bfloat16*>(ws + align256(attn_bytes) + extra / 2);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int32_t zero = 0;
+  const int kblk = mask == C2KV_MASK_STRUCTURED ? k : 1;
+  const int pos_mode = mask == C2KV_MASK_STRUCTURED ? kPosExtraction : kPosSequential;
+  s = run_append(geom, 1, &krot, &vt, &zero, &zero, nullptr, nullptr, N, N, pos_mode, n_doc, kblk, kk, v, st);
+  if (s != C2KV_OK) return s;
+  const __nv_bfloat16* kb = krot;
+  const __nv_bfloat16* vb = vt;
+  return run_attention(geom, 1, &kb, &vb, &zero, &zero, nullptr, nullptr, N, N, N, pos_mode,
+                       mask == C2KV_MASK_STRUCTURED ? kMaskStructured : kMaskCausal, n_doc, kblk, q, out,
+                       workspace, attn_bytes, st);
+}
+
+c2kv_status c2kv_device_error(int32_t* code) {
+  if (code == nullptr) return fail(C2KV_EINVAL, "code is null");
+  unsigned w = 0;
+  C2KV_CUDA(cudaDeviceSynchronize());
+  C2KV_CUDA(cudaMemcpyFromSymbol(&w, g_error_word, sizeof(w)));
+  const unsigned zero = 0;
+  C2KV_CUDA(cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)));
+  *code = (w & kErrTimeout) ? C2KV_ETIMEOUT : (w & kErrLength) ? C2KV_EDEVICE : C2KV_OK;
+  return C2KV_OK;
+}
+
+}  // extern "C"

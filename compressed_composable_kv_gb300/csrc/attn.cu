@@ -1,0 +1,417 @@
+// Split-K flash attention over a composed cache, on CUDA cores.
+//
+// C2KV explainer (paper-daily.com), section "pipeline: extract, store,
+// concatenate" (整体流程): after composition the question is appended and the
+// answer generated over the concatenated cache; section "results"
+// (实验结果：真的又快又准吗？): each decoded token reads the whole composed
+// cache, so decode is bound by the bytes of that cache.  Section "structured
+// information flow" (为什么需要“结构化信息流”？) gives the mask of the
+// extraction-time mode.
+//
+// Work decomposition.  A CTA owns one (sequence b, kv head h, token block,
+// key split).  Its key range is streamed through a 4-stage ring of 32-key
+// K/V tiles in shared memory, each tile fetched by two 1-D bulk copies (TMA
+// engine) completing on an mbarrier.  Rows are (token, q head of the group):
+// the G heads of a token share every K/V tile.  A "key group" of D/8 lanes
+// scores one key at a time (each lane holds 8 elements of d for all G heads,
+// partial dots reduced with xor shuffles) and keeps its own online-softmax
+// state (m, l, o); groups are merged through shared memory at the end.
+// Decode (one token) spreads the 4 warps over the keys; prefill and the mask
+// mode give each warp its own token.  With more than one split the CTA
+// writes (m, l, o) partials; the last CTA of its (b, token block, h) to
+// arrive (atomic counter) merges them and resets the counter.
+#include <float.h>
+
+#include "c2kv_internal.h"
+
+namespace c2kv {
+
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kWarps = 4;
+constexpr int kStages = 4;
+constexpr int T = kAttnTileKeys;
+
+template <int D, int G, int WPT>
+struct Cfg {
+  static constexpr int LPK = D / 8;          // lanes per key
+  static constexpr int GPW = 32 / LPK;       // key groups per warp
+  static constexpr int TPC = kWarps / WPT;   // tokens per CTA
+  static constexpr int GPT = WPT * GPW;      // key groups per token
+  static constexpr int KPG = T / GPT;        // keys per group per tile
+  static constexpr int CH = KPG < 8 ? KPG : 8;
+  static constexpr int TILE = T * D * 2;     // bytes of one K (or V) tile
+  static constexpr int PIPE = kStages * 2 * TILE;
+  static constexpr int CMB = TPC * GPT * G * (D + 2) * 4;
+  static constexpr int WTS = TPC * G * kMaxSplits * 4;
+  static constexpr int MAIN_RAW = (PIPE > CMB ? (PIPE > WTS ? PIPE : WTS) : (CMB > WTS ? CMB : WTS));
+  static constexpr int MAIN = (MAIN_RAW + 127) / 128 * 128;   // keeps the mbarriers 8-byte aligned
+  static constexpr int EXTRA = 2 * kStages * 8 + 2 * TPC * (D / 2) * 4 + 16;
+  static constexpr int SMEM = MAIN + EXTRA;
+  static_assert(KPG >= 1 && KPG * GPT == T, "tile must split evenly over key groups");
+};
+
+__device__ __forceinline__ int token_position(const AttnParams& p, int pos0, int tok) {
+  if (p.pos_mode == kPosSequential) return pos0 + tok;
+  return tok < p.n_doc ? tok : min((tok - p.n_doc + 1) * p.kblk, p.n_doc) - 1;
+}
+
+// Extra visibility of the structured mask beyond causality (section
+// "structured information flow"): slot i sees document tokens of the sink
+// block [0, k) and of its own block [i*k, min((i+1)k, n_doc)) only.
+// Document rows see no slot and slots see earlier slots; both follow from
+// the causal limit because slots come after the document.
+__device__ __forceinline__ bool structured_visible(const AttnParams& p, int tok, int key) {
+  if (tok < p.n_doc || key >= p.n_doc) return true;
+  const int i = tok - p.n_doc;
+  const int sink_end = min(p.kblk, p.n_doc);
+  return key < sink_end || (key >= i * p.kblk && key < min((i + 1) * p.kblk, p.n_doc));
+}
+
+template <int D, int G, int WPT>
+__global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ AttnParams p) {
+  using C = Cfg<D, G, WPT>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::MAIN);
+  uint64_t* empty = full + kStages;
+  float* cs = reinterpret_cast<float*>(empty + kStages);   // [TPC][D/2]
+  float* sn = cs + C::TPC * (D / 2);
+  int* flag = reinterpret_cast<int*>(sn + C::TPC * (D / 2));
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x;
+  const int h = blockIdx.y % p.n_kv;
+  const int tb = blockIdx.y / p.n_kv;
+  const int b = blockIdx.z;
+  const int n_tb = (p.t_len + C::TPC - 1) / C::TPC;
+
+  const int n_cached = p.n_cached_d ? p.n_cached_d[b] : p.n_cached_h[b];
+  const int pos0 = p.pos_d ? p.pos_d[b] : p.pos_h[b];
+  if (n_cached < 0 || n_cached + p.t_len > p.cap || n_cached + p.t_len > p.max_keys) {
+    // Uniform over every CTA of sequence b: nobody touches its counters.
+    if (tid == 0 && split == 0 && blockIdx.y == 0) atomicOr(p.err, kErrLength);
+    return;
+  }
+
+  const int tok0 = tb * C::TPC;
+  const int ntok = min(C::TPC, p.t_len - tok0);
+  const int kmax = n_cached + tok0 + ntok;        // causal limit of the block's last token
+  const int kb = split * p.split_keys;
+  const int ke = min(kb + p.split_keys, kmax);
+  const int ntiles = ke > kb ? (ke - kb + T - 1) / T : 0;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kWarps);
+    }
+    fence_barrier_init();
+  }
+  for (int i = tid; i < ntok * (D / 2); i += kThreads) {
+    const int t = i / (D / 2), f = i % (D / 2);
+    rope_cos_sin(token_position(p, pos0, tok0 + t), p.inv_freq[f], &cs[i], &sn[i]);
+  }
+  __syncthreads();
+
+  const __nv_bfloat16* kg = p.k_base[b] + (size_t)h * p.cap * D;
+  const __nv_bfloat16* vg = p.v_base[b] + (size_t)h * p.cap * D;
+  auto stage_k = [&](int s) { return smem + s * 2 * C::TILE; };
+  auto stage_v = [&](int s) { return smem + s * 2 * C::TILE + C::TILE; };
+  auto issue = [&](int t) {
+    const int s = t % kStages;
+    const int key0 = kb + t * T;
+    const uint32_t bytes = (uint32_t)min(T, ke - key0) * D * 2;
+    mbar_arrive_expect_tx(&full[s], 2 * bytes);
+    bulk_g2s(stage_k(s), kg + (size_t)key0 * D, bytes, &full[s]);
+    bulk_g2s(stage_v(s), vg + (size_t)key0 * D, bytes, &full[s]);
+  };
+  int issued = 0;
+  if (tid == 0) {
+    for (; issued < min(kStages, ntiles); ++issued) issue(issued);
+  }
+
+  // ---- per-lane role
+  const int wtok = warp / WPT;
+  const int gq = (warp % WPT) * C::GPW + lane / C::LPK;   // key group within token
+  const int sub = lane % C::LPK;                          // owns d elements [8 sub, 8 sub + 8)
+  const bool tok_ok = wtok < ntok;
+  const int tok = tok0 + wtok;
+  const int lim = n_cached + tok + 1;
+
+  float q[G][8];
+  {
+    const int half = D / 2;
+    const int e0 = sub * 8;
+    const int partner = (e0 + half) % D;
+    const float* c = cs + wtok * half;
+    const float* s = sn + wtok * half;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float x[8], y[8];
+      if (tok_ok) {
+        const __nv_bfloat16* row = p.q + (((size_t)b * p.t_len + tok) * p.n_q + h * G + g) * D;
+        unpack8(*reinterpret_cast<const uint4*>(row + e0), x);
+        unpack8(*reinterpret_cast<const uint4*>(row + partner), y);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = y[e] = 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int f = (e0 + e) % half;
+        const float r = (e0 < half) ? x[e] * c[f] - y[e] * s[f] : x[e] * c[f] + y[e] * s[f];
+        q[g][e] = r * p.scale_log2;
+      }
+    }
+  }
+
+  float m[G], l[G], o[G][8];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    m[g] = -INFINITY;
+    l[g] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[g][e] = 0.f;
+  }
+
+  bool aborted = false;
+  for (int t = 0; t < ntiles; ++t) {
+    const int s = t % kStages;
+    const uint32_t ph = (t / kStages) & 1;
+    if (!mbar_wait(&full[s], ph)) { aborted = true; break; }
+    const int key0 = kb + t * T;
+    const int nvalid = min(T, ke - key0);
+    const uint8_t* Ks = stage_k(s);
+    const uint8_t* Vs = stage_v(s);
+#pragma unroll
+    for (int c0 = 0; c0 < C::KPG; c0 += C::CH) {
+      float sc[C::CH][G];
+#pragma unroll
+      for (int kk = 0; kk < C::CH; ++kk) {
+        const int kl = (c0 + kk) * C::GPT + gq;
+        const int key = key0 + kl;
+        float kf[8];
+        if (kl < nvalid) {
+          unpack8(*reinterpret_cast<const uint4*>(Ks + (size_t)kl * D * 2 + sub * 16), kf);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) kf[e] = 0.f;
+        }
+        bool vis = tok_ok && kl < nvalid && key < lim;
+        if (p.mask_mode == kMaskStructured) vis = vis && structured_visible(p, tok, key);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float d = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) d = fmaf(q[g][e], kf[e], d);
+#pragma unroll
+          for (int off = C::LPK / 2; off >= 1; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+          sc[kk][g] = vis ? d : -INFINITY;
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float mc = sc[0][g];
+#pragma unroll
+        for (int kk = 1; kk < C::CH; ++kk) mc = fmaxf(mc, sc[kk][g]);
+        if (mc > m[g]) {
+          const float a = exp2f(m[g] - mc);   // 0 when m was -inf
+          l[g] *= a;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[g][e] *= a;
+          m[g] = mc;
+        }
+      }
+#pragma unroll
+      for (int kk = 0; kk < C::CH; ++kk) {
+        const int kl = (c0 + kk) * C::GPT + gq;
+        if (kl < nvalid) {
+          float vf[8];
+          unpack8(*reinterpret_cast<const uint4*>(Vs + (size_t)kl * D * 2 + sub * 16), vf);
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float mu = (m[g] == -INFINITY) ? 0.f : m[g];
+            const float pr = exp2f(sc[kk][g] - mu);
+            l[g] += pr;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[g][e] = fmaf(pr, vf[e], o[g][e]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (tid == 0 && issued < ntiles) {
+      if (!mbar_wait(&empty[s], ph)) { aborted = true; break; }
+      issue(issued);
+      ++issued;
+    }
+  }
+
+  if (__syncthreads_or(aborted)) {
+    // Let copies already in flight land before the shared memory is reused.
+    if (tid == 0) {
+      for (int t = max(0, issued - kStages); t < issued; ++t) mbar_wait(&full[t % kStages], (t / kStages) & 1);
+      atomicOr(p.err, kErrTimeout);
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      m[g] = -INFINITY;
+      l[g] = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[g][e] = 0.f;
+    }
+    __syncthreads();
+  }
+
+  // ---- merge the key groups of each token (shared memory reused)
+  float* cmb_o = reinterpret_cast<float*>(smem);              // [TPC][GPT][G][D]
+  float* cmb_ml = cmb_o + C::TPC * C::GPT * G * D;             // [TPC][GPT][G][2]
+  if (tok_ok) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float* dst = cmb_o + (((size_t)wtok * C::GPT + gq) * G + g) * D + sub * 8;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) dst[e] = o[g][e];
+      if (sub == 0) {
+        cmb_ml[((wtok * C::GPT + gq) * G + g) * 2 + 0] = m[g];
+        cmb_ml[((wtok * C::GPT + gq) * G + g) * 2 + 1] = l[g];
+      }
+    }
+  }
+  __syncthreads();
+
+  const int S = p.num_splits;
+  for (int i = tid; i < ntok * G * D; i += kThreads) {
+    const int dd = i % D, g = (i / D) % G, t = i / (G * D);
+    float M = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < C::GPT; ++j) M = fmaxf(M, cmb_ml[((t * C::GPT + j) * G + g) * 2]);
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int j = 0; j < C::GPT; ++j) {
+      const float mj = cmb_ml[((t * C::GPT + j) * G + g) * 2];
+      const float w = (mj == -INFINITY) ? 0.f : exp2f(mj - M);
+      L = fmaf(cmb_ml[((t * C::GPT + j) * G + g) * 2 + 1], w, L);
+      O = fmaf(cmb_o[((t * C::GPT + j) * G + g) * D + dd], w, O);
+    }
+    const int tk = tok0 + t;
+    if (S == 1) {
+      p.out[(((size_t)b * p.t_len + tk) * p.n_q + h * G + g) * D + dd] = __float2bfloat16_rn(O / L);
+    } else {
+      const size_t base = (((size_t)b * p.t_len + tk) * p.n_kv + h) * S + split;
+      p.part_o[(base * G + g) * D + dd] = O;
+      if (dd == 0) {
+        p.part_ml[(base * G + g) * 2 + 0] = M;
+        p.part_ml[(base * G + g) * 2 + 1] = L;
+      }
+    }
+  }
+  if (S == 1) return;
+
+  // ---- last CTA of (b, token block, h) merges the split partials
+  __threadfence();
+  __syncthreads();
+  const int cidx = (b * n_tb + tb) * p.n_kv + h;
+  if (tid == 0) {
+    const int prev = atomicAdd(&p.counters[cidx], 1);
+    *flag = (prev == S - 1);
+  }
+  __syncthreads();
+  if (!*flag) return;
+  __threadfence();
+
+  float* wts = reinterpret_cast<float*>(smem);   // [TPC][G][S]
+  for (int pair = warp; pair < ntok * G; pair += kWarps) {
+    const int t = pair / G, g = pair % G;
+    const size_t base = (((size_t)b * p.t_len + tok0 + t) * p.n_kv + h) * S;
+    float M = -INFINITY;
+    for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldcg(&p.part_ml[((base + s) * G + g) * 2]));
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f;
+    for (int s = lane; s < S; s += 32) {
+      const float ms = __ldcg(&p.part_ml[((base + s) * G + g) * 2]);
+      const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+      wts[pair * S + s] = w;
+      L = fmaf(__ldcg(&p.part_ml[((base + s) * G + g) * 2 + 1]), w, L);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    const float invL = 1.f / L;
+    __syncwarp();
+    for (int s = lane; s < S; s += 32) wts[pair * S + s] *= invL;
+  }
+  __syncthreads();
+  for (int i = tid; i < ntok * G * D; i += kThreads) {
+    const int dd = i % D, g = (i / D) % G, t = i / (G * D);
+    const size_t base = (((size_t)b * p.t_len + tok0 + t) * p.n_kv + h) * S;
+    const float* w = wts + (t * G + g) * S;
+    float acc = 0.f;
+    for (int s = 0; s < S; ++s) acc = fmaf(w[s], __ldcg(&p.part_o[((base + s) * G + g) * D + dd]), acc);
+    p.out[(((size_t)b * p.t_len + tok0 + t) * p.n_q + h * G + g) * D + dd] = __float2bfloat16_rn(acc);
+  }
+  if (tid == 0) p.counters[cidx] = 0;
+}
+
+template <int D, int G, int WPT>
+cudaError_t launch_one(const AttnParams& p, cudaStream_t st) {
+  using C = Cfg<D, G, WPT>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, G, WPT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int n_tb = (p.t_len + C::TPC - 1) / C::TPC;
+  const dim3 grid(p.num_splits, p.n_kv * n_tb, p.batch);
+  attn_kernel<D, G, WPT><<<grid, kThreads, C::SMEM, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D, int G>
+cudaError_t launch_g(const AttnParams& p, cudaStream_t st) {
+  return p.t_len == 1 ? launch_one<D, G, 4>(p, st) : launch_one<D, G, 1>(p, st);
+}
+
+template <int D>
+cudaError_t launch_d(const AttnParams& p, int group, cudaStream_t st) {
+  switch (group) {
+    case 1: return launch_g<D, 1>(p, st);
+    case 2: return launch_g<D, 2>(p, st);
+    case 4: return launch_g<D, 4>(p, st);
+    case 5: return launch_g<D, 5>(p, st);
+    case 8: return launch_g<D, 8>(p, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+int attn_tokens_per_cta(int t_len) { return t_len == 1 ? 1 : kWarps; }
+
+void attn_plan_splits(int units, int max_keys, int num_sms, int* num_splits, int* split_keys) {
+  const int target = num_sms * kAttnCtasPerSm;
+  int s = (target + units - 1) / units;
+  const int tiles = (max_keys + T - 1) / T;
+  if (s > tiles) s = tiles;
+  if (s > kMaxSplits) s = kMaxSplits;
+  if (s < 1) s = 1;
+  int sk = (max_keys + s - 1) / s;
+  sk = ((sk + T - 1) / T) * T;
+  if (sk < T) sk = T;
+  *split_keys = sk;
+  *num_splits = (max_keys + sk - 1) / sk;
+  if (*num_splits < 1) *num_splits = 1;
+}
+
+cudaError_t launch_attention(const AttnParams& p, int head_dim, int group, cudaStream_t st) {
+  if (head_dim == 128) return launch_d<128>(p, group, st);
+  if (head_dim == 64) return launch_d<64>(p, group, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace c2kv

@@ -1,0 +1,181 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "c2kv.h"
+
+namespace c2kv {
+
+constexpr int kMaxDocsPerCompose = 512;   // documents in one c2kv_compose call
+constexpr int kMaxBatch = 16;             // sequences in one attention call
+constexpr int kMaxHalfDim = 64;           // head_dim <= 128
+constexpr int kMaxSplits = 256;           // split-K partitions per (sequence, token, head)
+
+// Device error word bits (see c2kv_device_error).
+constexpr unsigned kErrTimeout = 1u;      // a bounded mbarrier wait expired
+constexpr unsigned kErrLength = 2u;       // a device-side length exceeded cap / max_keys
+
+// Bounded waits give up after this many SM cycles (about 2 s at 2 GHz).
+constexpr long long kWaitCycles = 4000000000LL;
+
+// ---------------------------------------------------------------- RoPE angles
+// The angle pos * inv_freq is formed in fp64 and reduced modulo 2*pi with a
+// two-constant Cody-Waite reduction (2*pi split into its fp64 value and the
+// fp64 remainder), so the reduced angle is accurate to ~1e-11 rad even at
+// positions past 1e5; cos/sin of the reduced angle (|r| <= pi) then use the
+// fp32 library routine.
+constexpr double kTwoPiHi = 6.283185307179586;
+constexpr double kTwoPiLo = 2.4492935982947064e-16;
+constexpr double kInvTwoPi = 0.15915494309189535;
+
+__device__ __forceinline__ void rope_cos_sin(int pos, double inv_freq, float* c, float* s) {
+  const double a = (double)pos * inv_freq;
+  const double n = rint(a * kInvTwoPi);
+  double r = fma(-n, kTwoPiHi, a);
+  r = fma(-n, kTwoPiLo, r);
+  sincosf((float)r, s, c);
+}
+
+// ---------------------------------------------------------------- bf16 helpers
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+  f[0] = __uint_as_float(u.x << 16); f[1] = __uint_as_float(u.x & 0xffff0000u);
+  f[2] = __uint_as_float(u.y << 16); f[3] = __uint_as_float(u.y & 0xffff0000u);
+  f[4] = __uint_as_float(u.z << 16); f[5] = __uint_as_float(u.z & 0xffff0000u);
+  f[6] = __uint_as_float(u.w << 16); f[7] = __uint_as_float(u.w & 0xffff0000u);
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+}
+
+// ---------------------------------------------------------------- mbarrier / bulk copy
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitCycles) return false;
+  }
+  return true;
+}
+
+// 1-D bulk copy (TMA engine) global -> shared; bytes and both addresses must
+// be multiples of 16.  Completion is signalled on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// ---------------------------------------------------------------- kernel parameters
+
+struct SegDesc {
+  int32_t slot0;     // first composed row of this document
+  int32_t n_slots;
+  int32_t off;       // position offset: original tokens of the documents before it
+  int32_t n_tokens;
+};
+
+struct RopeParams {
+  __nv_bfloat16* k_cache;   // [L][Hkv][cap][d]
+  int32_t* pos_out;         // optional [cap]
+  unsigned* err;
+  int32_t cap, n_kv, layer0, layer1, n_total, k, n_docs;
+  double inv_freq[kMaxHalfDim];
+  SegDesc seg[kMaxDocsPerCompose];
+};
+
+enum PosMode : int32_t { kPosSequential = 0, kPosExtraction = 1 };
+enum MaskMode : int32_t { kMaskCausal = 0, kMaskStructured = 1 };
+
+struct AppendParams {
+  __nv_bfloat16* k_dst[kMaxBatch];   // layer base [Hkv][cap][d]
+  __nv_bfloat16* v_dst[kMaxBatch];
+  int32_t row_h[kMaxBatch];          // first destination row (host value) ...
+  int32_t pos_h[kMaxBatch];          // ... and first position
+  const int32_t* row_d;              // or device values (decode)
+  const int32_t* pos_d;
+  const __nv_bfloat16* k_src;        // [B][t_len][Hkv][d]
+  const __nv_bfloat16* v_src;
+  unsigned* err;
+  int32_t t_len, n_kv, cap, pos_mode, n_doc, kblk;
+  double inv_freq[kMaxHalfDim];
+};
+
+struct AttnParams {
+  const __nv_bfloat16* k_base[kMaxBatch];   // layer base [Hkv][cap][d]
+  const __nv_bfloat16* v_base[kMaxBatch];
+  int32_t n_cached_h[kMaxBatch];
+  int32_t pos_h[kMaxBatch];
+  const int32_t* n_cached_d;   // device lengths (decode) or null
+  const int32_t* pos_d;
+  const __nv_bfloat16* q;      // [B][t_len][Hq][d]
+  __nv_bfloat16* out;          // [B][t_len][Hq][d]
+  float* part_o;               // [B][t_len][Hkv][S][G][d]
+  float* part_ml;              // [B][t_len][Hkv][S][G][2]
+  int32_t* counters;           // [B][token blocks][Hkv]
+  unsigned* err;
+  int32_t batch, t_len, n_q, n_kv, cap, max_keys;
+  int32_t num_splits, split_keys;
+  int32_t pos_mode, mask_mode, n_doc, kblk;
+  float scale_log2;
+  double inv_freq[kMaxHalfDim];
+};
+
+// Launchers (return cudaGetLastError()).
+cudaError_t launch_rerope(const RopeParams& p, int head_dim, cudaStream_t st);
+cudaError_t launch_append(const AppendParams& p, int head_dim, int batch, cudaStream_t st);
+cudaError_t launch_attention(const AttnParams& p, int head_dim, int group, cudaStream_t st);
+cudaError_t launch_advance(int batch, int32_t* n_cached, int32_t* pos, int delta, cudaStream_t st);
+
+// Attention work decomposition shared by the launcher and the workspace query.
+int attn_tokens_per_cta(int t_len);
+void attn_plan_splits(int units, int max_keys, int num_sms, int* num_splits, int* split_keys);
+constexpr int kAttnTileKeys = 32;
+constexpr int kAttnCtasPerSm = 3;
+
+}  // namespace c2kv

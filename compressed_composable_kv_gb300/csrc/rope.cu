@@ -1,0 +1,184 @@
+// Re-rotation of composed segments, and rotate-and-append of new tokens.
+//
+// C2KV explainer (paper-daily.com), section "positions at concatenation"
+// (拼接时位置怎么处理？): segments are stored before RoPE and rotated at
+// composition time; slot j of composed document c sits at
+// off_c + min((j+1)k, n_c) - 1, where off_c is the summed original length of
+// the documents before it.  Rotation is the rotate-half form: pair
+// (i, i + d/2) turns by pos * theta^(-2i/d).
+#include "c2kv_internal.h"
+
+namespace c2kv {
+
+namespace {
+
+// Rotates 8 pairs: a holds elements [8c, 8c+8) of the first half, b the same
+// offsets of the second half.
+__device__ __forceinline__ void rotate8(uint4& a, uint4& b, const float* cs, const float* sn) {
+  float x[8], y[8], xo[8], yo[8];
+  unpack8(a, x);
+  unpack8(b, y);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    xo[e] = x[e] * cs[e] - y[e] * sn[e];
+    yo[e] = y[e] * cs[e] + x[e] * sn[e];
+  }
+  a = pack8(xo);
+  b = pack8(yo);
+}
+
+// ---------------------------------------------------------------------------
+// K1: in-place re-rotation of composed K rows for a group of layers.
+// One CTA owns kSlots consecutive composed slots: it derives their positions
+// from the segment table, builds their cos/sin table in shared memory once,
+// and rotates those slots' rows in every (layer, kv head) of the group with
+// 16-byte loads/stores.  V rows are never touched (they land by DMA).
+// ---------------------------------------------------------------------------
+constexpr int kSlots = 32;
+constexpr int kRopeThreads = 256;
+
+template <int D>
+__global__ void __launch_bounds__(kRopeThreads) rerope_kernel(const __grid_constant__ RopeParams p) {
+  constexpr int H = D / 2;
+  constexpr int TPR = H / 8;   // threads per row, each owns 8 pairs
+  __shared__ float cs[kSlots][H];
+  __shared__ float sn[kSlots][H];
+  __shared__ int spos[kSlots];
+
+  const int slot0 = blockIdx.x * kSlots;
+  const int n_here = min(kSlots, p.n_total - slot0);
+  if (threadIdx.x < kSlots) {
+    const int slot = slot0 + threadIdx.x;
+    int pos = -1;
+    if (threadIdx.x < n_here) {
+      int lo = 0, hi = p.n_docs - 1;   // last segment with seg.slot0 <= slot
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.seg[mid].slot0 <= slot) lo = mid; else hi = mid - 1;
+      }
+      const SegDesc sd = p.seg[lo];
+      const int j = slot - sd.slot0;
+      pos = sd.off + min((j + 1) * p.k, sd.n_tokens) - 1;
+      if (p.pos_out != nullptr && p.layer0 == 0) p.pos_out[slot] = pos;
+    }
+    spos[threadIdx.x] = pos;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n_here * H; i += kRopeThreads) {
+    const int r = i / H, f = i % H;
+    rope_cos_sin(spos[r], p.inv_freq[f], &cs[r][f], &sn[r][f]);
+  }
+  __syncthreads();
+
+  const int n_rows = (p.layer1 - p.layer0) * p.n_kv;   // (layer, head) row blocks
+  const int work = n_rows * kSlots * TPR;
+  constexpr int U = 4;
+  for (int w0 = threadIdx.x; w0 < work; w0 += kRopeThreads * U) {
+    uint4 a[U], b[U];
+    uint4* base[U];
+    int r_[U], c_[U];
+    bool ok[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int w = w0 + u * kRopeThreads;
+      const int c = w % TPR;
+      const int r = (w / TPR) % kSlots;
+      const int lh = w / (TPR * kSlots);
+      ok[u] = (w < work) && (r < n_here);
+      r_[u] = r;
+      c_[u] = c;
+      base[u] = nullptr;
+      if (ok[u]) {
+        const size_t row = ((size_t)(p.layer0 * p.n_kv + lh) * p.cap + slot0 + r) * D;
+        base[u] = reinterpret_cast<uint4*>(p.k_cache + row);
+        a[u] = base[u][c];
+        b[u] = base[u][c + TPR];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (ok[u]) {
+        rotate8(a[u], b[u], &cs[r_[u]][c_[u] * 8], &sn[r_[u]][c_[u] * 8]);
+        base[u][c_[u]] = a[u];
+        base[u][c_[u] + TPR] = b[u];
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// K4: rotate t_len new keys per sequence and append them (with their values)
+// at rows row0 + i of the cache.  grid (t_len, batch), one thread per
+// (kv head, 8-pair chunk).
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void append_kernel(const __grid_constant__ AppendParams p) {
+  constexpr int H = D / 2;
+  constexpr int TPR = H / 8;
+  __shared__ float cs[H];
+  __shared__ float sn[H];
+  const int i = blockIdx.x;
+  const int b = blockIdx.y;
+  const int row0 = p.row_d ? p.row_d[b] : p.row_h[b];
+  const int pos0 = p.pos_d ? p.pos_d[b] : p.pos_h[b];
+  if (row0 < 0 || row0 + p.t_len > p.cap) {
+    if (threadIdx.x == 0 && i == 0) atomicOr(p.err, kErrLength);
+    return;
+  }
+  int pos;
+  if (p.pos_mode == kPosSequential) {
+    pos = pos0 + i;
+  } else {   // extraction: documents at 0..n_doc-1, slot s at min((s+1)k, n_doc)-1
+    pos = (i < p.n_doc) ? i : min((i - p.n_doc + 1) * p.kblk, p.n_doc) - 1;
+  }
+  for (int f = threadIdx.x; f < H; f += blockDim.x) rope_cos_sin(pos, p.inv_freq[f], &cs[f], &sn[f]);
+  __syncthreads();
+  const int h = threadIdx.x / TPR;
+  const int c = threadIdx.x % TPR;
+  if (h >= p.n_kv) return;
+  const size_t src = (((size_t)b * p.t_len + i) * p.n_kv + h) * D;
+  const size_t dst = ((size_t)h * p.cap + row0 + i) * D;
+  const uint4* ks = reinterpret_cast<const uint4*>(p.k_src + src);
+  const uint4* vs = reinterpret_cast<const uint4*>(p.v_src + src);
+  uint4 a = ks[c], bb = ks[c + TPR];
+  rotate8(a, bb, &cs[c * 8], &sn[c * 8]);
+  uint4* kd = reinterpret_cast<uint4*>(p.k_dst[b] + dst);
+  uint4* vd = reinterpret_cast<uint4*>(p.v_dst[b] + dst);
+  kd[c] = a;
+  kd[c + TPR] = bb;
+  vd[c] = vs[c];
+  vd[c + TPR] = vs[c + TPR];
+}
+
+__global__ void advance_kernel(int batch, int32_t* n_cached, int32_t* pos, int delta) {
+  const int b = threadIdx.x;
+  if (b < batch) {
+    n_cached[b] += delta;
+    pos[b] += delta;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_rerope(const RopeParams& p, int head_dim, cudaStream_t st) {
+  const int blocks = (p.n_total + kSlots - 1) / kSlots;
+  if (blocks == 0) return cudaSuccess;
+  if (head_dim == 128) rerope_kernel<128><<<blocks, kRopeThreads, 0, st>>>(p);
+  else rerope_kernel<64><<<blocks, kRopeThreads, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append(const AppendParams& p, int head_dim, int batch, cudaStream_t st) {
+  const dim3 grid(p.t_len, batch);
+  const int threads = p.n_kv * (head_dim / 16);
+  if (head_dim == 128) append_kernel<128><<<grid, threads, 0, st>>>(p);
+  else append_kernel<64><<<grid, threads, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_advance(int batch, int32_t* n_cached, int32_t* pos, int delta, cudaStream_t st) {
+  advance_kernel<<<1, 32, 0, st>>>(batch, n_cached, pos, delta);
+  return cudaGetLastError();
+}
+
+}  // namespace c2kv

@@ -1,0 +1,88 @@
+"""Request-batch runtime over the C ABI: owns the device caches, the length
+arrays and the attention scratch of a batch of composed requests.
+
+It only allocates device memory (torch) and sequences C-ABI calls; every
+step of the path (composition, re-rotation, append, attention) runs in the
+CUDA library.  C2KV explainer (paper-daily.com), section "pipeline: extract,
+store, concatenate": compose the retrieved documents, append the question,
+then generate.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import List, Optional, Sequence
+
+import torch
+
+from . import binding as B
+
+
+@dataclass
+class RequestSpec:
+    doc_ids: List[int]
+    order: Optional[List[int]] = None
+
+
+class RequestBatch:
+    """Device state of `len(requests)` composed requests sharing one store."""
+
+    def __init__(self, store: int, geom, requests: Sequence[RequestSpec], k: int, q_len: int,
+                 decode_steps: int, device: str = "cuda", cap_multiple: int = 32):
+        self.store, self.geom, self.k = store, geom, k
+        self.requests = list(requests)
+        self.q_len, self.decode_steps = q_len, decode_steps
+        self.batch = len(self.requests)
+        L, H, D = geom.n_layers, geom.n_kv_heads, geom.head_dim
+        self.n_slots, self.l_tot = [], []
+        for r in self.requests:
+            nt, ns = [], []
+            for d in r.doc_ids:
+                a, b, _ = B.c2kv_store_lookup(store, d)
+                nt.append(a)
+                ns.append(b)
+            _, _, n, lt = B.c2kv_plan(nt, ns, r.order)
+            self.n_slots.append(n)
+            self.l_tot.append(lt)
+        need = max(self.n_slots) + q_len + decode_steps
+        self.cap = max(cap_multiple, -(-need // cap_multiple) * cap_multiple)
+        self.k_caches = [torch.empty((L, H, self.cap, D), dtype=torch.bfloat16, device=device)
+                         for _ in range(self.batch)]
+        self.v_caches = [torch.empty_like(t) for t in self.k_caches]
+        self.pos = [torch.full((self.cap,), -1, dtype=torch.int32, device=device)
+                    for _ in range(self.batch)]
+        self.n_cached_dev = torch.zeros(self.batch, dtype=torch.int32, device=device)
+        self.pos_dev = torch.zeros(self.batch, dtype=torch.int32, device=device)
+        self.max_keys_decode = max(self.n_slots) + q_len + decode_steps
+        ws = 256
+        if q_len > 0:
+            ws = max(ws, B.c2kv_attend_workspace_size(geom, self.batch, q_len, max(self.n_slots) + q_len))
+        ws = max(ws, B.c2kv_attend_workspace_size(geom, self.batch, 1, self.max_keys_decode))
+        self.workspace = torch.zeros(ws, dtype=torch.uint8, device=device)
+        B.c2kv_workspace_init(self.workspace)
+        self._dec_start = torch.tensor([n + q_len for n in self.n_slots], dtype=torch.int32)
+        self._pos_start = torch.tensor([lt + q_len for lt in self.l_tot], dtype=torch.int32)
+
+    def compose(self, stream=None) -> None:
+        for b, r in enumerate(self.requests):
+            n, nxt = B.c2kv_compose(self.store, r.doc_ids, r.order, self.k, self.k_caches[b],
+                                    self.v_caches[b], self.cap, self.pos[b], stream)
+            assert n == self.n_slots[b] and nxt == self.l_tot[b]
+
+    def prefill(self, layer: int, q, k_new, v_new, out, stream=None) -> None:
+        B.c2kv_attend_prefill(self.geom, layer, self.k_caches, self.v_caches, self.cap, self.n_slots,
+                              self.l_tot, q, k_new, v_new, out, self.workspace, stream)
+
+    def reset_decode(self, stream=None) -> None:
+        """Point the device lengths at the first decode step (after the question)."""
+        s = torch.cuda.current_stream() if stream is None else stream
+        with torch.cuda.stream(s):
+            self.n_cached_dev.copy_(self._dec_start, non_blocking=True)
+            self.pos_dev.copy_(self._pos_start, non_blocking=True)
+
+    def decode(self, layer: int, q, k_new, v_new, out, stream=None) -> None:
+        B.c2kv_attend_decode(self.geom, layer, self.k_caches, self.v_caches, self.cap, self.n_cached_dev,
+                             self.pos_dev, self.max_keys_decode, q, k_new, v_new, out, self.workspace,
+                             stream)
+
+    def advance(self, stream=None) -> None:
+        B.c2kv_seq_advance(self.n_cached_dev, self.pos_dev, 1, stream)

@@ -1,0 +1,268 @@
+/*
+ * c2kv.h -- C ABI of the GB300 (sm_103a) C2KV composed-cache hot path.
+ *
+ * C2KV (compressed, composable, non-prefix KV-cache reuse) stores one
+ * compressed, pre-RoPE K/V slot per k document tokens, keeps the stores in
+ * host memory, and at request time streams the selected documents to the
+ * GPU, re-applies RoPE at their new positions, concatenates them into one
+ * cache and then prefills the question and decodes the answer over it.
+ *
+ * Sources (cited by page title and section):
+ *   [EXPL]  "C 2 KV: Compressed and Composable KV Cache Reuse for Efficient
+ *           LLM Inference", paper-daily.com explainer.  Sections used:
+ *           "the problem" (它到底在解决什么问题？), "pipeline: extract, store,
+ *           concatenate" (整体流程：抽取、存储、拼接), "C2 tokens"
+ *           (C2 token：用额外的“记忆槽”承载压缩信息), "structured information flow"
+ *           (为什么需要“结构化信息流”？), "positions at concatenation"
+ *           (拼接时位置怎么处理？), "results" (实验结果：真的又快又准吗？).
+ *   [ABS]   arXiv 2607.17715 listing (arxivdaily.com), English abstract.
+ *
+ * Conventions for every entry point:
+ *   - No exception crosses the ABI; each call returns a c2kv_status and, on
+ *     failure, c2kv_last_error() (thread-local) describes it.  All argument
+ *     checks run on the host before anything is enqueued: a call that fails
+ *     validation enqueues nothing.
+ *   - All K/V/q tensors are bf16 (raw 16-bit patterns).  Device buffers are
+ *     owned by the caller; the library never frees them.  Host inputs are
+ *     read during the call only (copied where they must outlive it).
+ *   - Device work is enqueued on the caller's `stream` (a cudaStream_t passed
+ *     as void*; NULL is the legacy default stream) and is ordered after the
+ *     work already on it; calls return after enqueueing.
+ *   - Cache layout per sequence: k_cache and v_cache are each
+ *     [n_layers][n_kv_heads][cap][head_dim] bf16 (one contiguous key run per
+ *     layer and kv head).  q head h reads kv head h / (n_q_heads/n_kv_heads).
+ *   - RoPE is the rotate-half form with inv_freq_i = rope_theta^(-2i/d);
+ *     angles are formed in fp64, rotations are done in fp32 and rotated keys
+ *     are stored rounded to nearest even.
+ *   - A kernel that finds a device-side problem (a bounded wait that expired,
+ *     a device length beyond the cache capacity) records it in a device error
+ *     word and skips the affected output; c2kv_device_error() reads it.
+ */
+#ifndef C2KV_H_
+#define C2KV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct c2kv_store_s* c2kv_store;
+
+typedef struct {
+  int32_t n_layers;
+  int32_t n_q_heads;
+  int32_t n_kv_heads;   /* must divide n_q_heads; group = n_q/n_kv in {1,2,4,5,8} */
+  int32_t head_dim;     /* 64 or 128 */
+  double rope_theta;
+} c2kv_geometry;
+
+typedef enum {
+  C2KV_OK = 0,
+  C2KV_EINVAL = 1,     /* bad argument (null pointer, bad size, k mismatch, bad order) */
+  C2KV_ENOMEM = 2,     /* pinned pool exhausted or host allocation failed */
+  C2KV_ENOTFOUND = 3,  /* unknown document id */
+  C2KV_ECAPACITY = 4,  /* composed or appended rows exceed the cache capacity */
+  C2KV_ECUDA = 5,      /* a CUDA runtime call failed (message in c2kv_last_error) */
+  C2KV_ETIMEOUT = 6,   /* a kernel's bounded wait expired (from c2kv_device_error) */
+  C2KV_EDEVICE = 7     /* a kernel rejected a device-side value (from c2kv_device_error) */
+} c2kv_status;
+
+typedef enum {
+  C2KV_MASK_CAUSAL = 0,      /* plain causal mask over the whole sequence */
+  C2KV_MASK_STRUCTURED = 1   /* [EXPL] "structured information flow" rules */
+} c2kv_mask;
+
+/* Thread-local description of the last failure on this thread ("" if none). */
+const char* c2kv_last_error(void);
+
+/* Library version string. */
+const char* c2kv_version(void);
+
+/*
+ * Segment store: pinned host memory holding compressed pre-RoPE segments.
+ * [EXPL] "the problem": the caches live in host memory and are moved to the
+ * GPU when used; [EXPL] "positions at concatenation": they are kept before
+ * RoPE so they can be re-rotated wherever they are composed.
+ *
+ * Creates a store on the current CUDA device with a pinned pool of
+ * pinned_bytes (cudaHostAlloc), a non-blocking copy stream and events.
+ * Returns C2KV_EINVAL for a bad geometry, C2KV_ENOMEM if the pool cannot be
+ * pinned.  *out receives the handle (owned by the caller; free with
+ * c2kv_store_destroy).
+ */
+c2kv_status c2kv_store_create(const c2kv_geometry* geom, size_t pinned_bytes,
+                              c2kv_store* out);
+
+/* Waits for the store's copies in flight, then frees the pool and handles. */
+void c2kv_store_destroy(c2kv_store store);
+
+/*
+ * Copies n_docs compressed segments into the pinned pool.
+ * [EXPL] "C2 tokens": one slot per k document tokens, only the slots' K/V
+ * are kept.  For document i: doc_ids[i] (unique, not yet stored),
+ * n_tokens[i] >= 1 original tokens, 1 <= n_slots[i] <= n_tokens[i] slots
+ * stored at compression ratio k >= 1, and host pointers k_pre[i], v[i] to
+ * bf16 arrays [n_layers][n_kv_heads][n_slots[i]][head_dim] (K before RoPE).
+ * The inputs are copied; the caller keeps ownership.
+ * Errors: C2KV_EINVAL (bad sizes, null pointer, duplicate id),
+ * C2KV_ENOMEM (pool full; nothing of this call is stored).
+ */
+c2kv_status c2kv_store_segments(c2kv_store store, int32_t n_docs,
+                                const int32_t* doc_ids, const int32_t* n_tokens,
+                                const int32_t* n_slots, int32_t k,
+                                const void* const* k_pre, const void* const* v);
+
+/* Looks up one stored document: its original length, slot count and k. */
+c2kv_status c2kv_store_lookup(c2kv_store store, int32_t doc_id,
+                              int32_t* n_tokens, int32_t* n_slots, int32_t* k);
+
+/*
+ * Host-only composition planner (no device work; usable without a GPU).
+ * [EXPL] "positions at concatenation": documents are taken in composed
+ * order, composed doc c = input doc order[c] (order NULL = identity; order
+ * must be a permutation of 0..n_docs-1).  Each document occupies its
+ * original length of positions, so composed doc c starts at position
+ * pos_offset[c] = sum of n_tokens of the composed docs before it, and its
+ * slots start at row slot_start[c] = sum of their n_slots.  Outputs (host,
+ * n_docs entries each, may be NULL): slot_start, pos_offset; totals
+ * *total_slots = sum n_slots and *total_tokens = sum n_tokens (the position
+ * of the first appended question token).  Slot j of composed doc c sits at
+ * pos_offset[c] + min((j+1)k, n_tokens) - 1.
+ * Errors: C2KV_EINVAL (bad order, sizes, int32 overflow).
+ */
+c2kv_status c2kv_plan(int32_t n_docs, const int32_t* n_tokens,
+                      const int32_t* n_slots, const int32_t* order,
+                      int32_t* slot_start, int32_t* pos_offset,
+                      int32_t* total_slots, int32_t* total_tokens);
+
+/*
+ * Composes one request's cache.  [EXPL] "pipeline": fetch the documents'
+ * compressed caches, re-apply position encoding at their new positions and
+ * concatenate them, with no repair step; [EXPL] "positions at
+ * concatenation": slot j of composed doc c is rotated at
+ * pos_offset[c] + min((j+1)k, n_tokens_c) - 1.
+ *
+ * doc_ids[n_docs] (repeats allowed), order as in c2kv_plan, k must equal the
+ * k every document was stored with.  k_cache/v_cache: caller-owned device
+ * buffers [n_layers][n_kv_heads][cap][head_dim] bf16; rows [0, N) of every
+ * layer and kv head are written (N = total slots), rows >= N are untouched.
+ * pos_dev_out: optional device int32 [cap] receiving the N slot positions.
+ * Host outputs (optional): *n_slots_out = N, *next_pos_out = total original
+ * tokens (where the question starts).
+ * The segments are copied host->device on the store's copy stream in layer
+ * groups; the re-rotation of each group runs on `stream` once its copy has
+ * landed, and all of it is ordered before later work on `stream`.  The store
+ * must not be destroyed before that work completes.
+ * Errors: C2KV_EINVAL, C2KV_ENOTFOUND, C2KV_ECAPACITY (N > cap), C2KV_ECUDA.
+ */
+c2kv_status c2kv_compose(c2kv_store store, int32_t n_docs, const int32_t* doc_ids,
+                         const int32_t* order, int32_t k, void* k_cache,
+                         void* v_cache, int32_t cap, int32_t* pos_dev_out,
+                         int32_t* n_slots_out, int32_t* next_pos_out, void* stream);
+
+/*
+ * Device scratch (bytes) that c2kv_attend_prefill / c2kv_attend_decode /
+ * c2kv_attend_masked need for `batch` sequences of `t_len` new tokens each,
+ * with at most `max_keys` keys per sequence (cached + new).  The scratch
+ * holds split-K partial results and per-(sequence, head) arrival counters;
+ * it must be zeroed once before first use (c2kv_workspace_init) and may then
+ * be reused by calls that do not overlap on the GPU.  Returns 0 on bad input.
+ */
+size_t c2kv_attend_workspace_size(const c2kv_geometry* geom, int32_t batch,
+                                  int32_t t_len, int32_t max_keys);
+
+/* Zeroes a workspace on `stream` (cudaMemsetAsync). */
+c2kv_status c2kv_workspace_init(void* workspace, size_t bytes, void* stream);
+
+/*
+ * Question prefill for one layer of `batch` requests.
+ * [EXPL] "pipeline": after composition the question is appended and
+ * generation starts; reading: question token i of request b sits at position
+ * start_pos[b] + i (start_pos = the composed original length).
+ *
+ * k_caches[b], v_caches[b]: host array of device pointers to request b's
+ * cache base (layer 0, layout as above); `layer` selects the layer.
+ * n_cached[b] (host): rows already in the cache; start_pos[b] (host).
+ * q: device [batch][q_len][n_q_heads][head_dim] (before RoPE);
+ * k_new, v_new: device [batch][q_len][n_kv_heads][head_dim] (k before RoPE).
+ * The new keys are rotated and appended at rows n_cached[b] + i together
+ * with the values; then out[b][i] = softmax(q_i K^T / sqrt(d)) V over the
+ * n_cached[b] + i + 1 visible keys (all cached rows plus question tokens
+ * 0..i), written to device out [batch][q_len][n_q_heads][head_dim] bf16.
+ * workspace: device scratch of c2kv_attend_workspace_size(geom, batch,
+ * q_len, max_b(n_cached[b] + q_len)) bytes, zeroed once.
+ * Errors: C2KV_EINVAL, C2KV_ECAPACITY (n_cached[b] + q_len > cap), C2KV_ECUDA.
+ */
+c2kv_status c2kv_attend_prefill(const c2kv_geometry* geom, int32_t layer,
+                                int32_t batch, void* const* k_caches,
+                                void* const* v_caches, int32_t cap,
+                                const int32_t* n_cached, const int32_t* start_pos,
+                                int32_t q_len, const void* q, const void* k_new,
+                                const void* v_new, void* out, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/*
+ * One decode step for one layer of `batch` sequences.  [EXPL] "results":
+ * each generated token reads the whole composed cache, which C2KV shrinks.
+ *
+ * As prefill with one new token per sequence, except that the lengths live
+ * on the device so a captured sequence of calls can be replayed:
+ * n_cached_dev[b] (device int32) rows are cached, the new token is appended
+ * at row n_cached_dev[b] and rotated at position pos_dev[b] (device int32),
+ * and attends over n_cached_dev[b] + 1 keys.  max_keys (host) bounds
+ * n_cached_dev[b] + 1 for every b and sizes the grid; a device length over
+ * max_keys or cap is recorded in the device error word and that sequence's
+ * output is skipped.  q: [batch][n_q_heads][head_dim]; k_new, v_new:
+ * [batch][n_kv_heads][head_dim]; out: [batch][n_q_heads][head_dim].
+ * The lengths are not advanced (see c2kv_seq_advance).
+ * workspace: c2kv_attend_workspace_size(geom, batch, 1, max_keys) bytes.
+ */
+c2kv_status c2kv_attend_decode(const c2kv_geometry* geom, int32_t layer,
+                               int32_t batch, void* const* k_caches,
+                               void* const* v_caches, int32_t cap,
+                               const int32_t* n_cached_dev, const int32_t* pos_dev,
+                               int32_t max_keys, const void* q, const void* k_new,
+                               const void* v_new, void* out, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/* Adds `delta` to n_cached_dev[b] and pos_dev[b] for b < batch (device kernel). */
+c2kv_status c2kv_seq_advance(int32_t batch, int32_t* n_cached_dev, int32_t* pos_dev,
+                             int32_t delta, void* stream);
+
+/*
+ * Attention over one extraction sequence under a mask (the "mask mode").
+ * [EXPL] "structured information flow": n_doc document tokens followed by
+ * n_slot slot tokens.  C2KV_MASK_STRUCTURED: document tokens keep the
+ * causal mask and see no slot; slot i sees the sink block B(0) (document
+ * tokens [0, k)), its own block [i*k, min((i+1)k, n_doc)) and slots 0..i.
+ * [EXPL] "positions at concatenation": documents sit at 0..n_doc-1 and slot
+ * i at min((i+1)k, n_doc) - 1.  C2KV_MASK_CAUSAL: plain causal attention,
+ * token t at position t (n_slot must be 0).
+ * q: device [N][n_q_heads][head_dim], kk, v: device [N][n_kv_heads][head_dim]
+ * with N = n_doc + n_slot, all before RoPE; out: device [N][n_q_heads][d].
+ * workspace: c2kv_attend_workspace_size(geom, 1, N, N) + c2kv_masked_extra_bytes
+ * (geom, N) bytes (rotated keys and values are staged there), zeroed once.
+ */
+c2kv_status c2kv_attend_masked(const c2kv_geometry* geom, int32_t mask,
+                               int32_t n_doc, int32_t n_slot, int32_t k,
+                               const void* q, const void* kk, const void* v,
+                               void* out, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/* Extra scratch bytes c2kv_attend_masked needs beyond the attention scratch. */
+size_t c2kv_masked_extra_bytes(const c2kv_geometry* geom, int32_t n_tokens);
+
+/*
+ * Reads and clears the device error word of the current device (waits for
+ * the device).  *code receives C2KV_OK, C2KV_ETIMEOUT or C2KV_EDEVICE; the
+ * return value is C2KV_ECUDA only if the read itself failed.
+ */
+c2kv_status c2kv_device_error(int32_t* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* C2KV_H_ */

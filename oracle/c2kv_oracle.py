@@ -205,6 +205,12 @@ def masked_softmax_attention(q: np.ndarray, K: np.ndarray, V: np.ndarray,
     return p @ V
 
 
+def rotate_keys_bf16(k_pre: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
+    """Rotate new keys k_pre bits [t][Hkv][d] at positions pos[t] and round
+    them to bf16 as they are stored in the cache: returns bits [Hkv][t][d]."""
+    return f64_to_bf16(rope_rotate(bf16_to_f64(k_pre).transpose(1, 0, 2), pos, theta))
+
+
 def attend_new_tokens(q_pre: np.ndarray, k_new_pre: np.ndarray, v_new: np.ndarray,
                       k_cache: np.ndarray, v_cache: np.ndarray,
                       start_pos: int, theta: float):
@@ -225,7 +231,7 @@ def attend_new_tokens(q_pre: np.ndarray, k_new_pre: np.ndarray, v_new: np.ndarra
     n = k_cache.shape[1]
     pos = start_pos + np.arange(t, dtype=np.int64)
     q = rope_rotate(bf16_to_f64(q_pre).transpose(1, 0, 2), pos, theta)   # [Hq][t][d]
-    k_new_rot = f64_to_bf16(rope_rotate(bf16_to_f64(k_new_pre).transpose(1, 0, 2), pos, theta))
+    k_new_rot = rotate_keys_bf16(k_new_pre, pos, theta)
     K = np.concatenate([bf16_to_f64(k_cache), bf16_to_f64(k_new_rot)], axis=1)
     V = np.concatenate([bf16_to_f64(v_cache), bf16_to_f64(v_new).transpose(1, 0, 2)], axis=1)
     mask = np.arange(n + t)[None, :] < (n + 1 + np.arange(t))[:, None]

@@ -1,0 +1,113 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+symbol include/c2kv.h declares, and its host-side logic (planner, argument
+checks, scratch sizing) behaves; no compute call is made."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.c2kv_oracle as O
+from compressed_composable_kv_gb300 import build
+from compressed_composable_kv_gb300 import synth as S
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def P():
+    build.build_library()
+    import compressed_composable_kv_gb300 as pkg
+    pkg.load_library()
+    return pkg
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "c2kv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return sorted(set(re.findall(r"\b(c2kv_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["c2kv_store_create", "c2kv_store_segments", "c2kv_compose", "c2kv_attend_prefill",
+              "c2kv_attend_decode", "c2kv_attend_masked", "c2kv_last_error"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(P):
+    lib = ctypes.CDLL(build.LIB)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert P.c2kv_version().startswith("c2kv-gb300")
+
+
+def test_binding_covers_every_declared_symbol(P):
+    import compressed_composable_kv_gb300.binding as bnd
+    for n in declared_functions():
+        assert n in bnd._SIGNATURES, n
+
+
+def test_plan_matches_oracle_positions(P):
+    rng = np.random.default_rng(1)
+    for _ in range(50):
+        k = int(rng.choice([1, 4, 16]))
+        n = int(rng.integers(1, 9))
+        lens = [int(x) for x in rng.integers(1, 300, n)]
+        slots = [O.slot_count(x, k) for x in lens]
+        order = None if rng.random() < 0.3 else [int(x) for x in rng.permutation(n)]
+        ss, po, total, l_tot = P.c2kv_plan(lens, slots, order)
+        seq = O.composed_order(list(range(n)), order)
+        pos, lt = O.composed_positions([lens[i] for i in seq], [slots[i] for i in seq], k)
+        assert total == len(pos) and l_tot == lt
+        for c, d in enumerate(seq):
+            first = pos[ss[c]]
+            assert first == O.extraction_slot_position(0, lens[d], k) + po[c]
+            assert pos[ss[c] + slots[d] - 1] == po[c] + lens[d] - 1
+
+
+@pytest.mark.parametrize("lens,slots,order", [
+    ([4, 4], [1, 1], [0, 0]),        # not a permutation
+    ([4, 4], [1, 1], [0, 2]),        # index out of range
+    ([4, 0], [1, 1], None),          # empty document
+    ([4, 4], [5, 1], None),          # more slots than tokens
+    ([2**30, 2**30], [1, 1], None),  # position overflow
+])
+def test_plan_rejects_bad_input(P, lens, slots, order):
+    with pytest.raises(P.C2KVError) as e:
+        P.c2kv_plan(lens, slots, order)
+    assert e.value.status == P.C2KV_EINVAL
+    assert P.c2kv_last_error()
+
+
+def test_plan_empty(P):
+    assert P.c2kv_plan([], [], None) == ([], [], 0, 0)
+
+
+def test_workspace_sizing(P):
+    g = S.LLAMA31_8B
+    assert P.c2kv_attend_workspace_size(g, 1, 1, 8257) > 0
+    assert P.c2kv_attend_workspace_size(g, 0, 1, 100) == 0
+    bad = S.Geometry(32, 32, 8, 96, 5e5)
+    assert P.c2kv_attend_workspace_size(bad, 1, 1, 100) == 0
+    # more keys never needs fewer bytes
+    sizes = [P.c2kv_attend_workspace_size(g, 4, 1, n) for n in (33, 1000, 8000, 33000)]
+    assert sizes == sorted(sizes)
+    assert P.c2kv_masked_extra_bytes(S.TINY, 15) >= 2 * 2 * 15 * 64 * 2
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU failure path")
+def test_store_create_fails_cleanly_without_gpu(P):
+    with pytest.raises(P.C2KVError) as e:
+        P.c2kv_store_create(S.TINY, 1 << 20)
+    assert e.value.status in (P.C2KV_ECUDA, P.C2KV_ENOMEM)
+
+
+def test_geometry_validation(P):
+    for g in [S.Geometry(1, 6, 4, 64, 1e4), S.Geometry(1, 4, 2, 80, 1e4), S.Geometry(1, 4, 2, 64, 0.5)]:
+        with pytest.raises(P.C2KVError) as e:
+            P.c2kv_store_create(g, 0)
+        assert e.value.status == P.C2KV_EINVAL

@@ -1,0 +1,319 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bars: positions and composition order bit-exact, values bit-exact, re-rotated
+keys within 1 bf16 ulp, attention outputs within max-abs 2e-2 / mean-abs
+2e-3 (and mean error under 2 % of the output RMS).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle.c2kv_oracle as O
+import compressed_composable_kv_gb300 as P
+from compressed_composable_kv_gb300 import synth as S
+from gpu_util import Scenario, check_attention, check_keys, to_bits, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def upload(inputs: S.StepInputs):
+    return {name: to_dev(getattr(inputs, name)) for name in
+            ("q_pre", "kq_pre", "vq", "qd_pre", "kd_pre", "vd")}
+
+
+def run_all(sc: Scenario, dev):
+    """Compose, prefill every layer, decode every step (the bench's launch
+    configuration, without graphs).  Returns the output tensors."""
+    bt = sc.batch
+    L = sc.geom.n_layers
+    bt.compose()
+    pre = []
+    if bt.q_len:
+        for l in range(L):
+            out = torch.empty_like(dev["q_pre"][l])
+            bt.prefill(l, dev["q_pre"][l], dev["kq_pre"][l], dev["vq"][l], out)
+            pre.append(out)
+    bt.reset_decode()
+    dec = []
+    for t in range(bt.decode_steps):
+        row = []
+        for l in range(L):
+            out = torch.empty_like(dev["qd_pre"][t, l])
+            bt.decode(l, dev["qd_pre"][t, l], dev["kd_pre"][t, l], dev["vd"][t, l], out)
+            row.append(out)
+        bt.advance()
+        dec.append(row)
+    torch.cuda.synchronize()
+    assert P.c2kv_device_error() == P.C2KV_OK
+    return pre, dec
+
+
+def check_request(sc: Scenario, inputs: S.StepInputs, pre, dec, b: int, layers, steps):
+    bt = sc.batch
+    g = sc.geom
+    req = sc.reqs[b]
+    st = sc.oracle_store()
+    N, lt, Q = bt.n_slots[b], bt.l_tot[b], bt.q_len
+    seq = O.composed_order(req.doc_ids, req.order)
+    pos_ref, lt_ref = O.composed_positions([sc.docs[d].n_tokens for d in seq],
+                                           [sc.docs[d].n_slots for d in seq], sc.k)
+    assert lt_ref == lt
+    assert np.array_equal(bt.pos[b][:N].cpu().numpy(), pos_ref)
+    kc = bt.k_caches[b]
+    vc = bt.v_caches[b]
+    for l in layers:
+        _, _, kref, vref = O.compose(st, req.doc_ids, req.order, sc.k, g.rope_theta, layers=[l])
+        kg = to_bits(kc[l, :, :N])
+        vg = to_bits(vc[l, :, :N])
+        assert np.array_equal(vg, vref[0]), f"V rows differ (layer {l})"
+        check_keys(kg, kref[0], f"composed K layer {l}")
+        kcache, vcache = kref[0], vref[0]
+        if Q:
+            o_ref, kq_rot = O.attend_new_tokens(inputs.q_pre[l, b], inputs.kq_pre[l, b], inputs.vq[l, b],
+                                                kcache, vcache, lt, g.rope_theta)
+            check_attention(pre[l][b], o_ref, f"prefill layer {l} seq {b}")
+            check_keys(to_bits(kc[l, :, N:N + Q]), kq_rot, f"question keys layer {l}")
+            assert np.array_equal(to_bits(vc[l, :, N:N + Q]), inputs.vq[l, b].transpose(1, 0, 2))
+            kcache = np.concatenate([kcache, kq_rot], axis=1)
+            vcache = np.concatenate([vcache, inputs.vq[l, b].transpose(1, 0, 2)], axis=1)
+        for t in steps:
+            if t > 0:
+                prev_pos = lt + Q + np.arange(t)
+                kd = O.rotate_keys_bf16(inputs.kd_pre[:t, l, b], prev_pos, g.rope_theta)
+                kc_t = np.concatenate([kcache, kd], axis=1)
+                vc_t = np.concatenate([vcache, inputs.vd[:t, l, b].transpose(1, 0, 2)], axis=1)
+            else:
+                kc_t, vc_t = kcache, vcache
+            o_ref, kn = O.attend_new_tokens(inputs.qd_pre[t:t + 1, l, b], inputs.kd_pre[t:t + 1, l, b],
+                                            inputs.vd[t:t + 1, l, b], kc_t, vc_t, lt + Q + t, g.rope_theta)
+            check_attention(dec[t][l][b], o_ref[0], f"decode layer {l} step {t} seq {b}")
+            row = N + Q + t
+            check_keys(to_bits(kc[l, :, row:row + 1]), kn, f"decode key layer {l} step {t}")
+
+
+def test_tiny_end_to_end():
+    w = S.WORKLOADS["tiny"]
+    docs, reqs = S.make_requests(w)
+    sc = Scenario(w.geom, w.k, [(i, n, s) for i, (n, s) in docs.items()],
+                  [(r.doc_ids, r.order) for r in reqs], w.q_len, w.decode_steps, seed=w.seed)
+    inputs = S.make_step_inputs(w)
+    pre, dec = run_all(sc, upload(inputs))
+    assert sc.batch.n_slots == [113] and sc.batch.l_tot == [452]
+    check_request(sc, inputs, pre, dec, 0, layers=[0], steps=range(w.decode_steps))
+    sc.close()
+
+
+def test_tiny_sharp_softmax():
+    """q scaled by 4: a few keys dominate, so errors are not hidden by a flat softmax."""
+    w = S.WORKLOADS["tiny"]
+    docs, reqs = S.make_requests(w)
+    sc = Scenario(w.geom, w.k, [(i, n, s) for i, (n, s) in docs.items()],
+                  [([2, 0, 1], None)], w.q_len, 4, seed=w.seed)
+    inputs = S.make_step_inputs(w, decode_steps=4, q_scale=4.0)
+    pre, dec = run_all(sc, upload(inputs))
+    check_request(sc, inputs, pre, dec, 0, layers=[0], steps=range(4))
+    sc.close()
+
+
+def test_compose_orders_repeats_and_ragged_docs():
+    """Partial last blocks, a one-slot document, repeated ids, permutations,
+    cap equal to N (no tail), rows past N untouched."""
+    g = S.Geometry(2, 8, 2, 128, 5.0e5)
+    specs = [(7, 3, 1), (8, 10, 3), (9, 401, 101), (10, 64, 16), (11, 33, 9)]
+    requests = [([9, 7, 8, 9], [3, 1, 0, 2]), ([10, 11, 7], None), ([8], None)]
+    sc = Scenario(g, 4, specs, requests, q_len=0, decode_steps=0)
+    bt = sc.batch
+    for b in range(len(requests)):
+        bt.k_caches[b].fill_(7.0)
+        bt.v_caches[b].fill_(7.0)
+    bt.compose()
+    torch.cuda.synchronize()
+    st = sc.oracle_store()
+    for b, (ids, order) in enumerate(requests):
+        N = bt.n_slots[b]
+        _, _, kref, vref = O.compose(st, ids, order, 4, g.rope_theta)
+        pos_ref, lt = O.composed_positions([sc.docs[d].n_tokens for d in O.composed_order(ids, order)],
+                                           [sc.docs[d].n_slots for d in O.composed_order(ids, order)], 4)
+        assert np.array_equal(bt.pos[b][:N].cpu().numpy(), pos_ref)
+        assert np.array_equal(to_bits(bt.v_caches[b][:, :, :N]), vref)
+        check_keys(to_bits(bt.k_caches[b][:, :, :N]), kref, f"request {b}")
+        assert torch.all(bt.k_caches[b][:, :, N:] == 7.0) and torch.all(bt.v_caches[b][:, :, N:] == 7.0)
+    # cap exactly N: a direct compose into a tight buffer
+    N = bt.n_slots[0]
+    kt = torch.empty((2, 2, N, 128), dtype=torch.bfloat16, device="cuda")
+    vt = torch.empty_like(kt)
+    n, nxt = P.c2kv_compose(sc.store, *requests[0], 4, kt, vt, N)
+    torch.cuda.synchronize()
+    assert n == N
+    assert torch.equal(kt, bt.k_caches[0][:, :, :N]) and torch.equal(vt, bt.v_caches[0][:, :, :N])
+    sc.close()
+
+
+def test_k1_composition_equals_uncompressed():
+    """k=1 keeps every token: the composed cache and the attention over it must
+    equal the plain RoPE cache of the concatenated documents."""
+    g = S.Geometry(1, 8, 2, 128, 5.0e5)
+    lens = [300, 17, 512, 45]
+    sc = Scenario(g, 1, [(i, n, n) for i, n in enumerate(lens)], [([0, 1, 2, 3], [2, 0, 3, 1])],
+                  q_len=8, decode_steps=3)
+    w = S.Workload("k1", g, 1, 1, 8, 3, doc_tokens=tuple(lens))
+    inputs = S.make_step_inputs(w)
+    pre, dec = run_all(sc, upload(inputs))
+    bt = sc.batch
+    assert bt.pos[0][:sum(lens)].cpu().numpy().tolist() == list(range(sum(lens)))
+    check_request(sc, inputs, pre, dec, 0, layers=[0], steps=range(3))
+    sc.close()
+
+
+def test_varlen_batch_pool():
+    """Batch of 16 requests drawn from a document pool in random order
+    (lengths 500..4000 tokens, one not a multiple of k), 2 layers."""
+    g = S.Geometry(2, 32, 8, 128, 5.0e5)
+    rng = np.random.default_rng(0xC2C2)
+    lens = [int(x) for x in rng.choice(np.arange(500, 4001, 4), 40)]
+    lens[5] = 1003
+    specs = [(i, n, -(-n // 4)) for i, n in enumerate(lens)]
+    requests = []
+    for _ in range(16):
+        ids = [int(x) for x in rng.choice(40, 8, replace=False)]
+        requests.append((ids, [int(x) for x in rng.permutation(8)]))
+    sc = Scenario(g, 4, specs, requests, q_len=32, decode_steps=4)
+    w = S.Workload("pool", g, 4, 16, 32, 4, seed=0xC2C2)
+    inputs = S.make_step_inputs(w)
+    pre, dec = run_all(sc, upload(inputs))
+    for b in (0, 5, 15):
+        check_request(sc, inputs, pre, dec, b, layers=[1], steps=[0, 3])
+    sc.close()
+
+
+def test_qwen_group5_k16():
+    """Qwen3-14B attention geometry (G=5, theta 1e6) at k=16: 16 x 8000-token
+    documents -> 8000 slots, 2 layers, batch 2, 128-token question."""
+    g = S.Geometry(2, 40, 8, 128, 1.0e6)
+    specs = [(i, 8000, 500) for i in range(16)]
+    rng = np.random.default_rng(4)
+    requests = [(list(range(16)), None), (list(range(16)), [int(x) for x in rng.permutation(16)])]
+    sc = Scenario(g, 16, specs, requests, q_len=128, decode_steps=2)
+    w = S.Workload("qwen", g, 16, 2, 128, 2, seed=0xC2C4)
+    inputs = S.make_step_inputs(w)
+    pre, dec = run_all(sc, upload(inputs))
+    check_request(sc, inputs, pre, dec, 1, layers=[0], steps=[0, 1])
+    sc.close()
+
+
+def test_llama_8x4000_full_size():
+    """The benchmark workload at full size (32 layers, 8000 slots, 64-token
+    question, 128 decode steps), checked on sampled layers and steps."""
+    w = S.WORKLOADS["llama8b_8x4000_k4"]
+    docs, reqs = S.make_requests(w)
+    sc = Scenario(w.geom, w.k, [(i, n, s) for i, (n, s) in docs.items()],
+                  [(r.doc_ids, r.order) for r in reqs], w.q_len, w.decode_steps, seed=w.seed)
+    inputs = S.make_step_inputs(w)
+    pre, dec = run_all(sc, upload(inputs))
+    bt = sc.batch
+    N = bt.n_slots[0]
+    assert N == 8000 and bt.l_tot[0] == 32000
+    # V rows of every layer are the stored segments back to back
+    seq = O.composed_order(sc.reqs[0].doc_ids, sc.reqs[0].order)
+    vcat = np.concatenate([sc.docs[d].v for d in seq], axis=2)
+    assert np.array_equal(to_bits(bt.v_caches[0][:, :, :N]), vcat)
+    check_request(sc, inputs, pre, dec, 0, layers=[0, 31], steps=[0, 1, 127])
+    sc.close()
+
+
+def test_decode_multi_split_long_cache():
+    """One long sequence (32768 slots as in the 128k-token workload, 1 layer):
+    many key splits merged by the last-arriving CTA."""
+    g = S.Geometry(1, 32, 8, 128, 5.0e5)
+    specs = [(i, 4096, 1024) for i in range(32)]
+    sc = Scenario(g, 4, specs, [(list(range(32)), None)], q_len=0, decode_steps=3)
+    w = S.Workload("long", g, 4, 1, 0, 3, seed=0xC2C3)
+    inputs = S.make_step_inputs(w)
+    pre, dec = run_all(sc, upload(inputs))
+    check_request(sc, inputs, pre, dec, 0, layers=[0], steps=[0, 2])
+    sc.close()
+
+
+@pytest.mark.parametrize("n_doc,n_slot,k", [(12, 3, 4), (200, 50, 4), (257, 17, 16), (40, 40, 1)])
+def test_structured_mask_mode(n_doc, n_slot, k):
+    g = S.TINY
+    rng = np.random.default_rng(n_doc * 131 + n_slot)
+    N = n_doc + n_slot
+    q = S.normal_bf16(rng, (N, g.n_q_heads, g.head_dim))
+    kk = S.normal_bf16(rng, (N, g.n_kv_heads, g.head_dim))
+    v = S.normal_bf16(rng, (N, g.n_kv_heads, g.head_dim))
+    ws = torch.zeros(P.masked_workspace_bytes(g, N), dtype=torch.uint8, device="cuda")
+    out = torch.empty((N, g.n_q_heads, g.head_dim), dtype=torch.bfloat16, device="cuda")
+    P.c2kv_attend_masked(g, P.C2KV_MASK_STRUCTURED, n_doc, n_slot, k, to_dev(q), to_dev(kk), to_dev(v), out, ws)
+    torch.cuda.synchronize()
+    ref = O.masked_extraction_attention(q, kk, v, n_doc, n_slot, k, g.rope_theta)
+    check_attention(out, ref, f"structured mask {n_doc}+{n_slot} k={k}")
+
+
+def test_causal_mask_mode_llama_heads():
+    g = S.Geometry(1, 32, 8, 128, 5.0e5)
+    N = 300
+    rng = np.random.default_rng(3)
+    q = S.normal_bf16(rng, (N, 32, 128))
+    kk = S.normal_bf16(rng, (N, 8, 128))
+    v = S.normal_bf16(rng, (N, 8, 128))
+    ws = torch.zeros(P.masked_workspace_bytes(g, N), dtype=torch.uint8, device="cuda")
+    out = torch.empty((N, 32, 128), dtype=torch.bfloat16, device="cuda")
+    P.c2kv_attend_masked(g, P.C2KV_MASK_CAUSAL, N, 0, 1, to_dev(q), to_dev(kk), to_dev(v), out, ws)
+    torch.cuda.synchronize()
+    ref = O.masked_extraction_attention(q, kk, v, N, 0, 1, g.rope_theta)
+    check_attention(out, ref, "causal mask mode")
+
+
+def test_host_side_errors():
+    g = S.Geometry(1, 8, 2, 128, 5.0e5)
+    sc = Scenario(g, 4, [(1, 40, 10), (2, 8, 2)], [([1, 2], None)], q_len=4, decode_steps=2)
+    kc = torch.empty((1, 2, 16, 128), dtype=torch.bfloat16, device="cuda")
+    vc = torch.empty_like(kc)
+    with pytest.raises(P.C2KVError) as e:
+        P.c2kv_compose(sc.store, [1, 2], None, 4, kc, vc, 11)
+    assert e.value.status == P.C2KV_ECAPACITY
+    with pytest.raises(P.C2KVError) as e:
+        P.c2kv_compose(sc.store, [1, 99], None, 4, kc, vc, 16)
+    assert e.value.status == P.C2KV_ENOTFOUND
+    with pytest.raises(P.C2KVError) as e:
+        P.c2kv_compose(sc.store, [1, 2], None, 8, kc, vc, 16)
+    assert e.value.status == P.C2KV_EINVAL
+    with pytest.raises(P.C2KVError) as e:
+        P.c2kv_compose(sc.store, [1, 2], [1, 1], 4, kc, vc, 16)
+    assert e.value.status == P.C2KV_EINVAL
+    with pytest.raises(P.C2KVError) as e:
+        P.c2kv_store_segments(sc.store, [1], [40], [10], 4, [sc.docs[1].k_pre], [sc.docs[1].v])
+    assert e.value.status == P.C2KV_EINVAL
+    bt = sc.batch
+    q = torch.zeros((1, 5, 8, 128), dtype=torch.bfloat16, device="cuda")
+    kn = torch.zeros((1, 5, 2, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(P.C2KVError) as e:
+        P.c2kv_attend_prefill(g, 0, bt.k_caches, bt.v_caches, bt.cap, [bt.cap - 2], [0], q, kn, kn,
+                              torch.empty_like(q), bt.workspace)
+    assert e.value.status == P.C2KV_ECAPACITY
+    with pytest.raises(P.C2KVError) as e:
+        P.c2kv_attend_prefill(g, 1, bt.k_caches, bt.v_caches, bt.cap, [0], [0], q, kn, kn,
+                              torch.empty_like(q), bt.workspace)
+    assert e.value.status == P.C2KV_EINVAL
+    sc.close()
+
+
+def test_device_length_beyond_capacity_is_reported():
+    """A device-side length past the cache capacity is caught by the kernels:
+    the output is skipped and c2kv_device_error reports C2KV_EDEVICE."""
+    g = S.Geometry(1, 8, 2, 128, 5.0e5)
+    sc = Scenario(g, 4, [(1, 40, 10)], [([1], None)], q_len=0, decode_steps=2)
+    bt = sc.batch
+    bt.compose()
+    bt.reset_decode()
+    bt.n_cached_dev.fill_(bt.cap)   # no room for the new token
+    q = torch.ones((1, 8, 128), dtype=torch.bfloat16, device="cuda")
+    kn = torch.ones((1, 2, 128), dtype=torch.bfloat16, device="cuda")
+    out = torch.full_like(q, 3.0)
+    bt.decode(0, q, kn, kn, out)
+    torch.cuda.synchronize()
+    assert P.c2kv_device_error() == P.C2KV_EDEVICE
+    assert torch.all(out == 3.0)
+    assert P.c2kv_device_error() == P.C2KV_OK   # reading clears the word
+    sc.close()
