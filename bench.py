@@ -1,0 +1,482 @@
+"""Benchmark of the C2KV composed-cache hot path on one GB300 (or N replicas).
+
+One step = one full request of the workload: compose the documents'
+compressed pre-RoPE segments from the pinned host store into HBM (host->
+device copies + re-rotation), prefill the question on every layer, then
+decode every answer token on every layer.  Headline value: answer tokens
+per second over the whole request.  Prefill and decode are replayed from
+CUDA graphs captured once (the graphs hold only this library's kernels).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W]
+                       [--impl ours|reference] [--workload NAME]
+Under torchrun (N > 1) every rank serves its own replica of the workload;
+value = all ranks' tokens / max-over-ranks time ("weak" scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "composed-cache decode tok/s + attention HBM GB/s vs peak; compose+TTFT ms"
+DEFAULT_WORKLOAD = "llama8b_8x4000_k4"
+
+
+# ------------------------------------------------------------------ oracle leg
+
+def _oracle_sample(workload: str, budget_s: float, out_q) -> None:
+    """Runs in a spawned single-threaded process: times the CPU oracle on one
+    layer of compose + prefill and one decode step, repeated until budget_s,
+    and extrapolates to a full request."""
+    import numpy as np
+    import oracle.c2kv_oracle as O
+    from compressed_composable_kv_gb300 import synth as S
+
+    w = S.WORKLOADS[workload]
+    g = w.geom
+    docs_meta, reqs = S.make_requests(w)
+    req = reqs[0]
+    st = {}
+    for i in set(req.doc_ids):
+        n, s = docs_meta[i]
+        d = S.make_document(g, i, n, w.k, w.seed, n_slots=s, layers=1)
+        st[i] = (n, s, d.k_pre, d.v)
+    inp = S.make_step_inputs(w, layers=1, decode_steps=1)
+    t_comp, t_pre, t_dec, reps = [], [], [], 0
+    t_start = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        pos, lt, kr, vr = O.compose(st, req.doc_ids, req.order, w.k, g.rope_theta)
+        t1 = time.perf_counter()
+        kc, vc = kr[0], vr[0]
+        if w.q_len:
+            _, kq = O.attend_new_tokens(inp.q_pre[0, 0], inp.kq_pre[0, 0], inp.vq[0, 0], kc, vc, lt,
+                                        g.rope_theta)
+            kc = np.concatenate([kc, kq], axis=1)
+            vc = np.concatenate([vc, inp.vq[0, 0].transpose(1, 0, 2)], axis=1)
+        t2 = time.perf_counter()
+        O.attend_new_tokens(inp.qd_pre[0:1, 0, 0], inp.kd_pre[0:1, 0, 0], inp.vd[0:1, 0, 0], kc, vc,
+                            lt + w.q_len, g.rope_theta)
+        t3 = time.perf_counter()
+        t_comp.append(t1 - t0)
+        t_pre.append(t2 - t1)
+        t_dec.append(t3 - t2)
+        reps += 1
+        if time.perf_counter() - t_start >= budget_s:
+            break
+    L, T, B = g.n_layers, w.decode_steps, w.batch
+    per_req = L * (statistics.median(t_comp) + statistics.median(t_pre)) + L * T * statistics.median(t_dec)
+    out_q.put({
+        "request_s": per_req * B,   # B requests, one after the other on one core
+        "tok_s": B * T / (per_req * B),
+        "reps": reps,
+        "wall_s": time.perf_counter() - t_start,
+        "sample": (f"request 0 of {workload}: 1 layer compose ({len(pos)} slots) + 1 layer question "
+                   f"prefill ({w.q_len} tokens) + 1 decode step, x{reps}; extrapolated to "
+                   f"{L} layers x {T} decode steps x {B} requests"),
+    })
+
+
+def run_oracle_sample(workload: str, budget_s: float) -> dict:
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k in saved:
+        os.environ[k] = "1"
+    try:
+        q = ctx.Queue()
+        p = ctx.Process(target=_oracle_sample, args=(workload, budget_s, q))
+        p.start()
+        res = q.get(timeout=budget_s * 10 + 120)
+        p.join()
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    res["cores"] = 1
+    res["kind"] = "oracle"
+    return res
+
+
+# ------------------------------------------------------------------ helpers
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+def profiled_traffic(kernel: str):
+    """dram bytes per key-row of `kernel` from the committed ncu summary, if the
+    kernel source is unchanged since the capture (sha256 of its .cu file)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    for ln in lines:
+        if ln.startswith("#") or not ln.strip():
+            continue
+        name, src, sha, per_unit = ln.split()[:4]
+        if name != kernel:
+            continue
+        cur = hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest()[:16]
+        return float(per_unit) if cur == sha else None
+    return None
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank: int, world: int) -> dict:
+    import numpy as np
+    import torch
+    import compressed_composable_kv_gb300 as P
+    from compressed_composable_kv_gb300 import synth as S
+
+    w = S.WORKLOADS[args.workload]
+    g = w.geom
+    L, Bn, Q, T = g.n_layers, w.batch, w.q_len, w.decode_steps
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    dev = torch.device("cuda")
+
+    # -------- setup (untimed): pinned store, caches, inputs, graphs
+    docs_meta, reqs = S.make_requests(w)
+    used = sorted({d for r in reqs for d in r.doc_ids})
+    docs = {i: S.make_document(g, i, docs_meta[i][0], w.k, w.seed, n_slots=docs_meta[i][1]) for i in used}
+    pool = sum(2 * d.k_pre.nbytes + 512 for d in docs.values()) + (1 << 20)
+    store = P.c2kv_store_create(g, pool)
+    P.c2kv_store_segments(store, used, [docs[i].n_tokens for i in used], [docs[i].n_slots for i in used],
+                          w.k, [docs[i].k_pre for i in used], [docs[i].v for i in used])
+    compose_bytes = sum(2 * docs[d].k_pre.nbytes for r in reqs for d in r.doc_ids)
+    del docs
+    bt = P.RequestBatch(store, g, [P.RequestSpec(r.doc_ids, r.order) for r in reqs], w.k, Q, T)
+    inp = S.make_step_inputs(w)
+    names = ["q_pre", "kq_pre", "vq", "qd_pre", "kd_pre", "vd"]
+    host = {}
+    dev_in = {}
+    for n in names:
+        a = getattr(inp, n)
+        if a.size == 0:
+            continue
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+        host[n] = t.pin_memory()
+        dev_in[n] = host[n].to(dev)
+    h2d_bytes = sum(t.numel() * 2 for t in host.values())
+    pre_out = torch.empty((L, Bn, Q, g.n_q_heads, g.head_dim), dtype=torch.bfloat16, device=dev) if Q else None
+    dec_out = torch.empty((T, L, Bn, g.n_q_heads, g.head_dim), dtype=torch.bfloat16, device=dev)
+    res_host = torch.empty((T, Bn, g.n_q_heads, g.head_dim), dtype=torch.bfloat16).pin_memory()
+    d2h_bytes = res_host.numel() * 2
+
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def prefill_all():
+        for l in range(L):
+            bt.prefill(l, dev_in["q_pre"][l], dev_in["kq_pre"][l], dev_in["vq"][l], pre_out[l], stream)
+
+    def decode_all():
+        for t in range(T):
+            for l in range(L):
+                bt.decode(l, dev_in["qd_pre"][t, l], dev_in["kd_pre"][t, l], dev_in["vd"][t, l],
+                          dec_out[t, l], stream)
+            bt.advance(stream)
+
+    # Warm the launch paths eagerly once (sets kernel attributes), then capture.
+    with torch.cuda.stream(stream):
+        bt.compose(stream)
+        if Q:
+            prefill_all()
+        bt.reset_decode(stream)
+        decode_all()
+    torch.cuda.synchronize()
+    g_pre = torch.cuda.CUDAGraph() if Q else None
+    g_dec = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        if Q:
+            with torch.cuda.graph(g_pre, stream=stream):
+                prefill_all()
+        with torch.cuda.graph(g_dec, stream=stream):
+            decode_all()
+    torch.cuda.synchronize()
+    assert P.c2kv_device_error() == P.C2KV_OK
+    launches_per_step = (bt.batch * min(L, 4) + (2 * L if Q else 0) + T * (2 * L + 1))
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+
+    def step(e=None, with_host=False):
+        with torch.cuda.stream(stream):
+            if with_host:
+                for n in dev_in:
+                    dev_in[n].copy_(host[n], non_blocking=True)
+            if e:
+                e[0].record(stream)
+            bt.compose(stream)
+            bt.reset_decode(stream)
+            if e:
+                e[1].record(stream)
+            if Q:
+                g_pre.replay()
+            if e:
+                e[2].record(stream)
+            g_dec.replay()
+            if e:
+                e[3].record(stream)
+            if with_host:
+                res_host.copy_(dec_out[:, L - 1], non_blocking=True)
+
+    # pinned host->device copy bandwidth (denominator of the compose copies)
+    big = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+    big_d = torch.empty_like(big, device=dev)
+    best = 1e9
+    for _ in range(5):
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        with torch.cuda.stream(stream):
+            big_d.copy_(big, non_blocking=True)
+        b_.record(stream)
+        b_.synchronize()
+        best = min(best, a.elapsed_time(b_) / 1e3)
+    pinned_gbs = big.numel() / best / 1e9
+    del big, big_d
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    t_beg, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gpu_idx = torch.cuda.current_device()
+    with ClockSampler(gpu_idx) as clk:
+        t_beg.record(stream)
+        for i in range(args.steps):
+            step(ev[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    elapsed = t_beg.elapsed_time(t_end) / 1e3
+    err = P.c2kv_device_error()
+    assert err == P.C2KV_OK, f"device error {err}"
+    comp = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+    pre = statistics.mean(e[1].elapsed_time(e[2]) for e in ev) / 1e3
+    dec = statistics.mean(e[2].elapsed_time(e[3]) for e in ev) / 1e3
+
+    # e2e: the same step with inputs copied from pinned host memory and the
+    # answer read back, all inside the timed region
+    step(with_host=True)
+    torch.cuda.synchronize()
+    barrier()
+    e_beg, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_beg.record(stream)
+    for i in range(args.steps):
+        step(with_host=True)
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_elapsed = e_beg.elapsed_time(e_end) / 1e3
+
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([elapsed, e2e_elapsed], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed, e2e_elapsed = float(tt[0]), float(tt[1])
+
+    toks = Bn * T * args.steps * world
+    # algorithmic decode bytes: every key row (K and V) of every sequence,
+    # layer and step, plus q/out/new k,v rows
+    keys = sum((n + Q + t + 1) for n in bt.n_slots for t in range(T))
+    row = g.n_kv_heads * g.head_dim * 2 * 2
+    small = Bn * (2 * g.n_q_heads + 2 * g.n_kv_heads) * g.head_dim * 2
+    dec_bytes_layer = keys * row + T * small
+    dec_launches = T * L
+    bytes_per_launch = dec_bytes_layer / T
+    avg_launch_s = dec / dec_launches
+    achieved = bytes_per_launch / avg_launch_s / 1e9
+    peaks = measured_peaks()
+    hbm_peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if hbm_peak else "fallback"
+    hbm_peak = hbm_peak or 6800.0
+    per_key = profiled_traffic("attn_kernel")
+    traffic = None if per_key is None else per_key * (keys / T)
+    clocks = clk.summary()
+    ttft = comp + pre + dec / T
+    out = {
+        "metric": METRIC,
+        "value": toks / elapsed,
+        "unit": "tok/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": elapsed / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": w.name,
+            "geometry": f"{L} layers, {g.n_q_heads} q / {g.n_kv_heads} kv heads, head_dim {g.head_dim}, "
+                        f"rope_theta {g.rope_theta:g}",
+            "k": w.k, "batch": Bn, "composed_slots": bt.n_slots, "original_tokens": bt.l_tot,
+            "question_tokens": Q, "decode_steps": T,
+            "l2": "inputs larger than L2 (composed cache per request > 1 GB; 129 MB L2)",
+            "graphs": "prefill and decode replayed from CUDA graphs of this library's kernels",
+            "parallelism": f"replicas x{world}",
+            "attention_only": "no projection/MLP weights: attention over the composed cache only",
+        },
+        "compose_ms": comp * 1e3,
+        "prefill_ms": pre * 1e3,
+        "decode_ms": dec * 1e3,
+        "ttft_ms": ttft * 1e3,
+        "decode_only_tok_s": Bn * T / dec,
+        "attention_hbm_gbs": achieved,
+        "h2d": {"compose_bytes": compose_bytes, "achieved_gbs": compose_bytes / comp / 1e9,
+                "pinned_copy_gbs": pinned_gbs, "frac": compose_bytes / comp / 1e9 / pinned_gbs,
+                "note": "compose = host->device copies + re-rotation, wall time on the stream"},
+        "roofline": {"kernel": "attn_kernel (decode)", "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} (hbm_gbs, burst)",
+                     "launch_time": "decode-phase time / attention launches (includes the append "
+                                    "kernel and launch gaps)"},
+        "e2e": {"value": toks / e2e_elapsed, "unit": "tok/s", "h2d_bytes_per_step": h2d_bytes + compose_bytes,
+                "d2h_bytes_per_step": d2h_bytes},
+        "clocks": clocks,
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    torch.cuda.synchronize()
+    P.c2kv_store_destroy(store)
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+
+    if args.impl == "reference":
+        # The reference arm is the CPU oracle; only rank 0 runs it.
+        if rank != 0:
+            return
+        samples = []
+        for i in range(args.warmup + args.steps):
+            r = run_oracle_sample(args.workload, budget_s=0.5)
+            if i >= args.warmup:
+                samples.append(r)
+        tok_s = statistics.mean(s["tok_s"] for s in samples)
+        line = {
+            "impl": "reference", "metric": METRIC, "value": tok_s, "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": statistics.mean(s["request_s"] for s in samples) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.workload},
+            "cpu_baseline": {"value": tok_s, "unit": "tok/s", "cores": 1, "kind": "oracle",
+                             "sample": samples[0]["sample"] + " (one sample per step)"},
+            "e2e": {"value": tok_s, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line))
+        return
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = run_oracle_sample(args.workload, args.cpu_budget)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    out = run_ours(args, rank, world)
+    if cpu is not None:
+        out["cpu_baseline"] = {"value": cpu["tok_s"], "unit": "tok/s", "cores": cpu["cores"],
+                               "kind": "oracle", "sample": cpu["sample"]}
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

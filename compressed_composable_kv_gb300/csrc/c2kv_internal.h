@@ -39,6 +39,59 @@ __device__ __forceinline__ void rope_cos_sin(int pos, double inv_freq, float* c,
   sincosf((float)r, s, c);
 }
 
+// cos/sin of one angle as unevaluated fp32 pairs (hi + lo), from the fp64
+// library sincos of the reduced angle: ~2^-48 accurate, enough to round a
+// rotated key correctly even when x cos - y sin nearly cancels.
+struct CosSin2 {
+  float ch, cl, sh, sl;
+};
+
+__device__ __forceinline__ CosSin2 rope_cos_sin2(int pos, double inv_freq) {
+  const double a = (double)pos * inv_freq;
+  const double n = rint(a * kInvTwoPi);
+  double r = fma(-n, kTwoPiHi, a);
+  r = fma(-n, kTwoPiLo, r);
+  double s, c;
+  sincos(r, &s, &c);
+  CosSin2 t;
+  t.ch = (float)c;
+  t.cl = (float)(c - (double)t.ch);
+  t.sh = (float)s;
+  t.sl = (float)(s - (double)t.sh);
+  return t;
+}
+
+// a*(bh+bl) + c*(dh+dl) for fp32 a, c, as a double-float (hi, lo): exact
+// products by FMA (TwoProduct) and exact TwoSums.  The _rn intrinsics keep
+// the compiler from contracting the error-free steps into FMAs.
+__device__ __forceinline__ void dot2_df(float a, float bh, float bl, float c, float dh, float dl, float& hi,
+                                        float& lo) {
+  const float p1 = __fmul_rn(a, bh);
+  const float e1 = fmaf(a, bh, -p1);
+  const float p2 = __fmul_rn(c, dh);
+  const float e2 = fmaf(c, dh, -p2);
+  const float s = __fadd_rn(p1, p2);
+  const float bb = __fsub_rn(s, p1);
+  const float es = __fadd_rn(__fsub_rn(p1, __fsub_rn(s, bb)), __fsub_rn(p2, bb));
+  const float t = __fadd_rn(__fadd_rn(es, __fadd_rn(e1, e2)), fmaf(a, bl, __fmul_rn(c, dl)));
+  hi = __fadd_rn(s, t);
+  const float b2 = __fsub_rn(hi, s);
+  lo = __fadd_rn(__fsub_rn(s, __fsub_rn(hi, b2)), __fsub_rn(t, b2));
+}
+
+// Rounds the double-float hi + lo to bf16 (nearest, ties to even).  Only an
+// fp32 hi lying exactly on a bf16 midpoint needs lo to break the tie.
+__device__ __forceinline__ uint32_t df_to_bf16_bits(float hi, float lo) {
+  const uint32_t u = __float_as_uint(hi);
+  const uint32_t low = u & 0xFFFFu;
+  const uint32_t r = u >> 16;
+  bool up;
+  if (low != 0x8000u) up = low > 0x8000u;
+  else if (lo == 0.f) up = (r & 1u) != 0;
+  else up = (lo > 0.f) == (hi > 0.f);
+  return r + (up ? 1u : 0u);
+}
+
 // ---------------------------------------------------------------- bf16 helpers
 __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
   f[0] = __uint_as_float(u.x << 16); f[1] = __uint_as_float(u.x & 0xffff0000u);

@@ -13,18 +13,24 @@ namespace c2kv {
 namespace {
 
 // Rotates 8 pairs: a holds elements [8c, 8c+8) of the first half, b the same
-// offsets of the second half.
-__device__ __forceinline__ void rotate8(uint4& a, uint4& b, const float* cs, const float* sn) {
-  float x[8], y[8], xo[8], yo[8];
+// offsets of the second half.  Each output is evaluated in double-float and
+// rounded once to bf16, so it is the correctly rounded rotation of the
+// stored bf16 inputs (to ~2^-44), also when x cos - y sin nearly cancels.
+__device__ __forceinline__ void rotate8(uint4& a, uint4& b, const CosSin2* t) {
+  float x[8], y[8];
   unpack8(a, x);
   unpack8(b, y);
+  uint32_t xo[8], yo[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    xo[e] = x[e] * cs[e] - y[e] * sn[e];
-    yo[e] = y[e] * cs[e] + x[e] * sn[e];
+    float hi, lo;
+    dot2_df(x[e], t[e].ch, t[e].cl, -y[e], t[e].sh, t[e].sl, hi, lo);   // x cos - y sin
+    xo[e] = df_to_bf16_bits(hi, lo);
+    dot2_df(y[e], t[e].ch, t[e].cl, x[e], t[e].sh, t[e].sl, hi, lo);    // y cos + x sin
+    yo[e] = df_to_bf16_bits(hi, lo);
   }
-  a = pack8(xo);
-  b = pack8(yo);
+  a = make_uint4(xo[0] | (xo[1] << 16), xo[2] | (xo[3] << 16), xo[4] | (xo[5] << 16), xo[6] | (xo[7] << 16));
+  b = make_uint4(yo[0] | (yo[1] << 16), yo[2] | (yo[3] << 16), yo[4] | (yo[5] << 16), yo[6] | (yo[7] << 16));
 }
 
 // ---------------------------------------------------------------------------
@@ -41,8 +47,7 @@ template <int D>
 __global__ void __launch_bounds__(kRopeThreads) rerope_kernel(const __grid_constant__ RopeParams p) {
   constexpr int H = D / 2;
   constexpr int TPR = H / 8;   // threads per row, each owns 8 pairs
-  __shared__ float cs[kSlots][H];
-  __shared__ float sn[kSlots][H];
+  __shared__ CosSin2 tab[kSlots][H];
   __shared__ int spos[kSlots];
 
   const int slot0 = blockIdx.x * kSlots;
@@ -66,7 +71,7 @@ __global__ void __launch_bounds__(kRopeThreads) rerope_kernel(const __grid_const
   __syncthreads();
   for (int i = threadIdx.x; i < n_here * H; i += kRopeThreads) {
     const int r = i / H, f = i % H;
-    rope_cos_sin(spos[r], p.inv_freq[f], &cs[r][f], &sn[r][f]);
+    tab[r][f] = rope_cos_sin2(spos[r], p.inv_freq[f]);
   }
   __syncthreads();
 
@@ -98,7 +103,7 @@ __global__ void __launch_bounds__(kRopeThreads) rerope_kernel(const __grid_const
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       if (ok[u]) {
-        rotate8(a[u], b[u], &cs[r_[u]][c_[u] * 8], &sn[r_[u]][c_[u] * 8]);
+        rotate8(a[u], b[u], &tab[r_[u]][c_[u] * 8]);
         base[u][c_[u]] = a[u];
         base[u][c_[u] + TPR] = b[u];
       }
@@ -115,8 +120,7 @@ template <int D>
 __global__ void append_kernel(const __grid_constant__ AppendParams p) {
   constexpr int H = D / 2;
   constexpr int TPR = H / 8;
-  __shared__ float cs[H];
-  __shared__ float sn[H];
+  __shared__ CosSin2 tab[H];
   const int i = blockIdx.x;
   const int b = blockIdx.y;
   const int row0 = p.row_d ? p.row_d[b] : p.row_h[b];
@@ -131,7 +135,7 @@ __global__ void append_kernel(const __grid_constant__ AppendParams p) {
   } else {   // extraction: documents at 0..n_doc-1, slot s at min((s+1)k, n_doc)-1
     pos = (i < p.n_doc) ? i : min((i - p.n_doc + 1) * p.kblk, p.n_doc) - 1;
   }
-  for (int f = threadIdx.x; f < H; f += blockDim.x) rope_cos_sin(pos, p.inv_freq[f], &cs[f], &sn[f]);
+  for (int f = threadIdx.x; f < H; f += blockDim.x) tab[f] = rope_cos_sin2(pos, p.inv_freq[f]);
   __syncthreads();
   const int h = threadIdx.x / TPR;
   const int c = threadIdx.x % TPR;
@@ -141,7 +145,7 @@ __global__ void append_kernel(const __grid_constant__ AppendParams p) {
   const uint4* ks = reinterpret_cast<const uint4*>(p.k_src + src);
   const uint4* vs = reinterpret_cast<const uint4*>(p.v_src + src);
   uint4 a = ks[c], bb = ks[c + TPR];
-  rotate8(a, bb, &cs[c * 8], &sn[c * 8]);
+  rotate8(a, bb, &tab[c * 8]);
   uint4* kd = reinterpret_cast<uint4*>(p.k_dst[b] + dst);
   uint4* vd = reinterpret_cast<uint4*>(p.v_dst[b] + dst);
   kd[c] = a;
