@@ -196,6 +196,23 @@ def profiled_traffic(kernel: str):
     return None
 
 
+def max_over_ranks(values, world: int, device="cpu"):
+    """Element-wise max of per-rank timings (replicas finish when the slowest
+    does).  world == 1 returns the values unchanged."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def replica_tokens(batch: int, decode_steps: int, steps: int, world: int) -> int:
+    """Answer tokens all ranks produce in `steps` requests each (weak scaling)."""
+    return batch * decode_steps * steps * world
+
+
 # ------------------------------------------------------------------ our arm
 
 def run_ours(args, rank: int, world: int) -> dict:
@@ -245,20 +262,21 @@ def run_ours(args, rank: int, world: int) -> dict:
         for l in range(L):
             bt.prefill(l, dev_in["q_pre"][l], dev_in["kq_pre"][l], dev_in["vq"][l], pre_out[l], stream)
 
-    def decode_all():
-        for t in range(T):
+    def decode_all(steps=T):
+        for t in range(steps):
             for l in range(L):
                 bt.decode(l, dev_in["qd_pre"][t, l], dev_in["kd_pre"][t, l], dev_in["vd"][t, l],
                           dec_out[t, l], stream)
             bt.advance(stream)
 
-    # Warm the launch paths eagerly once (sets kernel attributes), then capture.
+    # Warm the launch paths eagerly once (one decode step is enough to set the
+    # kernels' attributes), then capture.
     with torch.cuda.stream(stream):
         bt.compose(stream)
         if Q:
             prefill_all()
         bt.reset_decode(stream)
-        decode_all()
+        decode_all(1)
     torch.cuda.synchronize()
     g_pre = torch.cuda.CUDAGraph() if Q else None
     g_dec = torch.cuda.CUDAGraph()
@@ -270,7 +288,7 @@ def run_ours(args, rank: int, world: int) -> dict:
             decode_all()
     torch.cuda.synchronize()
     assert P.c2kv_device_error() == P.C2KV_OK
-    launches_per_step = (bt.batch * min(L, 4) + (2 * L if Q else 0) + T * (2 * L + 1))
+    launches_per_step = (bt.batch * min(L, 4) + (2 * L if Q else 0) + T * (L + 1))
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
 
@@ -351,13 +369,8 @@ def run_ours(args, rank: int, world: int) -> dict:
     barrier()
     e2e_elapsed = e_beg.elapsed_time(e_end) / 1e3
 
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([elapsed, e2e_elapsed], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed, e2e_elapsed = float(tt[0]), float(tt[1])
-
-    toks = Bn * T * args.steps * world
+    elapsed, e2e_elapsed = max_over_ranks([elapsed, e2e_elapsed], world, dev)
+    toks = replica_tokens(Bn, T, args.steps, world)
     # algorithmic decode bytes: every key row (K and V) of every sequence,
     # layer and step, plus q/out/new k,v rows
     keys = sum((n + Q + t + 1) for n in bt.n_slots for t in range(T))
@@ -412,8 +425,8 @@ def run_ours(args, rank: int, world: int) -> dict:
         "roofline": {"kernel": "attn_kernel (decode)", "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
                      "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
                      "peak_source": f"{peak_src} (hbm_gbs, burst)",
-                     "launch_time": "decode-phase time / attention launches (includes the append "
-                                    "kernel and launch gaps)"},
+                     "launch_time": "decode-phase time / attention launches (includes the per-step "
+                                    "length-advance kernel and launch gaps)"},
         "e2e": {"value": toks / e2e_elapsed, "unit": "tok/s", "h2d_bytes_per_step": h2d_bytes + compose_bytes,
                 "d2h_bytes_per_step": d2h_bytes},
         "clocks": clocks,

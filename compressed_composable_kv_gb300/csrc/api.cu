@@ -11,6 +11,8 @@
 #include <unordered_set>
 #include <vector>
 
+#include <cudaTypedefs.h>
+
 #include "c2kv_internal.h"
 
 using namespace c2kv;
@@ -144,30 +146,135 @@ c2kv_status plan_impl(int32_t n_docs, const int32_t* n_tokens, const int32_t* n_
   return C2KV_OK;
 }
 
+// Scratch of one attention call: split-K partials and arrival counters, and
+// for multi-token calls the rotated q in the tensor-core tile layout.
 struct AttnWs {
   int n_tb, num_splits, split_keys;
-  size_t counters_off, ml_off, o_off, total;
+  size_t counters_off, ml_off, o_off, qrot_off, total;
 };
 
 AttnWs attn_workspace(const c2kv_geometry* g, int batch, int t_len, int max_keys, int num_sms) {
   AttnWs w{};
-  const int tpc = attn_tokens_per_cta(t_len);
-  w.n_tb = (t_len + tpc - 1) / tpc;
-  attn_plan_splits(batch * w.n_tb * g->n_kv_heads, max_keys, num_sms, &w.num_splits, &w.split_keys);
   const int grp = g->n_q_heads / g->n_kv_heads;
+  if (t_len == 1) {
+    w.n_tb = 1;
+    attn_plan_splits(batch * g->n_kv_heads, max_keys, num_sms, &w.num_splits, &w.split_keys);
+  } else {
+    const int tok = prefill_tc_tokens_per_tile(grp);
+    const int kt = prefill_tc_key_tile();
+    w.n_tb = (t_len + tok - 1) / tok;
+    const int units = batch * w.n_tb * g->n_kv_heads;
+    int s = (num_sms + units - 1) / units;
+    s = std::min(s, (max_keys + kt - 1) / kt);
+    s = std::max(1, std::min(s, kTcMaxSplits));
+    int sk = (max_keys + s - 1) / s;
+    sk = std::max(kt, (sk + kt - 1) / kt * kt);
+    w.split_keys = sk;
+    w.num_splits = (max_keys + sk - 1) / sk;
+  }
   const size_t rows = (size_t)batch * t_len * g->n_kv_heads * w.num_splits * grp;
-  w.counters_off = 0;
-  w.ml_off = align256((size_t)batch * w.n_tb * g->n_kv_heads * sizeof(int32_t));
-  w.o_off = w.ml_off + align256(rows * 2 * sizeof(float));
-  w.total = w.num_splits > 1 ? w.o_off + align256(rows * g->head_dim * sizeof(float)) : 0;
+  size_t off = 0;
+  if (w.num_splits > 1) {
+    w.counters_off = off;
+    off += align256((size_t)batch * w.n_tb * g->n_kv_heads * sizeof(int32_t));
+    w.ml_off = off;
+    off += align256(rows * 2 * sizeof(float));
+    w.o_off = off;
+    off += align256(rows * g->head_dim * sizeof(float));
+  }
+  w.qrot_off = off;
+  if (t_len > 1) off += align256((size_t)batch * g->n_q_heads * t_len * g->head_dim * 2);
+  w.total = off;
   return w;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    cudaGetLastError();
+  });
+  return fn;
+}
+
+// bf16 tensor map with a 64-element (128-byte) inner box and 128-byte swizzle.
+// rank 2: {d, rows}, box {64, box_rows}; rank 3: {d, keys, blocks} with the
+// block stride given, box {64, box_rows, 1}.
+c2kv_status encode_map(CUtensorMap* m, const void* base, int rank, uint64_t d, uint64_t n1, uint64_t n2,
+                       uint64_t stride2_bytes, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return fail(C2KV_ECUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[3] = {d, n1, n2};
+  const cuuint64_t strides[2] = {d * 2, stride2_bytes};
+  const cuuint32_t box[3] = {64, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(C2KV_ECUDA, "cuTensorMapEncodeTiled failed: " + std::to_string((int)r));
+  return C2KV_OK;
+}
+
+// Multi-token attention on the tensor cores.  kb0/vb0: per-sequence layer-0
+// bases of [n_blocks = layers * kv heads][block_rows][d] key/value arrays;
+// valid[b] keys of each block are real, the rest read as zeros.
+c2kv_status run_prefill_tc(const c2kv_geometry* g, int batch, const void* const* kb0, const void* const* vb0,
+                           const int32_t* n_cached, const int32_t* valid, int n_blocks, int block_rows,
+                           int layer, int t_len, int max_keys, int mask_mode, int n_doc, int kblk,
+                           void* out, const AttnWs& w, uint8_t* ws, cudaStream_t st) {
+  unsigned* err = nullptr;
+  c2kv_status s = device_state(&err, nullptr);
+  if (s != C2KV_OK) return s;
+  static PrefillTcParams p;   // large (tensor maps); guarded by the mutex below
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  std::memset(&p, 0, sizeof(p));
+  const int D = g->head_dim;
+  const int grp = g->n_q_heads / g->n_kv_heads;
+  s = encode_map(&p.tm_q, ws + w.qrot_off, 2, D, (uint64_t)batch * g->n_q_heads * t_len, 0, 0, 128);
+  if (s != C2KV_OK) return s;
+  for (int b = 0; b < batch; ++b) {
+    const uint64_t stride2 = (uint64_t)block_rows * D * 2;
+    s = encode_map(&p.tm_k[b], kb0[b], 3, D, valid[b], n_blocks, stride2, 64);
+    if (s != C2KV_OK) return s;
+    s = encode_map(&p.tm_v[b], vb0[b], 3, D, valid[b], n_blocks, stride2, 64);
+    if (s != C2KV_OK) return s;
+    p.n_cached[b] = n_cached[b];
+  }
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.part_o = w.num_splits > 1 ? reinterpret_cast<float*>(ws + w.o_off) : nullptr;
+  p.part_ml = w.num_splits > 1 ? reinterpret_cast<float*>(ws + w.ml_off) : nullptr;
+  p.counters = w.num_splits > 1 ? reinterpret_cast<int32_t*>(ws + w.counters_off) : nullptr;
+  p.err = err;
+  p.batch = batch;
+  p.t_len = t_len;
+  p.n_q = g->n_q_heads;
+  p.n_kv = g->n_kv_heads;
+  p.layer = layer;
+  p.num_splits = w.num_splits;
+  p.split_keys = w.split_keys;
+  p.mask_mode = mask_mode;
+  p.n_doc = n_doc;
+  p.kblk = kblk;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+  (void)grp;
+  (void)max_keys;
+  C2KV_CUDA(launch_prefill_tc(p, D, grp, st));
+  return C2KV_OK;
 }
 
 c2kv_status run_attention(const c2kv_geometry* g, int batch, const __nv_bfloat16* const* kb,
                           const __nv_bfloat16* const* vb, const int32_t* n_cached_h, const int32_t* pos_h,
                           const int32_t* n_cached_d, const int32_t* pos_d, int cap, int max_keys, int t_len,
                           int pos_mode, int mask_mode, int n_doc, int kblk, const void* q, void* out,
-                          void* workspace, size_t workspace_bytes, cudaStream_t st) {
+                          void* workspace, size_t workspace_bytes, cudaStream_t st,
+                          const void* fused_k_new = nullptr, const void* fused_v_new = nullptr) {
   unsigned* err = nullptr;
   int sms = 0;
   c2kv_status s = device_state(&err, &sms);
@@ -188,9 +295,9 @@ c2kv_status run_attention(const c2kv_geometry* g, int batch, const __nv_bfloat16
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.out = static_cast<__nv_bfloat16*>(out);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  p.counters = w.total ? reinterpret_cast<int32_t*>(ws + w.counters_off) : nullptr;
-  p.part_ml = w.total ? reinterpret_cast<float*>(ws + w.ml_off) : nullptr;
-  p.part_o = w.total ? reinterpret_cast<float*>(ws + w.o_off) : nullptr;
+  p.counters = w.num_splits > 1 ? reinterpret_cast<int32_t*>(ws + w.counters_off) : nullptr;
+  p.part_ml = w.num_splits > 1 ? reinterpret_cast<float*>(ws + w.ml_off) : nullptr;
+  p.part_o = w.num_splits > 1 ? reinterpret_cast<float*>(ws + w.o_off) : nullptr;
   p.err = err;
   p.batch = batch;
   p.t_len = t_len;
@@ -204,6 +311,9 @@ c2kv_status run_attention(const c2kv_geometry* g, int batch, const __nv_bfloat16
   p.mask_mode = mask_mode;
   p.n_doc = n_doc;
   p.kblk = kblk;
+  p.fuse_append = fused_k_new != nullptr ? 1 : 0;
+  p.k_new = static_cast<const __nv_bfloat16*>(fused_k_new);
+  p.v_new = static_cast<const __nv_bfloat16*>(fused_v_new);
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)g->head_dim));
   fill_inv_freq(g, p.inv_freq);
   C2KV_CUDA(launch_attention(p, g->head_dim, g->n_q_heads / g->n_kv_heads, st));
@@ -213,7 +323,7 @@ c2kv_status run_attention(const c2kv_geometry* g, int batch, const __nv_bfloat16
 c2kv_status run_append(const c2kv_geometry* g, int batch, __nv_bfloat16* const* kd, __nv_bfloat16* const* vd,
                        const int32_t* row_h, const int32_t* pos_h, const int32_t* row_d, const int32_t* pos_d,
                        int cap, int t_len, int pos_mode, int n_doc, int kblk, const void* k_src,
-                       const void* v_src, cudaStream_t st) {
+                       const void* v_src, cudaStream_t st, const void* q_src = nullptr, void* q_dst = nullptr) {
   unsigned* err = nullptr;
   c2kv_status s = device_state(&err, nullptr);
   if (s != C2KV_OK) return s;
@@ -229,9 +339,12 @@ c2kv_status run_append(const c2kv_geometry* g, int batch, __nv_bfloat16* const* 
   p.pos_d = pos_d;
   p.k_src = static_cast<const __nv_bfloat16*>(k_src);
   p.v_src = static_cast<const __nv_bfloat16*>(v_src);
+  p.q_src = static_cast<const __nv_bfloat16*>(q_src);
+  p.q_dst = static_cast<__nv_bfloat16*>(q_dst);
   p.err = err;
   p.t_len = t_len;
   p.n_kv = g->n_kv_heads;
+  p.n_q = g->n_q_heads;
   p.cap = cap;
   p.pos_mode = pos_mode;
   p.n_doc = n_doc;
@@ -461,7 +574,7 @@ c2kv_status c2kv_compose(c2kv_store st, int32_t n_docs, const int32_t* doc_ids, 
 size_t c2kv_attend_workspace_size(const c2kv_geometry* geom, int32_t batch, int32_t t_len, int32_t max_keys) {
   if (check_geom(geom) != C2KV_OK || batch < 1 || t_len < 1 || max_keys < 1) return 0;
   const AttnWs w = attn_workspace(geom, batch, t_len, max_keys, sm_count_for_sizing());
-  return w.total > 0 ? w.total : 256;
+  return std::max<size_t>(w.total, 256);
 }
 
 size_t c2kv_masked_extra_bytes(const c2kv_geometry* geom, int32_t n_tokens) {
@@ -507,11 +620,33 @@ c2kv_status c2kv_attend_prefill(const c2kv_geometry* geom, int32_t layer, int32_
     vb[b] = static_cast<__nv_bfloat16*>(v_caches[b]) + layer * lstride;
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  s = run_append(geom, batch, kb, vb, n_cached, start_pos, nullptr, nullptr, cap, q_len, kPosSequential, 0, 0,
-                 k_new, v_new, st);
+  if (q_len == 1) {
+    s = run_append(geom, batch, kb, vb, n_cached, start_pos, nullptr, nullptr, cap, 1, kPosSequential, 0, 0,
+                   k_new, v_new, st);
+    if (s != C2KV_OK) return s;
+    return run_attention(geom, batch, kb, vb, n_cached, start_pos, nullptr, nullptr, cap, max_keys, 1,
+                         kPosSequential, kMaskCausal, 0, 0, q, out, workspace, workspace_bytes, st);
+  }
+  int sms = 0;
+  s = device_state(nullptr, &sms);
   if (s != C2KV_OK) return s;
-  return run_attention(geom, batch, kb, vb, n_cached, start_pos, nullptr, nullptr, cap, max_keys, q_len,
-                       kPosSequential, kMaskCausal, 0, 0, q, out, workspace, workspace_bytes, st);
+  const AttnWs w = attn_workspace(geom, batch, q_len, max_keys, sms);
+  if (workspace == nullptr || workspace_bytes < w.total)
+    return fail(C2KV_EINVAL, "workspace too small: need " + std::to_string(w.total) + " bytes");
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  s = run_append(geom, batch, kb, vb, n_cached, start_pos, nullptr, nullptr, cap, q_len, kPosSequential, 0, 0,
+                 k_new, v_new, st, q, ws + w.qrot_off);
+  if (s != C2KV_OK) return s;
+  const void* k0[kMaxBatch];
+  const void* v0[kMaxBatch];
+  int32_t valid[kMaxBatch];
+  for (int b = 0; b < batch; ++b) {
+    k0[b] = k_caches[b];
+    v0[b] = v_caches[b];
+    valid[b] = n_cached[b] + q_len;
+  }
+  return run_prefill_tc(geom, batch, k0, v0, n_cached, valid, geom->n_layers * geom->n_kv_heads, cap, layer,
+                        q_len, max_keys, kMaskCausal, 0, 0, out, w, ws, st);
 }
 
 c2kv_status c2kv_attend_decode(const c2kv_geometry* geom, int32_t layer, int32_t batch, void* const* k_caches,
@@ -537,11 +672,9 @@ c2kv_status c2kv_attend_decode(const c2kv_geometry* geom, int32_t layer, int32_t
     vb[b] = static_cast<__nv_bfloat16*>(v_caches[b]) + layer * lstride;
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  s = run_append(geom, batch, kb, vb, nullptr, nullptr, n_cached_dev, pos_dev, cap, 1, kPosSequential, 0, 0,
-                 k_new, v_new, st);
-  if (s != C2KV_OK) return s;
+  // One launch: the kernel rotates and stores the new key/value itself.
   return run_attention(geom, batch, kb, vb, nullptr, nullptr, n_cached_dev, pos_dev, cap, max_keys, 1,
-                       kPosSequential, kMaskCausal, 0, 0, q, out, workspace, workspace_bytes, st);
+                       kPosSequential, kMaskCausal, 0, 0, q, out, workspace, workspace_bytes, st, k_new, v_new);
 }
 
 c2kv_status c2kv_seq_advance(int32_t batch, int32_t* n_cached_dev, int32_t* pos_dev, int32_t delta, void* stream) {
@@ -576,13 +709,26 @@ c2kv_status c2kv_attend_masked(const c2kv_geometry* geom, int32_t mask, int32_t 
   const int32_t zero = 0;
   const int kblk = mask == C2KV_MASK_STRUCTURED ? k : 1;
   const int pos_mode = mask == C2KV_MASK_STRUCTURED ? kPosExtraction : kPosSequential;
-  s = run_append(geom, 1, &krot, &vt, &zero, &zero, nullptr, nullptr, N, N, pos_mode, n_doc, kblk, kk, v, st);
+  const int mmode = mask == C2KV_MASK_STRUCTURED ? kMaskStructured : kMaskCausal;
+  if (N == 1) {
+    s = run_append(geom, 1, &krot, &vt, &zero, &zero, nullptr, nullptr, N, N, pos_mode, n_doc, kblk, kk, v, st);
+    if (s != C2KV_OK) return s;
+    const __nv_bfloat16* kb = krot;
+    const __nv_bfloat16* vb = vt;
+    return run_attention(geom, 1, &kb, &vb, &zero, &zero, nullptr, nullptr, N, N, N, pos_mode, mmode, n_doc,
+                         kblk, q, out, workspace, attn_bytes, st);
+  }
+  int sms = 0;
+  s = device_state(nullptr, &sms);
   if (s != C2KV_OK) return s;
-  const __nv_bfloat16* kb = krot;
-  const __nv_bfloat16* vb = vt;
-  return run_attention(geom, 1, &kb, &vb, &zero, &zero, nullptr, nullptr, N, N, N, pos_mode,
-                       mask == C2KV_MASK_STRUCTURED ? kMaskStructured : kMaskCausal, n_doc, kblk, q, out,
-                       workspace, attn_bytes, st);
+  const AttnWs w = attn_workspace(geom, 1, N, N, sms);
+  s = run_append(geom, 1, &krot, &vt, &zero, &zero, nullptr, nullptr, N, N, pos_mode, n_doc, kblk, kk, v, st, q,
+                 ws + w.qrot_off);
+  if (s != C2KV_OK) return s;
+  const void* k0 = krot;
+  const void* v0 = vt;
+  return run_prefill_tc(geom, 1, &k0, &v0, &zero, &N, geom->n_kv_heads, N, 0, N, N, mmode, n_doc, kblk, out, w,
+                        ws, st);
 }
 
 c2kv_status c2kv_device_error(int32_t* code) {

@@ -47,7 +47,7 @@ struct Cfg {
   static constexpr int WTS = TPC * G * kMaxSplits * 4;
   static constexpr int MAIN_RAW = (PIPE > CMB ? (PIPE > WTS ? PIPE : WTS) : (CMB > WTS ? CMB : WTS));
   static constexpr int MAIN = (MAIN_RAW + 127) / 128 * 128;   // keeps the mbarriers 8-byte aligned
-  static constexpr int EXTRA = 2 * kStages * 8 + 2 * TPC * (D / 2) * 4 + 16;
+  static constexpr int EXTRA = (2 * kStages + 2) * 8 + 2 * TPC * (D / 2) * 4 + (D / 2) * 16 + 16;
   static constexpr int SMEM = MAIN + EXTRA;
   static_assert(KPG >= 1 && KPG * GPT == T, "tile must split evenly over key groups");
 };
@@ -75,7 +75,9 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::MAIN);
   uint64_t* empty = full + kStages;
-  float* cs = reinterpret_cast<float*>(empty + kStages);   // [TPC][D/2]
+  uint64_t* inj = empty + kStages;                          // new-key row injected (fused append)
+  CosSin2* tab2 = reinterpret_cast<CosSin2*>(inj + 2);      // [D/2], position of the new key
+  float* cs = reinterpret_cast<float*>(tab2 + D / 2);       // [TPC][D/2]
   float* sn = cs + C::TPC * (D / 2);
   int* flag = reinterpret_cast<int*>(sn + C::TPC * (D / 2));
 
@@ -101,18 +103,27 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
   const int kb = split * p.split_keys;
   const int ke = min(kb + p.split_keys, kmax);
   const int ntiles = ke > kb ? (ke - kb + T - 1) / T : 0;
+  // Fused append (decode): key nk = n_cached is the new token; the split that
+  // holds it builds the row itself, every other key comes from the cache.
+  constexpr int TPR = D / 16;
+  const int nk = n_cached + p.t_len - 1;
+  const bool has_new = p.fuse_append && nk >= kb && nk < ke;
+  const int t_new = has_new ? (nk - kb) / T : -1;
+  const int k_res_end = p.fuse_append ? min(ke, nk) : ke;   // end of cache-resident keys
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kWarps);
     }
+    mbar_init(inj, TPR);
     fence_barrier_init();
   }
   for (int i = tid; i < ntok * (D / 2); i += kThreads) {
     const int t = i / (D / 2), f = i % (D / 2);
     rope_cos_sin(token_position(p, pos0, tok0 + t), p.inv_freq[f], &cs[i], &sn[i]);
   }
+  if (has_new && tid < D / 2) tab2[tid] = rope_cos_sin2(pos0, p.inv_freq[tid]);
   __syncthreads();
 
   const __nv_bfloat16* kg = p.k_base[b] + (size_t)h * p.cap * D;
@@ -122,7 +133,12 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
   auto issue = [&](int t) {
     const int s = t % kStages;
     const int key0 = kb + t * T;
-    const uint32_t bytes = (uint32_t)min(T, ke - key0) * D * 2;
+    const int cnt = max(0, min(T, k_res_end - key0));
+    if (cnt == 0) {   // the tile holds only the new key
+      mbar_arrive(&full[s]);
+      return;
+    }
+    const uint32_t bytes = (uint32_t)cnt * D * 2;
     mbar_arrive_expect_tx(&full[s], 2 * bytes);
     bulk_g2s(stage_k(s), kg + (size_t)key0 * D, bytes, &full[s]);
     bulk_g2s(stage_v(s), vg + (size_t)key0 * D, bytes, &full[s]);
@@ -176,11 +192,45 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
     for (int e = 0; e < 8; ++e) o[g][e] = 0.f;
   }
 
+  // The new key's rotated k and v, prepared by warp 1 (lane c owns pairs
+  // [8c, 8c+8)); written to the cache now and into the smem tile later.
+  uint4 nk_a = make_uint4(0, 0, 0, 0), nk_b = nk_a, nv_a = nk_a, nv_b = nk_a;
+  if (has_new && warp == 1 && lane < TPR) {
+    const uint4* ks = reinterpret_cast<const uint4*>(p.k_new + ((size_t)b * p.n_kv + h) * D);
+    const uint4* vs = reinterpret_cast<const uint4*>(p.v_new + ((size_t)b * p.n_kv + h) * D);
+    nk_a = ks[lane];
+    nk_b = ks[lane + TPR];
+    nv_a = vs[lane];
+    nv_b = vs[lane + TPR];
+    rotate8_df(nk_a, nk_b, &tab2[lane * 8]);
+    uint4* kd = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(kg) + (size_t)nk * D);
+    uint4* vd = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(vg) + (size_t)nk * D);
+    kd[lane] = nk_a;
+    kd[lane + TPR] = nk_b;
+    vd[lane] = nv_a;
+    vd[lane + TPR] = nv_b;
+  }
+
   bool aborted = false;
   for (int t = 0; t < ntiles; ++t) {
     const int s = t % kStages;
     const uint32_t ph = (t / kStages) & 1;
     if (!mbar_wait(&full[s], ph)) { aborted = true; break; }
+    if (t == t_new) {
+      // The row after the copied keys is free in this stage: fill it with the
+      // new key, then let every warp read the tile.
+      if (warp == 1 && lane < TPR) {
+        const int r = nk - (kb + t * T);
+        uint4* ksm = reinterpret_cast<uint4*>(stage_k(s) + (size_t)r * D * 2);
+        uint4* vsm = reinterpret_cast<uint4*>(stage_v(s) + (size_t)r * D * 2);
+        ksm[lane] = nk_a;
+        ksm[lane + TPR] = nk_b;
+        vsm[lane] = nv_a;
+        vsm[lane + TPR] = nv_b;
+        mbar_arrive(inj);
+      }
+      if (!mbar_wait(inj, 0)) { aborted = true; break; }
+    }
     const int key0 = kb + t * T;
     const int nvalid = min(T, ke - key0);
     const uint8_t* Ks = stage_k(s);
@@ -374,7 +424,10 @@ cudaError_t launch_one(const AttnParams& p, cudaStream_t st) {
 
 template <int D, int G>
 cudaError_t launch_g(const AttnParams& p, cudaStream_t st) {
-  return p.t_len == 1 ? launch_one<D, G, 4>(p, st) : launch_one<D, G, 1>(p, st);
+  // One token per sequence: the 4 warps split its keys.  Multi-token calls
+  // go to the tensor-core kernel.
+  if (p.t_len != 1) return cudaErrorInvalidValue;
+  return launch_one<D, G, 4>(p, st);
 }
 
 template <int D>
@@ -392,6 +445,7 @@ cudaError_t launch_d(const AttnParams& p, int group, cudaStream_t st) {
 }  // namespace
 
 int attn_tokens_per_cta(int t_len) { return t_len == 1 ? 1 : kWarps; }
+
 
 void attn_plan_splits(int units, int max_keys, int num_sms, int* num_splits, int* split_keys) {
   const int target = num_sms * kAttnCtasPerSm;

@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -109,6 +110,27 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
   return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
 }
 
+// Rotates 8 pairs: a holds elements [8c, 8c+8) of the first half, b the same
+// offsets of the second half.  Each output is evaluated in double-float and
+// rounded once to bf16, so it is the correctly rounded rotation of the
+// stored bf16 inputs (to ~2^-44), also when x cos - y sin nearly cancels.
+__device__ __forceinline__ void rotate8_df(uint4& a, uint4& b, const CosSin2* t) {
+  float x[8], y[8];
+  unpack8(a, x);
+  unpack8(b, y);
+  uint32_t xo[8], yo[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    float hi, lo;
+    dot2_df(x[e], t[e].ch, t[e].cl, -y[e], t[e].sh, t[e].sl, hi, lo);   // x cos - y sin
+    xo[e] = df_to_bf16_bits(hi, lo);
+    dot2_df(y[e], t[e].ch, t[e].cl, x[e], t[e].sh, t[e].sl, hi, lo);    // y cos + x sin
+    yo[e] = df_to_bf16_bits(hi, lo);
+  }
+  a = make_uint4(xo[0] | (xo[1] << 16), xo[2] | (xo[3] << 16), xo[4] | (xo[5] << 16), xo[6] | (xo[7] << 16));
+  b = make_uint4(yo[0] | (yo[1] << 16), yo[2] | (yo[3] << 16), yo[4] | (yo[5] << 16), yo[6] | (yo[7] << 16));
+}
+
 // ---------------------------------------------------------------- mbarrier / bulk copy
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -194,9 +216,27 @@ struct AppendParams {
   const int32_t* pos_d;
   const __nv_bfloat16* k_src;        // [B][t_len][Hkv][d]
   const __nv_bfloat16* v_src;
+  const __nv_bfloat16* q_src;        // optional [B][t_len][Hq][d], rotated into ...
+  __nv_bfloat16* q_dst;              // ... [B][Hkv][t_len][G][d]
   unsigned* err;
-  int32_t t_len, n_kv, cap, pos_mode, n_doc, kblk;
+  int32_t t_len, n_kv, n_q, cap, pos_mode, n_doc, kblk;
   double inv_freq[kMaxHalfDim];
+};
+
+// Tensor-core prefill: Q from the rotated-q scratch, K/V from 3-D maps
+// {d, valid keys, layer * kv head} of each sequence's cache.
+struct PrefillTcParams {
+  CUtensorMap tm_q;
+  CUtensorMap tm_k[kMaxBatch];
+  CUtensorMap tm_v[kMaxBatch];
+  int32_t n_cached[kMaxBatch];
+  __nv_bfloat16* out;          // [B][t_len][Hq][d]
+  float* part_o;               // [B][t_len][Hkv][S][G][d]
+  float* part_ml;              // [B][t_len][Hkv][S][G][2]
+  int32_t* counters;           // [B][M tiles][Hkv]
+  unsigned* err;
+  int32_t batch, t_len, n_q, n_kv, layer, num_splits, split_keys, mask_mode, n_doc, kblk;
+  float scale_log2;
 };
 
 struct AttnParams {
@@ -215,6 +255,11 @@ struct AttnParams {
   int32_t batch, t_len, n_q, n_kv, cap, max_keys;
   int32_t num_splits, split_keys;
   int32_t pos_mode, mask_mode, n_doc, kblk;
+  // Decode with the append fused in: the new token's k (pre-RoPE) and v,
+  // [B][Hkv][d]; the key is rotated at pos, stored at row n_cached and used.
+  int32_t fuse_append;
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
   float scale_log2;
   double inv_freq[kMaxHalfDim];
 };
@@ -224,6 +269,11 @@ cudaError_t launch_rerope(const RopeParams& p, int head_dim, cudaStream_t st);
 cudaError_t launch_append(const AppendParams& p, int head_dim, int batch, cudaStream_t st);
 cudaError_t launch_attention(const AttnParams& p, int head_dim, int group, cudaStream_t st);
 cudaError_t launch_advance(int batch, int32_t* n_cached, int32_t* pos, int delta, cudaStream_t st);
+
+cudaError_t launch_prefill_tc(const PrefillTcParams& p, int head_dim, int group, cudaStream_t st);
+int prefill_tc_tokens_per_tile(int group);
+int prefill_tc_key_tile();
+constexpr int kTcMaxSplits = 128;
 
 // Attention work decomposition shared by the launcher and the workspace query.
 int attn_tokens_per_cta(int t_len);

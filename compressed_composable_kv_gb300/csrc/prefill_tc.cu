@@ -1,0 +1,536 @@
+// Question prefill (and the extraction mask mode) on the 5th-generation
+// tensor cores: QK^T and PV run as tcgen05.mma with TMEM accumulators.
+//
+// C2KV explainer (paper-daily.com), section "pipeline: extract, store,
+// concatenate" (整体流程): once the composed cache is in place the question is
+// appended and prefilled over it; section "structured information flow"
+// (为什么需要“结构化信息流”？) gives the extraction-time mask.
+//
+// One CTA owns a 128-row M tile of (question token, q head of the group)
+// rows for one (sequence, kv head, key split), token-major: row r is token
+// tok0 + r / G, head r % G (G = 5 uses 125 rows).  Warps 0-3 are the softmax
+// warps (thread t owns row t, i.e. TMEM lane t); warp 4's first lane issues
+// every TMA load and every MMA.
+//   Q   : [128 rows][d] bf16, TMA (2-D map over the rotated-q scratch), SW128
+//   K,V : 64-key tiles, TMA (3-D map over [layer*kv head][keys][d]), 3 stages,
+//         keys at or past the sequence's valid length read as zeros (OOB)
+//   S   : Q K^T, fp32 in TMEM, double-buffered (2 x 64 columns)
+//   P   : bf16 in shared memory (K-major SW128), double-buffered
+//   O   : P V accumulated in TMEM (d columns), rescaled in place only when a
+//         row's running max grows by more than 2^8 (the final O / l uses the
+//         same stale max, so the result is exact)
+// With several key splits the CTA writes (m, l, O) partials; the last CTA of
+// its (sequence, M tile, kv head) merges them and resets the counter.
+#include <cuda.h>
+
+#include "c2kv_internal.h"
+
+namespace c2kv {
+
+namespace {
+
+constexpr int BM = 128;        // rows per M tile (TMEM lanes)
+constexpr int BN = 64;         // keys per tile
+constexpr int STAGES = 3;
+constexpr int kSoftmaxThreads = 128;
+constexpr int kThreadsTc = 160;
+constexpr float kRescaleLog2 = 8.f;
+
+template <int D>
+struct TcCfg {
+  static constexpr int NSUB = D / 64;           // 128-byte column blocks of d
+  static constexpr int Q_BYTES = NSUB * BM * 128;
+  static constexpr int KV_BYTES = NSUB * BN * 128;
+  static constexpr int P_BYTES = BM * BN * 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
+  static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int N_BAR = 1 + 2 * STAGES + 2 + 2 + 2 + 2 + 1;
+  static constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;
+  static constexpr int SMEM = OFF_MISC + 64 + 1024;   // + slack for 1024-byte alignment
+  static constexpr int TMEM_S = 0;                    // two 64-column S buffers
+  static constexpr int TMEM_O = 2 * BN;               // d columns
+  static constexpr int TMEM_COLS = 256;
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major or MN-major, 128-byte swizzle.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;   // descriptor version of the 5th-generation tensor core
+  d |= (uint64_t)2 << 61;   // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M=128, N given.
+__host__ __device__ constexpr uint32_t idesc_bf16(int n, bool b_mn_major) {
+  return (1u << 4)                        // D format: f32
+         | (1u << 7)                      // A format: bf16
+         | (1u << 10)                     // B format: bf16
+         | ((b_mn_major ? 1u : 0u) << 16) // B major-ness
+         | ((uint32_t)(n >> 3) << 17)     // N / 8
+         | ((uint32_t)(BM >> 4) << 24);   // M / 16
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32]) {
+  uint32_t u[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
+        "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15]),
+        "=r"(u[16]), "=r"(u[17]), "=r"(u[18]), "=r"(u[19]), "=r"(u[20]), "=r"(u[21]), "=r"(u[22]), "=r"(u[23]),
+        "=r"(u[24]), "=r"(u[25]), "=r"(u[26]), "=r"(u[27]), "=r"(u[28]), "=r"(u[29]), "=r"(u[30]), "=r"(u[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) r[i] = __uint_as_float(u[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(__float_as_uint(r[0])), "r"(__float_as_uint(r[1])), "r"(__float_as_uint(r[2])),
+      "r"(__float_as_uint(r[3])), "r"(__float_as_uint(r[4])), "r"(__float_as_uint(r[5])),
+      "r"(__float_as_uint(r[6])), "r"(__float_as_uint(r[7])), "r"(__float_as_uint(r[8])),
+      "r"(__float_as_uint(r[9])), "r"(__float_as_uint(r[10])), "r"(__float_as_uint(r[11])),
+      "r"(__float_as_uint(r[12])), "r"(__float_as_uint(r[13])), "r"(__float_as_uint(r[14])),
+      "r"(__float_as_uint(r[15])), "r"(__float_as_uint(r[16])), "r"(__float_as_uint(r[17])),
+      "r"(__float_as_uint(r[18])), "r"(__float_as_uint(r[19])), "r"(__float_as_uint(r[20])),
+      "r"(__float_as_uint(r[21])), "r"(__float_as_uint(r[22])), "r"(__float_as_uint(r[23])),
+      "r"(__float_as_uint(r[24])), "r"(__float_as_uint(r[25])), "r"(__float_as_uint(r[26])),
+      "r"(__float_as_uint(r[27])), "r"(__float_as_uint(r[28])), "r"(__float_as_uint(r[29])),
+      "r"(__float_as_uint(r[30])), "r"(__float_as_uint(r[31]))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Bounded wait that also gives up once another thread has aborted the CTA.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              unsigned* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort_flag = 1;
+      atomicOr(err, kErrTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ bool tc_structured_visible(const PrefillTcParams& p, int tok, int key) {
+  if (tok < p.n_doc || key >= p.n_doc) return true;
+  const int i = tok - p.n_doc;
+  return key < min(p.kblk, p.n_doc) || (key >= i * p.kblk && key < min((i + 1) * p.kblk, p.n_doc));
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
+  using C = TcCfg<D>;
+  constexpr int TOK = BM / G;    // tokens per M tile
+  constexpr int ROWS = TOK * G;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = kv_full + STAGES;
+  uint64_t* s_full = kv_empty + STAGES;
+  uint64_t* s_free = s_full + 2;
+  uint64_t* p_full = s_free + 2;
+  uint64_t* p_free = p_full + 2;
+  uint64_t* o_done = p_free + 2;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x;
+  const int h = blockIdx.y % p.n_kv;
+  const int mt = blockIdx.y / p.n_kv;
+  const int b = blockIdx.z;
+  const int n_mt = (p.t_len + TOK - 1) / TOK;
+  const int n_cached = p.n_cached[b];
+  const int tok0 = mt * TOK;
+  const int ntok = min(TOK, p.t_len - tok0);
+  const int kmax = n_cached + tok0 + ntok;
+  const int kb = split * p.split_keys;
+  const int ke = min(kb + p.split_keys, kmax);
+  const int ntiles = ke > kb ? (ke - kb + BN - 1) / BN : 0;
+
+  if (tid == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], kSoftmaxThreads);
+      mbar_init(&p_full[i], kSoftmaxThreads);
+      mbar_init(&p_free[i], 1);
+    }
+    mbar_init(o_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr((const void*)tmem_slot)),
+                 "r"(C::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  uint8_t* sQ = smem + C::OFF_Q;
+  uint8_t* sK = smem + C::OFF_K;
+  uint8_t* sV = smem + C::OFF_V;
+  uint8_t* sP = smem + C::OFF_P;
+  const int kv_z = p.layer * p.n_kv + h;
+
+  if (warp == 4) {
+    if (lane == 0 && ntiles > 0) {
+      // ---------------- producer + MMA issuer (one thread)
+      const int q_row0 = ((b * p.n_kv + h) * p.t_len + tok0) * G;
+      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+      for (int sub = 0; sub < C::NSUB; ++sub) tma_load_2d(sQ + sub * BM * 128, &p.tm_q, sub * 64, q_row0, q_full);
+      auto issue_kv = [&](int t) {
+        const int s = t % STAGES;
+        mbar_arrive_expect_tx(&kv_full[s], 2 * C::KV_BYTES);
+        for (int sub = 0; sub < C::NSUB; ++sub) {
+          tma_load_3d(sK + s * C::KV_BYTES + sub * BN * 128, &p.tm_k[b], sub * 64, kb + t * BN, kv_z, &kv_full[s]);
+          tma_load_3d(sV + s * C::KV_BYTES + sub * BN * 128, &p.tm_v[b], sub * 64, kb + t * BN, kv_z, &kv_full[s]);
+        }
+      };
+      int next = 0;
+      for (; next < min(STAGES, ntiles); ++next) issue_kv(next);
+      constexpr uint32_t IDESC_QK = idesc_bf16(BN, false);
+      constexpr uint32_t IDESC_PV = idesc_bf16(D, true);
+      auto issue_pv = [&](int t) -> bool {
+        const int pb = t & 1, s = t % STAGES;
+        if (!wait_or_abort(&p_full[pb], (t >> 1) & 1, abort_flag, p.err)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t a = sw128_desc(smem_addr(sP + pb * C::P_BYTES) + kk * 32, 16, 1024);
+          const uint64_t bdesc = sw128_desc(smem_addr(sV + s * C::KV_BYTES) + kk * 2048, BN * 128, 1024);
+          mma_bf16(tmem + C::TMEM_O, a, bdesc, IDESC_PV, (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&kv_empty[s]);
+        mma_commit(&p_free[pb]);
+        mma_commit(o_done);
+        return true;
+      };
+      bool ok = wait_or_abort(q_full, 0, abort_flag, p.err);
+      for (int j = 0; ok && j < ntiles; ++j) {
+        const int s = j % STAGES, sb = j & 1;
+        ok = wait_or_abort(&kv_full[s], (j / STAGES) & 1, abort_flag, p.err);
+        if (ok && j >= 2) ok = wait_or_abort(&s_free[sb], ((j - 2) >> 1) & 1, abort_flag, p.err);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int sub = kk / 4, ko = (kk % 4) * 32;
+          const uint64_t a = sw128_desc(smem_addr(sQ + sub * BM * 128) + ko, 16, 1024);
+          const uint64_t bdesc = sw128_desc(smem_addr(sK + s * C::KV_BYTES + sub * BN * 128) + ko, 16, 1024);
+          mma_bf16(tmem + C::TMEM_S + sb * BN, a, bdesc, IDESC_QK, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s_full[sb]);
+        if (j >= 1) {
+          ok = issue_pv(j - 1);
+          if (ok && next < ntiles) {
+            ok = wait_or_abort(&kv_empty[(j - 1) % STAGES], ((j - 1) / STAGES) & 1, abort_flag, p.err);
+            if (ok) issue_kv(next++);
+          }
+        }
+      }
+      if (ok) issue_pv(ntiles - 1);
+    }
+  } else {
+    // ---------------- softmax warps: thread tid owns row tid (TMEM lane tid)
+    const int row = tid;
+    const int tl = row / G, g = row % G;
+    const int tok = tok0 + tl;
+    const bool row_ok = row < ROWS && tl < ntok;
+    const int lim = n_cached + tok + 1;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const int sb = j & 1;
+      if (!__all_sync(0xffffffffu, wait_or_abort(&s_full[sb], (j >> 1) & 1, abort_flag, p.err))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float sv[BN];
+      {
+        float t0[32], t1[32];
+        tmem_ld32(lane_base + C::TMEM_S + sb * BN, t0);
+        tmem_ld32(lane_base + C::TMEM_S + sb * BN + 32, t1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          sv[c] = t0[c];
+          sv[32 + c] = t1[c];
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&s_free[sb]);
+      const int key0 = kb + j * BN;
+      float mt_ = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BN; ++c) {
+        const int key = key0 + c;
+        bool vis = row_ok && key < ke && key < lim;
+        if (p.mask_mode == kMaskStructured) vis = vis && tc_structured_visible(p, tok, key);
+        sv[c] = vis ? sv[c] * p.scale_log2 : -INFINITY;
+        mt_ = fmaxf(mt_, sv[c]);
+      }
+      float alpha = 1.f;
+      bool rescale = false;
+      if (mt_ > m_run) {
+        if (m_run == -INFINITY) {
+          m_run = mt_;   // nothing accumulated yet for this row: O holds zeros
+        } else if (mt_ - m_run > kRescaleLog2) {
+          alpha = exp2f(m_run - mt_);
+          m_run = mt_;
+          rescale = true;
+        }
+      }
+      const float mu = (m_run == -INFINITY) ? 0.f : m_run;
+      float lsum = 0.f;
+      uint32_t pk[BN / 2];
+#pragma unroll
+      for (int c = 0; c < BN; c += 2) {
+        const float p0 = exp2f(sv[c] - mu), p1 = exp2f(sv[c + 1] - mu);
+        lsum += p0 + p1;
+        pk[c / 2] = pack2(p0, p1);
+      }
+      l_run = l_run * alpha + lsum;
+      // O rescale needs PV(j-1) finished; the warp shares the TMEM access, so
+      // the whole warp takes the path when any of its rows needs it.
+      if (__any_sync(0xffffffffu, rescale)) {
+        if (!__all_sync(0xffffffffu, wait_or_abort(o_done, (j - 1) & 1, abort_flag, p.err))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float o[32];
+          tmem_ld32(lane_base + C::TMEM_O + c0, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] *= alpha;
+          tmem_st32(lane_base + C::TMEM_O + c0, o);
+        }
+        tmem_wait_st();
+      }
+      const int pb = j & 1;
+      if (j >= 2 && !__all_sync(0xffffffffu, wait_or_abort(&p_free[pb], ((j - 2) >> 1) & 1, abort_flag, p.err))) {
+        ok = false;
+        break;
+      }
+      uint8_t* prow = sP + pb * C::P_BYTES + row * 128;
+#pragma unroll
+      for (int ch = 0; ch < BN / 8; ++ch) {
+        const uint4 v = make_uint4(pk[ch * 4 + 0], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
+        *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) = v;
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      mbar_arrive(&p_full[pb]);
+    }
+
+    // ---------------- epilogue: O / l, or split partials
+    const int S = p.num_splits;
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok && ntiles > 0 && !__all_sync(0xffffffffu, wait_or_abort(o_done, (ntiles - 1) & 1, abort_flag, p.err)))
+      ok = false;
+    if (ok && ntiles > 0) tc_fence_after();
+    const float invl = (l_run > 0.f) ? 1.f / l_run : 0.f;
+#pragma unroll
+    for (int c0 = 0; c0 < D; c0 += 32) {
+      float o[32];
+      if (ok && ntiles > 0) {
+        tmem_ld32(lane_base + C::TMEM_O + c0, o);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) o[c] = 0.f;
+      }
+      if (!row_ok) continue;
+      if (S == 1) {
+        __nv_bfloat16* dst = p.out + (((size_t)b * p.t_len + tok) * p.n_q + h * G + g) * D + c0;
+#pragma unroll
+        for (int c = 0; c < 32; c += 8) {
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = o[c + e] * invl;
+          *reinterpret_cast<uint4*>(dst + c) = pack8(f);
+        }
+      } else {
+        const size_t base = (((size_t)b * p.t_len + tok) * p.n_kv + h) * S + split;
+        float* dst = p.part_o + (base * G + g) * D + c0;
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+        if (c0 == 0) {
+          p.part_ml[(base * G + g) * 2 + 0] = (ntiles > 0 && ok) ? m_run : -INFINITY;
+          p.part_ml[(base * G + g) * 2 + 1] = (ntiles > 0 && ok) ? l_run : 0.f;
+        }
+      }
+    }
+  }
+
+  // ---------------- teardown: every tcgen05 access of the CTA is done here
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    // let TMA copies in flight land before the shared memory is released
+    if (tid == 0) {
+      mbar_wait(q_full, 0);
+      for (int s = 0; s < STAGES; ++s) mbar_wait(&kv_full[s], 0);
+    }
+    __syncthreads();
+  }
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");
+  }
+  if (p.num_splits == 1) return;
+
+  // ---------------- last CTA of (b, M tile, h) merges the split partials
+  __threadfence();
+  __syncthreads();
+  const int cidx = (b * n_mt + mt) * p.n_kv + h;
+  if (tid == 0) *last_flag = (atomicAdd(&p.counters[cidx], 1) == p.num_splits - 1);
+  __syncthreads();
+  if (!*last_flag) return;
+  __threadfence();
+  const int S = p.num_splits;
+  float* wts = reinterpret_cast<float*>(smem);   // [ntok*G][S]
+  for (int pair = warp; pair < ntok * G; pair += kThreadsTc / 32) {
+    const int t = pair / G, g = pair % G;
+    const size_t base = (((size_t)b * p.t_len + tok0 + t) * p.n_kv + h) * S;
+    float M = -INFINITY;
+    for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldcg(&p.part_ml[((base + s) * G + g) * 2]));
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f;
+    for (int s = lane; s < S; s += 32) {
+      const float ms = __ldcg(&p.part_ml[((base + s) * G + g) * 2]);
+      const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+      wts[pair * S + s] = w;
+      L = fmaf(__ldcg(&p.part_ml[((base + s) * G + g) * 2 + 1]), w, L);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    __syncwarp();
+    for (int s = lane; s < S; s += 32) wts[pair * S + s] *= inv;
+  }
+  __syncthreads();
+  for (int i = tid; i < ntok * G * D; i += kThreadsTc) {
+    const int dd = i % D, pair = i / D;
+    const int t = pair / G, g = pair % G;
+    const size_t base = (((size_t)b * p.t_len + tok0 + t) * p.n_kv + h) * S;
+    const float* w = wts + pair * S;
+    float acc = 0.f;
+    for (int s = 0; s < S; ++s) acc = fmaf(w[s], __ldcg(&p.part_o[((base + s) * G + g) * D + dd]), acc);
+    p.out[(((size_t)b * p.t_len + tok0 + t) * p.n_q + h * G + g) * D + dd] = __float2bfloat16_rn(acc);
+  }
+  if (tid == 0) p.counters[cidx] = 0;
+}
+
+template <int D, int G>
+cudaError_t launch_tc(const PrefillTcParams& p, cudaStream_t st) {
+  using C = TcCfg<D>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int tok = BM / G;
+  const int n_mt = (p.t_len + tok - 1) / tok;
+  const dim3 grid(p.num_splits, p.n_kv * n_mt, p.batch);
+  prefill_tc_kernel<D, G><<<grid, kThreadsTc, C::SMEM, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_tc_d(const PrefillTcParams& p, int group, cudaStream_t st) {
+  switch (group) {
+    case 1: return launch_tc<D, 1>(p, st);
+    case 2: return launch_tc<D, 2>(p, st);
+    case 4: return launch_tc<D, 4>(p, st);
+    case 5: return launch_tc<D, 5>(p, st);
+    case 8: return launch_tc<D, 8>(p, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+int prefill_tc_tokens_per_tile(int group) { return BM / group; }
+
+int prefill_tc_key_tile() { return BN; }
+
+cudaError_t launch_prefill_tc(const PrefillTcParams& p, int head_dim, int group, cudaStream_t st) {
+  if (head_dim == 128) return launch_tc_d<128>(p, group, st);
+  if (head_dim == 64) return launch_tc_d<64>(p, group, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace c2kv

@@ -12,27 +12,6 @@ namespace c2kv {
 
 namespace {
 
-// Rotates 8 pairs: a holds elements [8c, 8c+8) of the first half, b the same
-// offsets of the second half.  Each output is evaluated in double-float and
-// rounded once to bf16, so it is the correctly rounded rotation of the
-// stored bf16 inputs (to ~2^-44), also when x cos - y sin nearly cancels.
-__device__ __forceinline__ void rotate8(uint4& a, uint4& b, const CosSin2* t) {
-  float x[8], y[8];
-  unpack8(a, x);
-  unpack8(b, y);
-  uint32_t xo[8], yo[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    float hi, lo;
-    dot2_df(x[e], t[e].ch, t[e].cl, -y[e], t[e].sh, t[e].sl, hi, lo);   // x cos - y sin
-    xo[e] = df_to_bf16_bits(hi, lo);
-    dot2_df(y[e], t[e].ch, t[e].cl, x[e], t[e].sh, t[e].sl, hi, lo);    // y cos + x sin
-    yo[e] = df_to_bf16_bits(hi, lo);
-  }
-  a = make_uint4(xo[0] | (xo[1] << 16), xo[2] | (xo[3] << 16), xo[4] | (xo[5] << 16), xo[6] | (xo[7] << 16));
-  b = make_uint4(yo[0] | (yo[1] << 16), yo[2] | (yo[3] << 16), yo[4] | (yo[5] << 16), yo[6] | (yo[7] << 16));
-}
-
 // ---------------------------------------------------------------------------
 // K1: in-place re-rotation of composed K rows for a group of layers.
 // One CTA owns kSlots consecutive composed slots: it derives their positions
@@ -103,7 +82,7 @@ __global__ void __launch_bounds__(kRopeThreads) rerope_kernel(const __grid_const
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       if (ok[u]) {
-        rotate8(a[u], b[u], &tab[r_[u]][c_[u] * 8]);
+        rotate8_df(a[u], b[u], &tab[r_[u]][c_[u] * 8]);
         base[u][c_[u]] = a[u];
         base[u][c_[u] + TPR] = b[u];
       }
@@ -139,13 +118,26 @@ __global__ void append_kernel(const __grid_constant__ AppendParams p) {
   __syncthreads();
   const int h = threadIdx.x / TPR;
   const int c = threadIdx.x % TPR;
-  if (h >= p.n_kv) return;
+  if (h >= p.n_kv) {
+    // threads past the kv heads rotate q head hq into [B][Hkv][t_len][G][d]
+    const int hq = h - p.n_kv;
+    if (p.q_src == nullptr || hq >= p.n_q) return;
+    const int grp = p.n_q / p.n_kv;
+    const uint4* qs = reinterpret_cast<const uint4*>(p.q_src + (((size_t)b * p.t_len + i) * p.n_q + hq) * D);
+    uint4 a = qs[c], bb = qs[c + TPR];
+    rotate8_df(a, bb, &tab[c * 8]);
+    uint4* qd = reinterpret_cast<uint4*>(
+        p.q_dst + ((((size_t)b * p.n_kv + hq / grp) * p.t_len + i) * grp + hq % grp) * D);
+    qd[c] = a;
+    qd[c + TPR] = bb;
+    return;
+  }
   const size_t src = (((size_t)b * p.t_len + i) * p.n_kv + h) * D;
   const size_t dst = ((size_t)h * p.cap + row0 + i) * D;
   const uint4* ks = reinterpret_cast<const uint4*>(p.k_src + src);
   const uint4* vs = reinterpret_cast<const uint4*>(p.v_src + src);
   uint4 a = ks[c], bb = ks[c + TPR];
-  rotate8(a, bb, &tab[c * 8]);
+  rotate8_df(a, bb, &tab[c * 8]);
   uint4* kd = reinterpret_cast<uint4*>(p.k_dst[b] + dst);
   uint4* vd = reinterpret_cast<uint4*>(p.v_dst[b] + dst);
   kd[c] = a;
@@ -174,7 +166,7 @@ cudaError_t launch_rerope(const RopeParams& p, int head_dim, cudaStream_t st) {
 
 cudaError_t launch_append(const AppendParams& p, int head_dim, int batch, cudaStream_t st) {
   const dim3 grid(p.t_len, batch);
-  const int threads = p.n_kv * (head_dim / 16);
+  const int threads = (p.n_kv + (p.q_src ? p.n_q : 0)) * (head_dim / 16);
   if (head_dim == 128) append_kernel<128><<<grid, threads, 0, st>>>(p);
   else append_kernel<64><<<grid, threads, 0, st>>>(p);
   return cudaGetLastError();

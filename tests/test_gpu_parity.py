@@ -317,3 +317,17 @@ def test_device_length_beyond_capacity_is_reported():
     assert torch.all(out == 3.0)
     assert P.c2kv_device_error() == P.C2KV_OK   # reading clears the word
     sc.close()
+
+
+@pytest.mark.parametrize("hq,hkv,d,q_len", [(8, 8, 128, 40), (16, 2, 128, 33), (4, 2, 64, 1), (8, 1, 64, 130)])
+def test_prefill_group_sizes_and_ragged_tiles(hq, hkv, d, q_len):
+    """Tensor-core prefill for G = 1 and 8, a ragged last M tile, a one-token
+    question (which takes the CUDA-core path) and a single kv head."""
+    g = S.Geometry(1, hq, hkv, d, 1.0e4)
+    specs = [(1, 700, 175), (2, 13, 4)]
+    sc = Scenario(g, 4, specs, [([2, 1], None)], q_len=q_len, decode_steps=2)
+    w = S.Workload("g", g, 4, 1, q_len, 2, seed=hq * 100 + q_len)
+    inputs = S.make_step_inputs(w)
+    pre, dec = run_all(sc, upload(inputs))
+    check_request(sc, inputs, pre, dec, 0, layers=[0], steps=[0, 1])
+    sc.close()
