@@ -58,6 +58,8 @@ _SIGNATURES = {
                                    _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "c2kv_attend_decode": (_i32, [_pg, _i32, _i32, _pvp, _pvp, _i32, _vp, _vp, _i32,
                                   _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "c2kv_attend_decode_noalloc": (_i32, [_pg, _i32, _i32, _pvp, _pvp, _i32, _vp, _vp, _i32,
+                                          _vp, _vp, _vp, _vp, _vp]),
     "c2kv_seq_advance": (_i32, [_i32, _vp, _vp, _i32, _vp]),
     "c2kv_attend_masked": (_i32, [_pg, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "c2kv_device_error": (_i32, [_pi32]),
@@ -239,6 +241,21 @@ def c2kv_attend_decode(geom, layer: int, k_caches, v_caches, cap: int, n_cached_
         int(max_keys), _dev(q, torch.bfloat16, "q"), _dev(k_new, torch.bfloat16, "k_new"),
         _dev(v_new, torch.bfloat16, "v_new"), _dev(out, torch.bfloat16, "out"),
         _dev(workspace, None, "workspace"), ws, _stream(stream)))
+
+
+def c2kv_attend_decode_noalloc(geom, layer: int, k_caches, v_caches, cap: int, n_cached_dev: torch.Tensor,
+                               pos_dev: torch.Tensor, max_keys: int, q: torch.Tensor, k_new: torch.Tensor,
+                               v_new: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    """c2kv_attend_decode for callers that cannot allocate device memory: the
+    split-K scratch is the library's own fixed 4 MiB device array (shared by
+    all calls, so calls must not overlap on the GPU)."""
+    g = as_geometry(geom)
+    B = len(k_caches)
+    _check(load_library().c2kv_attend_decode_noalloc(
+        ctypes.byref(g), int(layer), B, _ptrs(k_caches, "k_cache"), _ptrs(v_caches, "v_cache"), int(cap),
+        _dev(n_cached_dev, torch.int32, "n_cached_dev"), _dev(pos_dev, torch.int32, "pos_dev"),
+        int(max_keys), _dev(q, torch.bfloat16, "q"), _dev(k_new, torch.bfloat16, "k_new"),
+        _dev(v_new, torch.bfloat16, "v_new"), _dev(out, torch.bfloat16, "out"), _stream(stream)))
 
 
 def c2kv_seq_advance(n_cached_dev: torch.Tensor, pos_dev: torch.Tensor, delta: int = 1, stream=None) -> None:

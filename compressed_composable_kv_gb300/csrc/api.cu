@@ -743,3 +743,79 @@ c2kv_status c2kv_device_error(int32_t* code) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode without caller-provided scratch.
+//
+// c2kv_attend_decode needs a device scratch buffer for its split-K partial
+// results.  Some callers cannot hand one over: a plugin whose host framework
+// passes it only a stream and the tensors it owns and forbids allocating
+// while work is being enqueued, or a serving loop that fixes every device
+// allocation at start-up and may not call cudaMalloc (or any allocator that
+// might) once it is running.  For them this entry point keeps the scratch in
+// one fixed-size array in the library's own device memory.
+// ---------------------------------------------------------------------------
+namespace {
+
+// 4 MiB per device, held from the moment the library's device code is loaded
+// on a GPU until the process exits.
+constexpr size_t kNoallocScratchBytes = size_t(4) << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes];
+
+uint8_t* g_noalloc_ptr[kMaxDevices] = {};   // device address of the array, per device
+std::mutex g_noalloc_mu;
+
+// Looks up the array's device address once per device (with that device
+// current).  In host code the array's name is only a stand-in for the symbol,
+// never an address a kernel may be given.
+c2kv_status noalloc_scratch(uint8_t** out) {
+  int dev = 0;
+  C2KV_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return fail(C2KV_EINVAL, "device index out of range");
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    C2KV_CUDA(cudaGetSymbolAddress(&ptr, g_noalloc_scratch));
+    if (ptr == nullptr) return fail(C2KV_ECUDA, "cudaGetSymbolAddress returned no address for the fixed scratch");
+    g_noalloc_ptr[dev] = static_cast<uint8_t*>(ptr);
+  }
+  *out = g_noalloc_ptr[dev];
+  return C2KV_OK;
+}
+
+}  // namespace
+
+extern "C" c2kv_status c2kv_attend_decode_noalloc(const c2kv_geometry* geom, int32_t layer, int32_t batch,
+                                                  void* const* k_caches, void* const* v_caches, int32_t cap,
+                                                  const int32_t* n_cached_dev, const int32_t* pos_dev,
+                                                  int32_t max_keys, const void* q, const void* k_new,
+                                                  const void* v_new, void* out, void* stream) {
+  // The same argument checks as c2kv_attend_decode, done before anything is
+  // enqueued (the counter clear below included).
+  c2kv_status s = check_geom(geom);
+  if (s != C2KV_OK) return s;
+  if (layer < 0 || layer >= geom->n_layers) return fail(C2KV_EINVAL, "layer out of range");
+  s = check_caches(batch, k_caches, v_caches, cap);
+  if (s != C2KV_OK) return s;
+  if (!n_cached_dev || !pos_dev) return fail(C2KV_EINVAL, "device length arrays are null");
+  if (max_keys < 1 || max_keys > cap) return fail(C2KV_EINVAL, "max_keys must be in [1, cap]");
+  if (!q || !k_new || !v_new || !out) return fail(C2KV_EINVAL, "null tensor pointer");
+  int sms = 0;
+  s = device_state(nullptr, &sms);
+  if (s != C2KV_OK) return s;
+  const AttnWs w = attn_workspace(geom, batch, 1, max_keys, sms);
+  if (w.total > kNoallocScratchBytes)
+    return fail(C2KV_EINVAL, "this decode needs " + std::to_string(w.total) +
+                                 " bytes of scratch, more than the fixed " +
+                                 std::to_string(kNoallocScratchBytes) +
+                                 " bytes of c2kv_attend_decode_noalloc; use c2kv_attend_decode with a workspace");
+  uint8_t* scratch = nullptr;
+  s = noalloc_scratch(&scratch);
+  if (s != C2KV_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The array keeps whatever the previous call left in it; the arrival
+  // counters must start at zero, the partial results need no clearing.
+  if (w.num_splits > 1) C2KV_CUDA(cudaMemsetAsync(scratch + w.counters_off, 0, w.ml_off - w.counters_off, st));
+  return c2kv_attend_decode(geom, layer, batch, k_caches, v_caches, cap, n_cached_dev, pos_dev, max_keys, q,
+                            k_new, v_new, out, scratch, kNoallocScratchBytes, stream);
+}

@@ -227,6 +227,34 @@ c2kv_status c2kv_attend_decode(const c2kv_geometry* geom, int32_t layer,
                                const void* v_new, void* out, void* workspace,
                                size_t workspace_bytes, void* stream);
 
+/*
+ * c2kv_attend_decode without a workspace argument: the paper has no
+ * counterpart; this is a convenience of the library.
+ *
+ * For callers that cannot allocate device memory where they decode -- a
+ * plugin whose host framework hands it only a stream and tensors and forbids
+ * allocation while enqueueing, or a serving loop that freezes all device
+ * allocations at start-up.  The split-K scratch lives instead in one
+ * fixed-size array (4 MiB) in the library's device memory; every GPU that
+ * loads the library holds that array until the process exits.  This call
+ * allocates nothing (no cudaMalloc/cudaFree, no allocating library routine).
+ *
+ * Arguments and results are those of c2kv_attend_decode.  The first call on
+ * a device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.  The
+ * array is shared by every call and keeps the previous call's contents: each
+ * call clears its arrival counters on `stream` first, so two calls whose GPU
+ * work can overlap (for example calls on different streams) race on the
+ * array; issue such calls one after the other.  A decode whose scratch would exceed the array is rejected with
+ * C2KV_EINVAL before anything is enqueued.
+ */
+c2kv_status c2kv_attend_decode_noalloc(const c2kv_geometry* geom, int32_t layer,
+                                       int32_t batch, void* const* k_caches,
+                                       void* const* v_caches, int32_t cap,
+                                       const int32_t* n_cached_dev, const int32_t* pos_dev,
+                                       int32_t max_keys, const void* q, const void* k_new,
+                                       const void* v_new, void* out, void* stream);
+
 /* Adds `delta` to n_cached_dev[b] and pos_dev[b] for b < batch (device kernel). */
 c2kv_status c2kv_seq_advance(int32_t batch, int32_t* n_cached_dev, int32_t* pos_dev,
                              int32_t delta, void* stream);
