@@ -288,7 +288,7 @@ def run_ours(args, rank: int, world: int) -> dict:
             decode_all()
     torch.cuda.synchronize()
     assert P.c2kv_device_error() == P.C2KV_OK
-    launches_per_step = (bt.batch * min(L, 4) + (2 * L if Q else 0) + T * (L + 1))
+    launches_per_step = (bt.batch * (1 + min(L, 4)) + (2 * L if Q else 0) + T * (L + 1))
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
 

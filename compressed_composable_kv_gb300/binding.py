@@ -50,17 +50,19 @@ _SIGNATURES = {
     "c2kv_store_segments": (_i32, [_vp, _i32, _pi32, _pi32, _pi32, _i32, _pvp, _pvp]),
     "c2kv_store_lookup": (_i32, [_vp, _i32, _pi32, _pi32, _pi32]),
     "c2kv_plan": (_i32, [_i32, _pi32, _pi32, _pi32, _pi32, _pi32, _pi32, _pi32]),
-    "c2kv_compose": (_i32, [_vp, _i32, _pi32, _pi32, _i32, _vp, _vp, _i32, _vp, _pi32, _pi32, _vp]),
+    "c2kv_compose": (_i32, [_vp, _i32, _pi32, _pi32, _i32, _vp, _vp, _i32, _vp, _vp, _pi32, _pi32, _vp]),
+    "c2kv_rope_table_bytes": (_sz, [_pg, _i32]),
+    "c2kv_rope_table": (_i32, [_pg, _vp, _i32, _vp, _vp]),
     "c2kv_attend_workspace_size": (_sz, [_pg, _i32, _i32, _i32]),
     "c2kv_masked_extra_bytes": (_sz, [_pg, _i32]),
     "c2kv_workspace_init": (_i32, [_vp, _sz, _vp]),
-    "c2kv_attend_prefill": (_i32, [_pg, _i32, _i32, _pvp, _pvp, _i32, _pi32, _pi32, _i32,
+    "c2kv_attend_prefill": (_i32, [_pg, _i32, _i32, _pvp, _pvp, _pvp, _i32, _pi32, _i32,
                                    _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
-    "c2kv_attend_decode": (_i32, [_pg, _i32, _i32, _pvp, _pvp, _i32, _vp, _vp, _i32,
+    "c2kv_attend_decode": (_i32, [_pg, _i32, _i32, _pvp, _pvp, _pvp, _i32, _vp, _i32,
                                   _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
-    "c2kv_attend_decode_noalloc": (_i32, [_pg, _i32, _i32, _pvp, _pvp, _i32, _vp, _vp, _i32,
+    "c2kv_attend_decode_noalloc": (_i32, [_pg, _i32, _i32, _pvp, _pvp, _pvp, _i32, _vp, _i32,
                                           _vp, _vp, _vp, _vp, _vp]),
-    "c2kv_seq_advance": (_i32, [_i32, _vp, _vp, _i32, _vp]),
+    "c2kv_seq_advance": (_i32, [_i32, _vp, _i32, _vp]),
     "c2kv_attend_masked": (_i32, [_pg, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "c2kv_device_error": (_i32, [_pi32]),
 }
@@ -183,15 +185,28 @@ def c2kv_plan(n_tokens: Sequence[int], n_slots: Sequence[int], order: Optional[S
 
 
 def c2kv_compose(store: int, doc_ids, order, k: int, k_cache: torch.Tensor, v_cache: torch.Tensor,
-                 cap: int, pos_dev_out: Optional[torch.Tensor] = None, stream=None):
-    """Returns (n_slots, next_pos)."""
+                 cap: int, rope_table: torch.Tensor, pos_dev_out: Optional[torch.Tensor] = None, stream=None):
+    """Returns (n_slots, next_pos).  rope_table: device buffer of
+    c2kv_rope_table_bytes(geom, cap) bytes (any dtype)."""
     ns, nxt = ctypes.c_int32(), ctypes.c_int32()
     _check(load_library().c2kv_compose(
         store, len(doc_ids), _i32arr(doc_ids), None if order is None else _i32arr(order), int(k),
         _dev(k_cache, torch.bfloat16, "k_cache"), _dev(v_cache, torch.bfloat16, "v_cache"), int(cap),
-        _dev(pos_dev_out, torch.int32, "pos_dev_out"), ctypes.byref(ns), ctypes.byref(nxt),
-        _stream(stream)))
+        _dev(rope_table, None, "rope_table"), _dev(pos_dev_out, torch.int32, "pos_dev_out"),
+        ctypes.byref(ns), ctypes.byref(nxt), _stream(stream)))
     return ns.value, nxt.value
+
+
+def c2kv_rope_table_bytes(geom, rows: int) -> int:
+    g = as_geometry(geom)
+    return int(load_library().c2kv_rope_table_bytes(ctypes.byref(g), int(rows)))
+
+
+def c2kv_rope_table(geom, pos_dev: torch.Tensor, table_out: torch.Tensor, stream=None) -> None:
+    g = as_geometry(geom)
+    _check(load_library().c2kv_rope_table(ctypes.byref(g), _dev(pos_dev, torch.int32, "pos_dev"),
+                                          pos_dev.numel(), _dev(table_out, None, "table_out"),
+                                          _stream(stream)))
 
 
 def c2kv_attend_workspace_size(geom, batch: int, t_len: int, max_keys: int) -> int:
@@ -214,7 +229,11 @@ def _ptrs(ts, name):
     return (ctypes.c_void_p * len(ts))(*[_dev(t, torch.bfloat16, name) for t in ts])
 
 
-def c2kv_attend_prefill(geom, layer: int, k_caches, v_caches, cap: int, n_cached, start_pos,
+def _tabs(ts):
+    return (ctypes.c_void_p * len(ts))(*[_dev(t, None, "rope_table") for t in ts])
+
+
+def c2kv_attend_prefill(geom, layer: int, k_caches, v_caches, rope_tables, cap: int, n_cached,
                         q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, out: torch.Tensor,
                         workspace: Optional[torch.Tensor], stream=None) -> None:
     g = as_geometry(geom)
@@ -222,29 +241,27 @@ def c2kv_attend_prefill(geom, layer: int, k_caches, v_caches, cap: int, n_cached
     q_len = q.shape[1]
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load_library().c2kv_attend_prefill(
-        ctypes.byref(g), int(layer), B, _ptrs(k_caches, "k_cache"), _ptrs(v_caches, "v_cache"), int(cap),
-        _i32arr(n_cached), _i32arr(start_pos), int(q_len), _dev(q, torch.bfloat16, "q"),
+        ctypes.byref(g), int(layer), B, _ptrs(k_caches, "k_cache"), _ptrs(v_caches, "v_cache"),
+        _tabs(rope_tables), int(cap), _i32arr(n_cached), int(q_len), _dev(q, torch.bfloat16, "q"),
         _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
         _dev(out, torch.bfloat16, "out"), _dev(workspace, None, "workspace"), ws, _stream(stream)))
 
 
-def c2kv_attend_decode(geom, layer: int, k_caches, v_caches, cap: int, n_cached_dev: torch.Tensor,
-                       pos_dev: torch.Tensor, max_keys: int, q: torch.Tensor, k_new: torch.Tensor,
-                       v_new: torch.Tensor, out: torch.Tensor, workspace: Optional[torch.Tensor],
-                       stream=None) -> None:
+def c2kv_attend_decode(geom, layer: int, k_caches, v_caches, rope_tables, cap: int, n_cached_dev: torch.Tensor,
+                       max_keys: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                       out: torch.Tensor, workspace: Optional[torch.Tensor], stream=None) -> None:
     g = as_geometry(geom)
     B = len(k_caches)
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load_library().c2kv_attend_decode(
-        ctypes.byref(g), int(layer), B, _ptrs(k_caches, "k_cache"), _ptrs(v_caches, "v_cache"), int(cap),
-        _dev(n_cached_dev, torch.int32, "n_cached_dev"), _dev(pos_dev, torch.int32, "pos_dev"),
-        int(max_keys), _dev(q, torch.bfloat16, "q"), _dev(k_new, torch.bfloat16, "k_new"),
-        _dev(v_new, torch.bfloat16, "v_new"), _dev(out, torch.bfloat16, "out"),
-        _dev(workspace, None, "workspace"), ws, _stream(stream)))
+        ctypes.byref(g), int(layer), B, _ptrs(k_caches, "k_cache"), _ptrs(v_caches, "v_cache"),
+        _tabs(rope_tables), int(cap), _dev(n_cached_dev, torch.int32, "n_cached_dev"), int(max_keys),
+        _dev(q, torch.bfloat16, "q"), _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
+        _dev(out, torch.bfloat16, "out"), _dev(workspace, None, "workspace"), ws, _stream(stream)))
 
 
-def c2kv_attend_decode_noalloc(geom, layer: int, k_caches, v_caches, cap: int, n_cached_dev: torch.Tensor,
-                               pos_dev: torch.Tensor, max_keys: int, q: torch.Tensor, k_new: torch.Tensor,
+def c2kv_attend_decode_noalloc(geom, layer: int, k_caches, v_caches, rope_tables, cap: int,
+                               n_cached_dev: torch.Tensor, max_keys: int, q: torch.Tensor, k_new: torch.Tensor,
                                v_new: torch.Tensor, out: torch.Tensor, stream=None) -> None:
     """c2kv_attend_decode for callers that cannot allocate device memory: the
     split-K scratch is the library's own fixed 4 MiB device array (shared by
@@ -252,15 +269,15 @@ def c2kv_attend_decode_noalloc(geom, layer: int, k_caches, v_caches, cap: int, n
     g = as_geometry(geom)
     B = len(k_caches)
     _check(load_library().c2kv_attend_decode_noalloc(
-        ctypes.byref(g), int(layer), B, _ptrs(k_caches, "k_cache"), _ptrs(v_caches, "v_cache"), int(cap),
-        _dev(n_cached_dev, torch.int32, "n_cached_dev"), _dev(pos_dev, torch.int32, "pos_dev"),
-        int(max_keys), _dev(q, torch.bfloat16, "q"), _dev(k_new, torch.bfloat16, "k_new"),
-        _dev(v_new, torch.bfloat16, "v_new"), _dev(out, torch.bfloat16, "out"), _stream(stream)))
+        ctypes.byref(g), int(layer), B, _ptrs(k_caches, "k_cache"), _ptrs(v_caches, "v_cache"),
+        _tabs(rope_tables), int(cap), _dev(n_cached_dev, torch.int32, "n_cached_dev"), int(max_keys),
+        _dev(q, torch.bfloat16, "q"), _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
+        _dev(out, torch.bfloat16, "out"), _stream(stream)))
 
 
-def c2kv_seq_advance(n_cached_dev: torch.Tensor, pos_dev: torch.Tensor, delta: int = 1, stream=None) -> None:
+def c2kv_seq_advance(n_cached_dev: torch.Tensor, delta: int = 1, stream=None) -> None:
     _check(load_library().c2kv_seq_advance(n_cached_dev.numel(), _dev(n_cached_dev, torch.int32),
-                                           _dev(pos_dev, torch.int32), int(delta), _stream(stream)))
+                                           int(delta), _stream(stream)))
 
 
 def c2kv_attend_masked(geom, mask: int, n_doc: int, n_slot: int, k: int, q: torch.Tensor,

@@ -269,12 +269,12 @@ c2kv_status run_prefill_tc(const c2kv_geometry* g, int batch, const void* const*
   return C2KV_OK;
 }
 
+// tabs[b]: per-row cos/sin table of sequence b (token t at row n_cached + t).
 c2kv_status run_attention(const c2kv_geometry* g, int batch, const __nv_bfloat16* const* kb,
-                          const __nv_bfloat16* const* vb, const int32_t* n_cached_h, const int32_t* pos_h,
-                          const int32_t* n_cached_d, const int32_t* pos_d, int cap, int max_keys, int t_len,
-                          int pos_mode, int mask_mode, int n_doc, int kblk, const void* q, void* out,
-                          void* workspace, size_t workspace_bytes, cudaStream_t st,
-                          const void* fused_k_new = nullptr, const void* fused_v_new = nullptr) {
+                          const __nv_bfloat16* const* vb, const CosSin2* const* tabs, const int32_t* n_cached_h,
+                          const int32_t* n_cached_d, int cap, int max_keys, int t_len, int mask_mode, int n_doc,
+                          int kblk, const void* q, void* out, void* workspace, size_t workspace_bytes,
+                          cudaStream_t st, const void* fused_k_new = nullptr, const void* fused_v_new = nullptr) {
   unsigned* err = nullptr;
   int sms = 0;
   c2kv_status s = device_state(&err, &sms);
@@ -287,11 +287,10 @@ c2kv_status run_attention(const c2kv_geometry* g, int batch, const __nv_bfloat16
   for (int b = 0; b < batch; ++b) {
     p.k_base[b] = kb[b];
     p.v_base[b] = vb[b];
+    p.tab[b] = tabs[b];
     p.n_cached_h[b] = n_cached_h ? n_cached_h[b] : 0;
-    p.pos_h[b] = pos_h ? pos_h[b] : 0;
   }
   p.n_cached_d = n_cached_d;
-  p.pos_d = pos_d;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.out = static_cast<__nv_bfloat16*>(out);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -307,7 +306,6 @@ c2kv_status run_attention(const c2kv_geometry* g, int batch, const __nv_bfloat16
   p.max_keys = max_keys;
   p.num_splits = w.num_splits;
   p.split_keys = w.split_keys;
-  p.pos_mode = pos_mode;
   p.mask_mode = mask_mode;
   p.n_doc = n_doc;
   p.kblk = kblk;
@@ -315,15 +313,14 @@ c2kv_status run_attention(const c2kv_geometry* g, int batch, const __nv_bfloat16
   p.k_new = static_cast<const __nv_bfloat16*>(fused_k_new);
   p.v_new = static_cast<const __nv_bfloat16*>(fused_v_new);
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)g->head_dim));
-  fill_inv_freq(g, p.inv_freq);
   C2KV_CUDA(launch_attention(p, g->head_dim, g->n_q_heads / g->n_kv_heads, st));
   return C2KV_OK;
 }
 
 c2kv_status run_append(const c2kv_geometry* g, int batch, __nv_bfloat16* const* kd, __nv_bfloat16* const* vd,
-                       const int32_t* row_h, const int32_t* pos_h, const int32_t* row_d, const int32_t* pos_d,
-                       int cap, int t_len, int pos_mode, int n_doc, int kblk, const void* k_src,
-                       const void* v_src, cudaStream_t st, const void* q_src = nullptr, void* q_dst = nullptr) {
+                       const CosSin2* const* tabs, const int32_t* row_h, const int32_t* row_d, int cap, int t_len,
+                       const void* k_src, const void* v_src, cudaStream_t st, const void* q_src = nullptr,
+                       void* q_dst = nullptr) {
   unsigned* err = nullptr;
   c2kv_status s = device_state(&err, nullptr);
   if (s != C2KV_OK) return s;
@@ -332,11 +329,10 @@ c2kv_status run_append(const c2kv_geometry* g, int batch, __nv_bfloat16* const* 
   for (int b = 0; b < batch; ++b) {
     p.k_dst[b] = kd[b];
     p.v_dst[b] = vd[b];
+    p.tab[b] = tabs[b];
     p.row_h[b] = row_h ? row_h[b] : 0;
-    p.pos_h[b] = pos_h ? pos_h[b] : 0;
   }
   p.row_d = row_d;
-  p.pos_d = pos_d;
   p.k_src = static_cast<const __nv_bfloat16*>(k_src);
   p.v_src = static_cast<const __nv_bfloat16*>(v_src);
   p.q_src = static_cast<const __nv_bfloat16*>(q_src);
@@ -346,13 +342,11 @@ c2kv_status run_append(const c2kv_geometry* g, int batch, __nv_bfloat16* const* 
   p.n_kv = g->n_kv_heads;
   p.n_q = g->n_q_heads;
   p.cap = cap;
-  p.pos_mode = pos_mode;
-  p.n_doc = n_doc;
-  p.kblk = kblk;
-  fill_inv_freq(g, p.inv_freq);
   C2KV_CUDA(launch_append(p, g->head_dim, batch, st));
   return C2KV_OK;
 }
+
+size_t table_bytes(const c2kv_geometry* g, int rows) { return (size_t)rows * (g->head_dim / 2) * sizeof(CosSin2); }
 
 c2kv_status check_caches(int batch, void* const* kc, void* const* vc, int cap) {
   if (batch < 1 || batch > kMaxBatch) return fail(C2KV_EINVAL, "batch must be in [1, 16]");
@@ -478,8 +472,8 @@ c2kv_status c2kv_plan(int32_t n_docs, const int32_t* n_tokens, const int32_t* n_
 }
 
 c2kv_status c2kv_compose(c2kv_store st, int32_t n_docs, const int32_t* doc_ids, const int32_t* order, int32_t k,
-                         void* k_cache, void* v_cache, int32_t cap, int32_t* pos_dev_out, int32_t* n_slots_out,
-                         int32_t* next_pos_out, void* stream) {
+                         void* k_cache, void* v_cache, int32_t cap, void* rope_table_out, int32_t* pos_dev_out,
+                         int32_t* n_slots_out, int32_t* next_pos_out, void* stream) {
   if (st == nullptr) return fail(C2KV_EINVAL, "store is null");
   if (n_docs < 0 || n_docs > kMaxDocsPerCompose)
     return fail(C2KV_EINVAL, "n_docs must be in [0, " + std::to_string(kMaxDocsPerCompose) + "]");
@@ -506,11 +500,14 @@ c2kv_status c2kv_compose(c2kv_store st, int32_t n_docs, const int32_t* doc_ids, 
   if (s != C2KV_OK) return s;
   if (total > cap)
     return fail(C2KV_ECAPACITY, "composed slots " + std::to_string(total) + " exceed cap " + std::to_string(cap));
+  if ((int64_t)l_tot + (cap - total) > INT32_MAX / 2) return fail(C2KV_EINVAL, "positions overflow int32");
   if (n_slots_out) *n_slots_out = total;
   if (next_pos_out) *next_pos_out = l_tot;
-  if (total == 0) return C2KV_OK;
-  if (k_cache == nullptr || v_cache == nullptr) return fail(C2KV_EINVAL, "cache pointer is null");
-  if (!aligned16(k_cache) || !aligned16(v_cache)) return fail(C2KV_EINVAL, "cache pointers must be 16-byte aligned");
+  if (cap == 0) return C2KV_OK;
+  if (rope_table_out == nullptr) return fail(C2KV_EINVAL, "rope_table_out is null");
+  if (total > 0 && (k_cache == nullptr || v_cache == nullptr)) return fail(C2KV_EINVAL, "cache pointer is null");
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(rope_table_out))
+    return fail(C2KV_EINVAL, "cache and table pointers must be 16-byte aligned");
   int dev = -1;
   C2KV_CUDA(cudaGetDevice(&dev));
   if (dev != st->device) return fail(C2KV_EINVAL, "current device differs from the store's device");
@@ -521,29 +518,51 @@ c2kv_status c2kv_compose(c2kv_store st, int32_t n_docs, const int32_t* doc_ids, 
   cudaStream_t us = static_cast<cudaStream_t>(stream);
   const int D = g.head_dim, H = g.n_kv_heads, L = g.n_layers;
   const size_t elem = 2;
+  CosSin2* tab = static_cast<CosSin2*>(rope_table_out);
+
+  // Copies run on the store's stream after the caller's earlier work.
+  C2KV_CUDA(cudaEventRecord(st->fork, us));
+  C2KV_CUDA(cudaStreamWaitEvent(st->side, st->fork, 0));
+
+  // The cos/sin table of every cache row is built on the caller's stream
+  // while the first copies are in flight.
+  static TableParams tp;   // large (segment table); guarded by the store mutex and g_tab_mu
+  static std::mutex g_tab_mu;
+  {
+    std::lock_guard<std::mutex> tl(g_tab_mu);
+    std::memset(&tp, 0, sizeof(tp));
+    tp.tab = tab;
+    tp.pos_out = pos_dev_out;
+    tp.rows = cap;
+    tp.half = D / 2;
+    tp.mode = kTableComposed;
+    tp.n_total = total;
+    tp.l_tot = l_tot;
+    tp.k = k;
+    tp.n_docs = n_docs;
+    fill_inv_freq(&g, tp.inv_freq);
+    for (int c = 0; c < n_docs; ++c) {
+      const int d = order ? order[c] : c;
+      tp.seg[c].slot0 = slot0[c];
+      tp.seg[c].n_slots = nsl[d];
+      tp.seg[c].off = off[c];
+      tp.seg[c].n_tokens = ntok[d];
+    }
+    C2KV_CUDA(launch_rope_table(tp, us));
+  }
+  if (total == 0) return C2KV_OK;
+
   RopeParams rp;
   std::memset(&rp, 0, sizeof(rp));
   rp.k_cache = static_cast<__nv_bfloat16*>(k_cache);
-  rp.pos_out = pos_dev_out;
+  rp.tab = tab;
   rp.err = err;
   rp.cap = cap;
   rp.n_kv = H;
   rp.n_total = total;
-  rp.k = k;
-  rp.n_docs = n_docs;
-  fill_inv_freq(&g, rp.inv_freq);
-  for (int c = 0; c < n_docs; ++c) {
-    const int d = order ? order[c] : c;
-    rp.seg[c].slot0 = slot0[c];
-    rp.seg[c].n_slots = nsl[d];
-    rp.seg[c].off = off[c];
-    rp.seg[c].n_tokens = ntok[d];
-  }
 
-  // Copies run on the store's stream after the caller's earlier work; each
-  // layer group's re-rotation runs on the caller's stream once it has landed.
-  C2KV_CUDA(cudaEventRecord(st->fork, us));
-  C2KV_CUDA(cudaStreamWaitEvent(st->side, st->fork, 0));
+  // Each layer group's re-rotation runs on the caller's stream once its
+  // copies have landed (and after the table, which is earlier on that stream).
   const int ngroups = std::min(L, kLayerGroups);
   uint8_t* kc = static_cast<uint8_t*>(k_cache);
   uint8_t* vc = static_cast<uint8_t*>(v_cache);
@@ -571,6 +590,33 @@ c2kv_status c2kv_compose(c2kv_store st, int32_t n_docs, const int32_t* doc_ids, 
   return C2KV_OK;
 }
 
+size_t c2kv_rope_table_bytes(const c2kv_geometry* geom, int32_t rows) {
+  if (check_geom(geom) != C2KV_OK || rows < 0) return 0;
+  return table_bytes(geom, rows);
+}
+
+c2kv_status c2kv_rope_table(const c2kv_geometry* geom, const int32_t* pos_dev, int32_t rows, void* table_out,
+                            void* stream) {
+  c2kv_status s = check_geom(geom);
+  if (s != C2KV_OK) return s;
+  if (rows < 0) return fail(C2KV_EINVAL, "rows < 0");
+  if (rows == 0) return C2KV_OK;
+  if (pos_dev == nullptr || table_out == nullptr) return fail(C2KV_EINVAL, "null pointer");
+  if (!aligned16(table_out)) return fail(C2KV_EINVAL, "table_out must be 16-byte aligned");
+  s = device_state(nullptr, nullptr);
+  if (s != C2KV_OK) return s;
+  TableParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.tab = static_cast<CosSin2*>(table_out);
+  p.pos_in = pos_dev;
+  p.rows = rows;
+  p.half = geom->head_dim / 2;
+  p.mode = kTableExplicit;
+  fill_inv_freq(geom, p.inv_freq);
+  C2KV_CUDA(launch_rope_table(p, static_cast<cudaStream_t>(stream)));
+  return C2KV_OK;
+}
+
 size_t c2kv_attend_workspace_size(const c2kv_geometry* geom, int32_t batch, int32_t t_len, int32_t max_keys) {
   if (check_geom(geom) != C2KV_OK || batch < 1 || t_len < 1 || max_keys < 1) return 0;
   const AttnWs w = attn_workspace(geom, batch, t_len, max_keys, sm_count_for_sizing());
@@ -579,7 +625,7 @@ size_t c2kv_attend_workspace_size(const c2kv_geometry* geom, int32_t batch, int3
 
 size_t c2kv_masked_extra_bytes(const c2kv_geometry* geom, int32_t n_tokens) {
   if (check_geom(geom) != C2KV_OK || n_tokens < 1) return 0;
-  return 2 * align256((size_t)geom->n_kv_heads * n_tokens * geom->head_dim * 2);
+  return 2 * align256((size_t)geom->n_kv_heads * n_tokens * geom->head_dim * 2) + align256(table_bytes(geom, n_tokens));
 }
 
 c2kv_status c2kv_workspace_init(void* workspace, size_t bytes, void* stream) {
@@ -590,8 +636,8 @@ c2kv_status c2kv_workspace_init(void* workspace, size_t bytes, void* stream) {
 }
 
 c2kv_status c2kv_attend_prefill(const c2kv_geometry* geom, int32_t layer, int32_t batch, void* const* k_caches,
-                                void* const* v_caches, int32_t cap, const int32_t* n_cached,
-                                const int32_t* start_pos, int32_t q_len, const void* q, const void* k_new,
+                                void* const* v_caches, const void* const* rope_tables, int32_t cap,
+                                const int32_t* n_cached, int32_t q_len, const void* q, const void* k_new,
                                 const void* v_new, void* out, void* workspace, size_t workspace_bytes,
                                 void* stream) {
   c2kv_status s = check_geom(geom);
@@ -600,16 +646,18 @@ c2kv_status c2kv_attend_prefill(const c2kv_geometry* geom, int32_t layer, int32_
   s = check_caches(batch, k_caches, v_caches, cap);
   if (s != C2KV_OK) return s;
   if (q_len < 1) return fail(C2KV_EINVAL, "q_len must be >= 1");
-  if (!n_cached || !start_pos) return fail(C2KV_EINVAL, "n_cached / start_pos is null");
+  if (!n_cached || !rope_tables) return fail(C2KV_EINVAL, "n_cached / rope_tables is null");
   if (!q || !k_new || !v_new || !out) return fail(C2KV_EINVAL, "null tensor pointer");
   if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new))
     return fail(C2KV_EINVAL, "q / k_new / v_new must be 16-byte aligned");
   int max_keys = 0;
+  const CosSin2* tabs[kMaxBatch];
   for (int b = 0; b < batch; ++b) {
-    if (n_cached[b] < 0 || start_pos[b] < 0) return fail(C2KV_EINVAL, "negative n_cached / start_pos");
+    if (n_cached[b] < 0) return fail(C2KV_EINVAL, "negative n_cached");
     if ((int64_t)n_cached[b] + q_len > cap)
       return fail(C2KV_ECAPACITY, "n_cached + q_len exceeds cap for sequence " + std::to_string(b));
-    if ((int64_t)start_pos[b] + q_len > INT32_MAX / 2) return fail(C2KV_EINVAL, "position overflows int32");
+    if (rope_tables[b] == nullptr || !aligned16(rope_tables[b])) return fail(C2KV_EINVAL, "bad rope table pointer");
+    tabs[b] = static_cast<const CosSin2*>(rope_tables[b]);
     max_keys = std::max(max_keys, n_cached[b] + q_len);
   }
   const size_t lstride = (size_t)geom->n_kv_heads * cap * geom->head_dim;
@@ -621,11 +669,10 @@ c2kv_status c2kv_attend_prefill(const c2kv_geometry* geom, int32_t layer, int32_
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (q_len == 1) {
-    s = run_append(geom, batch, kb, vb, n_cached, start_pos, nullptr, nullptr, cap, 1, kPosSequential, 0, 0,
-                   k_new, v_new, st);
+    s = run_append(geom, batch, kb, vb, tabs, n_cached, nullptr, cap, 1, k_new, v_new, st);
     if (s != C2KV_OK) return s;
-    return run_attention(geom, batch, kb, vb, n_cached, start_pos, nullptr, nullptr, cap, max_keys, 1,
-                         kPosSequential, kMaskCausal, 0, 0, q, out, workspace, workspace_bytes, st);
+    return run_attention(geom, batch, kb, vb, tabs, n_cached, nullptr, cap, max_keys, 1, kMaskCausal, 0, 0, q, out,
+                         workspace, workspace_bytes, st);
   }
   int sms = 0;
   s = device_state(nullptr, &sms);
@@ -634,8 +681,7 @@ c2kv_status c2kv_attend_prefill(const c2kv_geometry* geom, int32_t layer, int32_
   if (workspace == nullptr || workspace_bytes < w.total)
     return fail(C2KV_EINVAL, "workspace too small: need " + std::to_string(w.total) + " bytes");
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  s = run_append(geom, batch, kb, vb, n_cached, start_pos, nullptr, nullptr, cap, q_len, kPosSequential, 0, 0,
-                 k_new, v_new, st, q, ws + w.qrot_off);
+  s = run_append(geom, batch, kb, vb, tabs, n_cached, nullptr, cap, q_len, k_new, v_new, st, q, ws + w.qrot_off);
   if (s != C2KV_OK) return s;
   const void* k0[kMaxBatch];
   const void* v0[kMaxBatch];
@@ -650,8 +696,8 @@ c2kv_status c2kv_attend_prefill(const c2kv_geometry* geom, int32_t layer, int32_
 }
 
 c2kv_status c2kv_attend_decode(const c2kv_geometry* geom, int32_t layer, int32_t batch, void* const* k_caches,
-                               void* const* v_caches, int32_t cap, const int32_t* n_cached_dev,
-                               const int32_t* pos_dev, int32_t max_keys, const void* q, const void* k_new,
+                               void* const* v_caches, const void* const* rope_tables, int32_t cap,
+                               const int32_t* n_cached_dev, int32_t max_keys, const void* q, const void* k_new,
                                const void* v_new, void* out, void* workspace, size_t workspace_bytes,
                                void* stream) {
   c2kv_status s = check_geom(geom);
@@ -659,7 +705,7 @@ c2kv_status c2kv_attend_decode(const c2kv_geometry* geom, int32_t layer, int32_t
   if (layer < 0 || layer >= geom->n_layers) return fail(C2KV_EINVAL, "layer out of range");
   s = check_caches(batch, k_caches, v_caches, cap);
   if (s != C2KV_OK) return s;
-  if (!n_cached_dev || !pos_dev) return fail(C2KV_EINVAL, "device length arrays are null");
+  if (!n_cached_dev || !rope_tables) return fail(C2KV_EINVAL, "n_cached_dev / rope_tables is null");
   if (max_keys < 1 || max_keys > cap) return fail(C2KV_EINVAL, "max_keys must be in [1, cap]");
   if (!q || !k_new || !v_new || !out) return fail(C2KV_EINVAL, "null tensor pointer");
   if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new))
@@ -667,20 +713,23 @@ c2kv_status c2kv_attend_decode(const c2kv_geometry* geom, int32_t layer, int32_t
   const size_t lstride = (size_t)geom->n_kv_heads * cap * geom->head_dim;
   __nv_bfloat16* kb[kMaxBatch];
   __nv_bfloat16* vb[kMaxBatch];
+  const CosSin2* tabs[kMaxBatch];
   for (int b = 0; b < batch; ++b) {
+    if (rope_tables[b] == nullptr || !aligned16(rope_tables[b])) return fail(C2KV_EINVAL, "bad rope table pointer");
+    tabs[b] = static_cast<const CosSin2*>(rope_tables[b]);
     kb[b] = static_cast<__nv_bfloat16*>(k_caches[b]) + layer * lstride;
     vb[b] = static_cast<__nv_bfloat16*>(v_caches[b]) + layer * lstride;
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // One launch: the kernel rotates and stores the new key/value itself.
-  return run_attention(geom, batch, kb, vb, nullptr, nullptr, n_cached_dev, pos_dev, cap, max_keys, 1,
-                       kPosSequential, kMaskCausal, 0, 0, q, out, workspace, workspace_bytes, st, k_new, v_new);
+  return run_attention(geom, batch, kb, vb, tabs, nullptr, n_cached_dev, cap, max_keys, 1, kMaskCausal, 0, 0, q, out,
+                       workspace, workspace_bytes, st, k_new, v_new);
 }
 
-c2kv_status c2kv_seq_advance(int32_t batch, int32_t* n_cached_dev, int32_t* pos_dev, int32_t delta, void* stream) {
+c2kv_status c2kv_seq_advance(int32_t batch, int32_t* n_cached_dev, int32_t delta, void* stream) {
   if (batch < 1 || batch > 32) return fail(C2KV_EINVAL, "batch must be in [1, 32]");
-  if (!n_cached_dev || !pos_dev) return fail(C2KV_EINVAL, "null device array");
-  C2KV_CUDA(launch_advance(batch, n_cached_dev, pos_dev, delta, static_cast<cudaStream_t>(stream)));
+  if (!n_cached_dev) return fail(C2KV_EINVAL, "null device array");
+  C2KV_CUDA(launch_advance(batch, n_cached_dev, delta, static_cast<cudaStream_t>(stream)));
   return C2KV_OK;
 }
 
@@ -703,27 +752,42 @@ c2kv_status c2kv_attend_masked(const c2kv_geometry* geom, int32_t mask, int32_t 
   if (workspace_bytes < align256(attn_bytes) + extra)
     return fail(C2KV_EINVAL, "workspace too small: need " + std::to_string(align256(attn_bytes) + extra));
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t kv_bytes = align256((size_t)geom->n_kv_heads * N * geom->head_dim * 2);
   __nv_bfloat16* krot = reinterpret_cast<__nv_bfloat16*>(ws + align256(attn_bytes));
-  __nv_bfloat16* vt = reinterpret_cast<__nv_bfloat16*>(ws + align256(attn_bytes) + extra / 2);
+  __nv_bfloat16* vt = reinterpret_cast<__nv_bfloat16*>(ws + align256(attn_bytes) + kv_bytes);
+  CosSin2* tab = reinterpret_cast<CosSin2*>(ws + align256(attn_bytes) + 2 * kv_bytes);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int32_t zero = 0;
+  s = device_state(nullptr, nullptr);
+  if (s != C2KV_OK) return s;
+  // Rows are the sequence's tokens: extraction positions (documents at
+  // 0..n_doc-1, slot s at min((s+1)k, n_doc) - 1), or t for the causal mask.
   const int kblk = mask == C2KV_MASK_STRUCTURED ? k : 1;
-  const int pos_mode = mask == C2KV_MASK_STRUCTURED ? kPosExtraction : kPosSequential;
+  TableParams tp;
+  std::memset(&tp, 0, sizeof(tp));
+  tp.tab = tab;
+  tp.rows = N;
+  tp.half = geom->head_dim / 2;
+  tp.mode = kTableExtraction;
+  tp.n_doc = mask == C2KV_MASK_STRUCTURED ? n_doc : N;
+  tp.kblk = kblk;
+  fill_inv_freq(geom, tp.inv_freq);
+  C2KV_CUDA(launch_rope_table(tp, st));
+  const int32_t zero = 0;
+  const CosSin2* tabs[1] = {tab};
   const int mmode = mask == C2KV_MASK_STRUCTURED ? kMaskStructured : kMaskCausal;
   if (N == 1) {
-    s = run_append(geom, 1, &krot, &vt, &zero, &zero, nullptr, nullptr, N, N, pos_mode, n_doc, kblk, kk, v, st);
+    s = run_append(geom, 1, &krot, &vt, tabs, &zero, nullptr, N, N, kk, v, st);
     if (s != C2KV_OK) return s;
     const __nv_bfloat16* kb = krot;
     const __nv_bfloat16* vb = vt;
-    return run_attention(geom, 1, &kb, &vb, &zero, &zero, nullptr, nullptr, N, N, N, pos_mode, mmode, n_doc,
-                         kblk, q, out, workspace, attn_bytes, st);
+    return run_attention(geom, 1, &kb, &vb, tabs, &zero, nullptr, N, N, N, mmode, n_doc, kblk, q, out, workspace,
+                         attn_bytes, st);
   }
   int sms = 0;
   s = device_state(nullptr, &sms);
   if (s != C2KV_OK) return s;
   const AttnWs w = attn_workspace(geom, 1, N, N, sms);
-  s = run_append(geom, 1, &krot, &vt, &zero, &zero, nullptr, nullptr, N, N, pos_mode, n_doc, kblk, kk, v, st, q,
-                 ws + w.qrot_off);
+  s = run_append(geom, 1, &krot, &vt, tabs, &zero, nullptr, N, N, kk, v, st, q, ws + w.qrot_off);
   if (s != C2KV_OK) return s;
   const void* k0 = krot;
   const void* v0 = vt;
@@ -786,10 +850,10 @@ c2kv_status noalloc_scratch(uint8_t** out) {
 }  // namespace
 
 extern "C" c2kv_status c2kv_attend_decode_noalloc(const c2kv_geometry* geom, int32_t layer, int32_t batch,
-                                                  void* const* k_caches, void* const* v_caches, int32_t cap,
-                                                  const int32_t* n_cached_dev, const int32_t* pos_dev,
-                                                  int32_t max_keys, const void* q, const void* k_new,
-                                                  const void* v_new, void* out, void* stream) {
+                                                  void* const* k_caches, void* const* v_caches,
+                                                  const void* const* rope_tables, int32_t cap,
+                                                  const int32_t* n_cached_dev, int32_t max_keys, const void* q,
+                                                  const void* k_new, const void* v_new, void* out, void* stream) {
   // The same argument checks as c2kv_attend_decode, done before anything is
   // enqueued (the counter clear below included).
   c2kv_status s = check_geom(geom);
@@ -797,7 +861,7 @@ extern "C" c2kv_status c2kv_attend_decode_noalloc(const c2kv_geometry* geom, int
   if (layer < 0 || layer >= geom->n_layers) return fail(C2KV_EINVAL, "layer out of range");
   s = check_caches(batch, k_caches, v_caches, cap);
   if (s != C2KV_OK) return s;
-  if (!n_cached_dev || !pos_dev) return fail(C2KV_EINVAL, "device length arrays are null");
+  if (!n_cached_dev || !rope_tables) return fail(C2KV_EINVAL, "n_cached_dev / rope_tables is null");
   if (max_keys < 1 || max_keys > cap) return fail(C2KV_EINVAL, "max_keys must be in [1, cap]");
   if (!q || !k_new || !v_new || !out) return fail(C2KV_EINVAL, "null tensor pointer");
   int sms = 0;
@@ -816,6 +880,6 @@ extern "C" c2kv_status c2kv_attend_decode_noalloc(const c2kv_geometry* geom, int
   // The array keeps whatever the previous call left in it; the arrival
   // counters must start at zero, the partial results need no clearing.
   if (w.num_splits > 1) C2KV_CUDA(cudaMemsetAsync(scratch + w.counters_off, 0, w.ml_off - w.counters_off, st));
-  return c2kv_attend_decode(geom, layer, batch, k_caches, v_caches, cap, n_cached_dev, pos_dev, max_keys, q,
+  return c2kv_attend_decode(geom, layer, batch, k_caches, v_caches, rope_tables, cap, n_cached_dev, max_keys, q,
                             k_new, v_new, out, scratch, kNoallocScratchBytes, stream);
 }

@@ -52,11 +52,6 @@ struct Cfg {
   static_assert(KPG >= 1 && KPG * GPT == T, "tile must split evenly over key groups");
 };
 
-__device__ __forceinline__ int token_position(const AttnParams& p, int pos0, int tok) {
-  if (p.pos_mode == kPosSequential) return pos0 + tok;
-  return tok < p.n_doc ? tok : min((tok - p.n_doc + 1) * p.kblk, p.n_doc) - 1;
-}
-
 // Extra visibility of the structured mask beyond causality (section
 // "structured information flow"): slot i sees document tokens of the sink
 // block [0, k) and of its own block [i*k, min((i+1)k, n_doc)) only.
@@ -90,7 +85,6 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
   const int n_tb = (p.t_len + C::TPC - 1) / C::TPC;
 
   const int n_cached = p.n_cached_d ? p.n_cached_d[b] : p.n_cached_h[b];
-  const int pos0 = p.pos_d ? p.pos_d[b] : p.pos_h[b];
   if (n_cached < 0 || n_cached + p.t_len > p.cap || n_cached + p.t_len > p.max_keys) {
     // Uniform over every CTA of sequence b: nobody touches its counters.
     if (tid == 0 && split == 0 && blockIdx.y == 0) atomicOr(p.err, kErrLength);
@@ -119,11 +113,15 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
     mbar_init(inj, TPR);
     fence_barrier_init();
   }
+  // cos/sin of each token's position: row n_cached + t of the sequence's table
+  // (hi parts rotate q; the full pairs rotate the new key when fused).
   for (int i = tid; i < ntok * (D / 2); i += kThreads) {
     const int t = i / (D / 2), f = i % (D / 2);
-    rope_cos_sin(token_position(p, pos0, tok0 + t), p.inv_freq[f], &cs[i], &sn[i]);
+    const CosSin2 e = p.tab[b][(size_t)(n_cached + tok0 + t) * (D / 2) + f];
+    cs[i] = e.ch;
+    sn[i] = e.sh;
+    if (has_new && t == 0) tab2[f] = e;
   }
-  if (has_new && tid < D / 2) tab2[tid] = rope_cos_sin2(pos0, p.inv_freq[tid]);
   __syncthreads();
 
   const __nv_bfloat16* kg = p.k_base[b] + (size_t)h * p.cap * D;

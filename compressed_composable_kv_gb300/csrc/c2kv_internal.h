@@ -26,19 +26,12 @@ constexpr long long kWaitCycles = 4000000000LL;
 // The angle pos * inv_freq is formed in fp64 and reduced modulo 2*pi with a
 // two-constant Cody-Waite reduction (2*pi split into its fp64 value and the
 // fp64 remainder), so the reduced angle is accurate to ~1e-11 rad even at
-// positions past 1e5; cos/sin of the reduced angle (|r| <= pi) then use the
-// fp32 library routine.
+// positions past 1e5.  GB300's fp64 rate is a small fraction of its fp32
+// rate, so only the table kernel evaluates this; every other kernel reads
+// the table.
 constexpr double kTwoPiHi = 6.283185307179586;
 constexpr double kTwoPiLo = 2.4492935982947064e-16;
 constexpr double kInvTwoPi = 0.15915494309189535;
-
-__device__ __forceinline__ void rope_cos_sin(int pos, double inv_freq, float* c, float* s) {
-  const double a = (double)pos * inv_freq;
-  const double n = rint(a * kInvTwoPi);
-  double r = fma(-n, kTwoPiHi, a);
-  r = fma(-n, kTwoPiLo, r);
-  sincosf((float)r, s, c);
-}
 
 // cos/sin of one angle as unevaluated fp32 pairs (hi + lo), from the fp64
 // library sincos of the reduced angle: ~2^-48 accurate, enough to round a
@@ -197,12 +190,24 @@ struct SegDesc {
 
 struct RopeParams {
   __nv_bfloat16* k_cache;   // [L][Hkv][cap][d]
-  int32_t* pos_out;         // optional [cap]
+  const CosSin2* tab;       // [cap][d/2]: cos/sin of every cache row's position
   unsigned* err;
-  int32_t cap, n_kv, layer0, layer1, n_total, k, n_docs;
+  int32_t cap, n_kv, layer0, layer1, n_total;
+};
+
+// Builds the per-row cos/sin table (the only kernel that calls fp64 sincos).
+struct TableParams {
+  CosSin2* tab;              // [rows][d/2]
+  int32_t* pos_out;          // optional [rows]
+  const int32_t* pos_in;     // kTableExplicit: positions of the rows
+  int32_t rows, half, mode;
+  int32_t n_total, l_tot, k, n_docs;   // kTableComposed
+  int32_t n_doc, kblk;                 // kTableExtraction
   double inv_freq[kMaxHalfDim];
   SegDesc seg[kMaxDocsPerCompose];
 };
+
+enum TableMode : int32_t { kTableComposed = 0, kTableExplicit = 1, kTableExtraction = 2 };
 
 enum PosMode : int32_t { kPosSequential = 0, kPosExtraction = 1 };
 enum MaskMode : int32_t { kMaskCausal = 0, kMaskStructured = 1 };
@@ -210,17 +215,15 @@ enum MaskMode : int32_t { kMaskCausal = 0, kMaskStructured = 1 };
 struct AppendParams {
   __nv_bfloat16* k_dst[kMaxBatch];   // layer base [Hkv][cap][d]
   __nv_bfloat16* v_dst[kMaxBatch];
+  const CosSin2* tab[kMaxBatch];     // per-row cos/sin table of each sequence
   int32_t row_h[kMaxBatch];          // first destination row (host value) ...
-  int32_t pos_h[kMaxBatch];          // ... and first position
-  const int32_t* row_d;              // or device values (decode)
-  const int32_t* pos_d;
+  const int32_t* row_d;              // ... or device values (decode)
   const __nv_bfloat16* k_src;        // [B][t_len][Hkv][d]
   const __nv_bfloat16* v_src;
   const __nv_bfloat16* q_src;        // optional [B][t_len][Hq][d], rotated into ...
   __nv_bfloat16* q_dst;              // ... [B][Hkv][t_len][G][d]
   unsigned* err;
-  int32_t t_len, n_kv, n_q, cap, pos_mode, n_doc, kblk;
-  double inv_freq[kMaxHalfDim];
+  int32_t t_len, n_kv, n_q, cap;
 };
 
 // Tensor-core prefill: Q from the rotated-q scratch, K/V from 3-D maps
@@ -242,10 +245,10 @@ struct PrefillTcParams {
 struct AttnParams {
   const __nv_bfloat16* k_base[kMaxBatch];   // layer base [Hkv][cap][d]
   const __nv_bfloat16* v_base[kMaxBatch];
+  const CosSin2* tab[kMaxBatch];            // per-row cos/sin table: token t of
+                                            // sequence b sits at row n_cached + t
   int32_t n_cached_h[kMaxBatch];
-  int32_t pos_h[kMaxBatch];
   const int32_t* n_cached_d;   // device lengths (decode) or null
-  const int32_t* pos_d;
   const __nv_bfloat16* q;      // [B][t_len][Hq][d]
   __nv_bfloat16* out;          // [B][t_len][Hq][d]
   float* part_o;               // [B][t_len][Hkv][S][G][d]
@@ -254,21 +257,21 @@ struct AttnParams {
   unsigned* err;
   int32_t batch, t_len, n_q, n_kv, cap, max_keys;
   int32_t num_splits, split_keys;
-  int32_t pos_mode, mask_mode, n_doc, kblk;
+  int32_t mask_mode, n_doc, kblk;
   // Decode with the append fused in: the new token's k (pre-RoPE) and v,
-  // [B][Hkv][d]; the key is rotated at pos, stored at row n_cached and used.
+  // [B][Hkv][d]; the key is rotated, stored at row n_cached and used.
   int32_t fuse_append;
   const __nv_bfloat16* k_new;
   const __nv_bfloat16* v_new;
   float scale_log2;
-  double inv_freq[kMaxHalfDim];
 };
 
 // Launchers (return cudaGetLastError()).
 cudaError_t launch_rerope(const RopeParams& p, int head_dim, cudaStream_t st);
+cudaError_t launch_rope_table(const TableParams& p, cudaStream_t st);
 cudaError_t launch_append(const AppendParams& p, int head_dim, int batch, cudaStream_t st);
 cudaError_t launch_attention(const AttnParams& p, int head_dim, int group, cudaStream_t st);
-cudaError_t launch_advance(int batch, int32_t* n_cached, int32_t* pos, int delta, cudaStream_t st);
+cudaError_t launch_advance(int batch, int32_t* n_cached, int delta, cudaStream_t st);
 
 cudaError_t launch_prefill_tc(const PrefillTcParams& p, int head_dim, int group, cudaStream_t st);
 int prefill_tc_tokens_per_tile(int group);

@@ -13,11 +13,44 @@ namespace c2kv {
 namespace {
 
 // ---------------------------------------------------------------------------
+// Per-row cos/sin table: for every cache row r, the d/2 angles of its
+// position as fp32 hi/lo pairs of the fp64 sincos.  Composed mode: rows below
+// n_total are composed slots (slot j of composed document c at
+// off_c + min((j+1)k, n_c) - 1, found by binary search over the segment
+// table); later rows are the appended question and answer tokens at
+// l_tot + (r - n_total).  Explicit mode reads positions from pos_in;
+// extraction mode puts n_doc document tokens at 0..n_doc-1 and slot s at
+// min((s+1)k, n_doc) - 1.  One thread per (row, frequency).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int table_position(const TableParams& p, int r) {
+  if (p.mode == kTableExplicit) return p.pos_in[r];
+  if (p.mode == kTableExtraction) return r < p.n_doc ? r : min((r - p.n_doc + 1) * p.kblk, p.n_doc) - 1;
+  if (r >= p.n_total) return p.l_tot + (r - p.n_total);
+  int lo = 0, hi = p.n_docs - 1;   // last segment with seg.slot0 <= r
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.seg[mid].slot0 <= r) lo = mid; else hi = mid - 1;
+  }
+  const SegDesc sd = p.seg[lo];
+  return sd.off + min((r - sd.slot0 + 1) * p.k, sd.n_tokens) - 1;
+}
+
+__global__ void rope_table_kernel(const __grid_constant__ TableParams p) {
+  const int total = p.rows * p.half;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    const int r = i / p.half, f = i % p.half;
+    const int pos = table_position(p, r);
+    if (f == 0 && p.pos_out != nullptr) p.pos_out[r] = pos;
+    p.tab[i] = rope_cos_sin2(pos, p.inv_freq[f]);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // K1: in-place re-rotation of composed K rows for a group of layers.
-// One CTA owns kSlots consecutive composed slots: it derives their positions
-// from the segment table, builds their cos/sin table in shared memory once,
-// and rotates those slots' rows in every (layer, kv head) of the group with
-// 16-byte loads/stores.  V rows are never touched (they land by DMA).
+// One CTA owns kSlots consecutive composed slots: it stages their rows of
+// the cos/sin table in shared memory once and rotates those slots' rows in
+// every (layer, kv head) of the group with 16-byte loads/stores.  V rows are
+// never touched (they land by DMA).
 // ---------------------------------------------------------------------------
 constexpr int kSlots = 32;
 constexpr int kRopeThreads = 256;
@@ -27,31 +60,10 @@ __global__ void __launch_bounds__(kRopeThreads) rerope_kernel(const __grid_const
   constexpr int H = D / 2;
   constexpr int TPR = H / 8;   // threads per row, each owns 8 pairs
   __shared__ CosSin2 tab[kSlots][H];
-  __shared__ int spos[kSlots];
 
   const int slot0 = blockIdx.x * kSlots;
   const int n_here = min(kSlots, p.n_total - slot0);
-  if (threadIdx.x < kSlots) {
-    const int slot = slot0 + threadIdx.x;
-    int pos = -1;
-    if (threadIdx.x < n_here) {
-      int lo = 0, hi = p.n_docs - 1;   // last segment with seg.slot0 <= slot
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (p.seg[mid].slot0 <= slot) lo = mid; else hi = mid - 1;
-      }
-      const SegDesc sd = p.seg[lo];
-      const int j = slot - sd.slot0;
-      pos = sd.off + min((j + 1) * p.k, sd.n_tokens) - 1;
-      if (p.pos_out != nullptr && p.layer0 == 0) p.pos_out[slot] = pos;
-    }
-    spos[threadIdx.x] = pos;
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < n_here * H; i += kRopeThreads) {
-    const int r = i / H, f = i % H;
-    tab[r][f] = rope_cos_sin2(spos[r], p.inv_freq[f]);
-  }
+  for (int i = threadIdx.x; i < n_here * H; i += kRopeThreads) tab[i / H][i % H] = p.tab[(size_t)slot0 * H + i];
   __syncthreads();
 
   const int n_rows = (p.layer1 - p.layer0) * p.n_kv;   // (layer, head) row blocks
@@ -92,8 +104,9 @@ __global__ void __launch_bounds__(kRopeThreads) rerope_kernel(const __grid_const
 
 // ---------------------------------------------------------------------------
 // K4: rotate t_len new keys per sequence and append them (with their values)
-// at rows row0 + i of the cache.  grid (t_len, batch), one thread per
-// (kv head, 8-pair chunk).
+// at rows row0 + i of the cache, rotating with the table row of that cache
+// row.  Threads past the kv heads rotate q into the tensor-core tile layout.
+// grid (t_len, batch), one thread per (head, 8-pair chunk).
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void append_kernel(const __grid_constant__ AppendParams p) {
@@ -103,23 +116,15 @@ __global__ void append_kernel(const __grid_constant__ AppendParams p) {
   const int i = blockIdx.x;
   const int b = blockIdx.y;
   const int row0 = p.row_d ? p.row_d[b] : p.row_h[b];
-  const int pos0 = p.pos_d ? p.pos_d[b] : p.pos_h[b];
   if (row0 < 0 || row0 + p.t_len > p.cap) {
     if (threadIdx.x == 0 && i == 0) atomicOr(p.err, kErrLength);
     return;
   }
-  int pos;
-  if (p.pos_mode == kPosSequential) {
-    pos = pos0 + i;
-  } else {   // extraction: documents at 0..n_doc-1, slot s at min((s+1)k, n_doc)-1
-    pos = (i < p.n_doc) ? i : min((i - p.n_doc + 1) * p.kblk, p.n_doc) - 1;
-  }
-  for (int f = threadIdx.x; f < H; f += blockDim.x) tab[f] = rope_cos_sin2(pos, p.inv_freq[f]);
+  for (int f = threadIdx.x; f < H; f += blockDim.x) tab[f] = p.tab[b][(size_t)(row0 + i) * H + f];
   __syncthreads();
   const int h = threadIdx.x / TPR;
   const int c = threadIdx.x % TPR;
   if (h >= p.n_kv) {
-    // threads past the kv heads rotate q head hq into [B][Hkv][t_len][G][d]
     const int hq = h - p.n_kv;
     if (p.q_src == nullptr || hq >= p.n_q) return;
     const int grp = p.n_q / p.n_kv;
@@ -146,12 +151,9 @@ __global__ void append_kernel(const __grid_constant__ AppendParams p) {
   vd[c + TPR] = vs[c + TPR];
 }
 
-__global__ void advance_kernel(int batch, int32_t* n_cached, int32_t* pos, int delta) {
+__global__ void advance_kernel(int batch, int32_t* n_cached, int delta) {
   const int b = threadIdx.x;
-  if (b < batch) {
-    n_cached[b] += delta;
-    pos[b] += delta;
-  }
+  if (b < batch) n_cached[b] += delta;
 }
 
 }  // namespace
@@ -172,8 +174,16 @@ cudaError_t launch_append(const AppendParams& p, int head_dim, int batch, cudaSt
   return cudaGetLastError();
 }
 
-cudaError_t launch_advance(int batch, int32_t* n_cached, int32_t* pos, int delta, cudaStream_t st) {
-  advance_kernel<<<1, 32, 0, st>>>(batch, n_cached, pos, delta);
+cudaError_t launch_advance(int batch, int32_t* n_cached, int delta, cudaStream_t st) {
+  advance_kernel<<<1, 32, 0, st>>>(batch, n_cached, delta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_table(const TableParams& p, cudaStream_t st) {
+  const int total = p.rows * p.half;
+  if (total == 0) return cudaSuccess;
+  const int blocks = (total + 255) / 256;
+  rope_table_kernel<<<blocks, 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 

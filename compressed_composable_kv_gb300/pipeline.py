@@ -50,8 +50,10 @@ class RequestBatch:
         self.v_caches = [torch.empty_like(t) for t in self.k_caches]
         self.pos = [torch.full((self.cap,), -1, dtype=torch.int32, device=device)
                     for _ in range(self.batch)]
+        tb = B.c2kv_rope_table_bytes(geom, self.cap)
+        self.rope_tables = [torch.empty(tb // 4, dtype=torch.float32, device=device)
+                            for _ in range(self.batch)]
         self.n_cached_dev = torch.zeros(self.batch, dtype=torch.int32, device=device)
-        self.pos_dev = torch.zeros(self.batch, dtype=torch.int32, device=device)
         self.max_keys_decode = max(self.n_slots) + q_len + decode_steps
         ws = 256
         if q_len > 0:
@@ -60,29 +62,27 @@ class RequestBatch:
         self.workspace = torch.zeros(ws, dtype=torch.uint8, device=device)
         B.c2kv_workspace_init(self.workspace)
         self._dec_start = torch.tensor([n + q_len for n in self.n_slots], dtype=torch.int32)
-        self._pos_start = torch.tensor([lt + q_len for lt in self.l_tot], dtype=torch.int32)
 
     def compose(self, stream=None) -> None:
         for b, r in enumerate(self.requests):
             n, nxt = B.c2kv_compose(self.store, r.doc_ids, r.order, self.k, self.k_caches[b],
-                                    self.v_caches[b], self.cap, self.pos[b], stream)
+                                    self.v_caches[b], self.cap, self.rope_tables[b], self.pos[b], stream)
             assert n == self.n_slots[b] and nxt == self.l_tot[b]
 
     def prefill(self, layer: int, q, k_new, v_new, out, stream=None) -> None:
-        B.c2kv_attend_prefill(self.geom, layer, self.k_caches, self.v_caches, self.cap, self.n_slots,
-                              self.l_tot, q, k_new, v_new, out, self.workspace, stream)
+        B.c2kv_attend_prefill(self.geom, layer, self.k_caches, self.v_caches, self.rope_tables, self.cap,
+                              self.n_slots, q, k_new, v_new, out, self.workspace, stream)
 
     def reset_decode(self, stream=None) -> None:
         """Point the device lengths at the first decode step (after the question)."""
         s = torch.cuda.current_stream() if stream is None else stream
         with torch.cuda.stream(s):
             self.n_cached_dev.copy_(self._dec_start, non_blocking=True)
-            self.pos_dev.copy_(self._pos_start, non_blocking=True)
 
     def decode(self, layer: int, q, k_new, v_new, out, stream=None) -> None:
-        B.c2kv_attend_decode(self.geom, layer, self.k_caches, self.v_caches, self.cap, self.n_cached_dev,
-                             self.pos_dev, self.max_keys_decode, q, k_new, v_new, out, self.workspace,
+        B.c2kv_attend_decode(self.geom, layer, self.k_caches, self.v_caches, self.rope_tables, self.cap,
+                             self.n_cached_dev, self.max_keys_decode, q, k_new, v_new, out, self.workspace,
                              stream)
 
     def advance(self, stream=None) -> None:
-        B.c2kv_seq_advance(self.n_cached_dev, self.pos_dev, 1, stream)
+        B.c2kv_seq_advance(self.n_cached_dev, 1, stream)

@@ -32,8 +32,9 @@
  *     [n_layers][n_kv_heads][cap][head_dim] bf16 (one contiguous key run per
  *     layer and kv head).  q head h reads kv head h / (n_q_heads/n_kv_heads).
  *   - RoPE is the rotate-half form with inv_freq_i = rope_theta^(-2i/d);
- *     angles are formed in fp64, rotations are done in fp32 and rotated keys
- *     are stored rounded to nearest even.
+ *     angles are formed and reduced in fp64 (once per cache row, into a RoPE
+ *     table); stored keys are rotated in double-float arithmetic on the fp32
+ *     pipe and rounded once to bf16 (nearest even).
  *   - A kernel that finds a device-side problem (a bounded wait that expired,
  *     a device length beyond the cache capacity) records it in a device error
  *     word and skips the affected output; c2kv_device_error() reads it.
@@ -148,19 +149,40 @@ c2kv_status c2kv_plan(int32_t n_docs, const int32_t* n_tokens,
  * k every document was stored with.  k_cache/v_cache: caller-owned device
  * buffers [n_layers][n_kv_heads][cap][head_dim] bf16; rows [0, N) of every
  * layer and kv head are written (N = total slots), rows >= N are untouched.
- * pos_dev_out: optional device int32 [cap] receiving the N slot positions.
- * Host outputs (optional): *n_slots_out = N, *next_pos_out = total original
- * tokens (where the question starts).
+ * rope_table_out (required): caller-owned device buffer of
+ * c2kv_rope_table_bytes(geom, cap) bytes receiving, for every cache row r,
+ * the cos/sin of its position for the head_dim/2 RoPE frequencies as fp32
+ * (hi, lo) pairs, layout [cap][head_dim/2][cos_hi, cos_lo, sin_hi, sin_lo].
+ * Row r < N holds slot r's position; row r >= N holds L_tot + (r - N), the
+ * position of the (r-N)-th token appended after the documents (reading: the
+ * question starts right after the documents' original length L_tot).
+ * Prefill and decode rotate with this table.
+ * pos_dev_out: optional device int32 [cap] receiving the position of every row.
+ * Host outputs (optional): *n_slots_out = N, *next_pos_out = L_tot.
  * The segments are copied host->device on the store's copy stream in layer
- * groups; the re-rotation of each group runs on `stream` once its copy has
- * landed, and all of it is ordered before later work on `stream`.  The store
- * must not be destroyed before that work completes.
+ * groups; the table and the re-rotation of each group run on `stream` (the
+ * latter once its copy has landed), and all of it is ordered before later
+ * work on `stream`.  The store must not be destroyed before that work
+ * completes.
  * Errors: C2KV_EINVAL, C2KV_ENOTFOUND, C2KV_ECAPACITY (N > cap), C2KV_ECUDA.
  */
 c2kv_status c2kv_compose(c2kv_store store, int32_t n_docs, const int32_t* doc_ids,
                          const int32_t* order, int32_t k, void* k_cache,
-                         void* v_cache, int32_t cap, int32_t* pos_dev_out,
-                         int32_t* n_slots_out, int32_t* next_pos_out, void* stream);
+                         void* v_cache, int32_t cap, void* rope_table_out,
+                         int32_t* pos_dev_out, int32_t* n_slots_out,
+                         int32_t* next_pos_out, void* stream);
+
+/* Bytes of a RoPE table of `rows` rows: rows * (head_dim/2) * 16. */
+size_t c2kv_rope_table_bytes(const c2kv_geometry* geom, int32_t rows);
+
+/*
+ * Builds a RoPE table (layout as in c2kv_compose) for arbitrary positions:
+ * row r gets the cos/sin of position pos_dev[r] (device int32 [rows]), for
+ * caches filled by other means than c2kv_compose.  Angles pos * inv_freq are
+ * formed in fp64 and reduced mod 2*pi before the fp64 sincos.
+ */
+c2kv_status c2kv_rope_table(const c2kv_geometry* geom, const int32_t* pos_dev,
+                            int32_t rows, void* table_out, void* stream);
 
 /*
  * Device scratch (bytes) that c2kv_attend_prefill / c2kv_attend_decode /
@@ -179,29 +201,30 @@ c2kv_status c2kv_workspace_init(void* workspace, size_t bytes, void* stream);
 /*
  * Question prefill for one layer of `batch` requests.
  * [EXPL] "pipeline": after composition the question is appended and
- * generation starts; reading: question token i of request b sits at position
- * start_pos[b] + i (start_pos = the composed original length).
+ * generation starts.
  *
  * k_caches[b], v_caches[b]: host array of device pointers to request b's
  * cache base (layer 0, layout as above); `layer` selects the layer.
- * n_cached[b] (host): rows already in the cache; start_pos[b] (host).
+ * rope_tables[b]: host array of device pointers to request b's RoPE table
+ * (from c2kv_compose).  n_cached[b] (host): rows already in the cache.
  * q: device [batch][q_len][n_q_heads][head_dim] (before RoPE);
  * k_new, v_new: device [batch][q_len][n_kv_heads][head_dim] (k before RoPE).
- * The new keys are rotated and appended at rows n_cached[b] + i together
- * with the values; then out[b][i] = softmax(q_i K^T / sqrt(d)) V over the
- * n_cached[b] + i + 1 visible keys (all cached rows plus question tokens
- * 0..i), written to device out [batch][q_len][n_q_heads][head_dim] bf16.
+ * Question token i lands at row n_cached[b] + i and is rotated with that
+ * row of the table (q and k alike); then out[b][i] = softmax(q_i K^T /
+ * sqrt(d)) V over the n_cached[b] + i + 1 visible keys (all cached rows plus
+ * question tokens 0..i), written to device out [batch][q_len][n_q_heads]
+ * [head_dim] bf16.  q_len > 1 runs QK^T and PV on the tcgen05 tensor cores.
  * workspace: device scratch of c2kv_attend_workspace_size(geom, batch,
  * q_len, max_b(n_cached[b] + q_len)) bytes, zeroed once.
  * Errors: C2KV_EINVAL, C2KV_ECAPACITY (n_cached[b] + q_len > cap), C2KV_ECUDA.
  */
 c2kv_status c2kv_attend_prefill(const c2kv_geometry* geom, int32_t layer,
                                 int32_t batch, void* const* k_caches,
-                                void* const* v_caches, int32_t cap,
-                                const int32_t* n_cached, const int32_t* start_pos,
-                                int32_t q_len, const void* q, const void* k_new,
-                                const void* v_new, void* out, void* workspace,
-                                size_t workspace_bytes, void* stream);
+                                void* const* v_caches, const void* const* rope_tables,
+                                int32_t cap, const int32_t* n_cached, int32_t q_len,
+                                const void* q, const void* k_new, const void* v_new,
+                                void* out, void* workspace, size_t workspace_bytes,
+                                void* stream);
 
 /*
  * One decode step for one layer of `batch` sequences.  [EXPL] "results":
@@ -209,23 +232,24 @@ c2kv_status c2kv_attend_prefill(const c2kv_geometry* geom, int32_t layer,
  *
  * As prefill with one new token per sequence, except that the lengths live
  * on the device so a captured sequence of calls can be replayed:
- * n_cached_dev[b] (device int32) rows are cached, the new token is appended
- * at row n_cached_dev[b] and rotated at position pos_dev[b] (device int32),
- * and attends over n_cached_dev[b] + 1 keys.  max_keys (host) bounds
- * n_cached_dev[b] + 1 for every b and sizes the grid; a device length over
- * max_keys or cap is recorded in the device error word and that sequence's
- * output is skipped.  q: [batch][n_q_heads][head_dim]; k_new, v_new:
- * [batch][n_kv_heads][head_dim]; out: [batch][n_q_heads][head_dim].
- * The lengths are not advanced (see c2kv_seq_advance).
+ * n_cached_dev[b] (device int32) rows are cached; the new token's key is
+ * rotated with table row n_cached_dev[b], stored with its value at that row,
+ * and the token attends over n_cached_dev[b] + 1 keys -- all in one kernel
+ * launch.  max_keys (host) bounds n_cached_dev[b] + 1 for every b and sizes
+ * the grid; a device length over max_keys or cap is recorded in the device
+ * error word and that sequence's output is skipped.
+ * q: [batch][n_q_heads][head_dim]; k_new, v_new: [batch][n_kv_heads]
+ * [head_dim]; out: [batch][n_q_heads][head_dim].  The lengths are not
+ * advanced (see c2kv_seq_advance).
  * workspace: c2kv_attend_workspace_size(geom, batch, 1, max_keys) bytes.
  */
 c2kv_status c2kv_attend_decode(const c2kv_geometry* geom, int32_t layer,
                                int32_t batch, void* const* k_caches,
-                               void* const* v_caches, int32_t cap,
-                               const int32_t* n_cached_dev, const int32_t* pos_dev,
-                               int32_t max_keys, const void* q, const void* k_new,
-                               const void* v_new, void* out, void* workspace,
-                               size_t workspace_bytes, void* stream);
+                               void* const* v_caches, const void* const* rope_tables,
+                               int32_t cap, const int32_t* n_cached_dev, int32_t max_keys,
+                               const void* q, const void* k_new, const void* v_new,
+                               void* out, void* workspace, size_t workspace_bytes,
+                               void* stream);
 
 /*
  * c2kv_attend_decode without a workspace argument: the paper has no
@@ -245,19 +269,19 @@ c2kv_status c2kv_attend_decode(const c2kv_geometry* geom, int32_t layer,
  * array is shared by every call and keeps the previous call's contents: each
  * call clears its arrival counters on `stream` first, so two calls whose GPU
  * work can overlap (for example calls on different streams) race on the
- * array; issue such calls one after the other.  A decode whose scratch would exceed the array is rejected with
- * C2KV_EINVAL before anything is enqueued.
+ * array; issue such calls one after the other.  A decode whose scratch would
+ * exceed the array is rejected with C2KV_EINVAL before anything is enqueued.
  */
 c2kv_status c2kv_attend_decode_noalloc(const c2kv_geometry* geom, int32_t layer,
                                        int32_t batch, void* const* k_caches,
-                                       void* const* v_caches, int32_t cap,
-                                       const int32_t* n_cached_dev, const int32_t* pos_dev,
+                                       void* const* v_caches, const void* const* rope_tables,
+                                       int32_t cap, const int32_t* n_cached_dev,
                                        int32_t max_keys, const void* q, const void* k_new,
                                        const void* v_new, void* out, void* stream);
 
-/* Adds `delta` to n_cached_dev[b] and pos_dev[b] for b < batch (device kernel). */
-c2kv_status c2kv_seq_advance(int32_t batch, int32_t* n_cached_dev, int32_t* pos_dev,
-                             int32_t delta, void* stream);
+/* Adds `delta` to n_cached_dev[b] for b < batch (device kernel). */
+c2kv_status c2kv_seq_advance(int32_t batch, int32_t* n_cached_dev, int32_t delta,
+                             void* stream);
 
 /*
  * Attention over one extraction sequence under a mask (the "mask mode").
@@ -271,7 +295,8 @@ c2kv_status c2kv_seq_advance(int32_t batch, int32_t* n_cached_dev, int32_t* pos_
  * q: device [N][n_q_heads][head_dim], kk, v: device [N][n_kv_heads][head_dim]
  * with N = n_doc + n_slot, all before RoPE; out: device [N][n_q_heads][d].
  * workspace: c2kv_attend_workspace_size(geom, 1, N, N) + c2kv_masked_extra_bytes
- * (geom, N) bytes (rotated keys and values are staged there), zeroed once.
+ * (geom, N) bytes (the sequence's RoPE table and its rotated keys and values
+ * are staged there), zeroed once.
  */
 c2kv_status c2kv_attend_masked(const c2kv_geometry* geom, int32_t mask,
                                int32_t n_doc, int32_t n_slot, int32_t k,

@@ -142,7 +142,8 @@ def test_compose_orders_repeats_and_ragged_docs():
     N = bt.n_slots[0]
     kt = torch.empty((2, 2, N, 128), dtype=torch.bfloat16, device="cuda")
     vt = torch.empty_like(kt)
-    n, nxt = P.c2kv_compose(sc.store, *requests[0], 4, kt, vt, N)
+    tab = torch.empty(P.c2kv_rope_table_bytes(g, N) // 4, dtype=torch.float32, device="cuda")
+    n, nxt = P.c2kv_compose(sc.store, *requests[0], 4, kt, vt, N, tab)
     torch.cuda.synchronize()
     assert n == N
     assert torch.equal(kt, bt.k_caches[0][:, :, :N]) and torch.equal(vt, bt.v_caches[0][:, :, :N])
@@ -270,17 +271,18 @@ def test_host_side_errors():
     sc = Scenario(g, 4, [(1, 40, 10), (2, 8, 2)], [([1, 2], None)], q_len=4, decode_steps=2)
     kc = torch.empty((1, 2, 16, 128), dtype=torch.bfloat16, device="cuda")
     vc = torch.empty_like(kc)
+    tab = torch.empty(P.c2kv_rope_table_bytes(g, 16) // 4, dtype=torch.float32, device="cuda")
     with pytest.raises(P.C2KVError) as e:
-        P.c2kv_compose(sc.store, [1, 2], None, 4, kc, vc, 11)
+        P.c2kv_compose(sc.store, [1, 2], None, 4, kc, vc, 11, tab)
     assert e.value.status == P.C2KV_ECAPACITY
     with pytest.raises(P.C2KVError) as e:
-        P.c2kv_compose(sc.store, [1, 99], None, 4, kc, vc, 16)
+        P.c2kv_compose(sc.store, [1, 99], None, 4, kc, vc, 16, tab)
     assert e.value.status == P.C2KV_ENOTFOUND
     with pytest.raises(P.C2KVError) as e:
-        P.c2kv_compose(sc.store, [1, 2], None, 8, kc, vc, 16)
+        P.c2kv_compose(sc.store, [1, 2], None, 8, kc, vc, 16, tab)
     assert e.value.status == P.C2KV_EINVAL
     with pytest.raises(P.C2KVError) as e:
-        P.c2kv_compose(sc.store, [1, 2], [1, 1], 4, kc, vc, 16)
+        P.c2kv_compose(sc.store, [1, 2], [1, 1], 4, kc, vc, 16, tab)
     assert e.value.status == P.C2KV_EINVAL
     with pytest.raises(P.C2KVError) as e:
         P.c2kv_store_segments(sc.store, [1], [40], [10], 4, [sc.docs[1].k_pre], [sc.docs[1].v])
@@ -289,11 +291,11 @@ def test_host_side_errors():
     q = torch.zeros((1, 5, 8, 128), dtype=torch.bfloat16, device="cuda")
     kn = torch.zeros((1, 5, 2, 128), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(P.C2KVError) as e:
-        P.c2kv_attend_prefill(g, 0, bt.k_caches, bt.v_caches, bt.cap, [bt.cap - 2], [0], q, kn, kn,
+        P.c2kv_attend_prefill(g, 0, bt.k_caches, bt.v_caches, bt.rope_tables, bt.cap, [bt.cap - 2], q, kn, kn,
                               torch.empty_like(q), bt.workspace)
     assert e.value.status == P.C2KV_ECAPACITY
     with pytest.raises(P.C2KVError) as e:
-        P.c2kv_attend_prefill(g, 1, bt.k_caches, bt.v_caches, bt.cap, [0], [0], q, kn, kn,
+        P.c2kv_attend_prefill(g, 1, bt.k_caches, bt.v_caches, bt.rope_tables, bt.cap, [0], q, kn, kn,
                               torch.empty_like(q), bt.workspace)
     assert e.value.status == P.C2KV_EINVAL
     sc.close()
@@ -331,3 +333,19 @@ def test_prefill_group_sizes_and_ragged_tiles(hq, hkv, d, q_len):
     pre, dec = run_all(sc, upload(inputs))
     check_request(sc, inputs, pre, dec, 0, layers=[0], steps=[0, 1])
     sc.close()
+
+
+def test_rope_table_matches_fp64_angles():
+    """The per-row cos/sin table (hi + lo fp32 pairs) against the oracle's fp64
+    cos/sin of pos * theta^(-2i/d), at positions up to ~1.3e5."""
+    for g in (S.Geometry(1, 32, 8, 128, 5.0e5), S.Geometry(1, 4, 2, 64, 1.0e4)):
+        pos = np.array([0, 1, 3, 7, 403, 32000, 99991, 131071, 131072 + 255], dtype=np.int32)
+        tab = torch.empty(P.c2kv_rope_table_bytes(g, len(pos)) // 4, dtype=torch.float32, device="cuda")
+        P.c2kv_rope_table(g, torch.from_numpy(pos).cuda(), tab)
+        torch.cuda.synchronize()
+        t = tab.cpu().numpy().astype(np.float64).reshape(len(pos), g.head_dim // 2, 4)
+        ang = pos.astype(np.float64)[:, None] * O.rope_inv_freq(g.rope_theta, g.head_dim)[None, :]
+        assert np.abs(t[..., 0] + t[..., 1] - np.cos(ang)).max() < 1e-12
+        assert np.abs(t[..., 2] + t[..., 3] - np.sin(ang)).max() < 1e-12
+        # the hi parts alone are the fp32-rounded values
+        assert np.abs(t[..., 0] - np.cos(ang)).max() < 1e-7

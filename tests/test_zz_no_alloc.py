@@ -35,12 +35,12 @@ def test_noalloc_decode_matches_workspace_decode_on_two_calls():
     kn = to_dev(S.normal_bf16(rng, (2, 8, 128)))
     vn = to_dev(S.normal_bf16(rng, (2, 8, 128)))
     ref = torch.empty_like(q)
-    P.c2kv_attend_decode(g, 0, bt.k_caches, bt.v_caches, bt.cap, bt.n_cached_dev, bt.pos_dev,
+    P.c2kv_attend_decode(g, 0, bt.k_caches, bt.v_caches, bt.rope_tables, bt.cap, bt.n_cached_dev,
                          bt.max_keys_decode, q, kn, vn, ref, bt.workspace)
     outs = []
     for _ in range(2):
         o = torch.full_like(q, float("nan"))
-        P.c2kv_attend_decode_noalloc(g, 0, bt.k_caches, bt.v_caches, bt.cap, bt.n_cached_dev, bt.pos_dev,
+        P.c2kv_attend_decode_noalloc(g, 0, bt.k_caches, bt.v_caches, bt.rope_tables, bt.cap, bt.n_cached_dev,
                                      bt.max_keys_decode, q, kn, vn, o)
         outs.append(o)
     torch.cuda.synchronize()
@@ -57,7 +57,7 @@ def test_noalloc_decode_rejects_bad_arguments_before_enqueueing():
     q = torch.zeros((1, 32, 128), dtype=torch.bfloat16, device="cuda")
     kn = torch.zeros((1, 8, 128), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(P.C2KVError) as e:
-        P.c2kv_attend_decode_noalloc(g, 0, bt.k_caches, bt.v_caches, bt.cap, bt.n_cached_dev, bt.pos_dev,
+        P.c2kv_attend_decode_noalloc(g, 0, bt.k_caches, bt.v_caches, bt.rope_tables, bt.cap, bt.n_cached_dev,
                                      bt.cap + 1, q, kn, kn, torch.empty_like(q))
     assert e.value.status == P.C2KV_EINVAL
     sc.close()
