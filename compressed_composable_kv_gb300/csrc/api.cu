@@ -158,7 +158,7 @@ AttnWs attn_workspace(const c2kv_geometry* g, int batch, int t_len, int max_keys
   const int grp = g->n_q_heads / g->n_kv_heads;
   if (t_len == 1) {
     w.n_tb = 1;
-    attn_plan_splits(batch * g->n_kv_heads, max_keys, num_sms, &w.num_splits, &w.split_keys);
+    attn_plan_splits(batch * g->n_kv_heads, max_keys, num_sms, grp, &w.num_splits, &w.split_keys);
   } else {
     const int tok = prefill_tc_tokens_per_tile(grp);
     const int kt = prefill_tc_key_tile();

@@ -1,4 +1,4 @@
-// Split-K flash attention over a composed cache, on CUDA cores.
+// Split-K flash-decode over a composed cache, on CUDA cores.
 //
 // C2KV explainer (paper-daily.com), section "pipeline: extract, store,
 // concatenate" (整体流程): after composition the question is appended and the
@@ -6,20 +6,27 @@
 // (实验结果：真的又快又准吗？): each decoded token reads the whole composed
 // cache, so decode is bound by the bytes of that cache.  Section "structured
 // information flow" (为什么需要“结构化信息流”？) gives the mask of the
-// extraction-time mode.
+// extraction-time mode (used here only for one-token sequences).
 //
-// Work decomposition.  A CTA owns one (sequence b, kv head h, token block,
-// key split).  Its key range is streamed through a 4-stage ring of 32-key
-// K/V tiles in shared memory, each tile fetched by two 1-D bulk copies (TMA
-// engine) completing on an mbarrier.  Rows are (token, q head of the group):
-// the G heads of a token share every K/V tile.  A "key group" of D/8 lanes
-// scores one key at a time (each lane holds 8 elements of d for all G heads,
-// partial dots reduced with xor shuffles) and keeps its own online-softmax
-// state (m, l, o); groups are merged through shared memory at the end.
-// Decode (one token) spreads the 4 warps over the keys; prefill and the mask
-// mode give each warp its own token.  With more than one split the CTA
-// writes (m, l, o) partials; the last CTA of its (b, token block, h) to
-// arrive (atomic counter) merges them and resets the counter.
+// One token per sequence.  A CTA owns one (sequence b, kv head h, key split)
+// and is wide (NW warps, one wave of CTAs over the GPU) so that few splits
+// cover a layer and their merge stays short.  The split's keys stream through
+// a 3-stage ring of K/V tiles in shared memory, each tile fetched by two 1-D
+// bulk copies (TMA engine) completing on an mbarrier.  A "key group" of d/8
+// lanes scores one key at a time: each lane holds 8 elements of d for all G
+// q heads of the kv head (as fp32 pairs for the packed fma.rn.f32x2), the
+// partial dots are reduced with xor shuffles, and each group keeps its own
+// online-softmax state (m, l, o), rescaled lazily (only when the running max
+// grows by more than 2^8).  Groups are merged in shared memory; with several
+// splits the CTA writes (m, l, o) partials and the last CTA of its (b, h) to
+// arrive (atomic counter) merges them, one output element per thread, and
+// resets the counter.
+//
+// Decode fuses the append: the CTA whose split holds the new key rotates it
+// (double-float, correctly rounded, from the sequence's RoPE table), stores
+// it with its value at row n_cached, and writes it into its last shared-memory
+// tile, which the bulk copy leaves free; an mbarrier orders that write before
+// the other warps read the tile.
 #include <float.h>
 
 #include "c2kv_internal.h"
@@ -28,35 +35,48 @@ namespace c2kv {
 
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kWarps = 4;
-constexpr int kStages = 4;
-constexpr int T = kAttnTileKeys;
+constexpr int kStages = 3;
+constexpr int KPG = 4;   // keys per key group per tile
 
-template <int D, int G, int WPT>
-struct Cfg {
-  static constexpr int LPK = D / 8;          // lanes per key
-  static constexpr int GPW = 32 / LPK;       // key groups per warp
-  static constexpr int TPC = kWarps / WPT;   // tokens per CTA
-  static constexpr int GPT = WPT * GPW;      // key groups per token
-  static constexpr int KPG = T / GPT;        // keys per group per tile
-  static constexpr int CH = KPG < 8 ? KPG : 8;
-  static constexpr int TILE = T * D * 2;     // bytes of one K (or V) tile
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(r)
+      : "l"(*reinterpret_cast<unsigned long long*>(&a)), "l"(*reinterpret_cast<unsigned long long*>(&b)),
+        "l"(*reinterpret_cast<unsigned long long*>(&c)));
+  return *reinterpret_cast<float2*>(&r);
+}
+
+// 8 bf16 -> 4 fp32 pairs (element 2i in .x, 2i+1 in .y)
+__device__ __forceinline__ void unpack8x2(const uint4& u, float2 (&f)[4]) {
+  f[0] = make_float2(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u));
+  f[1] = make_float2(__uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+  f[2] = make_float2(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xffff0000u));
+  f[3] = make_float2(__uint_as_float(u.w << 16), __uint_as_float(u.w & 0xffff0000u));
+}
+
+template <int D, int G>
+struct DCfg {
+  static constexpr int NW = G <= 4 ? 16 : 8;          // warps per CTA
+  static constexpr int THREADS = NW * 32;
+  static constexpr int CTAS_PER_SM = 1;
+  static constexpr int LPK = D / 8;                   // lanes per key
+  static constexpr int GPW = 32 / LPK;                // key groups per warp
+  static constexpr int NG = NW * GPW;                 // key groups per CTA
+  static constexpr int T = NG * KPG;                  // keys per tile
+  static constexpr int TILE = T * D * 2;              // bytes of one K (or V) tile
   static constexpr int PIPE = kStages * 2 * TILE;
-  static constexpr int CMB = TPC * GPT * G * (D + 2) * 4;
-  static constexpr int WTS = TPC * G * kMaxSplits * 4;
+  static constexpr int CMB = NG * G * (D + 2) * 4;
+  static constexpr int WTS = G * kMaxSplits * 4;
   static constexpr int MAIN_RAW = (PIPE > CMB ? (PIPE > WTS ? PIPE : WTS) : (CMB > WTS ? CMB : WTS));
   static constexpr int MAIN = (MAIN_RAW + 127) / 128 * 128;   // keeps the mbarriers 8-byte aligned
-  static constexpr int EXTRA = (2 * kStages + 2) * 8 + 2 * TPC * (D / 2) * 4 + (D / 2) * 16 + 16;
+  static constexpr int EXTRA = (2 * kStages + 2) * 8 + (D / 2) * 16 + 2 * (D / 2) * 4 + 16;
   static constexpr int SMEM = MAIN + EXTRA;
-  static_assert(KPG >= 1 && KPG * GPT == T, "tile must split evenly over key groups");
 };
 
 // Extra visibility of the structured mask beyond causality (section
 // "structured information flow"): slot i sees document tokens of the sink
 // block [0, k) and of its own block [i*k, min((i+1)k, n_doc)) only.
-// Document rows see no slot and slots see earlier slots; both follow from
-// the causal limit because slots come after the document.
 __device__ __forceinline__ bool structured_visible(const AttnParams& p, int tok, int key) {
   if (tok < p.n_doc || key >= p.n_doc) return true;
   const int i = tok - p.n_doc;
@@ -64,65 +84,42 @@ __device__ __forceinline__ bool structured_visible(const AttnParams& p, int tok,
   return key < sink_end || (key >= i * p.kblk && key < min((i + 1) * p.kblk, p.n_doc));
 }
 
-template <int D, int G, int WPT>
-__global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ AttnParams p) {
-  using C = Cfg<D, G, WPT>;
+template <int D, int G>
+__global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::CTAS_PER_SM)
+    decode_kernel(const __grid_constant__ AttnParams p) {
+  using C = DCfg<D, G>;
+  constexpr int T = C::T;
+  constexpr int NW = C::NW;
+  constexpr int TPR = D / 16;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::MAIN);
   uint64_t* empty = full + kStages;
   uint64_t* inj = empty + kStages;                          // new-key row injected (fused append)
-  CosSin2* tab2 = reinterpret_cast<CosSin2*>(inj + 2);      // [D/2], position of the new key
-  float* cs = reinterpret_cast<float*>(tab2 + D / 2);       // [TPC][D/2]
-  float* sn = cs + C::TPC * (D / 2);
-  int* flag = reinterpret_cast<int*>(sn + C::TPC * (D / 2));
+  CosSin2* tab2 = reinterpret_cast<CosSin2*>(inj + 2);      // [D/2], row of the new key
+  float* cs = reinterpret_cast<float*>(tab2 + D / 2);       // [D/2]
+  float* sn = cs + D / 2;
+  int* flag = reinterpret_cast<int*>(sn + D / 2);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x;
-  const int h = blockIdx.y % p.n_kv;
-  const int tb = blockIdx.y / p.n_kv;
+  const int h = blockIdx.y;
   const int b = blockIdx.z;
-  const int n_tb = (p.t_len + C::TPC - 1) / C::TPC;
 
   const int n_cached = p.n_cached_d ? p.n_cached_d[b] : p.n_cached_h[b];
-  if (n_cached < 0 || n_cached + p.t_len > p.cap || n_cached + p.t_len > p.max_keys) {
+  if (n_cached < 0 || n_cached + 1 > p.cap || n_cached + 1 > p.max_keys) {
     // Uniform over every CTA of sequence b: nobody touches its counters.
-    if (tid == 0 && split == 0 && blockIdx.y == 0) atomicOr(p.err, kErrLength);
+    if (tid == 0 && split == 0 && h == 0) atomicOr(p.err, kErrLength);
     return;
   }
-
-  const int tok0 = tb * C::TPC;
-  const int ntok = min(C::TPC, p.t_len - tok0);
-  const int kmax = n_cached + tok0 + ntok;        // causal limit of the block's last token
+  const int kmax = n_cached + 1;   // the token sees every cached key and itself
   const int kb = split * p.split_keys;
   const int ke = min(kb + p.split_keys, kmax);
   const int ntiles = ke > kb ? (ke - kb + T - 1) / T : 0;
-  // Fused append (decode): key nk = n_cached is the new token; the split that
-  // holds it builds the row itself, every other key comes from the cache.
-  constexpr int TPR = D / 16;
-  const int nk = n_cached + p.t_len - 1;
+  const int nk = n_cached;         // index of the new key
   const bool has_new = p.fuse_append && nk >= kb && nk < ke;
   const int t_new = has_new ? (nk - kb) / T : -1;
   const int k_res_end = p.fuse_append ? min(ke, nk) : ke;   // end of cache-resident keys
-
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kWarps);
-    }
-    mbar_init(inj, TPR);
-    fence_barrier_init();
-  }
-  // cos/sin of each token's position: row n_cached + t of the sequence's table
-  // (hi parts rotate q; the full pairs rotate the new key when fused).
-  for (int i = tid; i < ntok * (D / 2); i += kThreads) {
-    const int t = i / (D / 2), f = i % (D / 2);
-    const CosSin2 e = p.tab[b][(size_t)(n_cached + tok0 + t) * (D / 2) + f];
-    cs[i] = e.ch;
-    sn[i] = e.sh;
-    if (has_new && t == 0) tab2[f] = e;
-  }
-  __syncthreads();
 
   const __nv_bfloat16* kg = p.k_base[b] + (size_t)h * p.cap * D;
   const __nv_bfloat16* vg = p.v_base[b] + (size_t)h * p.cap * D;
@@ -141,53 +138,61 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
     bulk_g2s(stage_k(s), kg + (size_t)key0 * D, bytes, &full[s]);
     bulk_g2s(stage_v(s), vg + (size_t)key0 * D, bytes, &full[s]);
   };
+  // The first tiles are requested before anything else waits on memory.
   int issued = 0;
   if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], NW);
+    }
+    mbar_init(inj, TPR);
+    fence_barrier_init();
     for (; issued < min(kStages, ntiles); ++issued) issue(issued);
   }
+  // cos/sin of the token's position: row n_cached of the sequence's table
+  // (hi parts rotate q; the full pairs rotate the new key when fused).
+  for (int f = tid; f < D / 2; f += C::THREADS) {
+    const CosSin2 e = p.tab[b][(size_t)n_cached * (D / 2) + f];
+    cs[f] = e.ch;
+    sn[f] = e.sh;
+    if (has_new) tab2[f] = e;
+  }
+  __syncthreads();
 
   // ---- per-lane role
-  const int wtok = warp / WPT;
-  const int gq = (warp % WPT) * C::GPW + lane / C::LPK;   // key group within token
-  const int sub = lane % C::LPK;                          // owns d elements [8 sub, 8 sub + 8)
-  const bool tok_ok = wtok < ntok;
-  const int tok = tok0 + wtok;
-  const int lim = n_cached + tok + 1;
+  const int gq = warp * C::GPW + lane / C::LPK;   // key group
+  const int sub = lane % C::LPK;                  // owns d elements [8 sub, 8 sub + 8)
 
-  float q[G][8];
+  float2 q2[G][4];
   {
     const int half = D / 2;
     const int e0 = sub * 8;
     const int partner = (e0 + half) % D;
-    const float* c = cs + wtok * half;
-    const float* s = sn + wtok * half;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       float x[8], y[8];
-      if (tok_ok) {
-        const __nv_bfloat16* row = p.q + (((size_t)b * p.t_len + tok) * p.n_q + h * G + g) * D;
-        unpack8(*reinterpret_cast<const uint4*>(row + e0), x);
-        unpack8(*reinterpret_cast<const uint4*>(row + partner), y);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = y[e] = 0.f;
-      }
+      const __nv_bfloat16* row = p.q + ((size_t)b * p.n_q + h * G + g) * D;
+      unpack8(*reinterpret_cast<const uint4*>(row + e0), x);
+      unpack8(*reinterpret_cast<const uint4*>(row + partner), y);
+      float r[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int f = (e0 + e) % half;
-        const float r = (e0 < half) ? x[e] * c[f] - y[e] * s[f] : x[e] * c[f] + y[e] * s[f];
-        q[g][e] = r * p.scale_log2;
+        r[e] = ((e0 < half) ? x[e] * cs[f] - y[e] * sn[f] : x[e] * cs[f] + y[e] * sn[f]) * p.scale_log2;
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) q2[g][e] = make_float2(r[2 * e], r[2 * e + 1]);
     }
   }
 
-  float m[G], l[G], o[G][8];
+  float m[G], l[G];
+  float2 o2[G][4];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     m[g] = -INFINITY;
     l[g] = 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o[g][e] = 0.f;
+    for (int e = 0; e < 4; ++e) o2[g][e] = make_float2(0.f, 0.f);
   }
 
   // The new key's rotated k and v, prepared by warp 1 (lane c owns pairs
@@ -209,14 +214,13 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
     vd[lane + TPR] = nv_b;
   }
 
+  const bool structured = p.mask_mode == kMaskStructured;
   bool aborted = false;
   for (int t = 0; t < ntiles; ++t) {
     const int s = t % kStages;
     const uint32_t ph = (t / kStages) & 1;
     if (!mbar_wait(&full[s], ph)) { aborted = true; break; }
     if (t == t_new) {
-      // The row after the copied keys is free in this stage: fill it with the
-      // new key, then let every warp read the tile.
       if (warp == 1 && lane < TPR) {
         const int r = nk - (kb + t * T);
         uint4* ksm = reinterpret_cast<uint4*>(stage_k(s) + (size_t)r * D * 2);
@@ -233,59 +237,60 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
     const int nvalid = min(T, ke - key0);
     const uint8_t* Ks = stage_k(s);
     const uint8_t* Vs = stage_v(s);
+    float sc[KPG][G];
 #pragma unroll
-    for (int c0 = 0; c0 < C::KPG; c0 += C::CH) {
-      float sc[C::CH][G];
+    for (int kk = 0; kk < KPG; ++kk) {
+      const int kl = kk * C::NG + gq;
+      float2 k2[4];
+      const bool in = kl < nvalid;
+      if (in) {
+        unpack8x2(*reinterpret_cast<const uint4*>(Ks + (size_t)kl * D * 2 + sub * 16), k2);
+      } else {
 #pragma unroll
-      for (int kk = 0; kk < C::CH; ++kk) {
-        const int kl = (c0 + kk) * C::GPT + gq;
-        const int key = key0 + kl;
-        float kf[8];
-        if (kl < nvalid) {
-          unpack8(*reinterpret_cast<const uint4*>(Ks + (size_t)kl * D * 2 + sub * 16), kf);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) kf[e] = 0.f;
-        }
-        bool vis = tok_ok && kl < nvalid && key < lim;
-        if (p.mask_mode == kMaskStructured) vis = vis && structured_visible(p, tok, key);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float d = 0.f;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) d = fmaf(q[g][e], kf[e], d);
-#pragma unroll
-          for (int off = C::LPK / 2; off >= 1; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-          sc[kk][g] = vis ? d : -INFINITY;
-        }
+        for (int e = 0; e < 4; ++e) k2[e] = make_float2(0.f, 0.f);
       }
+      bool vis = in;
+      if (structured) vis = vis && structured_visible(p, n_cached, key0 + kl);
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        float mc = sc[0][g];
+        float2 a = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int kk = 1; kk < C::CH; ++kk) mc = fmaxf(mc, sc[kk][g]);
-        if (mc > m[g]) {
-          const float a = exp2f(m[g] - mc);   // 0 when m was -inf
-          l[g] *= a;
+        for (int e = 0; e < 4; ++e) a = ffma2(q2[g][e], k2[e], a);
+        float d = a.x + a.y;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) o[g][e] *= a;
-          m[g] = mc;
-        }
+        for (int off = C::LPK / 2; off >= 1; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+        sc[kk][g] = vis ? d : -INFINITY;
       }
+    }
 #pragma unroll
-      for (int kk = 0; kk < C::CH; ++kk) {
-        const int kl = (c0 + kk) * C::GPT + gq;
-        if (kl < nvalid) {
-          float vf[8];
-          unpack8(*reinterpret_cast<const uint4*>(Vs + (size_t)kl * D * 2 + sub * 16), vf);
+    for (int g = 0; g < G; ++g) {
+      float mc = sc[0][g];
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float mu = (m[g] == -INFINITY) ? 0.f : m[g];
-            const float pr = exp2f(sc[kk][g] - mu);
-            l[g] += pr;
+      for (int kk = 1; kk < KPG; ++kk) mc = fmaxf(mc, sc[kk][g]);
+      // Lazy rescale: keep the running max unless it grows by more than 2^8
+      // (weights stay below 2^8; the final o / l is unaffected).
+      if (mc > m[g] + 8.f || (m[g] == -INFINITY && mc > -INFINITY)) {
+        const float a = exp2f(m[g] - mc);   // 0 when m was -inf
+        l[g] *= a;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o[g][e] = fmaf(pr, vf[e], o[g][e]);
-          }
+        for (int e = 0; e < 4; ++e) o2[g][e] = make_float2(o2[g][e].x * a, o2[g][e].y * a);
+        m[g] = mc;
+      }
+    }
+#pragma unroll
+    for (int kk = 0; kk < KPG; ++kk) {
+      const int kl = kk * C::NG + gq;
+      if (kl < nvalid) {
+        float2 v2[4];
+        unpack8x2(*reinterpret_cast<const uint4*>(Vs + (size_t)kl * D * 2 + sub * 16), v2);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float mu = (m[g] == -INFINITY) ? 0.f : m[g];
+          const float pr = exp2f(sc[kk][g] - mu);
+          l[g] += pr;
+          const float2 p2 = make_float2(pr, pr);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o2[g][e] = ffma2(p2, v2[e], o2[g][e]);
         }
       }
     }
@@ -309,47 +314,44 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
       m[g] = -INFINITY;
       l[g] = 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[g][e] = 0.f;
+      for (int e = 0; e < 4; ++e) o2[g][e] = make_float2(0.f, 0.f);
     }
     __syncthreads();
   }
 
-  // ---- merge the key groups of each token (shared memory reused)
-  float* cmb_o = reinterpret_cast<float*>(smem);              // [TPC][GPT][G][D]
-  float* cmb_ml = cmb_o + C::TPC * C::GPT * G * D;             // [TPC][GPT][G][2]
-  if (tok_ok) {
+  // ---- merge the key groups (shared memory reused)
+  float* cmb_o = reinterpret_cast<float*>(smem);   // [NG][G][D]
+  float* cmb_ml = cmb_o + C::NG * G * D;           // [NG][G][2]
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float* dst = cmb_o + (((size_t)wtok * C::GPT + gq) * G + g) * D + sub * 8;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) dst[e] = o[g][e];
-      if (sub == 0) {
-        cmb_ml[((wtok * C::GPT + gq) * G + g) * 2 + 0] = m[g];
-        cmb_ml[((wtok * C::GPT + gq) * G + g) * 2 + 1] = l[g];
-      }
+  for (int g = 0; g < G; ++g) {
+    float4* dst = reinterpret_cast<float4*>(cmb_o + ((size_t)gq * G + g) * D + sub * 8);
+    dst[0] = make_float4(o2[g][0].x, o2[g][0].y, o2[g][1].x, o2[g][1].y);
+    dst[1] = make_float4(o2[g][2].x, o2[g][2].y, o2[g][3].x, o2[g][3].y);
+    if (sub == 0) {
+      cmb_ml[(gq * G + g) * 2 + 0] = m[g];
+      cmb_ml[(gq * G + g) * 2 + 1] = l[g];
     }
   }
   __syncthreads();
 
   const int S = p.num_splits;
-  for (int i = tid; i < ntok * G * D; i += kThreads) {
-    const int dd = i % D, g = (i / D) % G, t = i / (G * D);
+  for (int i = tid; i < G * D; i += C::THREADS) {
+    const int dd = i % D, g = i / D;
     float M = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < C::GPT; ++j) M = fmaxf(M, cmb_ml[((t * C::GPT + j) * G + g) * 2]);
+#pragma unroll 8
+    for (int j = 0; j < C::NG; ++j) M = fmaxf(M, cmb_ml[(j * G + g) * 2]);
     float L = 0.f, O = 0.f;
-#pragma unroll
-    for (int j = 0; j < C::GPT; ++j) {
-      const float mj = cmb_ml[((t * C::GPT + j) * G + g) * 2];
+#pragma unroll 8
+    for (int j = 0; j < C::NG; ++j) {
+      const float mj = cmb_ml[(j * G + g) * 2];
       const float w = (mj == -INFINITY) ? 0.f : exp2f(mj - M);
-      L = fmaf(cmb_ml[((t * C::GPT + j) * G + g) * 2 + 1], w, L);
-      O = fmaf(cmb_o[((t * C::GPT + j) * G + g) * D + dd], w, O);
+      L = fmaf(cmb_ml[(j * G + g) * 2 + 1], w, L);
+      O = fmaf(cmb_o[((size_t)j * G + g) * D + dd], w, O);
     }
-    const int tk = tok0 + t;
     if (S == 1) {
-      p.out[(((size_t)b * p.t_len + tk) * p.n_q + h * G + g) * D + dd] = __float2bfloat16_rn(O / L);
+      p.out[((size_t)b * p.n_q + h * G + g) * D + dd] = __float2bfloat16_rn(O / L);
     } else {
-      const size_t base = (((size_t)b * p.t_len + tk) * p.n_kv + h) * S + split;
+      const size_t base = ((size_t)b * p.n_kv + h) * S + split;
       p.part_o[(base * G + g) * D + dd] = O;
       if (dd == 0) {
         p.part_ml[(base * G + g) * 2 + 0] = M;
@@ -359,22 +361,18 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
   }
   if (S == 1) return;
 
-  // ---- last CTA of (b, token block, h) merges the split partials
+  // ---- last CTA of (b, h) merges the split partials
   __threadfence();
   __syncthreads();
-  const int cidx = (b * n_tb + tb) * p.n_kv + h;
-  if (tid == 0) {
-    const int prev = atomicAdd(&p.counters[cidx], 1);
-    *flag = (prev == S - 1);
-  }
+  const int cidx = b * p.n_kv + h;
+  if (tid == 0) *flag = (atomicAdd(&p.counters[cidx], 1) == S - 1);
   __syncthreads();
   if (!*flag) return;
   __threadfence();
 
-  float* wts = reinterpret_cast<float*>(smem);   // [TPC][G][S]
-  for (int pair = warp; pair < ntok * G; pair += kWarps) {
-    const int t = pair / G, g = pair % G;
-    const size_t base = (((size_t)b * p.t_len + tok0 + t) * p.n_kv + h) * S;
+  float* wts = reinterpret_cast<float*>(smem);   // [G][S]
+  const size_t base = ((size_t)b * p.n_kv + h) * S;
+  for (int g = warp; g < G; g += NW) {
     float M = -INFINITY;
     for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldcg(&p.part_ml[((base + s) * G + g) * 2]));
 #pragma unroll
@@ -383,84 +381,87 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
     for (int s = lane; s < S; s += 32) {
       const float ms = __ldcg(&p.part_ml[((base + s) * G + g) * 2]);
       const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-      wts[pair * S + s] = w;
+      wts[g * S + s] = w;
       L = fmaf(__ldcg(&p.part_ml[((base + s) * G + g) * 2 + 1]), w, L);
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-    const float invL = 1.f / L;
+    const float inv = 1.f / L;
     __syncwarp();
-    for (int s = lane; s < S; s += 32) wts[pair * S + s] *= invL;
+    for (int s = lane; s < S; s += 32) wts[g * S + s] *= inv;
   }
   __syncthreads();
-  for (int i = tid; i < ntok * G * D; i += kThreads) {
-    const int dd = i % D, g = (i / D) % G, t = i / (G * D);
-    const size_t base = (((size_t)b * p.t_len + tok0 + t) * p.n_kv + h) * S;
-    const float* w = wts + (t * G + g) * S;
-    float acc = 0.f;
-    for (int s = 0; s < S; ++s) acc = fmaf(w[s], __ldcg(&p.part_o[((base + s) * G + g) * D + dd]), acc);
-    p.out[(((size_t)b * p.t_len + tok0 + t) * p.n_q + h * G + g) * D + dd] = __float2bfloat16_rn(acc);
+  for (int i = tid; i < G * D; i += C::THREADS) {
+    const int dd = i % D, g = i / D;
+    const float* w = wts + g * S;
+    const float* po = p.part_o + (base * G + g) * D + dd;
+    // independent partial sums so the loads of several splits are in flight
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    int s = 0;
+    for (; s + 4 <= S; s += 4) {
+      const float x0 = __ldcg(po + (size_t)(s + 0) * G * D), x1 = __ldcg(po + (size_t)(s + 1) * G * D);
+      const float x2 = __ldcg(po + (size_t)(s + 2) * G * D), x3 = __ldcg(po + (size_t)(s + 3) * G * D);
+      a0 = fmaf(w[s + 0], x0, a0);
+      a1 = fmaf(w[s + 1], x1, a1);
+      a2 = fmaf(w[s + 2], x2, a2);
+      a3 = fmaf(w[s + 3], x3, a3);
+    }
+    for (; s < S; ++s) a0 = fmaf(w[s], __ldcg(po + (size_t)s * G * D), a0);
+    p.out[((size_t)b * p.n_q + h * G + g) * D + dd] = __float2bfloat16_rn((a0 + a1) + (a2 + a3));
   }
   if (tid == 0) p.counters[cidx] = 0;
 }
 
-template <int D, int G, int WPT>
+template <int D, int G>
 cudaError_t launch_one(const AttnParams& p, cudaStream_t st) {
-  using C = Cfg<D, G, WPT>;
+  using C = DCfg<D, G>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, G, WPT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const int n_tb = (p.t_len + C::TPC - 1) / C::TPC;
-  const dim3 grid(p.num_splits, p.n_kv * n_tb, p.batch);
-  attn_kernel<D, G, WPT><<<grid, kThreads, C::SMEM, st>>>(p);
+  const dim3 grid(p.num_splits, p.n_kv, p.batch);
+  decode_kernel<D, G><<<grid, C::THREADS, C::SMEM, st>>>(p);
   return cudaGetLastError();
-}
-
-template <int D, int G>
-cudaError_t launch_g(const AttnParams& p, cudaStream_t st) {
-  // One token per sequence: the 4 warps split its keys.  Multi-token calls
-  // go to the tensor-core kernel.
-  if (p.t_len != 1) return cudaErrorInvalidValue;
-  return launch_one<D, G, 4>(p, st);
 }
 
 template <int D>
 cudaError_t launch_d(const AttnParams& p, int group, cudaStream_t st) {
   switch (group) {
-    case 1: return launch_g<D, 1>(p, st);
-    case 2: return launch_g<D, 2>(p, st);
-    case 4: return launch_g<D, 4>(p, st);
-    case 5: return launch_g<D, 5>(p, st);
-    case 8: return launch_g<D, 8>(p, st);
+    case 1: return launch_one<D, 1>(p, st);
+    case 2: return launch_one<D, 2>(p, st);
+    case 4: return launch_one<D, 4>(p, st);
+    case 5: return launch_one<D, 5>(p, st);
+    case 8: return launch_one<D, 8>(p, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-int attn_tokens_per_cta(int t_len) { return t_len == 1 ? 1 : kWarps; }
+int attn_tokens_per_cta(int) { return 1; }
 
-
-void attn_plan_splits(int units, int max_keys, int num_sms, int* num_splits, int* split_keys) {
-  const int target = num_sms * kAttnCtasPerSm;
-  int s = (target + units - 1) / units;
-  const int tiles = (max_keys + T - 1) / T;
-  if (s > tiles) s = tiles;
+// One wave: units = sequences x kv heads; each unit's keys are split so that
+// the CTAs (one per SM: 16 warps for G <= 4, 8 warps for G = 5, 8) fill the
+// SMs once.
+void attn_plan_splits(int units, int max_keys, int num_sms, int group, int* num_splits, int* split_keys) {
+  (void)group;
+  int s = num_sms / units;
+  if (s < 1) s = 1;
   if (s > kMaxSplits) s = kMaxSplits;
+  const int min_keys = 64;   // keep each split at least a few tiles' worth of work
+  if (s > 1 && (max_keys + s - 1) / s < min_keys) s = (max_keys + min_keys - 1) / min_keys;
   if (s < 1) s = 1;
   int sk = (max_keys + s - 1) / s;
-  sk = ((sk + T - 1) / T) * T;
-  if (sk < T) sk = T;
+  sk = (sk + 7) / 8 * 8;
   *split_keys = sk;
   *num_splits = (max_keys + sk - 1) / sk;
   if (*num_splits < 1) *num_splits = 1;
 }
 
 cudaError_t launch_attention(const AttnParams& p, int head_dim, int group, cudaStream_t st) {
+  if (p.t_len != 1) return cudaErrorInvalidValue;
   if (head_dim == 128) return launch_d<128>(p, group, st);
   if (head_dim == 64) return launch_d<64>(p, group, st);
   return cudaErrorInvalidValue;

@@ -280,8 +280,6 @@ constexpr int kTcMaxSplits = 128;
 
 // Attention work decomposition shared by the launcher and the workspace query.
 int attn_tokens_per_cta(int t_len);
-void attn_plan_splits(int units, int max_keys, int num_sms, int* num_splits, int* split_keys);
-constexpr int kAttnTileKeys = 32;
-constexpr int kAttnCtasPerSm = 3;
+void attn_plan_splits(int units, int max_keys, int num_sms, int group, int* num_splits, int* split_keys);
 
 }  // namespace c2kv
