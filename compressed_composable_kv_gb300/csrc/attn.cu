@@ -57,21 +57,59 @@ __device__ __forceinline__ void unpack8x2(const uint4& u, float2 (&f)[4]) {
 
 template <int D, int G>
 struct DCfg {
-  static constexpr int NW = G <= 4 ? 16 : 8;          // warps per CTA
-  static constexpr int THREADS = NW * 32;
-  static constexpr int CTAS_PER_SM = 1;
-  static constexpr int LPK = D / 8;                   // lanes per key
+  // The G query heads of a kv head are split over HS warp slices of GW heads
+  // each, so a thread holds q and o of GW heads only and 16 warps fit an SM.
+  static constexpr int GW = (G % 2 == 0) ? 2 : 1;     // heads per warp
+  static constexpr int HS = G / GW;                   // head slices
+  static constexpr int EPL = 16;                      // d elements a lane owns
+  static constexpr int LPK = D / EPL;                 // lanes per key (a key group)
+  static constexpr int NCH = EPL / 8;                 // 16-byte chunks a lane owns
   static constexpr int GPW = 32 / LPK;                // key groups per warp
-  static constexpr int NG = NW * GPW;                 // key groups per CTA
+  static constexpr int NWK0 = 16 / HS;
+  // warps per slice, halved while the 3-stage K/V ring would exceed 192 KB
+  static constexpr int NWK1 = (NWK0 * GPW * KPG * D * 2 * 2 * kStages > 196608) ? NWK0 / 2 : NWK0;
+  static constexpr int NWK = (NWK1 * GPW * KPG * D * 2 * 2 * kStages > 196608) ? NWK1 / 2 : NWK1;
+  static constexpr int NW = HS * NWK;                 // warps per CTA
+  static constexpr int THREADS = NW * 32;
+  static constexpr int NG = NWK * GPW;                // key groups per slice
   static constexpr int T = NG * KPG;                  // keys per tile
+  static constexpr int V = KPG * GW;                  // (key, head) scores a group makes per tile
+  static constexpr int VP = ((V > LPK ? V : LPK) + LPK - 1) / LPK * LPK;   // padded to a multiple of LPK
+  static constexpr int VPL = VP / LPK;                // scores each lane ends up owning
   static constexpr int TILE = T * D * 2;              // bytes of one K (or V) tile
   static constexpr int PIPE = kStages * 2 * TILE;
   static constexpr int CMB = NG * G * (D + 2) * 4;
-  static constexpr int WTS = G * kMaxSplits * 4;
-  static constexpr int MAIN_RAW = (PIPE > CMB ? (PIPE > WTS ? PIPE : WTS) : (CMB > WTS ? CMB : WTS));
-  static constexpr int MAIN = (MAIN_RAW + 127) / 128 * 128;   // keeps the mbarriers 8-byte aligned
-  static constexpr int EXTRA = (2 * kStages + 2) * 8 + (D / 2) * 16 + 2 * (D / 2) * 4 + 16;
-  static constexpr int SMEM = MAIN + EXTRA;
+  static constexpr int MAIN = ((PIPE > CMB ? PIPE : CMB) + 127) / 128 * 128;
+  static constexpr int WN = NG > kMaxSplits ? NG : kMaxSplits;
+  static constexpr int OFF_QS = MAIN;                          // rotated, scaled q [G][D] fp32
+  static constexpr int OFF_SC = OFF_QS + G * D * 4;             // per-group scores [HS][NG][VP]
+  static constexpr int OFF_W = OFF_SC + HS * NG * VP * 4;       // merge weights [G][WN] + [G] M, L
+  static constexpr int OFF_BAR = (OFF_W + G * WN * 4 + 2 * G * 4 + 15) / 16 * 16;
+  static constexpr int OFF_TAB2 = OFF_BAR + (2 * kStages + 2) * 8;
+  static constexpr int OFF_CS = OFF_TAB2 + (D / 2) * 16;
+  static constexpr int SMEM = OFF_CS + 2 * (D / 2) * 4 + 16;
+  static_assert(G % GW == 0 && NWK >= 1 && NG % 2 == 0, "decode tiling");
+};
+
+// Sums VP partial values across the LPK lanes of a key group and scatters the
+// totals: afterwards lane li holds, in x[0..VP/LPK), the totals of values
+// [li * VP/LPK, (li+1) * VP/LPK).  Each step exchanges half of the current
+// values with the partner lane (xor OFF), so VP - VP/LPK values cross lanes
+// in all instead of VP * log2(LPK).
+template <int N, int OFF, int VP>
+struct ReduceScatter {
+  __device__ __forceinline__ static void run(float (&x)[VP], int li) {
+    if constexpr (OFF >= 1) {
+      const bool up = (li & OFF) != 0;
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i) {
+        const float send = up ? x[i] : x[i + N / 2];
+        const float keep = up ? x[i + N / 2] : x[i];
+        x[i] = keep + __shfl_xor_sync(0xffffffffu, send, OFF);
+      }
+      ReduceScatter<N / 2, OFF / 2, VP>::run(x, li);
+    }
+  }
 };
 
 // Extra visibility of the structured mask beyond causality (section
@@ -85,18 +123,22 @@ __device__ __forceinline__ bool structured_visible(const AttnParams& p, int tok,
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::CTAS_PER_SM)
-    decode_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__(DCfg<D, G>::THREADS, 1) decode_kernel(const __grid_constant__ AttnParams p) {
   using C = DCfg<D, G>;
   constexpr int T = C::T;
   constexpr int NW = C::NW;
+  constexpr int LPK = C::LPK;
+  constexpr int NCH = C::NCH;
   constexpr int TPR = D / 16;
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::MAIN);
+  float* qs = reinterpret_cast<float*>(smem + C::OFF_QS);
+  float* scs = reinterpret_cast<float*>(smem + C::OFF_SC);
+  float* wbuf = reinterpret_cast<float*>(smem + C::OFF_W);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + kStages;
-  uint64_t* inj = empty + kStages;                          // new-key row injected (fused append)
-  CosSin2* tab2 = reinterpret_cast<CosSin2*>(inj + 2);      // [D/2], row of the new key
-  float* cs = reinterpret_cast<float*>(tab2 + D / 2);       // [D/2]
+  uint64_t* inj = empty + kStages;                                     // new-key row injected
+  CosSin2* tab2 = reinterpret_cast<CosSin2*>(smem + C::OFF_TAB2);      // [D/2], row of the new key
+  float* cs = reinterpret_cast<float*>(smem + C::OFF_CS);              // [D/2]
   float* sn = cs + D / 2;
   int* flag = reinterpret_cast<int*>(sn + D / 2);
 
@@ -158,41 +200,48 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::CTAS_PER_SM)
     if (has_new) tab2[f] = e;
   }
   __syncthreads();
+  // q of the kv head's G query heads, rotated once per CTA and pre-scaled by
+  // log2(e)/sqrt(d), into shared memory.
+  for (int i = tid; i < G * (D / 2); i += C::THREADS) {
+    const int g = i / (D / 2), f = i % (D / 2);
+    const __nv_bfloat16* row = p.q + ((size_t)b * p.n_q + h * G + g) * D;
+    const float x = __bfloat162float(row[f]), y = __bfloat162float(row[f + D / 2]);
+    qs[g * D + f] = (x * cs[f] - y * sn[f]) * p.scale_log2;
+    qs[g * D + f + D / 2] = (y * cs[f] + x * sn[f]) * p.scale_log2;
+  }
+  __syncthreads();
 
-  // ---- per-lane role
-  const int gq = warp * C::GPW + lane / C::LPK;   // key group
-  const int sub = lane % C::LPK;                  // owns d elements [8 sub, 8 sub + 8)
-
-  float2 q2[G][4];
-  {
-    const int half = D / 2;
-    const int e0 = sub * 8;
-    const int partner = (e0 + half) % D;
+  // ---- per-lane role: head slice hs (heads g0 .. g0+GW-1), key group gq;
+  // lane li of the group owns the 16-byte chunks li, li + LPK of every row
+  // (for d = 128 a RoPE pair; the 8 lanes of a group read 8 consecutive
+  // chunks).
+  constexpr int GW = C::GW;
+  const int hs = warp / C::NWK;
+  const int g0 = hs * GW;
+  const int gq = (warp % C::NWK) * C::GPW + lane / LPK;
+  const int li = lane % LPK;
+  float2 q2[GW][NCH * 4];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float x[8], y[8];
-      const __nv_bfloat16* row = p.q + ((size_t)b * p.n_q + h * G + g) * D;
-      unpack8(*reinterpret_cast<const uint4*>(row + e0), x);
-      unpack8(*reinterpret_cast<const uint4*>(row + partner), y);
-      float r[8];
+  for (int g = 0; g < GW; ++g) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int f = (e0 + e) % half;
-        r[e] = ((e0 < half) ? x[e] * cs[f] - y[e] * sn[f] : x[e] * cs[f] + y[e] * sn[f]) * p.scale_log2;
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) q2[g][e] = make_float2(r[2 * e], r[2 * e + 1]);
+    for (int j = 0; j < NCH; ++j) {
+      const float4* src = reinterpret_cast<const float4*>(qs + (g0 + g) * D + (li + j * LPK) * 8);
+      const float4 a = src[0], c = src[1];
+      q2[g][j * 4 + 0] = make_float2(a.x, a.y);
+      q2[g][j * 4 + 1] = make_float2(a.z, a.w);
+      q2[g][j * 4 + 2] = make_float2(c.x, c.y);
+      q2[g][j * 4 + 3] = make_float2(c.z, c.w);
     }
   }
 
-  float m[G], l[G];
-  float2 o2[G][4];
+  float m[GW], l[GW];
+  float2 o2[GW][NCH * 4];
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
+  for (int g = 0; g < GW; ++g) {
     m[g] = -INFINITY;
     l[g] = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) o2[g][e] = make_float2(0.f, 0.f);
+    for (int e = 0; e < NCH * 4; ++e) o2[g][e] = make_float2(0.f, 0.f);
   }
 
   // The new key's rotated k and v, prepared by warp 1 (lane c owns pairs
@@ -215,6 +264,7 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::CTAS_PER_SM)
   }
 
   const bool structured = p.mask_mode == kMaskStructured;
+  float* scg = scs + (hs * C::NG + gq) * C::VP;
   bool aborted = false;
   for (int t = 0; t < ntiles; ++t) {
     const int s = t % kStages;
@@ -237,33 +287,52 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::CTAS_PER_SM)
     const int nvalid = min(T, ke - key0);
     const uint8_t* Ks = stage_k(s);
     const uint8_t* Vs = stage_v(s);
-    float sc[KPG][G];
+
+    // partial q.k of this lane's chunks for the group's KPG keys x GW heads
+    float x[C::VP];
 #pragma unroll
     for (int kk = 0; kk < KPG; ++kk) {
       const int kl = kk * C::NG + gq;
-      float2 k2[4];
-      const bool in = kl < nvalid;
-      if (in) {
-        unpack8x2(*reinterpret_cast<const uint4*>(Ks + (size_t)kl * D * 2 + sub * 16), k2);
+      float2 k2[NCH * 4];
+      if (kl < nvalid) {
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+          float2 t4[4];
+          unpack8x2(*reinterpret_cast<const uint4*>(Ks + (size_t)kl * D * 2 + (li + j * LPK) * 16), t4);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) k2[j * 4 + e] = t4[e];
+        }
       } else {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) k2[e] = make_float2(0.f, 0.f);
+        for (int e = 0; e < NCH * 4; ++e) k2[e] = make_float2(0.f, 0.f);
       }
-      bool vis = in;
-      if (structured) vis = vis && structured_visible(p, n_cached, key0 + kl);
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
+      for (int g = 0; g < GW; ++g) {
         float2 a = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) a = ffma2(q2[g][e], k2[e], a);
-        float d = a.x + a.y;
-#pragma unroll
-        for (int off = C::LPK / 2; off >= 1; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-        sc[kk][g] = vis ? d : -INFINITY;
+        for (int e = 0; e < NCH * 4; ++e) a = ffma2(q2[g][e], k2[e], a);
+        x[kk * GW + g] = a.x + a.y;
       }
     }
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
+    for (int v = C::V; v < C::VP; ++v) x[v] = 0.f;
+    ReduceScatter<C::VP, LPK / 2, C::VP>::run(x, li);
+    // every lane of the group needs every score: exchange through shared memory
+#pragma unroll
+    for (int i = 0; i < C::VPL; ++i) scg[li * C::VPL + i] = x[i];
+    __syncwarp();
+    float sc[KPG][GW];
+#pragma unroll
+    for (int kk = 0; kk < KPG; ++kk) {
+      const int kl = kk * C::NG + gq;
+      bool vis = kl < nvalid;
+      if (structured) vis = vis && structured_visible(p, n_cached, key0 + kl);
+#pragma unroll
+      for (int g = 0; g < GW; ++g) sc[kk][g] = vis ? scg[kk * GW + g] : -INFINITY;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int g = 0; g < GW; ++g) {
       float mc = sc[0][g];
 #pragma unroll
       for (int kk = 1; kk < KPG; ++kk) mc = fmaxf(mc, sc[kk][g]);
@@ -273,7 +342,7 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::CTAS_PER_SM)
         const float a = exp2f(m[g] - mc);   // 0 when m was -inf
         l[g] *= a;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) o2[g][e] = make_float2(o2[g][e].x * a, o2[g][e].y * a);
+        for (int e = 0; e < NCH * 4; ++e) o2[g][e] = make_float2(o2[g][e].x * a, o2[g][e].y * a);
         m[g] = mc;
       }
     }
@@ -281,16 +350,22 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::CTAS_PER_SM)
     for (int kk = 0; kk < KPG; ++kk) {
       const int kl = kk * C::NG + gq;
       if (kl < nvalid) {
-        float2 v2[4];
-        unpack8x2(*reinterpret_cast<const uint4*>(Vs + (size_t)kl * D * 2 + sub * 16), v2);
+        float2 v2[NCH * 4];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
+        for (int j = 0; j < NCH; ++j) {
+          float2 t4[4];
+          unpack8x2(*reinterpret_cast<const uint4*>(Vs + (size_t)kl * D * 2 + (li + j * LPK) * 16), t4);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v2[j * 4 + e] = t4[e];
+        }
+#pragma unroll
+        for (int g = 0; g < GW; ++g) {
           const float mu = (m[g] == -INFINITY) ? 0.f : m[g];
           const float pr = exp2f(sc[kk][g] - mu);
           l[g] += pr;
           const float2 p2 = make_float2(pr, pr);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) o2[g][e] = ffma2(p2, v2[e], o2[g][e]);
+          for (int e = 0; e < NCH * 4; ++e) o2[g][e] = ffma2(p2, v2[e], o2[g][e]);
         }
       }
     }
@@ -310,26 +385,53 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::CTAS_PER_SM)
       atomicOr(p.err, kErrTimeout);
     }
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
+    for (int g = 0; g < GW; ++g) {
       m[g] = -INFINITY;
       l[g] = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) o2[g][e] = make_float2(0.f, 0.f);
+      for (int e = 0; e < NCH * 4; ++e) o2[g][e] = make_float2(0.f, 0.f);
     }
     __syncthreads();
   }
 
-  // ---- merge the key groups (shared memory reused)
+  // ---- merge the key groups (pipeline shared memory reused)
   float* cmb_o = reinterpret_cast<float*>(smem);   // [NG][G][D]
   float* cmb_ml = cmb_o + C::NG * G * D;           // [NG][G][2]
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    float4* dst = reinterpret_cast<float4*>(cmb_o + ((size_t)gq * G + g) * D + sub * 8);
-    dst[0] = make_float4(o2[g][0].x, o2[g][0].y, o2[g][1].x, o2[g][1].y);
-    dst[1] = make_float4(o2[g][2].x, o2[g][2].y, o2[g][3].x, o2[g][3].y);
-    if (sub == 0) {
-      cmb_ml[(gq * G + g) * 2 + 0] = m[g];
-      cmb_ml[(gq * G + g) * 2 + 1] = l[g];
+  for (int gi = 0; gi < GW; ++gi) {
+    const int g = g0 + gi;
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      float4* dst = reinterpret_cast<float4*>(cmb_o + ((size_t)gq * G + g) * D + (li + j * LPK) * 8);
+      dst[0] = make_float4(o2[gi][j * 4 + 0].x, o2[gi][j * 4 + 0].y, o2[gi][j * 4 + 1].x, o2[gi][j * 4 + 1].y);
+      dst[1] = make_float4(o2[gi][j * 4 + 2].x, o2[gi][j * 4 + 2].y, o2[gi][j * 4 + 3].x, o2[gi][j * 4 + 3].y);
+    }
+    if (li == 0) {
+      cmb_ml[(gq * G + g) * 2 + 0] = m[gi];
+      cmb_ml[(gq * G + g) * 2 + 1] = l[gi];
+    }
+  }
+  __syncthreads();
+  // weight of group j for head g (one warp per head): w = 2^(m_j - M)
+  float* wg = wbuf;                    // [G][NG]
+  float* ML = wbuf + G * C::WN;        // [G][2]
+  for (int g = warp; g < G; g += NW) {
+    float M = -INFINITY;
+    for (int j = lane; j < C::NG; j += 32) M = fmaxf(M, cmb_ml[(j * G + g) * 2]);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f;
+    for (int j = lane; j < C::NG; j += 32) {
+      const float mj = cmb_ml[(j * G + g) * 2];
+      const float w = (mj == -INFINITY) ? 0.f : exp2f(mj - M);
+      wg[g * C::WN + j] = w;
+      L = fmaf(cmb_ml[(j * G + g) * 2 + 1], w, L);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    if (lane == 0) {
+      ML[g * 2 + 0] = M;
+      ML[g * 2 + 1] = L;
     }
   }
   __syncthreads();
@@ -337,25 +439,22 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::CTAS_PER_SM)
   const int S = p.num_splits;
   for (int i = tid; i < G * D; i += C::THREADS) {
     const int dd = i % D, g = i / D;
-    float M = -INFINITY;
+    const float* w = wg + g * C::WN;
+    float a0 = 0.f, a1 = 0.f;
 #pragma unroll 8
-    for (int j = 0; j < C::NG; ++j) M = fmaxf(M, cmb_ml[(j * G + g) * 2]);
-    float L = 0.f, O = 0.f;
-#pragma unroll 8
-    for (int j = 0; j < C::NG; ++j) {
-      const float mj = cmb_ml[(j * G + g) * 2];
-      const float w = (mj == -INFINITY) ? 0.f : exp2f(mj - M);
-      L = fmaf(cmb_ml[(j * G + g) * 2 + 1], w, L);
-      O = fmaf(cmb_o[((size_t)j * G + g) * D + dd], w, O);
+    for (int j = 0; j < C::NG; j += 2) {
+      a0 = fmaf(w[j], cmb_o[((size_t)j * G + g) * D + dd], a0);
+      a1 = fmaf(w[j + 1], cmb_o[((size_t)(j + 1) * G + g) * D + dd], a1);
     }
+    const float O = a0 + a1;
     if (S == 1) {
-      p.out[((size_t)b * p.n_q + h * G + g) * D + dd] = __float2bfloat16_rn(O / L);
+      p.out[((size_t)b * p.n_q + h * G + g) * D + dd] = __float2bfloat16_rn(O / ML[g * 2 + 1]);
     } else {
       const size_t base = ((size_t)b * p.n_kv + h) * S + split;
       p.part_o[(base * G + g) * D + dd] = O;
       if (dd == 0) {
-        p.part_ml[(base * G + g) * 2 + 0] = M;
-        p.part_ml[(base * G + g) * 2 + 1] = L;
+        p.part_ml[(base * G + g) * 2 + 0] = ML[g * 2 + 0];
+        p.part_ml[(base * G + g) * 2 + 1] = ML[g * 2 + 1];
       }
     }
   }
@@ -370,7 +469,7 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::CTAS_PER_SM)
   if (!*flag) return;
   __threadfence();
 
-  float* wts = reinterpret_cast<float*>(smem);   // [G][S]
+  float* wts = wbuf;   // [G][S] (S <= WN)
   const size_t base = ((size_t)b * p.n_kv + h) * S;
   for (int g = warp; g < G; g += NW) {
     float M = -INFINITY;
@@ -381,19 +480,19 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::CTAS_PER_SM)
     for (int s = lane; s < S; s += 32) {
       const float ms = __ldcg(&p.part_ml[((base + s) * G + g) * 2]);
       const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-      wts[g * S + s] = w;
+      wts[g * C::WN + s] = w;
       L = fmaf(__ldcg(&p.part_ml[((base + s) * G + g) * 2 + 1]), w, L);
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
     const float inv = 1.f / L;
     __syncwarp();
-    for (int s = lane; s < S; s += 32) wts[g * S + s] *= inv;
+    for (int s = lane; s < S; s += 32) wts[g * C::WN + s] *= inv;
   }
   __syncthreads();
   for (int i = tid; i < G * D; i += C::THREADS) {
     const int dd = i % D, g = i / D;
-    const float* w = wts + g * S;
+    const float* w = wts + g * C::WN;
     const float* po = p.part_o + (base * G + g) * D + dd;
     // independent partial sums so the loads of several splits are in flight
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
@@ -443,8 +542,7 @@ cudaError_t launch_d(const AttnParams& p, int group, cudaStream_t st) {
 int attn_tokens_per_cta(int) { return 1; }
 
 // One wave: units = sequences x kv heads; each unit's keys are split so that
-// the CTAs (one per SM: 16 warps for G <= 4, 8 warps for G = 5, 8) fill the
-// SMs once.
+// the CTAs (one wide CTA per SM) fill the SMs once.
 void attn_plan_splits(int units, int max_keys, int num_sms, int group, int* num_splits, int* split_keys) {
   (void)group;
   int s = num_sms / units;
