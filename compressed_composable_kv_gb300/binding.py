@@ -59,7 +59,7 @@ _SIGNATURES = {
     "c2kv_attend_prefill": (_i32, [_pg, _i32, _i32, _pvp, _pvp, _pvp, _i32, _pi32, _i32,
                                    _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "c2kv_attend_decode": (_i32, [_pg, _i32, _i32, _pvp, _pvp, _pvp, _i32, _vp, _i32,
-                                  _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+                                  _vp, _vp, _vp, _vp, _vp, _sz, ctypes.c_uint32, _vp]),
     "c2kv_attend_decode_noalloc": (_i32, [_pg, _i32, _i32, _pvp, _pvp, _pvp, _i32, _vp, _i32,
                                           _vp, _vp, _vp, _vp, _vp]),
     "c2kv_seq_advance": (_i32, [_i32, _vp, _i32, _vp]),
@@ -247,9 +247,12 @@ def c2kv_attend_prefill(geom, layer: int, k_caches, v_caches, rope_tables, cap: 
         _dev(out, torch.bfloat16, "out"), _dev(workspace, None, "workspace"), ws, _stream(stream)))
 
 
+C2KV_DECODE_OVERLAP_PREVIOUS = 1
+
+
 def c2kv_attend_decode(geom, layer: int, k_caches, v_caches, rope_tables, cap: int, n_cached_dev: torch.Tensor,
                        max_keys: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
-                       out: torch.Tensor, workspace: Optional[torch.Tensor], stream=None) -> None:
+                       out: torch.Tensor, workspace: Optional[torch.Tensor], stream=None, flags: int = 0) -> None:
     g = as_geometry(geom)
     B = len(k_caches)
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -257,7 +260,7 @@ def c2kv_attend_decode(geom, layer: int, k_caches, v_caches, rope_tables, cap: i
         ctypes.byref(g), int(layer), B, _ptrs(k_caches, "k_cache"), _ptrs(v_caches, "v_cache"),
         _tabs(rope_tables), int(cap), _dev(n_cached_dev, torch.int32, "n_cached_dev"), int(max_keys),
         _dev(q, torch.bfloat16, "q"), _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
-        _dev(out, torch.bfloat16, "out"), _dev(workspace, None, "workspace"), ws, _stream(stream)))
+        _dev(out, torch.bfloat16, "out"), _dev(workspace, None, "workspace"), ws, int(flags), _stream(stream)))
 
 
 def c2kv_attend_decode_noalloc(geom, layer: int, k_caches, v_caches, rope_tables, cap: int,

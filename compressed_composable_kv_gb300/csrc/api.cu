@@ -274,7 +274,8 @@ c2kv_status run_attention(const c2kv_geometry* g, int batch, const __nv_bfloat16
                           const __nv_bfloat16* const* vb, const CosSin2* const* tabs, const int32_t* n_cached_h,
                           const int32_t* n_cached_d, int cap, int max_keys, int t_len, int mask_mode, int n_doc,
                           int kblk, const void* q, void* out, void* workspace, size_t workspace_bytes,
-                          cudaStream_t st, const void* fused_k_new = nullptr, const void* fused_v_new = nullptr) {
+                          cudaStream_t st, const void* fused_k_new = nullptr, const void* fused_v_new = nullptr,
+                          bool overlap = false) {
   unsigned* err = nullptr;
   int sms = 0;
   c2kv_status s = device_state(&err, &sms);
@@ -313,7 +314,7 @@ c2kv_status run_attention(const c2kv_geometry* g, int batch, const __nv_bfloat16
   p.k_new = static_cast<const __nv_bfloat16*>(fused_k_new);
   p.v_new = static_cast<const __nv_bfloat16*>(fused_v_new);
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)g->head_dim));
-  C2KV_CUDA(launch_attention(p, g->head_dim, g->n_q_heads / g->n_kv_heads, st));
+  C2KV_CUDA(launch_attention(p, g->head_dim, g->n_q_heads / g->n_kv_heads, overlap, st));
   return C2KV_OK;
 }
 
@@ -699,8 +700,9 @@ c2kv_status c2kv_attend_decode(const c2kv_geometry* geom, int32_t layer, int32_t
                                void* const* v_caches, const void* const* rope_tables, int32_t cap,
                                const int32_t* n_cached_dev, int32_t max_keys, const void* q, const void* k_new,
                                const void* v_new, void* out, void* workspace, size_t workspace_bytes,
-                               void* stream) {
+                               uint32_t flags, void* stream) {
   c2kv_status s = check_geom(geom);
+  if (flags & ~uint32_t(C2KV_DECODE_OVERLAP_PREVIOUS)) return fail(C2KV_EINVAL, "unknown decode flags");
   if (s != C2KV_OK) return s;
   if (layer < 0 || layer >= geom->n_layers) return fail(C2KV_EINVAL, "layer out of range");
   s = check_caches(batch, k_caches, v_caches, cap);
@@ -723,7 +725,7 @@ c2kv_status c2kv_attend_decode(const c2kv_geometry* geom, int32_t layer, int32_t
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // One launch: the kernel rotates and stores the new key/value itself.
   return run_attention(geom, batch, kb, vb, tabs, nullptr, n_cached_dev, cap, max_keys, 1, kMaskCausal, 0, 0, q, out,
-                       workspace, workspace_bytes, st, k_new, v_new);
+                       workspace, workspace_bytes, st, k_new, v_new, (flags & C2KV_DECODE_OVERLAP_PREVIOUS) != 0);
 }
 
 c2kv_status c2kv_seq_advance(int32_t batch, int32_t* n_cached_dev, int32_t delta, void* stream) {
@@ -881,5 +883,5 @@ extern "C" c2kv_status c2kv_attend_decode_noalloc(const c2kv_geometry* geom, int
   // counters must start at zero, the partial results need no clearing.
   if (w.num_splits > 1) C2KV_CUDA(cudaMemsetAsync(scratch + w.counters_off, 0, w.ml_off - w.counters_off, st));
   return c2kv_attend_decode(geom, layer, batch, k_caches, v_caches, rope_tables, cap, n_cached_dev, max_keys, q,
-                            k_new, v_new, out, scratch, kNoallocScratchBytes, stream);
+                            k_new, v_new, out, scratch, kNoallocScratchBytes, 0, stream);
 }

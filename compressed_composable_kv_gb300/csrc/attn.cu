@@ -85,9 +85,8 @@ struct DCfg {
   static constexpr int OFF_SC = OFF_QS + G * D * 4;             // per-group scores [HS][NG][VP]
   static constexpr int OFF_W = OFF_SC + HS * NG * VP * 4;       // merge weights [G][WN] + [G] M, L
   static constexpr int OFF_BAR = (OFF_W + G * WN * 4 + 2 * G * 4 + 15) / 16 * 16;
-  static constexpr int OFF_TAB2 = OFF_BAR + (2 * kStages + 2) * 8;
-  static constexpr int OFF_CS = OFF_TAB2 + (D / 2) * 16;
-  static constexpr int SMEM = OFF_CS + 2 * (D / 2) * 4 + 16;
+  static constexpr int OFF_CS = OFF_BAR + (2 * kStages + 2) * 8;   // merge flag
+  static constexpr int SMEM = OFF_CS + 16;
   static_assert(G % GW == 0 && NWK >= 1 && NG % 2 == 0, "decode tiling");
 };
 
@@ -137,10 +136,7 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, 1) decode_kernel(const __
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + kStages;
   uint64_t* inj = empty + kStages;                                     // new-key row injected
-  CosSin2* tab2 = reinterpret_cast<CosSin2*>(smem + C::OFF_TAB2);      // [D/2], row of the new key
-  float* cs = reinterpret_cast<float*>(smem + C::OFF_CS);              // [D/2]
-  float* sn = cs + D / 2;
-  int* flag = reinterpret_cast<int*>(sn + D / 2);
+  int* flag = reinterpret_cast<int*>(smem + C::OFF_CS);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -191,23 +187,23 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, 1) decode_kernel(const __
     fence_barrier_init();
     for (; issued < min(kStages, ntiles); ++issued) issue(issued);
   }
-  // cos/sin of the token's position: row n_cached of the sequence's table
-  // (hi parts rotate q; the full pairs rotate the new key when fused).
-  for (int f = tid; f < D / 2; f += C::THREADS) {
-    const CosSin2 e = p.tab[b][(size_t)n_cached * (D / 2) + f];
-    cs[f] = e.ch;
-    sn[f] = e.sh;
-    if (has_new) tab2[f] = e;
-  }
-  __syncthreads();
-  // q of the kv head's G query heads, rotated once per CTA and pre-scaled by
-  // log2(e)/sqrt(d), into shared memory.
+  // Everything above reads only the lengths, the cache rows below n_cached
+  // and nothing written since; with an overlapping launch (the caller's
+  // C2KV_DECODE_OVERLAP_PREVIOUS) it runs while the previous kernel on the
+  // stream finishes.  From here on the previous kernel must be complete:
+  // q, the new k/v, the outputs and the scratch may be shared with it.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // q of the kv head's G query heads, rotated once per CTA (cos/sin from row
+  // n_cached of the sequence's table) and pre-scaled by log2(e)/sqrt(d).
+  const CosSin2* trow = p.tab[b] + (size_t)n_cached * (D / 2);
   for (int i = tid; i < G * (D / 2); i += C::THREADS) {
     const int g = i / (D / 2), f = i % (D / 2);
     const __nv_bfloat16* row = p.q + ((size_t)b * p.n_q + h * G + g) * D;
     const float x = __bfloat162float(row[f]), y = __bfloat162float(row[f + D / 2]);
-    qs[g * D + f] = (x * cs[f] - y * sn[f]) * p.scale_log2;
-    qs[g * D + f + D / 2] = (y * cs[f] + x * sn[f]) * p.scale_log2;
+    const float c = trow[f].ch, sn = trow[f].sh;
+    qs[g * D + f] = (x * c - y * sn) * p.scale_log2;
+    qs[g * D + f + D / 2] = (y * c + x * sn) * p.scale_log2;
   }
   __syncthreads();
 
@@ -254,7 +250,7 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, 1) decode_kernel(const __
     nk_b = ks[lane + TPR];
     nv_a = vs[lane];
     nv_b = vs[lane + TPR];
-    rotate8_df(nk_a, nk_b, &tab2[lane * 8]);
+    rotate8_df(nk_a, nk_b, trow + lane * 8);
     uint4* kd = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(kg) + (size_t)nk * D);
     uint4* vd = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(vg) + (size_t)nk * D);
     kd[lane] = nk_a;
@@ -512,7 +508,7 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, 1) decode_kernel(const __
 }
 
 template <int D, int G>
-cudaError_t launch_one(const AttnParams& p, cudaStream_t st) {
+cudaError_t launch_one(const AttnParams& p, bool overlap, cudaStream_t st) {
   using C = DCfg<D, G>;
   static bool configured = false;
   if (!configured) {
@@ -520,19 +516,27 @@ cudaError_t launch_one(const AttnParams& p, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const dim3 grid(p.num_splits, p.n_kv, p.batch);
-  decode_kernel<D, G><<<grid, C::THREADS, C::SMEM, st>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_splits, p.n_kv, p.batch);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<D, G>, p);
 }
 
 template <int D>
-cudaError_t launch_d(const AttnParams& p, int group, cudaStream_t st) {
+cudaError_t launch_d(const AttnParams& p, int group, bool overlap, cudaStream_t st) {
   switch (group) {
-    case 1: return launch_one<D, 1>(p, st);
-    case 2: return launch_one<D, 2>(p, st);
-    case 4: return launch_one<D, 4>(p, st);
-    case 5: return launch_one<D, 5>(p, st);
-    case 8: return launch_one<D, 8>(p, st);
+    case 1: return launch_one<D, 1>(p, overlap, st);
+    case 2: return launch_one<D, 2>(p, overlap, st);
+    case 4: return launch_one<D, 4>(p, overlap, st);
+    case 5: return launch_one<D, 5>(p, overlap, st);
+    case 8: return launch_one<D, 8>(p, overlap, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -558,10 +562,10 @@ void attn_plan_splits(int units, int max_keys, int num_sms, int group, int* num_
   if (*num_splits < 1) *num_splits = 1;
 }
 
-cudaError_t launch_attention(const AttnParams& p, int head_dim, int group, cudaStream_t st) {
+cudaError_t launch_attention(const AttnParams& p, int head_dim, int group, bool overlap, cudaStream_t st) {
   if (p.t_len != 1) return cudaErrorInvalidValue;
-  if (head_dim == 128) return launch_d<128>(p, group, st);
-  if (head_dim == 64) return launch_d<64>(p, group, st);
+  if (head_dim == 128) return launch_d<128>(p, group, overlap, st);
+  if (head_dim == 64) return launch_d<64>(p, group, overlap, st);
   return cudaErrorInvalidValue;
 }
 

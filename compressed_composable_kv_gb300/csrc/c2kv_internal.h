@@ -270,7 +270,7 @@ struct AttnParams {
 cudaError_t launch_rerope(const RopeParams& p, int head_dim, cudaStream_t st);
 cudaError_t launch_rope_table(const TableParams& p, cudaStream_t st);
 cudaError_t launch_append(const AppendParams& p, int head_dim, int batch, cudaStream_t st);
-cudaError_t launch_attention(const AttnParams& p, int head_dim, int group, cudaStream_t st);
+cudaError_t launch_attention(const AttnParams& p, int head_dim, int group, bool overlap, cudaStream_t st);
 cudaError_t launch_advance(int batch, int32_t* n_cached, int delta, cudaStream_t st);
 
 cudaError_t launch_prefill_tc(const PrefillTcParams& p, int head_dim, int group, cudaStream_t st);

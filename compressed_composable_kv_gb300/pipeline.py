@@ -79,10 +79,15 @@ class RequestBatch:
         with torch.cuda.stream(s):
             self.n_cached_dev.copy_(self._dec_start, non_blocking=True)
 
-    def decode(self, layer: int, q, k_new, v_new, out, stream=None) -> None:
+    def decode(self, layer: int, q, k_new, v_new, out, stream=None, overlap_previous: Optional[bool] = None) -> None:
+        """One decode step of one layer.  By default a layer > 0 call may start
+        while the previous kernel on the stream (this batch's decode of the
+        layer before) finishes: see C2KV_DECODE_OVERLAP_PREVIOUS."""
+        if overlap_previous is None:
+            overlap_previous = layer > 0
         B.c2kv_attend_decode(self.geom, layer, self.k_caches, self.v_caches, self.rope_tables, self.cap,
                              self.n_cached_dev, self.max_keys_decode, q, k_new, v_new, out, self.workspace,
-                             stream)
+                             stream, B.C2KV_DECODE_OVERLAP_PREVIOUS if overlap_previous else 0)
 
     def advance(self, stream=None) -> None:
         B.c2kv_seq_advance(self.n_cached_dev, 1, stream)

@@ -249,7 +249,19 @@ c2kv_status c2kv_attend_decode(const c2kv_geometry* geom, int32_t layer,
                                int32_t cap, const int32_t* n_cached_dev, int32_t max_keys,
                                const void* q, const void* k_new, const void* v_new,
                                void* out, void* workspace, size_t workspace_bytes,
-                               void* stream);
+                               uint32_t flags, void* stream);
+
+/*
+ * Decode flag: the launch may begin while the kernel enqueued just before it
+ * on `stream` is still finishing (programmatic dependent launch).  Before it
+ * waits for that kernel it reads only n_cached_dev, the RoPE table and the
+ * cache rows below n_cached_dev[b] of this layer, so the caller promises that
+ * the previous kernel writes none of these (e.g. it is the decode of another
+ * layer, or the projection producing q/k_new/v_new -- but not
+ * c2kv_seq_advance).  q, k_new, v_new, out and the workspace are touched only
+ * after the previous kernel has completed.
+ */
+#define C2KV_DECODE_OVERLAP_PREVIOUS 1u
 
 /*
  * c2kv_attend_decode without a workspace argument: the paper has no
@@ -263,7 +275,7 @@ c2kv_status c2kv_attend_decode(const c2kv_geometry* geom, int32_t layer,
  * loads the library holds that array until the process exits.  This call
  * allocates nothing (no cudaMalloc/cudaFree, no allocating library routine).
  *
- * Arguments and results are those of c2kv_attend_decode.  The first call on
+ * Arguments and results are those of c2kv_attend_decode (with flags 0).  The first call on
  * a device looks up the array's device address (cudaGetSymbolAddress) with
  * that device current; make that first call before any stream capture.  The
  * array is shared by every call and keeps the previous call's contents: each

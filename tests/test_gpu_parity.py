@@ -349,3 +349,32 @@ def test_rope_table_matches_fp64_angles():
         assert np.abs(t[..., 2] + t[..., 3] - np.sin(ang)).max() < 1e-12
         # the hi parts alone are the fp32-rounded values
         assert np.abs(t[..., 0] - np.cos(ang)).max() < 1e-7
+
+
+def test_decode_overlapped_launches_match_serial_ones():
+    """Layer > 0 decode launches may start while the previous layer's decode
+    finishes (C2KV_DECODE_OVERLAP_PREVIOUS); the results must be identical to
+    fully serialised launches."""
+    g = S.Geometry(4, 32, 8, 128, 5.0e5)
+    specs = [(i, 4000, 1000) for i in range(4)]
+    w = S.Workload("ovl", g, 4, 1, 0, 3, seed=0xC2C5)
+    inputs = upload(S.make_step_inputs(w))
+    outs = []
+    for overlap in (False, True):
+        sc = Scenario(g, 4, specs, [(list(range(4)), [2, 0, 3, 1])], q_len=0, decode_steps=3, seed=0xC2C5)
+        bt = sc.batch
+        bt.compose()
+        bt.reset_decode()
+        res = []
+        for t in range(3):
+            for l in range(4):
+                o = torch.empty_like(inputs["qd_pre"][t, l])
+                bt.decode(l, inputs["qd_pre"][t, l], inputs["kd_pre"][t, l], inputs["vd"][t, l], o,
+                          overlap_previous=overlap and l > 0)
+                res.append(o)
+            bt.advance()
+        torch.cuda.synchronize()
+        assert P.c2kv_device_error() == P.C2KV_OK
+        outs.append(torch.stack(res).cpu())
+        sc.close()
+    assert torch.equal(outs[0], outs[1])
