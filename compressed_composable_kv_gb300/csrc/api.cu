@@ -310,6 +310,25 @@ c2kv_status run_attention(const c2kv_geometry* g, int batch, const __nv_bfloat16
   p.mask_mode = mask_mode;
   p.n_doc = n_doc;
   p.kblk = kblk;
+  // Prefer merging the key splits inside a thread-block cluster (no global
+  // partials) when clusters of that many CTAs fit the GPU all at once.
+  {
+    const int units = batch * g->n_kv_heads;
+    int want = sms / units;
+    const int by_keys = (max_keys + 63) / 64;
+    if (want > by_keys) want = by_keys;
+    const int cs = attn_cluster_splits(units, want, g->head_dim, g->n_q_heads / g->n_kv_heads);
+    if (cs >= 2) {
+      int sk = (max_keys + cs - 1) / cs;
+      sk = (sk + 7) / 8 * 8;
+      const int ns = (max_keys + sk - 1) / sk;
+      if (ns >= 2) {
+        p.num_splits = ns;
+        p.split_keys = sk;
+        p.cluster_merge = 1;
+      }
+    }
+  }
   p.fuse_append = fused_k_new != nullptr ? 1 : 0;
   p.k_new = static_cast<const __nv_bfloat16*>(fused_k_new);
   p.v_new = static_cast<const __nv_bfloat16*>(fused_v_new);

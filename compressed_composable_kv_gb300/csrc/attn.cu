@@ -29,7 +29,11 @@
 // the other warps read the tile.
 #include <float.h>
 
+#include <cooperative_groups.h>
+
 #include "c2kv_internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace c2kv {
 
@@ -81,7 +85,8 @@ struct DCfg {
   static constexpr int CMB = NG * G * (D + 2) * 4;
   static constexpr int MAIN = ((PIPE > CMB ? PIPE : CMB) + 127) / 128 * 128;
   static constexpr int WN = NG > kMaxSplits ? NG : kMaxSplits;
-  static constexpr int OFF_QS = MAIN;                          // rotated, scaled q [G][D] fp32
+  static constexpr int OFF_OCL = MAIN;                         // this split's O [G][D] for the cluster merge
+  static constexpr int OFF_QS = OFF_OCL + G * D * 4;            // rotated, scaled q [G][D] fp32
   static constexpr int OFF_SC = OFF_QS + G * D * 4;             // per-group scores [HS][NG][VP]
   static constexpr int OFF_W = OFF_SC + HS * NG * VP * 4;       // merge weights [G][WN] + [G] M, L
   static constexpr int OFF_BAR = (OFF_W + G * WN * 4 + 2 * G * 4 + 15) / 16 * 16;
@@ -131,6 +136,7 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, 1) decode_kernel(const __
   constexpr int TPR = D / 16;
   extern __shared__ __align__(1024) uint8_t smem[];
   float* qs = reinterpret_cast<float*>(smem + C::OFF_QS);
+  float* ocl = reinterpret_cast<float*>(smem + C::OFF_OCL);
   float* scs = reinterpret_cast<float*>(smem + C::OFF_SC);
   float* wbuf = reinterpret_cast<float*>(smem + C::OFF_W);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -443,7 +449,9 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, 1) decode_kernel(const __
       a1 = fmaf(w[j + 1], cmb_o[((size_t)(j + 1) * G + g) * D + dd], a1);
     }
     const float O = a0 + a1;
-    if (S == 1) {
+    if (p.cluster_merge) {
+      ocl[g * D + dd] = O;
+    } else if (S == 1) {
       p.out[((size_t)b * p.n_q + h * G + g) * D + dd] = __float2bfloat16_rn(O / ML[g * 2 + 1]);
     } else {
       const size_t base = ((size_t)b * p.n_kv + h) * S + split;
@@ -453,6 +461,29 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, 1) decode_kernel(const __
         p.part_ml[(base * G + g) * 2 + 1] = ML[g * 2 + 1];
       }
     }
+  }
+  if (p.cluster_merge) {
+    // The splits of this (b, h) form one thread-block cluster: merge them
+    // through distributed shared memory, each CTA producing every S-th output.
+    cg::cluster_group cl = cg::this_cluster();
+    cl.sync();   // every split's O and (M, L) are in its shared memory
+    const int r = (int)cl.block_rank();
+    for (int i = r + S * tid; i < G * D; i += S * C::THREADS) {
+      const int dd = i % D, g = i / D;
+      float M = -INFINITY;
+      for (int sp = 0; sp < S; ++sp) M = fmaxf(M, cl.map_shared_rank(ML, sp)[g * 2]);
+      float L = 0.f, O = 0.f;
+      for (int sp = 0; sp < S; ++sp) {
+        const float* ml = cl.map_shared_rank(ML, sp);
+        const float ms = ml[g * 2];
+        const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+        L = fmaf(ml[g * 2 + 1], w, L);
+        O = fmaf(cl.map_shared_rank(ocl, sp)[g * D + dd], w, O);
+      }
+      p.out[((size_t)b * p.n_q + h * G + g) * D + dd] = __float2bfloat16_rn(O / L);
+    }
+    cl.sync();   // no CTA leaves while others still read its shared memory
+    return;
   }
   if (S == 1) return;
 
@@ -521,12 +552,76 @@ cudaError_t launch_one(const AttnParams& p, bool overlap, cudaStream_t st) {
   cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (overlap) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (p.cluster_merge) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = p.num_splits;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = overlap ? 1 : 0;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, decode_kernel<D, G>, p);
+}
+
+// Largest cluster of key splits (<= 16, one CTA per split) of which `units`
+// clusters can be resident at once; 0 if none of size >= 2 fits.
+template <int D, int G>
+int cluster_splits_for(int units, int want) {
+  using C = DCfg<D, G>;
+  static int cache[17] = {};   // max active clusters per size, -1 = unknown error
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    configured = true;
+  }
+  for (int cs = want < 16 ? want : 16; cs >= 2; --cs) {
+    if (cache[cs] == 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(cs, 1, 1);
+      cfg.blockDim = dim3(C::THREADS);
+      cfg.dynamicSmemBytes = C::SMEM;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = cs;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<D, G>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = -1;
+      }
+      cache[cs] = n == 0 ? -1 : n;
+    }
+    if (cache[cs] >= units) return cs;
+  }
+  return 0;
+}
+
+template <int D>
+int cluster_d(int units, int want, int group) {
+  switch (group) {
+    case 1: return cluster_splits_for<D, 1>(units, want);
+    case 2: return cluster_splits_for<D, 2>(units, want);
+    case 4: return cluster_splits_for<D, 4>(units, want);
+    case 5: return cluster_splits_for<D, 5>(units, want);
+    case 8: return cluster_splits_for<D, 8>(units, want);
+    default: return 0;
+  }
 }
 
 template <int D>
@@ -560,6 +655,13 @@ void attn_plan_splits(int units, int max_keys, int num_sms, int group, int* num_
   *split_keys = sk;
   *num_splits = (max_keys + sk - 1) / sk;
   if (*num_splits < 1) *num_splits = 1;
+}
+
+int attn_cluster_splits(int units, int want, int head_dim, int group) {
+  if (want < 2) return 0;
+  if (head_dim == 128) return cluster_d<128>(units, want, group);
+  if (head_dim == 64) return cluster_d<64>(units, want, group);
+  return 0;
 }
 
 cudaError_t launch_attention(const AttnParams& p, int head_dim, int group, bool overlap, cudaStream_t st) {

@@ -263,6 +263,9 @@ struct AttnParams {
   int32_t fuse_append;
   const __nv_bfloat16* k_new;
   const __nv_bfloat16* v_new;
+  // The num_splits CTAs of a (sequence, kv head) run as one thread-block
+  // cluster and merge their partial results in distributed shared memory.
+  int32_t cluster_merge;
   float scale_log2;
 };
 
@@ -281,5 +284,6 @@ constexpr int kTcMaxSplits = 128;
 // Attention work decomposition shared by the launcher and the workspace query.
 int attn_tokens_per_cta(int t_len);
 void attn_plan_splits(int units, int max_keys, int num_sms, int group, int* num_splits, int* split_keys);
+int attn_cluster_splits(int units, int want, int head_dim, int group);
 
 }  // namespace c2kv
