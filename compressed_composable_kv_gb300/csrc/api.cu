@@ -318,7 +318,8 @@ c2kv_status run_attention(const c2kv_geometry* g, int batch, const __nv_bfloat16
     const int by_keys = (max_keys + 63) / 64;
     if (want > by_keys) want = by_keys;
     const int cs = attn_cluster_splits(units, want, g->head_dim, g->n_q_heads / g->n_kv_heads);
-    if (cs >= 2) {
+    // only when the cluster keeps as many CTAs streaming as the global plan
+    if (cs >= 2 && cs >= w.num_splits) {
       int sk = (max_keys + cs - 1) / cs;
       sk = (sk + 7) / 8 * 8;
       const int ns = (max_keys + sk - 1) / sk;

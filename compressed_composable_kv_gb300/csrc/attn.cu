@@ -496,44 +496,25 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, 1) decode_kernel(const __
   if (!*flag) return;
   __threadfence();
 
-  float* wts = wbuf;   // [G][S] (S <= WN)
+  // One output per thread; all of its loads (the S partial values and the S
+  // (m, l) pairs of its head) are issued before any is used.
   const size_t base = ((size_t)b * p.n_kv + h) * S;
-  for (int g = warp; g < G; g += NW) {
-    float M = -INFINITY;
-    for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldcg(&p.part_ml[((base + s) * G + g) * 2]));
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float L = 0.f;
-    for (int s = lane; s < S; s += 32) {
-      const float ms = __ldcg(&p.part_ml[((base + s) * G + g) * 2]);
-      const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-      wts[g * C::WN + s] = w;
-      L = fmaf(__ldcg(&p.part_ml[((base + s) * G + g) * 2 + 1]), w, L);
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-    const float inv = 1.f / L;
-    __syncwarp();
-    for (int s = lane; s < S; s += 32) wts[g * C::WN + s] *= inv;
-  }
-  __syncthreads();
   for (int i = tid; i < G * D; i += C::THREADS) {
     const int dd = i % D, g = i / D;
-    const float* w = wts + g * C::WN;
     const float* po = p.part_o + (base * G + g) * D + dd;
-    // independent partial sums so the loads of several splits are in flight
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-    int s = 0;
-    for (; s + 4 <= S; s += 4) {
-      const float x0 = __ldcg(po + (size_t)(s + 0) * G * D), x1 = __ldcg(po + (size_t)(s + 1) * G * D);
-      const float x2 = __ldcg(po + (size_t)(s + 2) * G * D), x3 = __ldcg(po + (size_t)(s + 3) * G * D);
-      a0 = fmaf(w[s + 0], x0, a0);
-      a1 = fmaf(w[s + 1], x1, a1);
-      a2 = fmaf(w[s + 2], x2, a2);
-      a3 = fmaf(w[s + 3], x3, a3);
+    const float* pm = p.part_ml + (base * G + g) * 2;
+    float M = -INFINITY;
+#pragma unroll 8
+    for (int sp = 0; sp < S; ++sp) M = fmaxf(M, __ldcg(pm + (size_t)sp * G * 2));
+    float L = 0.f, O = 0.f;
+#pragma unroll 8
+    for (int sp = 0; sp < S; ++sp) {
+      const float ms = __ldcg(pm + (size_t)sp * G * 2);
+      const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+      L = fmaf(__ldcg(pm + (size_t)sp * G * 2 + 1), w, L);
+      O = fmaf(__ldcg(po + (size_t)sp * G * D), w, O);
     }
-    for (; s < S; ++s) a0 = fmaf(w[s], __ldcg(po + (size_t)s * G * D), a0);
-    p.out[((size_t)b * p.n_q + h * G + g) * D + dd] = __float2bfloat16_rn((a0 + a1) + (a2 + a3));
+    p.out[((size_t)b * p.n_q + h * G + g) * D + dd] = __float2bfloat16_rn(O / L);
   }
   if (tid == 0) p.counters[cidx] = 0;
 }
