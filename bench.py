@@ -437,6 +437,81 @@ def run_ours(args, rank: int, world: int) -> dict:
     return out
 
 
+def run_sweep(args) -> None:
+    """Decode time per token over a composed cache of 16k..128k original
+    tokens, compressed at k=4 vs uncompressed (k=1), batch 4, Llama3.1-8B
+    attention geometry (C2KV explainer, section "results": the full cache's
+    per-token decode time grows ~linearly with context, the compressed one
+    reads a quarter of the bytes).  Only decode attention is timed: each
+    step is the 32 layers' decode launches replayed from a CUDA graph; the
+    caches are filled with N(0,1) bf16 on the device outside the timed region.
+    Prints one JSON line per (context, k)."""
+    import torch
+    import compressed_composable_kv_gb300 as P
+    from compressed_composable_kv_gb300 import synth as S
+
+    g = S.LLAMA31_8B
+    L, H, D, B = g.n_layers, g.n_kv_heads, g.head_dim, 4
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    stream = torch.cuda.Stream()
+    peak = measured_peaks().get("hbm_gbs") or 6800.0
+    for ctx in (16384, 32768, 65536, 131072):
+        for k in (4, 1):
+            n = ctx // k
+            steps = 16
+            cap = n + steps + 32
+            kc = [torch.randn((L, H, cap, D), device="cuda").to(torch.bfloat16) for _ in range(B)]
+            vc = [torch.randn((L, H, cap, D), device="cuda").to(torch.bfloat16) for _ in range(B)]
+            tab_bytes = P.c2kv_rope_table_bytes(g, cap)
+            tabs = [torch.empty(tab_bytes // 4, dtype=torch.float32, device="cuda") for _ in range(B)]
+            pos = torch.arange(cap, dtype=torch.int32, device="cuda")
+            for t in tabs:
+                P.c2kv_rope_table(g, pos, t)
+            n_dev = torch.full((B,), n, dtype=torch.int32, device="cuda")
+            max_keys = n + steps
+            ws = torch.zeros(P.c2kv_attend_workspace_size(g, B, 1, max_keys), dtype=torch.uint8, device="cuda")
+            q = torch.randn((steps, L, B, g.n_q_heads, D), device="cuda").to(torch.bfloat16)
+            kn = torch.randn((steps, L, B, H, D), device="cuda").to(torch.bfloat16)
+            out = torch.empty((steps, L, B, g.n_q_heads, D), dtype=torch.bfloat16, device="cuda")
+
+            def decode_all():
+                for t in range(steps):
+                    for l in range(L):
+                        P.c2kv_attend_decode(g, l, kc, vc, tabs, cap, n_dev, max_keys, q[t, l], kn[t, l], kn[t, l],
+                                             out[t, l], ws, stream, P.C2KV_DECODE_OVERLAP_PREVIOUS if l else 0)
+                    P.c2kv_seq_advance(n_dev, 1, stream)
+
+            with torch.cuda.stream(stream):
+                decode_all()
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                with torch.cuda.graph(graph, stream=stream):
+                    decode_all()
+            times = []
+            for rep in range(args.warmup + args.steps):
+                with torch.cuda.stream(stream):
+                    n_dev.fill_(n)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    e0.record(stream)
+                    graph.replay()
+                    e1.record(stream)
+                e1.synchronize()
+                if rep >= args.warmup:
+                    times.append(e0.elapsed_time(e1) / 1e3)
+            assert P.c2kv_device_error() == P.C2KV_OK
+            t_step = statistics.median(times) / steps            # all layers, one token
+            keys = sum(n + i + 1 for i in range(steps)) / steps
+            gbs = B * keys * H * D * 2 * 2 * L / t_step / 1e9
+            print(json.dumps({"sweep": "decode_vs_context", "original_tokens": ctx, "k": k, "cache_rows": n,
+                              "batch": B, "layers": L, "ms_per_token": t_step * 1e3,
+                              "tok_s": B / t_step, "attention_hbm_gbs": gbs, "frac_of_hbm_peak": gbs / peak}))
+            del kc, vc, tabs, graph, ws, q, kn, out
+            torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -446,7 +521,12 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="decode time vs context (16k..128k), compressed k=4 vs uncompressed")
     args = ap.parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
 

@@ -487,34 +487,77 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, 1) decode_kernel(const __
   }
   if (S == 1) return;
 
-  // ---- last CTA of (b, h) merges the split partials
-  __threadfence();
+  // ---- last CTA of (b, h) merges the split partials.  The CTA barrier
+  // orders every thread's partial stores before thread 0's acq_rel arrival
+  // (release, cumulative); the last arriver's acquire, then the barrier,
+  // orders its threads' partial loads after every split's stores.
   __syncthreads();
   const int cidx = b * p.n_kv + h;
-  if (tid == 0) *flag = (atomicAdd(&p.counters[cidx], 1) == S - 1);
+  if (tid == 0) {
+    int prev;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(prev) : "l"(p.counters + cidx) : "memory");
+    *flag = (prev == S - 1);
+  }
   __syncthreads();
   if (!*flag) return;
-  __threadfence();
 
-  // One output per thread; all of its loads (the S partial values and the S
-  // (m, l) pairs of its head) are issued before any is used.
+  float* wts = wbuf;   // [G][S] (S <= WN)
   const size_t base = ((size_t)b * p.n_kv + h) * S;
+  // The partial outputs of the first kPre splits of this thread's first
+  // output are loaded now, in flight together with the (m, l) loads below.
+  constexpr int kPre = 24;
+  float pre[kPre];
+  if (tid < G * D) {
+    const float* po = p.part_o + (base * G + tid / D) * D + tid % D;
+#pragma unroll
+    for (int sp = 0; sp < kPre; ++sp) pre[sp] = sp < S ? __ldcg(po + (size_t)sp * G * D) : 0.f;
+  }
+  for (int g = warp; g < G; g += NW) {
+    float M = -INFINITY;
+    for (int sp = lane; sp < S; sp += 32) M = fmaxf(M, __ldcg(&p.part_ml[((base + sp) * G + g) * 2]));
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f;
+    for (int sp = lane; sp < S; sp += 32) {
+      const float ms = __ldcg(&p.part_ml[((base + sp) * G + g) * 2]);
+      const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+      wts[g * C::WN + sp] = w;
+      L = fmaf(__ldcg(&p.part_ml[((base + sp) * G + g) * 2 + 1]), w, L);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    const float inv = 1.f / L;
+    __syncwarp();
+    for (int sp = lane; sp < S; sp += 32) wts[g * C::WN + sp] *= inv;
+  }
+  __syncthreads();
   for (int i = tid; i < G * D; i += C::THREADS) {
     const int dd = i % D, g = i / D;
+    const float* w = wts + g * C::WN;
     const float* po = p.part_o + (base * G + g) * D + dd;
-    const float* pm = p.part_ml + (base * G + g) * 2;
-    float M = -INFINITY;
-#pragma unroll 8
-    for (int sp = 0; sp < S; ++sp) M = fmaxf(M, __ldcg(pm + (size_t)sp * G * 2));
-    float L = 0.f, O = 0.f;
-#pragma unroll 8
-    for (int sp = 0; sp < S; ++sp) {
-      const float ms = __ldcg(pm + (size_t)sp * G * 2);
-      const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-      L = fmaf(__ldcg(pm + (size_t)sp * G * 2 + 1), w, L);
-      O = fmaf(__ldcg(po + (size_t)sp * G * D), w, O);
+    // independent partial sums so the loads of several splits are in flight
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    int sp = 0;
+    if (i == tid) {
+#pragma unroll
+      for (int j = 0; j < kPre; j += 4) {
+        a0 = fmaf(j + 0 < S ? w[j + 0] : 0.f, pre[j + 0], a0);
+        a1 = fmaf(j + 1 < S ? w[j + 1] : 0.f, pre[j + 1], a1);
+        a2 = fmaf(j + 2 < S ? w[j + 2] : 0.f, pre[j + 2], a2);
+        a3 = fmaf(j + 3 < S ? w[j + 3] : 0.f, pre[j + 3], a3);
+      }
+      sp = kPre;
     }
-    p.out[((size_t)b * p.n_q + h * G + g) * D + dd] = __float2bfloat16_rn(O / L);
+    for (; sp + 4 <= S; sp += 4) {
+      const float x0 = __ldcg(po + (size_t)(sp + 0) * G * D), x1 = __ldcg(po + (size_t)(sp + 1) * G * D);
+      const float x2 = __ldcg(po + (size_t)(sp + 2) * G * D), x3 = __ldcg(po + (size_t)(sp + 3) * G * D);
+      a0 = fmaf(w[sp + 0], x0, a0);
+      a1 = fmaf(w[sp + 1], x1, a1);
+      a2 = fmaf(w[sp + 2], x2, a2);
+      a3 = fmaf(w[sp + 3], x3, a3);
+    }
+    for (; sp < S; ++sp) a0 = fmaf(w[sp], __ldcg(po + (size_t)sp * G * D), a0);
+    p.out[((size_t)b * p.n_q + h * G + g) * D + dd] = __float2bfloat16_rn((a0 + a1) + (a2 + a3));
   }
   if (tid == 0) p.counters[cidx] = 0;
 }
