@@ -160,23 +160,21 @@ AttnWs attn_workspace(const c2kv_geometry* g, int batch, int t_len, int max_keys
     w.n_tb = 1;
     attn_plan_splits(batch * g->n_kv_heads, max_keys, num_sms, grp, &w.num_splits, &w.split_keys);
   } else {
+    // tensor-core prefill: splits are merged inside a cluster (no partials
+    // here); the scratch holds only the rotated q
     const int tok = prefill_tc_tokens_per_tile(grp);
-    const int kt = prefill_tc_key_tile();
     w.n_tb = (t_len + tok - 1) / tok;
-    const int units = batch * w.n_tb * g->n_kv_heads;
-    int s = (num_sms + units - 1) / units;
-    s = std::min(s, (max_keys + kt - 1) / kt);
-    s = std::max(1, std::min(s, kTcMaxSplits));
-    int sk = (max_keys + s - 1) / s;
-    sk = std::max(kt, (sk + kt - 1) / kt * kt);
-    w.split_keys = sk;
-    w.num_splits = (max_keys + sk - 1) / sk;
+    w.num_splits = 1;
+    w.split_keys = max_keys;
   }
   const size_t rows = (size_t)batch * t_len * g->n_kv_heads * w.num_splits * grp;
+  // The arrival counters sit at the start of every layout, sized for the
+  // largest batch, so that no call's other scratch (partials, rotated q)
+  // overwrites counters another call relies on being zero.
   size_t off = 0;
+  w.counters_off = 0;
+  off += align256((size_t)kMaxBatch * g->n_kv_heads * sizeof(int32_t));
   if (w.num_splits > 1) {
-    w.counters_off = off;
-    off += align256((size_t)batch * w.n_tb * g->n_kv_heads * sizeof(int32_t));
     w.ml_off = off;
     off += align256(rows * 2 * sizeof(float));
     w.o_off = off;
@@ -229,7 +227,8 @@ c2kv_status run_prefill_tc(const c2kv_geometry* g, int batch, const void* const*
                            int layer, int t_len, int max_keys, int mask_mode, int n_doc, int kblk,
                            void* out, const AttnWs& w, uint8_t* ws, cudaStream_t st) {
   unsigned* err = nullptr;
-  c2kv_status s = device_state(&err, nullptr);
+  int sms = 0;
+  c2kv_status s = device_state(&err, &sms);
   if (s != C2KV_OK) return s;
   static PrefillTcParams p;   // large (tensor maps); guarded by the mutex below
   static std::mutex mu;
@@ -248,23 +247,17 @@ c2kv_status run_prefill_tc(const c2kv_geometry* g, int batch, const void* const*
     p.n_cached[b] = n_cached[b];
   }
   p.out = static_cast<__nv_bfloat16*>(out);
-  p.part_o = w.num_splits > 1 ? reinterpret_cast<float*>(ws + w.o_off) : nullptr;
-  p.part_ml = w.num_splits > 1 ? reinterpret_cast<float*>(ws + w.ml_off) : nullptr;
-  p.counters = w.num_splits > 1 ? reinterpret_cast<int32_t*>(ws + w.counters_off) : nullptr;
   p.err = err;
   p.batch = batch;
   p.t_len = t_len;
   p.n_q = g->n_q_heads;
   p.n_kv = g->n_kv_heads;
   p.layer = layer;
-  p.num_splits = w.num_splits;
-  p.split_keys = w.split_keys;
+  prefill_tc_plan(batch * w.n_tb * g->n_kv_heads, max_keys, sms, D, grp, &p.num_splits, &p.split_keys);
   p.mask_mode = mask_mode;
   p.n_doc = n_doc;
   p.kblk = kblk;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
-  (void)grp;
-  (void)max_keys;
   C2KV_CUDA(launch_prefill_tc(p, D, grp, st));
   return C2KV_OK;
 }

@@ -234,10 +234,8 @@ struct PrefillTcParams {
   CUtensorMap tm_v[kMaxBatch];
   int32_t n_cached[kMaxBatch];
   __nv_bfloat16* out;          // [B][t_len][Hq][d]
-  float* part_o;               // [B][t_len][Hkv][S][G][d]
-  float* part_ml;              // [B][t_len][Hkv][S][G][2]
-  int32_t* counters;           // [B][M tiles][Hkv]
   unsigned* err;
+  // num_splits key splits per unit, merged in a cluster of num_splits CTAs
   int32_t batch, t_len, n_q, n_kv, layer, num_splits, split_keys, mask_mode, n_doc, kblk;
   float scale_log2;
 };
@@ -279,7 +277,10 @@ cudaError_t launch_advance(int batch, int32_t* n_cached, int delta, cudaStream_t
 cudaError_t launch_prefill_tc(const PrefillTcParams& p, int head_dim, int group, cudaStream_t st);
 int prefill_tc_tokens_per_tile(int group);
 int prefill_tc_key_tile();
-constexpr int kTcMaxSplits = 128;
+// Key splits (one thread-block cluster per unit) and keys per split of the
+// tensor-core prefill for `units` (sequence, M tile, kv head) units.
+void prefill_tc_plan(int units, int max_keys, int num_sms, int head_dim, int group, int* num_splits,
+                     int* split_keys);
 
 // Attention work decomposition shared by the launcher and the workspace query.
 int attn_tokens_per_cta(int t_len);

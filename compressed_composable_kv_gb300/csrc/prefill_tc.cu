@@ -19,11 +19,20 @@
 //   O   : P V accumulated in TMEM (d columns), rescaled in place only when a
 //         row's running max grows by more than 2^8 (the final O / l uses the
 //         same stale max, so the result is exact)
-// With several key splits the CTA writes (m, l, O) partials; the last CTA of
-// its (sequence, M tile, kv head) merges them and resets the counter.
+// With several key splits, the S split CTAs of one (sequence, M tile, kv
+// head) form a thread-block cluster: each stages its unnormalised O (fp32)
+// and (m, l) in shared memory, and after a cluster barrier CTA r merges rows
+// [r * ceil(128 / S), ...) of all S splits through distributed shared memory
+// and writes them, so no partial result goes through global memory.
 #include <cuda.h>
 
+#include <algorithm>
+
+#include <cooperative_groups.h>
+
 #include "c2kv_internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace c2kv {
 
@@ -31,7 +40,8 @@ namespace {
 
 constexpr int BM = 128;        // rows per M tile (TMEM lanes)
 constexpr int BN = 64;         // keys per tile
-constexpr int STAGES = 3;
+constexpr int STAGES = 5;
+constexpr int kMaxClusterTc = 16;   // key splits merged in one cluster
 constexpr int kSoftmaxThreads = 128;
 constexpr int kThreadsTc = 160;
 constexpr float kRescaleLog2 = 8.f;
@@ -46,10 +56,18 @@ struct TcCfg {
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_ML = OFF_P + 2 * P_BYTES;   // split merge: (m, l) of every row
+  static constexpr int OFF_BAR = OFF_ML + BM * 2 * 4;
   static constexpr int N_BAR = 1 + 2 * STAGES + 2 + 2 + 2 + 2 + 1;
   static constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;   // + slack for 1024-byte alignment
+  // split merge: unnormalised O of every row (fp32, 16-byte chunks swizzled
+  // by row & 7) over the K ring, merge weights over the Q tile
+  static constexpr int OFF_OST = OFF_K;
+  static_assert(BM * D * 4 <= STAGES * KV_BYTES, "O staging must fit the K ring");
+  // [rows per CTA][S] m, l and weights; rows per CTA * S <= BM + S
+  static_assert((BM + kMaxClusterTc) * 3 * 4 <= Q_BYTES, "merge scratch must fit the Q tile");
+  static_assert(SMEM <= 232448, "shared memory per CTA");
   static constexpr int TMEM_S = 0;                    // two 64-column S buffers
   static constexpr int TMEM_O = 2 * BN;               // d columns
   static constexpr int TMEM_COLS = 256;
@@ -194,7 +212,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   const int h = blockIdx.y % p.n_kv;
   const int mt = blockIdx.y / p.n_kv;
   const int b = blockIdx.z;
-  const int n_mt = (p.t_len + TOK - 1) / TOK;
   const int n_cached = p.n_cached[b];
   const int tok0 = mt * TOK;
   const int ntok = min(TOK, p.t_len - tok0);
@@ -237,6 +254,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   uint8_t* sP = smem + C::OFF_P;
   const int kv_z = p.layer * p.n_kv + h;
 
+  float m_run = -INFINITY, l_run = 0.f;   // softmax threads: running max / sum of their row
   if (warp == 4) {
     if (lane == 0 && ntiles > 0) {
       // ---------------- producer + MMA issuer (one thread)
@@ -303,7 +321,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
     const bool row_ok = row < ROWS && tl < ntok;
     const int lim = n_cached + tok + 1;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
       const int sb = j & 1;
@@ -392,25 +409,24 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
       mbar_arrive(&p_full[pb]);
     }
 
-    // ---------------- epilogue: O / l, or split partials
-    const int S = p.num_splits;
+    // ---------------- epilogue: the last PV must be complete before O is read
     ok = __all_sync(0xffffffffu, ok);
     if (ok && ntiles > 0 && !__all_sync(0xffffffffu, wait_or_abort(o_done, (ntiles - 1) & 1, abort_flag, p.err)))
       ok = false;
     if (ok && ntiles > 0) tc_fence_after();
-    const float invl = (l_run > 0.f) ? 1.f / l_run : 0.f;
+    if (p.num_splits == 1) {
+      const float invl = (l_run > 0.f) ? 1.f / l_run : 0.f;
 #pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      float o[32];
-      if (ok && ntiles > 0) {
-        tmem_ld32(lane_base + C::TMEM_O + c0, o);
-        tmem_wait_ld();
-      } else {
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float o[32];
+        if (ok && ntiles > 0) {
+          tmem_ld32(lane_base + C::TMEM_O + c0, o);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) o[c] = 0.f;
-      }
-      if (!row_ok) continue;
-      if (S == 1) {
+          for (int c = 0; c < 32; ++c) o[c] = 0.f;
+        }
+        if (!row_ok) continue;
         __nv_bfloat16* dst = p.out + (((size_t)b * p.t_len + tok) * p.n_q + h * G + g) * D + c0;
 #pragma unroll
         for (int c = 0; c < 32; c += 8) {
@@ -419,94 +435,203 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
           for (int e = 0; e < 8; ++e) f[e] = o[c + e] * invl;
           *reinterpret_cast<uint4*>(dst + c) = pack8(f);
         }
-      } else {
-        const size_t base = (((size_t)b * p.t_len + tok) * p.n_kv + h) * S + split;
-        float* dst = p.part_o + (base * G + g) * D + c0;
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
-        if (c0 == 0) {
-          p.part_ml[(base * G + g) * 2 + 0] = (ntiles > 0 && ok) ? m_run : -INFINITY;
-          p.part_ml[(base * G + g) * 2 + 1] = (ntiles > 0 && ok) ? l_run : 0.f;
-        }
       }
     }
   }
 
-  // ---------------- teardown: every tcgen05 access of the CTA is done here
+  // ---------------- teardown of the pipeline
   tc_fence_before();
   __syncthreads();
-  if (*abort_flag) {
-    // let TMA copies in flight land before the shared memory is released
+  const bool aborted = *abort_flag != 0;
+  if (aborted) {
+    // let TMA copies in flight land before the shared memory is reused
     if (tid == 0) {
       mbar_wait(q_full, 0);
       for (int s = 0; s < STAGES; ++s) mbar_wait(&kv_full[s], 0);
     }
     __syncthreads();
   }
+  const int S = p.num_splits;
+  float* ost = reinterpret_cast<float*>(smem + C::OFF_OST);   // [BM][D], chunk c of row r at c ^ (r & 7)
+  float* mls = reinterpret_cast<float*>(smem + C::OFF_ML);    // [BM][2]
+  if (S > 1 && warp < 4) {
+    // Stage this split's rows: every MMA has completed (o_done) and every
+    // issued K/V copy has been consumed, so the K ring is free.
+    const int row = tid;
+    const bool have = !aborted && ntiles > 0;   // uniform over the CTA
+    if (have) tc_fence_after();
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+#pragma unroll
+    for (int c0 = 0; c0 < D; c0 += 32) {
+      float o[32];
+      if (have) {
+        tmem_ld32(lane_base + C::TMEM_O + c0, o);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) o[c] = 0.f;
+      }
+#pragma unroll
+      for (int c = 0; c < 32; c += 4) {
+        const int ch = (c0 + c) / 4;
+        *reinterpret_cast<float4*>(ost + row * D + ((ch ^ (row & 7)) << 2)) =
+            make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+      }
+    }
+    mls[row * 2 + 0] = have ? m_run : -INFINITY;
+    mls[row * 2 + 1] = have ? l_run : 0.f;
+  }
+  tc_fence_before();
+  __syncthreads();
   if (warp == 0) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");
   }
-  if (p.num_splits == 1) return;
+  if (S == 1) return;
 
-  // ---------------- last CTA of (b, M tile, h) merges the split partials
-  __threadfence();
+  // ---------------- merge the S splits of the cluster; CTA r owns a row range.
+  // Every CTA of the cluster reaches both cluster barriers on every path (all
+  // waits above are bounded), and none leaves before the peers' reads of its
+  // shared memory are done.
+  cg::cluster_group cl = cg::this_cluster();
+  cl.sync();
+  const int rank = (int)cl.block_rank();
+  const int rows_per = (BM + S - 1) / S;
+  const int r0 = rank * rows_per;
+  const int nr = max(0, min(BM, r0 + rows_per) - r0);
+  float* sm_m = reinterpret_cast<float*>(smem + C::OFF_Q);   // [nr][S]
+  float* sm_l = sm_m + nr * S;
+  float* sm_w = sm_l + nr * S;
+  for (int i = tid; i < nr * S; i += kThreadsTc) {
+    const int rr = i / S, sp = i % S;
+    const float* peer = cl.map_shared_rank(mls, sp);
+    sm_m[i] = peer[(r0 + rr) * 2 + 0];
+    sm_l[i] = peer[(r0 + rr) * 2 + 1];
+  }
   __syncthreads();
-  const int cidx = (b * n_mt + mt) * p.n_kv + h;
-  if (tid == 0) *last_flag = (atomicAdd(&p.counters[cidx], 1) == p.num_splits - 1);
-  __syncthreads();
-  if (!*last_flag) return;
-  __threadfence();
-  const int S = p.num_splits;
-  float* wts = reinterpret_cast<float*>(smem);   // [ntok*G][S]
-  for (int pair = warp; pair < ntok * G; pair += kThreadsTc / 32) {
-    const int t = pair / G, g = pair % G;
-    const size_t base = (((size_t)b * p.t_len + tok0 + t) * p.n_kv + h) * S;
+  for (int rr = tid; rr < nr; rr += kThreadsTc) {
     float M = -INFINITY;
-    for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldcg(&p.part_ml[((base + s) * G + g) * 2]));
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    for (int sp = 0; sp < S; ++sp) M = fmaxf(M, sm_m[rr * S + sp]);
     float L = 0.f;
-    for (int s = lane; s < S; s += 32) {
-      const float ms = __ldcg(&p.part_ml[((base + s) * G + g) * 2]);
+    for (int sp = 0; sp < S; ++sp) {
+      const float ms = sm_m[rr * S + sp];
       const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-      wts[pair * S + s] = w;
-      L = fmaf(__ldcg(&p.part_ml[((base + s) * G + g) * 2 + 1]), w, L);
+      sm_w[rr * S + sp] = w;
+      L = fmaf(sm_l[rr * S + sp], w, L);
     }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    __syncwarp();
-    for (int s = lane; s < S; s += 32) wts[pair * S + s] *= inv;
+    for (int sp = 0; sp < S; ++sp) sm_w[rr * S + sp] *= inv;
   }
   __syncthreads();
-  for (int i = tid; i < ntok * G * D; i += kThreadsTc) {
-    const int dd = i % D, pair = i / D;
-    const int t = pair / G, g = pair % G;
-    const size_t base = (((size_t)b * p.t_len + tok0 + t) * p.n_kv + h) * S;
-    const float* w = wts + pair * S;
-    float acc = 0.f;
-    for (int s = 0; s < S; ++s) acc = fmaf(w[s], __ldcg(&p.part_o[((base + s) * G + g) * D + dd]), acc);
-    p.out[(((size_t)b * p.t_len + tok0 + t) * p.n_q + h * G + g) * D + dd] = __float2bfloat16_rn(acc);
+  constexpr int CH = D / 4;   // 16-byte chunks of a row
+  for (int it = tid; it < nr * CH; it += kThreadsTc) {
+    const int rr = it / CH, c = it % CH;
+    const int row = r0 + rr;
+    const int tl = row / G, g = row % G;
+    if (row >= ROWS || tl >= ntok) continue;
+    const int off = row * D + ((c ^ (row & 7)) << 2);
+    float4 v[kMaxClusterTc];
+#pragma unroll
+    for (int sp = 0; sp < kMaxClusterTc; ++sp)
+      if (sp < S && sm_w[rr * S + sp] != 0.f)   // a split without keys holds no O
+        v[sp] = *reinterpret_cast<const float4*>(cl.map_shared_rank(ost, sp) + off);
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int sp = 0; sp < kMaxClusterTc; ++sp) {
+      if (sp < S && sm_w[rr * S + sp] != 0.f) {
+        const float w = sm_w[rr * S + sp];
+        a.x = fmaf(w, v[sp].x, a.x);
+        a.y = fmaf(w, v[sp].y, a.y);
+        a.z = fmaf(w, v[sp].z, a.z);
+        a.w = fmaf(w, v[sp].w, a.w);
+      }
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(p.out + (((size_t)b * p.t_len + tok0 + tl) * p.n_q + h * G + g) * D + c * 4) = pk;
   }
-  if (tid == 0) p.counters[cidx] = 0;
+  cl.sync();
+}
+
+template <int D, int G>
+bool configure_tc() {
+  using C = TcCfg<D>;
+  static int state = 0;   // 0 unknown, 1 ready, -1 failed
+  if (state == 0) {
+    const bool okk =
+        cudaFuncSetAttribute(prefill_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) ==
+            cudaSuccess &&
+        cudaFuncSetAttribute(prefill_tc_kernel<D, G>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+            cudaSuccess;
+    if (!okk) cudaGetLastError();
+    state = okk ? 1 : -1;
+  }
+  return state == 1;
 }
 
 template <int D, int G>
 cudaError_t launch_tc(const PrefillTcParams& p, cudaStream_t st) {
   using C = TcCfg<D>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  if (!configure_tc<D, G>()) return cudaErrorInvalidValue;
+  if (p.num_splits < 1 || p.num_splits > kMaxClusterTc) return cudaErrorInvalidValue;
   const int tok = BM / G;
   const int n_mt = (p.t_len + tok - 1) / tok;
-  const dim3 grid(p.num_splits, p.n_kv * n_mt, p.batch);
-  prefill_tc_kernel<D, G><<<grid, kThreadsTc, C::SMEM, st>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_splits, p.n_kv * n_mt, p.batch);
+  cfg.blockDim = dim3(kThreadsTc);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.num_splits;   // the key splits of one unit form a cluster
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, G>, p);
+}
+
+// Number of `cs`-CTA clusters of the kernel that can be resident at once
+// (cached; 0 when unknown).
+template <int D, int G>
+int tc_active_clusters(int cs) {
+  using C = TcCfg<D>;
+  static int cache[kMaxClusterTc + 1] = {};   // -1 = queried, none
+  if (cs < 1 || cs > kMaxClusterTc || !configure_tc<D, G>()) return 0;
+  if (cache[cs] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs, 1, 1);
+    cfg.blockDim = dim3(kThreadsTc);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, prefill_tc_kernel<D, G>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    cache[cs] = n > 0 ? n : -1;
+  }
+  return cache[cs] > 0 ? cache[cs] : 0;
+}
+
+template <int D>
+int active_clusters_d(int cs, int group) {
+  switch (group) {
+    case 1: return tc_active_clusters<D, 1>(cs);
+    case 2: return tc_active_clusters<D, 2>(cs);
+    case 4: return tc_active_clusters<D, 4>(cs);
+    case 5: return tc_active_clusters<D, 5>(cs);
+    case 8: return tc_active_clusters<D, 8>(cs);
+    default: return 0;
+  }
 }
 
 template <int D>
@@ -526,6 +651,27 @@ cudaError_t launch_tc_d(const PrefillTcParams& p, int group, cudaStream_t st) {
 int prefill_tc_tokens_per_tile(int group) { return BM / group; }
 
 int prefill_tc_key_tile() { return BN; }
+
+// Key splits of each (sequence, M tile, kv head) unit: as many as keep all
+// the units' clusters resident at once (one CTA per SM), at most 16 and at
+// most one per 64-key tile.  Small units counts thereby fill the SMs; with
+// units >= SMs / 2 there is one split and no merge.
+void prefill_tc_plan(int units, int max_keys, int num_sms, int head_dim, int group, int* num_splits,
+                     int* split_keys) {
+  int s = units > 0 ? num_sms / units : 1;
+  s = std::min(s, (max_keys + BN - 1) / BN);
+  s = std::min(s, kMaxClusterTc);
+  for (; s >= 2; --s) {
+    const int n = head_dim == 128 ? active_clusters_d<128>(s, group)
+                                  : head_dim == 64 ? active_clusters_d<64>(s, group) : 0;
+    if (n >= units) break;
+  }
+  if (s < 1) s = 1;
+  int sk = (max_keys + s - 1) / s;
+  sk = std::max(BN, (sk + BN - 1) / BN * BN);
+  *split_keys = sk;
+  *num_splits = std::max(1, (max_keys + sk - 1) / sk);
+}
 
 cudaError_t launch_prefill_tc(const PrefillTcParams& p, int head_dim, int group, cudaStream_t st) {
   if (head_dim == 128) return launch_tc_d<128>(p, group, st);
