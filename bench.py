@@ -385,7 +385,7 @@ def run_ours(args, rank: int, world: int) -> dict:
     hbm_peak = peaks.get("hbm_gbs")
     peak_src = "measured" if hbm_peak else "fallback"
     hbm_peak = hbm_peak or 6800.0
-    per_key = profiled_traffic("attn_kernel")
+    per_key = profiled_traffic("decode_kernel")
     traffic = None if per_key is None else per_key * (keys / T)
     clocks = clk.summary()
     ttft = comp + pre + dec / T
@@ -422,7 +422,7 @@ def run_ours(args, rank: int, world: int) -> dict:
         "h2d": {"compose_bytes": compose_bytes, "achieved_gbs": compose_bytes / comp / 1e9,
                 "pinned_copy_gbs": pinned_gbs, "frac": compose_bytes / comp / 1e9 / pinned_gbs,
                 "note": "compose = host->device copies + re-rotation, wall time on the stream"},
-        "roofline": {"kernel": "attn_kernel (decode)", "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
+        "roofline": {"kernel": "decode_kernel", "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
                      "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
                      "peak_source": f"{peak_src} (hbm_gbs, burst)",
                      "launch_time": "decode-phase time / attention launches (includes the per-step "
