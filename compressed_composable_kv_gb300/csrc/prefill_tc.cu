@@ -180,6 +180,13 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   return true;
 }
 
+// 2^x on the SFU (ex2.approx.ftz: relative error ~2^-22; -inf gives +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ bool tc_structured_visible(const PrefillTcParams& p, int tok, int key) {
   if (tok < p.n_doc || key >= p.n_doc) return true;
   const int i = tok - p.n_doc;
@@ -344,15 +351,27 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
       tc_fence_before();
       mbar_arrive(&s_free[sb]);
       const int key0 = kb + j * BN;
-      float mt_ = -INFINITY;
+      // keys [key0, key0 + nvis) pass the causal / split bounds of this row
+      const int nvis = row_ok ? min(min(ke, lim) - key0, BN) : 0;
+      float mraw = -INFINITY;   // max of the raw scores (the scale is positive)
+      if (p.mask_mode == kMaskStructured) {
 #pragma unroll
-      for (int c = 0; c < BN; ++c) {
-        const int key = key0 + c;
-        bool vis = row_ok && key < ke && key < lim;
-        if (p.mask_mode == kMaskStructured) vis = vis && tc_structured_visible(p, tok, key);
-        sv[c] = vis ? sv[c] * p.scale_log2 : -INFINITY;
-        mt_ = fmaxf(mt_, sv[c]);
+        for (int c = 0; c < BN; ++c) {
+          const bool vis = c < nvis && tc_structured_visible(p, tok, key0 + c);
+          sv[c] = vis ? sv[c] : -INFINITY;
+          mraw = fmaxf(mraw, sv[c]);
+        }
+      } else if (nvis >= BN) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c) mraw = fmaxf(mraw, sv[c]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < BN; ++c) {
+          sv[c] = c < nvis ? sv[c] : -INFINITY;
+          mraw = fmaxf(mraw, sv[c]);
+        }
       }
+      const float mt_ = mraw * p.scale_log2;   // log2 units; -inf stays -inf
       float alpha = 1.f;
       bool rescale = false;
       if (mt_ > m_run) {
@@ -365,14 +384,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
         }
       }
       const float mu = (m_run == -INFINITY) ? 0.f : m_run;
-      float lsum = 0.f;
+      // p = 2^(s * scale - mu): one FFMA and one ex2 per score (masked scores
+      // are -inf and give 0)
+      const float sc = p.scale_log2;
+      float lsum0 = 0.f, lsum1 = 0.f;
       uint32_t pk[BN / 2];
 #pragma unroll
       for (int c = 0; c < BN; c += 2) {
-        const float p0 = exp2f(sv[c] - mu), p1 = exp2f(sv[c + 1] - mu);
-        lsum += p0 + p1;
+        const float p0 = ex2_approx(fmaf(sv[c], sc, -mu)), p1 = ex2_approx(fmaf(sv[c + 1], sc, -mu));
+        lsum0 += p0;
+        lsum1 += p1;
         pk[c / 2] = pack2(p0, p1);
       }
+      const float lsum = lsum0 + lsum1;
       l_run = l_run * alpha + lsum;
       // O rescale needs PV(j-1) finished; the warp shares the TMEM access, so
       // the whole warp takes the path when any of its rows needs it.
