@@ -258,9 +258,19 @@ def run_ours(args, rank: int, world: int) -> dict:
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
 
-    def prefill_all():
-        for l in range(L):
+    # Compose and prefill are layer-pipelined: layer group i is composed
+    # (its copies queue behind group i-1's on the store's copy stream), then
+    # its question prefill is enqueued, so the prefill of early layers runs
+    # while later layers are still crossing the host link.
+    n_groups = min(L, 8)
+    groups = [(i * L // n_groups, (i + 1) * L // n_groups) for i in range(n_groups)]
+
+    def prefill_layers(l0, l1):
+        for l in range(l0, l1):
             bt.prefill(l, dev_in["q_pre"][l], dev_in["kq_pre"][l], dev_in["vq"][l], pre_out[l], stream)
+
+    def prefill_all():
+        prefill_layers(0, L)
 
     def decode_all(steps=T):
         for t in range(steps):
@@ -278,17 +288,21 @@ def run_ours(args, rank: int, world: int) -> dict:
         bt.reset_decode(stream)
         decode_all(1)
     torch.cuda.synchronize()
-    g_pre = torch.cuda.CUDAGraph() if Q else None
+    g_pre = [torch.cuda.CUDAGraph() for _ in groups] if Q else None
     g_dec = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         if Q:
-            with torch.cuda.graph(g_pre, stream=stream):
-                prefill_all()
+            for gr, (l0, l1) in zip(g_pre, groups):
+                with torch.cuda.graph(gr, stream=stream):
+                    prefill_layers(l0, l1)
         with torch.cuda.graph(g_dec, stream=stream):
             decode_all()
     torch.cuda.synchronize()
     assert P.c2kv_device_error() == P.C2KV_OK
-    launches_per_step = (bt.batch * (1 + min(L, 4)) + (2 * L if Q else 0) + T * (L + 1))
+    # per request: one table + one re-rotation per layer sub-group of each
+    # compose call; 2 launches per prefill layer; L decode + 1 advance per step
+    rerope_launches = sum(min(l1 - l0, 4) for l0, l1 in groups)
+    launches_per_step = (bt.batch * (1 + rerope_launches) + (2 * L if Q else 0) + T * (L + 1))
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
 
@@ -299,12 +313,13 @@ def run_ours(args, rank: int, world: int) -> dict:
                     dev_in[n].copy_(host[n], non_blocking=True)
             if e:
                 e[0].record(stream)
-            bt.compose(stream)
+            for gi, (l0, l1) in enumerate(groups):
+                bt.compose_layers(l0, l1, stream)
+                if gi == len(groups) - 1 and e:
+                    e[1].record(stream)   # the whole cache is composed
+                if Q:
+                    g_pre[gi].replay()
             bt.reset_decode(stream)
-            if e:
-                e[1].record(stream)
-            if Q:
-                g_pre.replay()
             if e:
                 e[2].record(stream)
             g_dec.replay()
@@ -410,6 +425,9 @@ def run_ours(args, rank: int, world: int) -> dict:
             "question_tokens": Q, "decode_steps": T,
             "l2": "inputs larger than L2 (composed cache per request > 1 GB; 129 MB L2)",
             "graphs": "prefill and decode replayed from CUDA graphs of this library's kernels",
+            "ttft_pipeline": (f"compose and prefill layer-pipelined in {len(groups)} groups: compose_ms = "
+                              "until the whole cache is composed (prefill of earlier groups overlaps it), "
+                              "prefill_ms = the rest of the prefill"),
             "parallelism": f"replicas x{world}",
             "attention_only": "no projection/MLP weights: attention over the composed cache only",
         },
@@ -439,7 +457,7 @@ def run_ours(args, rank: int, world: int) -> dict:
 
 def run_sweep(args) -> None:
     """Decode time per token over a composed cache of 16k..128k original
-    tokens, compressed at k=4 vs uncompressed (k=1), batch 4, Llama3.1-8B
+    tokens, compressed at k=16, 8, 4 vs uncompressed (k=1), batch 4, Llama3.1-8B
     attention geometry (C2KV explainer, section "results": the full cache's
     per-token decode time grows ~linearly with context, the compressed one
     reads a quarter of the bytes).  Only decode attention is timed: each
@@ -456,7 +474,7 @@ def run_sweep(args) -> None:
     stream = torch.cuda.Stream()
     peak = measured_peaks().get("hbm_gbs") or 6800.0
     for ctx in (16384, 32768, 65536, 131072):
-        for k in (4, 1):
+        for k in (16, 8, 4, 1):
             n = ctx // k
             steps = 16
             cap = n + steps + 32
@@ -481,6 +499,7 @@ def run_sweep(args) -> None:
                                              out[t, l], ws, stream, P.C2KV_DECODE_OVERLAP_PREVIOUS if l else 0)
                     P.c2kv_seq_advance(n_dev, 1, stream)
 
+            torch.cuda.synchronize()   # the caches, tables and lengths above were made on torch's stream
             with torch.cuda.stream(stream):
                 decode_all()
             torch.cuda.synchronize()
@@ -522,7 +541,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
-                    help="decode time vs context (16k..128k), compressed k=4 vs uncompressed")
+                    help="decode time vs context (16k..128k), compressed k=16/8/4 vs uncompressed")
     args = ap.parse_args()
     if args.sweep:
         run_sweep(args)

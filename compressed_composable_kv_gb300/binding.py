@@ -51,6 +51,8 @@ _SIGNATURES = {
     "c2kv_store_lookup": (_i32, [_vp, _i32, _pi32, _pi32, _pi32]),
     "c2kv_plan": (_i32, [_i32, _pi32, _pi32, _pi32, _pi32, _pi32, _pi32, _pi32]),
     "c2kv_compose": (_i32, [_vp, _i32, _pi32, _pi32, _i32, _vp, _vp, _i32, _vp, _vp, _pi32, _pi32, _vp]),
+    "c2kv_compose_layers": (_i32, [_vp, _i32, _pi32, _pi32, _i32, ctypes.c_uint32, _i32, _i32, _vp, _vp, _i32,
+                                   _vp, _vp, _pi32, _pi32, _vp]),
     "c2kv_rope_table_bytes": (_sz, [_pg, _i32]),
     "c2kv_rope_table": (_i32, [_pg, _vp, _i32, _vp, _vp]),
     "c2kv_attend_workspace_size": (_sz, [_pg, _i32, _i32, _i32]),
@@ -194,6 +196,24 @@ def c2kv_compose(store: int, doc_ids, order, k: int, k_cache: torch.Tensor, v_ca
         _dev(k_cache, torch.bfloat16, "k_cache"), _dev(v_cache, torch.bfloat16, "v_cache"), int(cap),
         _dev(rope_table, None, "rope_table"), _dev(pos_dev_out, torch.int32, "pos_dev_out"),
         ctypes.byref(ns), ctypes.byref(nxt), _stream(stream)))
+    return ns.value, nxt.value
+
+
+C2KV_COMPOSE_NO_REALIGN = 1
+C2KV_COMPOSE_CONTINUE = 2
+
+
+def c2kv_compose_layers(store: int, doc_ids, order, k: int, flags: int, layer_begin: int, layer_end: int,
+                        k_cache: torch.Tensor, v_cache: torch.Tensor, cap: int, rope_table: torch.Tensor,
+                        pos_dev_out: Optional[torch.Tensor] = None, stream=None):
+    """c2kv_compose over layers [layer_begin, layer_end) with C2KV_COMPOSE_* flags.
+    Returns (n_slots, next_pos)."""
+    ns, nxt = ctypes.c_int32(), ctypes.c_int32()
+    _check(load_library().c2kv_compose_layers(
+        store, len(doc_ids), _i32arr(doc_ids), None if order is None else _i32arr(order), int(k), int(flags),
+        int(layer_begin), int(layer_end), _dev(k_cache, torch.bfloat16, "k_cache"),
+        _dev(v_cache, torch.bfloat16, "v_cache"), int(cap), _dev(rope_table, None, "rope_table"),
+        _dev(pos_dev_out, torch.int32, "pos_dev_out"), ctypes.byref(ns), ctypes.byref(nxt), _stream(stream)))
     return ns.value, nxt.value
 
 

@@ -110,6 +110,15 @@ struct c2kv_store_s {
   cudaEvent_t fork = nullptr;
   std::vector<cudaEvent_t> ev;
   std::mutex mu;
+  // the last composition into each RoPE table (one per request), which a
+  // C2KV_COMPOSE_CONTINUE call must match
+  struct Composition {
+    std::vector<int32_t> doc_ids, order;
+    int32_t k = 0, cap = 0;
+    uint32_t flags = 0;
+    const void *k_cache = nullptr, *v_cache = nullptr;
+  };
+  std::unordered_map<const void*, Composition> last;
 };
 
 namespace {
@@ -489,6 +498,20 @@ c2kv_status c2kv_compose(c2kv_store st, int32_t n_docs, const int32_t* doc_ids, 
                          void* k_cache, void* v_cache, int32_t cap, void* rope_table_out, int32_t* pos_dev_out,
                          int32_t* n_slots_out, int32_t* next_pos_out, void* stream) {
   if (st == nullptr) return fail(C2KV_EINVAL, "store is null");
+  return c2kv_compose_layers(st, n_docs, doc_ids, order, k, 0u, 0, st->g.n_layers, k_cache, v_cache, cap,
+                             rope_table_out, pos_dev_out, n_slots_out, next_pos_out, stream);
+}
+
+c2kv_status c2kv_compose_layers(c2kv_store st, int32_t n_docs, const int32_t* doc_ids, const int32_t* order,
+                                int32_t k, uint32_t flags, int32_t layer_begin, int32_t layer_end, void* k_cache,
+                                void* v_cache, int32_t cap, void* rope_table_out, int32_t* pos_dev_out,
+                                int32_t* n_slots_out, int32_t* next_pos_out, void* stream) {
+  if (st == nullptr) return fail(C2KV_EINVAL, "store is null");
+  if (flags & ~(C2KV_COMPOSE_NO_REALIGN | C2KV_COMPOSE_CONTINUE)) return fail(C2KV_EINVAL, "unknown flags");
+  if (layer_begin < 0 || layer_end > st->g.n_layers || layer_begin >= layer_end)
+    return fail(C2KV_EINVAL, "need 0 <= layer_begin < layer_end <= n_layers");
+  const bool cont = (flags & C2KV_COMPOSE_CONTINUE) != 0;
+  const bool realign = (flags & C2KV_COMPOSE_NO_REALIGN) == 0;
   if (n_docs < 0 || n_docs > kMaxDocsPerCompose)
     return fail(C2KV_EINVAL, "n_docs must be in [0, " + std::to_string(kMaxDocsPerCompose) + "]");
   if (n_docs > 0 && doc_ids == nullptr) return fail(C2KV_EINVAL, "doc_ids is null");
@@ -515,6 +538,16 @@ c2kv_status c2kv_compose(c2kv_store st, int32_t n_docs, const int32_t* doc_ids, 
   if (total > cap)
     return fail(C2KV_ECAPACITY, "composed slots " + std::to_string(total) + " exceed cap " + std::to_string(cap));
   if ((int64_t)l_tot + (cap - total) > INT32_MAX / 2) return fail(C2KV_EINVAL, "positions overflow int32");
+  const uint32_t base_flags = flags & ~C2KV_COMPOSE_CONTINUE;
+  if (cont) {
+    const auto it = st->last.find(rope_table_out);
+    const std::vector<int32_t> ids(doc_ids, doc_ids + n_docs);
+    const std::vector<int32_t> ord = order ? std::vector<int32_t>(order, order + n_docs) : std::vector<int32_t>();
+    if (it == st->last.end() || it->second.doc_ids != ids || it->second.order != ord || it->second.k != k ||
+        it->second.cap != cap || it->second.flags != base_flags || it->second.k_cache != k_cache ||
+        it->second.v_cache != v_cache)
+      return fail(C2KV_EINVAL, "C2KV_COMPOSE_CONTINUE does not follow a composition of the same request");
+  }
   if (n_slots_out) *n_slots_out = total;
   if (next_pos_out) *next_pos_out = l_tot;
   if (cap == 0) return C2KV_OK;
@@ -530,19 +563,23 @@ c2kv_status c2kv_compose(c2kv_store st, int32_t n_docs, const int32_t* doc_ids, 
   if (s != C2KV_OK) return s;
 
   cudaStream_t us = static_cast<cudaStream_t>(stream);
-  const int D = g.head_dim, H = g.n_kv_heads, L = g.n_layers;
+  const int D = g.head_dim, H = g.n_kv_heads;
   const size_t elem = 2;
   CosSin2* tab = static_cast<CosSin2*>(rope_table_out);
 
-  // Copies run on the store's stream after the caller's earlier work.
-  C2KV_CUDA(cudaEventRecord(st->fork, us));
-  C2KV_CUDA(cudaStreamWaitEvent(st->side, st->fork, 0));
+  // Copies run on the store's stream after the caller's earlier work (a
+  // continuation: after the copies of the composition it continues).
+  if (!cont) {
+    C2KV_CUDA(cudaEventRecord(st->fork, us));
+    C2KV_CUDA(cudaStreamWaitEvent(st->side, st->fork, 0));
+    st->last.erase(rope_table_out);
+  }
 
   // The cos/sin table of every cache row is built on the caller's stream
   // while the first copies are in flight.
   static TableParams tp;   // large (segment table); guarded by the store mutex and g_tab_mu
   static std::mutex g_tab_mu;
-  {
+  if (!cont) {
     std::lock_guard<std::mutex> tl(g_tab_mu);
     std::memset(&tp, 0, sizeof(tp));
     tp.tab = tab;
@@ -559,10 +596,21 @@ c2kv_status c2kv_compose(c2kv_store st, int32_t n_docs, const int32_t* doc_ids, 
       const int d = order ? order[c] : c;
       tp.seg[c].slot0 = slot0[c];
       tp.seg[c].n_slots = nsl[d];
-      tp.seg[c].off = off[c];
+      tp.seg[c].off = realign ? off[c] : 0;   // no re-alignment: extraction positions
       tp.seg[c].n_tokens = ntok[d];
     }
     C2KV_CUDA(launch_rope_table(tp, us));
+    auto& lc = st->last[rope_table_out];
+    lc.doc_ids.assign(doc_ids, doc_ids + n_docs);
+    if (order)
+      lc.order.assign(order, order + n_docs);
+    else
+      lc.order.clear();
+    lc.k = k;
+    lc.cap = cap;
+    lc.flags = base_flags;
+    lc.k_cache = k_cache;
+    lc.v_cache = v_cache;
   }
   if (total == 0) return C2KV_OK;
 
@@ -577,11 +625,12 @@ c2kv_status c2kv_compose(c2kv_store st, int32_t n_docs, const int32_t* doc_ids, 
 
   // Each layer group's re-rotation runs on the caller's stream once its
   // copies have landed (and after the table, which is earlier on that stream).
-  const int ngroups = std::min(L, kLayerGroups);
+  const int nl = layer_end - layer_begin;
+  const int ngroups = std::min(nl, kLayerGroups);
   uint8_t* kc = static_cast<uint8_t*>(k_cache);
   uint8_t* vc = static_cast<uint8_t*>(v_cache);
   for (int gi = 0; gi < ngroups; ++gi) {
-    const int l0 = gi * L / ngroups, l1 = (gi + 1) * L / ngroups;
+    const int l0 = layer_begin + gi * nl / ngroups, l1 = layer_begin + (gi + 1) * nl / ngroups;
     for (int c = 0; c < n_docs; ++c) {
       const int d = order ? order[c] : c;
       const Seg& sg = segs[d];

@@ -27,8 +27,11 @@ class RequestBatch:
     """Device state of `len(requests)` composed requests sharing one store."""
 
     def __init__(self, store: int, geom, requests: Sequence[RequestSpec], k: int, q_len: int,
-                 decode_steps: int, device: str = "cuda", cap_multiple: int = 32):
+                 decode_steps: int, device: str = "cuda", cap_multiple: int = 32, realign: bool = True):
         self.store, self.geom, self.k = store, geom, k
+        # realign=False: the "no position re-alignment" ablation (documents
+        # keep their extraction positions)
+        self.compose_flags = 0 if realign else B.C2KV_COMPOSE_NO_REALIGN
         self.requests = list(requests)
         self.q_len, self.decode_steps = q_len, decode_steps
         self.batch = len(self.requests)
@@ -64,9 +67,19 @@ class RequestBatch:
         self._dec_start = torch.tensor([n + q_len for n in self.n_slots], dtype=torch.int32)
 
     def compose(self, stream=None) -> None:
+        self.compose_layers(0, self.geom.n_layers, stream)
+
+    def compose_layers(self, layer_begin: int, layer_end: int, stream=None) -> None:
+        """Compose layers [layer_begin, layer_end) of every request.  A call
+        with layer_begin > 0 continues the composition of the call before it
+        (C2KV_COMPOSE_CONTINUE): its copies follow that call's copies, so work
+        enqueued in between on the earlier layers (the question prefill)
+        overlaps them ("the problem": loading the cache dominates TTFT)."""
+        flags = self.compose_flags | (B.C2KV_COMPOSE_CONTINUE if layer_begin > 0 else 0)
         for b, r in enumerate(self.requests):
-            n, nxt = B.c2kv_compose(self.store, r.doc_ids, r.order, self.k, self.k_caches[b],
-                                    self.v_caches[b], self.cap, self.rope_tables[b], self.pos[b], stream)
+            n, nxt = B.c2kv_compose_layers(self.store, r.doc_ids, r.order, self.k, flags, layer_begin,
+                                           layer_end, self.k_caches[b], self.v_caches[b], self.cap,
+                                           self.rope_tables[b], self.pos[b], stream)
             assert n == self.n_slots[b] and nxt == self.l_tot[b]
 
     def prefill(self, layer: int, q, k_new, v_new, out, stream=None) -> None:

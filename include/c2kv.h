@@ -172,6 +172,44 @@ c2kv_status c2kv_compose(c2kv_store store, int32_t n_docs, const int32_t* doc_id
                          int32_t* pos_dev_out, int32_t* n_slots_out,
                          int32_t* next_pos_out, void* stream);
 
+/*
+ * c2kv_compose over the layers [layer_begin, layer_end) only, with flags:
+ *
+ * C2KV_COMPOSE_NO_REALIGN — the ablation of [EXPL] "results" that drops the
+ *   position re-alignment: every document keeps the positions it was
+ *   extracted at (slot j at min((j+1)k, n_c) - 1, no offset off_c), so all
+ *   documents start at position 0.  Appended tokens still start at L_tot,
+ *   the summed original length (reading: the ablation changes the
+ *   documents' positions only).  c2kv_plan's pos_offset does not apply.
+ *
+ * C2KV_COMPOSE_CONTINUE — continue the composition started by the last
+ *   c2kv_compose / c2kv_compose_layers call on this store into the same
+ *   RoPE table (same doc_ids, order, k, flags other than this one, caches
+ *   and cap): the table and pos_dev_out are not rebuilt, and the
+ *   copies of these layers are queued behind that call's copies on the
+ *   store's copy stream instead of waiting for the caller's stream.  So a
+ *   caller can compose layer group 0, enqueue work on those layers (the
+ *   question prefill), then compose group 1, and the prefill overlaps the
+ *   later groups' host->device copies ([EXPL] "the problem": loading the
+ *   cache is the dominant TTFT cost).  The caller guarantees that nothing
+ *   issued on `stream` since the first call reads or writes rows [0, N) of
+ *   the continued layers.  The re-rotation of the layers is ordered on
+ *   `stream` after their copies.
+ *
+ * 0 <= layer_begin < layer_end <= n_layers.  Other arguments, outputs and
+ * errors as c2kv_compose; C2KV_EINVAL also for a CONTINUE that does not
+ * follow a composition of the same request (documents, k, flags, caches,
+ * cap, table) on this store.
+ */
+#define C2KV_COMPOSE_NO_REALIGN 1u
+#define C2KV_COMPOSE_CONTINUE 2u
+c2kv_status c2kv_compose_layers(c2kv_store store, int32_t n_docs, const int32_t* doc_ids,
+                                const int32_t* order, int32_t k, uint32_t flags,
+                                int32_t layer_begin, int32_t layer_end, void* k_cache,
+                                void* v_cache, int32_t cap, void* rope_table_out,
+                                int32_t* pos_dev_out, int32_t* n_slots_out,
+                                int32_t* next_pos_out, void* stream);
+
 /* Bytes of a RoPE table of `rows` rows: rows * (head_dim/2) * 16. */
 size_t c2kv_rope_table_bytes(const c2kv_geometry* geom, int32_t rows);
 

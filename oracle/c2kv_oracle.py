@@ -30,6 +30,9 @@ Readings where the pages are silent (each listed in the design notes):
   S4  ``order`` is a permutation into doc_ids; None means identity.
   S9  softmax scale is 1/sqrt(d).
   S11 re-rotated K is stored as bf16, rounded to nearest even.
+  S15 the "no position re-alignment" ablation (section "results") keeps
+      every document at its extraction positions (no offset off_c); the
+      question still starts at L_tot.
 
 Parity pins: every function below is checked by tests/test_oracle_pins.py
 against the pages' worked values, closed forms, invariants or brute force.
@@ -107,17 +110,19 @@ def extraction_slot_position(j: int, n_tokens: int, k: int) -> int:
 
 
 def composed_positions(n_tokens: Sequence[int], n_slots: Sequence[int],
-                       k: int) -> Tuple[np.ndarray, int]:
+                       k: int, realign: bool = True) -> Tuple[np.ndarray, int]:
     """Position of every composed slot, documents taken in composed order.
 
     Each document occupies its original length of positions; document d's
     slots are shifted by off_d = sum of the original lengths before it.
+    realign=False is the ablation without that shift (reading S15): every
+    document keeps its extraction positions.
     Returns (int64 positions [sum n_slots], L_tot = sum n_tokens)."""
     pos: List[int] = []
     off = 0
     for n, s in zip(n_tokens, n_slots):
         for j in range(s):
-            pos.append(off + extraction_slot_position(j, n, k))
+            pos.append((off if realign else 0) + extraction_slot_position(j, n, k))
         off += n
     return np.asarray(pos, dtype=np.int64), off
 
@@ -163,7 +168,7 @@ StoreDoc = Tuple[int, int, np.ndarray, np.ndarray]  # (n_tokens, n_slots, k_pre,
 
 def compose(store: Dict[int, StoreDoc], doc_ids: Sequence[int],
             order: Optional[Sequence[int]], k: int, theta: float,
-            layers: Optional[Sequence[int]] = None):
+            layers: Optional[Sequence[int]] = None, realign: bool = True):
     """Compose one request's cache from stored pre-RoPE segments.
 
     store[doc_id] = (n_tokens, n_slots, k_pre bits [L][Hkv][s][d],
@@ -174,7 +179,7 @@ def compose(store: Dict[int, StoreDoc], doc_ids: Sequence[int],
     seq = composed_order(doc_ids, order)
     n_tok = [store[d][0] for d in seq]
     n_sl = [store[d][1] for d in seq]
-    pos, l_tot = composed_positions(n_tok, n_sl, k)
+    pos, l_tot = composed_positions(n_tok, n_sl, k, realign)
     L = store[seq[0]][2].shape[0]
     layers = list(range(L)) if layers is None else list(layers)
     k_cat = np.concatenate([store[d][2][layers] for d in seq], axis=2)

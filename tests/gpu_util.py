@@ -43,8 +43,8 @@ class Scenario:
     """Documents, store and per-request device state of one test workload."""
 
     def __init__(self, geom, k, doc_specs, requests, q_len, decode_steps, seed=0xC2C0, layers=None,
-                 cap_multiple=32):
-        self.geom, self.k, self.seed = geom, k, seed
+                 cap_multiple=32, realign=True):
+        self.geom, self.k, self.seed, self.realign = geom, k, seed, realign
         self.docs = {}
         for doc_id, n_tok, n_slot in doc_specs:
             self.docs[doc_id] = S.make_document(geom, doc_id, n_tok, k, seed, n_slots=n_slot, layers=layers)
@@ -56,7 +56,7 @@ class Scenario:
                               [self.docs[i].k_pre for i in ids], [self.docs[i].v for i in ids])
         self.reqs = [P.RequestSpec(list(r[0]), None if r[1] is None else list(r[1])) for r in requests]
         self.batch = P.RequestBatch(self.store, geom, self.reqs, k, q_len, decode_steps,
-                                    cap_multiple=cap_multiple)
+                                    cap_multiple=cap_multiple, realign=realign)
 
     def oracle_store(self):
         return {i: (d.n_tokens, d.n_slots, d.k_pre, d.v) for i, d in self.docs.items()}

@@ -78,6 +78,38 @@ def check_positions_bruteforce(o):
 
 # ------------------------------------------------------------------ mask
 
+def check_no_realign_positions(o):
+    """The "no position re-alignment" ablation (section "results", reading
+    S15): every document keeps the positions it was extracted at.  With the
+    worked example's 400-token document followed by a 40-token one, the second
+    document's slots restart at the extraction positions 3, 7, ... instead of
+    403; the question still starts after both documents' original length.
+    Also brute force: each document laid out alone from position 0."""
+    g = read_golden("positions_400tok_k4.txt")
+    k = g["k"][0]
+    n0, s0 = g["doc0_tokens"][0], g["doc0_slots"][0]
+    s1 = o.slot_count(40, k)
+    pos, l_tot = o.composed_positions([n0, 40], [s0, s1], k, realign=False)
+    want0 = np.arange(g["doc0_first"][0], g["doc0_last"][0] + 1, g["doc0_step"][0])
+    assert np.array_equal(pos[:s0], want0)
+    e = g["extraction_first_slots"]
+    assert list(pos[s0:s0 + len(e)]) == e, pos[s0:s0 + 4]
+    assert pos[s0] != g["doc1_first"][0]
+    assert l_tot == n0 + 40
+    rng = np.random.default_rng(11)
+    for _ in range(20):
+        kk = int(rng.integers(1, 9))
+        docs = []
+        for _ in range(int(rng.integers(1, 5))):
+            n = int(rng.integers(1, 60))
+            docs.append((n, -(-n // kk)))
+        brute = []
+        for n, s in docs:
+            brute += _brute_positions([(n, s)], kk)   # each document alone, from 0
+        got, lt = o.composed_positions([d[0] for d in docs], [d[1] for d in docs], kk, realign=False)
+        assert list(got) == brute and lt == sum(d[0] for d in docs)
+
+
 def check_blog_mask(o):
     g = read_golden("structured_mask_k4_12tok_3slot.txt")
     k, n, m = g["k"][0], g["n_doc"][0], g["n_slot"][0]
@@ -257,7 +289,7 @@ def check_llama3_bytes(o):
 
 
 ALL_CHECKS = [
-    check_blog_positions, check_slot_counts, check_positions_bruteforce,
+    check_blog_positions, check_slot_counts, check_positions_bruteforce, check_no_realign_positions,
     check_blog_mask, check_extraction_positions, check_bf16_conversion,
     check_rope, check_attention_special_cases, check_gqa_and_causality,
     check_k1_equals_uncompressed, check_llama3_bytes,

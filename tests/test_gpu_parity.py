@@ -56,13 +56,14 @@ def check_request(sc: Scenario, inputs: S.StepInputs, pre, dec, b: int, layers, 
     N, lt, Q = bt.n_slots[b], bt.l_tot[b], bt.q_len
     seq = O.composed_order(req.doc_ids, req.order)
     pos_ref, lt_ref = O.composed_positions([sc.docs[d].n_tokens for d in seq],
-                                           [sc.docs[d].n_slots for d in seq], sc.k)
+                                           [sc.docs[d].n_slots for d in seq], sc.k, sc.realign)
     assert lt_ref == lt
     assert np.array_equal(bt.pos[b][:N].cpu().numpy(), pos_ref)
     kc = bt.k_caches[b]
     vc = bt.v_caches[b]
     for l in layers:
-        _, _, kref, vref = O.compose(st, req.doc_ids, req.order, sc.k, g.rope_theta, layers=[l])
+        _, _, kref, vref = O.compose(st, req.doc_ids, req.order, sc.k, g.rope_theta, layers=[l],
+                                     realign=sc.realign)
         kg = to_bits(kc[l, :, :N])
         vg = to_bits(vc[l, :, :N])
         assert np.array_equal(vg, vref[0]), f"V rows differ (layer {l})"
@@ -112,6 +113,76 @@ def test_tiny_sharp_softmax():
     inputs = S.make_step_inputs(w, decode_steps=4, q_scale=4.0)
     pre, dec = run_all(sc, upload(inputs))
     check_request(sc, inputs, pre, dec, 0, layers=[0], steps=range(4))
+    sc.close()
+
+
+def test_no_position_realignment_ablation():
+    """C2KV_COMPOSE_NO_REALIGN: every document keeps its extraction positions
+    (the "results" ablation); the question and answer still follow L_tot."""
+    w = S.WORKLOADS["tiny"]
+    docs, reqs = S.make_requests(w)
+    sc = Scenario(w.geom, w.k, [(i, n, s) for i, (n, s) in docs.items()],
+                  [([1, 0, 2], [2, 0, 1])], w.q_len, 6, seed=w.seed, realign=False)
+    inputs = S.make_step_inputs(w, decode_steps=6)
+    pre, dec = run_all(sc, upload(inputs))
+    pos = sc.batch.pos[0][:sc.batch.n_slots[0]].cpu().numpy()
+    assert pos.min() == w.k - 1 and sc.batch.l_tot[0] == 452   # documents restart at 3
+    check_request(sc, inputs, pre, dec, 0, layers=[0], steps=range(6))
+    sc.close()
+
+
+def test_layer_pipelined_compose_matches_one_shot():
+    """Composing layer groups one by one (C2KV_COMPOSE_CONTINUE) with the
+    question prefill of each group enqueued in between gives the same caches
+    and outputs, bit for bit, as one compose followed by the prefill."""
+    g = S.Geometry(8, 16, 4, 128, 5.0e5)
+    specs = [(1, 900, 225), (2, 333, 84), (3, 1200, 300)]
+    requests = [([3, 1, 2], None), ([2, 3], [1, 0])]
+    sc = Scenario(g, 4, specs, requests, q_len=24, decode_steps=0)
+    bt = sc.batch
+    rng = np.random.default_rng(5)
+    q = to_dev(S.normal_bf16(rng, (g.n_layers, 2, 24, g.n_q_heads, g.head_dim)))
+    kq = to_dev(S.normal_bf16(rng, (g.n_layers, 2, 24, g.n_kv_heads, g.head_dim)))
+    vq = to_dev(S.normal_bf16(rng, (g.n_layers, 2, 24, g.n_kv_heads, g.head_dim)))
+
+    def prefill(layers):
+        outs = []
+        for l in layers:
+            o = torch.empty_like(q[l])
+            bt.prefill(l, q[l], kq[l], vq[l], o)
+            outs.append(o)
+        return outs
+
+    for t in bt.k_caches + bt.v_caches:
+        t.fill_(7.0)   # rows past N + Q stay untouched by both runs
+    bt.compose()
+    ref_out = prefill(range(8))
+    torch.cuda.synchronize()
+    ref_k = [t.clone() for t in bt.k_caches]
+    ref_v = [t.clone() for t in bt.v_caches]
+    for t in bt.k_caches + bt.v_caches:
+        t.fill_(7.0)
+    outs = []
+    for l0 in range(0, 8, 2):
+        bt.compose_layers(l0, l0 + 2)
+        outs += prefill(range(l0, l0 + 2))
+    torch.cuda.synchronize()
+    assert P.c2kv_device_error() == P.C2KV_OK
+    for b in range(2):
+        assert torch.equal(bt.k_caches[b], ref_k[b]) and torch.equal(bt.v_caches[b], ref_v[b])
+    for l in range(8):
+        assert torch.equal(outs[l], ref_out[l])
+    # a continuation must follow a composition of the same request into the same table
+    other = torch.empty_like(bt.rope_tables[0])
+    with pytest.raises(P.C2KVError):
+        P.c2kv_compose_layers(sc.store, [3, 1, 2], None, 4, P.C2KV_COMPOSE_CONTINUE, 2, 4, bt.k_caches[0],
+                              bt.v_caches[0], bt.cap, other)
+    with pytest.raises(P.C2KVError):
+        P.c2kv_compose_layers(sc.store, [3, 2, 1], None, 4, P.C2KV_COMPOSE_CONTINUE, 2, 4, bt.k_caches[0],
+                              bt.v_caches[0], bt.cap, bt.rope_tables[0])
+    with pytest.raises(P.C2KVError):
+        P.c2kv_compose_layers(sc.store, [3, 1, 2], None, 4, 0, 4, 4, bt.k_caches[0], bt.v_caches[0], bt.cap,
+                              bt.rope_tables[0])
     sc.close()
 
 

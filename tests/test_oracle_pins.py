@@ -15,20 +15,36 @@ def test_pin(check):
     check(O)
 
 
-def _positions_no_minus_one(n_tokens, n_slots, k):
+def _positions_no_minus_one(n_tokens, n_slots, k, realign=True):
     pos, off = [], 0
     for n, s in zip(n_tokens, n_slots):
-        pos += [off + min((j + 1) * k, n) for j in range(s)]
+        pos += [(off if realign else 0) + min((j + 1) * k, n) for j in range(s)]
         off += n
     return np.asarray(pos, np.int64), off
 
 
-def _positions_offset_by_slots(n_tokens, n_slots, k):
+def _positions_offset_by_slots(n_tokens, n_slots, k, realign=True):
+    pos, off = [], 0
+    for n, s in zip(n_tokens, n_slots):
+        pos += [(off if realign else 0) + min((j + 1) * k, n) - 1 for j in range(s)]
+        off += s
+    return np.asarray(pos, np.int64), off
+
+
+def _positions_realign_ignored(n_tokens, n_slots, k, realign=True):
     pos, off = [], 0
     for n, s in zip(n_tokens, n_slots):
         pos += [off + min((j + 1) * k, n) - 1 for j in range(s)]
-        off += s
+        off += n
     return np.asarray(pos, np.int64), off
+
+
+def _positions_no_realign_question_at_slots(n_tokens, n_slots, k, realign=True):
+    pos, off = [], 0
+    for n, s in zip(n_tokens, n_slots):
+        pos += [(off if realign else 0) + min((j + 1) * k, n) - 1 for j in range(s)]
+        off += n
+    return np.asarray(pos, np.int64), (off if realign else max(n_tokens))
 
 
 def _rope_sign_flipped(x, pos, theta):
@@ -94,6 +110,8 @@ def _bf16_double_round(x):
 MUTATIONS = [
     ("composed_positions", _positions_no_minus_one, pins.check_blog_positions),
     ("composed_positions", _positions_offset_by_slots, pins.check_blog_positions),
+    ("composed_positions", _positions_realign_ignored, pins.check_no_realign_positions),
+    ("composed_positions", _positions_no_realign_question_at_slots, pins.check_no_realign_positions),
     ("rope_rotate", _rope_sign_flipped, pins.check_rope),
     ("rope_rotate", _rope_interleaved, pins.check_rope),
     ("rope_inv_freq", _inv_freq_wrong_exponent, pins.check_rope),
