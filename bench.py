@@ -531,6 +531,65 @@ def run_sweep(args) -> None:
             torch.cuda.empty_cache()
 
 
+def run_extract(args) -> None:
+    """Extraction-side attention at full size (section "structured information
+    flow"): one document of 4000 tokens followed by its 1000 slots (k=4),
+    Llama3.1-8B attention geometry, one c2kv_attend_masked call per layer for
+    32 layers, under the structured mask and, for comparison, the plain causal
+    mask over the same 5000 tokens (which skips nothing).  achieved TFLOP/s
+    counts 4*d flops per visible (query head, key) pair."""
+    import torch
+    import compressed_composable_kv_gb300 as P
+    from compressed_composable_kv_gb300 import synth as S
+
+    g = S.LLAMA31_8B
+    L, n_doc, k = g.n_layers, 4000, 4
+    n_slot = -(-n_doc // k)
+    N = n_doc + n_slot
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    stream = torch.cuda.Stream()
+    gen = torch.Generator(device="cuda").manual_seed(7)
+    q = torch.randn((L, N, g.n_q_heads, g.head_dim), device="cuda", generator=gen).to(torch.bfloat16)
+    kk = torch.randn((L, N, g.n_kv_heads, g.head_dim), device="cuda", generator=gen).to(torch.bfloat16)
+    v = torch.randn((L, N, g.n_kv_heads, g.head_dim), device="cuda", generator=gen).to(torch.bfloat16)
+    out = torch.empty_like(q)
+    ws = torch.zeros(P.masked_workspace_bytes(g, N), dtype=torch.uint8, device="cuda")
+    peak = measured_peaks().get("bf16_tflops") or 1900.0
+    # visible (query, key) pairs: documents causal; slot i sees the sink, its
+    # own block (the union when they coincide) and slots 0..i
+    doc_pairs = n_doc * (n_doc + 1) // 2
+    slot_pairs = sum(len(set(range(min(k, n_doc))) | set(range(i * k, min((i + 1) * k, n_doc)))) + i + 1
+                     for i in range(n_slot))
+    for mask, n_d, n_s, pairs in ((P.C2KV_MASK_STRUCTURED, n_doc, n_slot, doc_pairs + slot_pairs),
+                                  (P.C2KV_MASK_CAUSAL, N, 0, N * (N + 1) // 2)):
+        def run_layers():
+            for l in range(L):
+                P.c2kv_attend_masked(g, mask, n_d, n_s, k, q[l], kk[l], v[l], out[l], ws, stream)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                run_layers()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(args.steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                run_layers()
+                e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1) / 1e3)
+        assert P.c2kv_device_error() == P.C2KV_OK
+        t = statistics.median(times)
+        flops = L * g.n_q_heads * pairs * 4 * g.head_dim
+        print(json.dumps({"extract": "structured" if mask == P.C2KV_MASK_STRUCTURED else "causal",
+                          "doc_tokens": n_doc, "slots": n_s, "k": k, "layers": L,
+                          "ms_per_document": t * 1e3, "tokens_per_s": N / t,
+                          "visible_pairs_per_head": pairs, "achieved_tflops": flops / t / 1e12,
+                          "peak_tflops": peak, "frac_of_bf16_peak": flops / t / 1e12 / peak,
+                          "note": "one c2kv_attend_masked call per layer (rotation, append, tcgen05 attention)"}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -542,9 +601,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="decode time vs context (16k..128k), compressed k=16/8/4 vs uncompressed")
+    ap.add_argument("--extract", action="store_true",
+                    help="extraction-side structured-mask attention, 4000-token document + 1000 slots")
     args = ap.parse_args()
     if args.sweep:
         run_sweep(args)
+        return
+    if args.extract:
+        run_extract(args)
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

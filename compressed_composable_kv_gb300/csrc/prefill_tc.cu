@@ -58,7 +58,7 @@ struct TcCfg {
   static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
   static constexpr int OFF_ML = OFF_P + 2 * P_BYTES;   // split merge: (m, l) of every row
   static constexpr int OFF_BAR = OFF_ML + BM * 2 * 4;
-  static constexpr int N_BAR = 1 + 2 * STAGES + 2 + 2 + 2 + 2 + 1;
+  static constexpr int N_BAR = 1 + 2 * STAGES + 2 + 2 + 2 + 2 + 2 + 1;
   static constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;   // + slack for 1024-byte alignment
   // split merge: unnormalised O of every row (fp32, 16-byte chunks swizzled
@@ -208,7 +208,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   uint64_t* s_free = s_full + 2;
   uint64_t* p_full = s_free + 2;
   uint64_t* p_free = p_full + 2;
+  // PV(t) completes phase t >> 1 of o_done[t & 1], so a wait for PV(j-1)
+  // can never mistake an older phase of the same parity for it; o_last
+  // (single use) completes with the last PV of the CTA.
   uint64_t* o_done = p_free + 2;
+  uint64_t* o_last = o_done + 2;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
@@ -226,6 +230,24 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   const int kb = split * p.split_keys;
   const int ke = min(kb + p.split_keys, kmax);
   const int ntiles = ke > kb ? (ke - kb + BN - 1) / BN : 0;
+  // Structured mask ("structured information flow"): an M tile of slot rows
+  // only sees the sink block, its own slots' document blocks and the slots,
+  // so the other document key tiles hold no visible key and are skipped.
+  // Every role walks the same list of live tiles.
+  auto tile_live = [&](int t) -> bool {
+    if (p.mask_mode != kMaskStructured || tok0 < p.n_doc) return true;   // document rows: causal
+    const int key0 = kb + t * BN;
+    if (key0 + BN > p.n_doc || key0 < min(p.kblk, p.n_doc)) return true;  // slot keys, sink block
+    const int lo = (tok0 - p.n_doc) * p.kblk;
+    const int hi = min((tok0 + ntok - p.n_doc) * p.kblk, p.n_doc);
+    return key0 < hi && key0 + BN > lo;
+  };
+  auto next_live = [&](int t) -> int {
+    while (t < ntiles && !tile_live(t)) ++t;
+    return t;
+  };
+  int nlive = 0;
+  for (int t = 0; t < ntiles; ++t) nlive += tile_live(t) ? 1 : 0;
 
   if (tid == 0) {
     mbar_init(q_full, 1);
@@ -239,7 +261,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
       mbar_init(&p_full[i], kSoftmaxThreads);
       mbar_init(&p_free[i], 1);
     }
-    mbar_init(o_done, 1);
+    mbar_init(&o_done[0], 1);
+    mbar_init(&o_done[1], 1);
+    mbar_init(o_last, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -263,21 +287,26 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
 
   float m_run = -INFINITY, l_run = 0.f;   // softmax threads: running max / sum of their row
   if (warp == 4) {
-    if (lane == 0 && ntiles > 0) {
+    if (lane == 0 && nlive > 0) {
       // ---------------- producer + MMA issuer (one thread)
       const int q_row0 = ((b * p.n_kv + h) * p.t_len + tok0) * G;
       mbar_arrive_expect_tx(q_full, C::Q_BYTES);
       for (int sub = 0; sub < C::NSUB; ++sub) tma_load_2d(sQ + sub * BM * 128, &p.tm_q, sub * 64, q_row0, q_full);
-      auto issue_kv = [&](int t) {
-        const int s = t % STAGES;
+      // the jj-th live tile (key tile t) goes to stage jj % STAGES
+      auto issue_kv = [&](int jj, int t) {
+        const int s = jj % STAGES;
         mbar_arrive_expect_tx(&kv_full[s], 2 * C::KV_BYTES);
         for (int sub = 0; sub < C::NSUB; ++sub) {
           tma_load_3d(sK + s * C::KV_BYTES + sub * BN * 128, &p.tm_k[b], sub * 64, kb + t * BN, kv_z, &kv_full[s]);
           tma_load_3d(sV + s * C::KV_BYTES + sub * BN * 128, &p.tm_v[b], sub * 64, kb + t * BN, kv_z, &kv_full[s]);
         }
       };
-      int next = 0;
-      for (; next < min(STAGES, ntiles); ++next) issue_kv(next);
+      int next = 0;                  // live tiles issued
+      int tnext = next_live(0);      // key tile of the next one
+      for (; next < min(STAGES, nlive); ++next) {
+        issue_kv(next, tnext);
+        tnext = next_live(tnext + 1);
+      }
       constexpr uint32_t IDESC_QK = idesc_bf16(BN, false);
       constexpr uint32_t IDESC_PV = idesc_bf16(D, true);
       auto issue_pv = [&](int t) -> bool {
@@ -292,11 +321,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
         }
         mma_commit(&kv_empty[s]);
         mma_commit(&p_free[pb]);
-        mma_commit(o_done);
+        mma_commit(&o_done[t & 1]);
         return true;
       };
       bool ok = wait_or_abort(q_full, 0, abort_flag, p.err);
-      for (int j = 0; ok && j < ntiles; ++j) {
+      for (int j = 0; ok && j < nlive; ++j) {
         const int s = j % STAGES, sb = j & 1;
         ok = wait_or_abort(&kv_full[s], (j / STAGES) & 1, abort_flag, p.err);
         if (ok && j >= 2) ok = wait_or_abort(&s_free[sb], ((j - 2) >> 1) & 1, abort_flag, p.err);
@@ -312,13 +341,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
         mma_commit(&s_full[sb]);
         if (j >= 1) {
           ok = issue_pv(j - 1);
-          if (ok && next < ntiles) {
+          if (ok && next < nlive) {
             ok = wait_or_abort(&kv_empty[(j - 1) % STAGES], ((j - 1) / STAGES) & 1, abort_flag, p.err);
-            if (ok) issue_kv(next++);
+            if (ok) {
+              issue_kv(next++, tnext);
+              tnext = next_live(tnext + 1);
+            }
           }
         }
       }
-      if (ok) issue_pv(ntiles - 1);
+      if (ok) ok = issue_pv(nlive - 1);
+      if (ok) mma_commit(o_last);   // every MMA of the CTA has completed
     }
   } else {
     // ---------------- softmax warps: thread tid owns row tid (TMEM lane tid)
@@ -329,7 +362,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
     const int lim = n_cached + tok + 1;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     bool ok = true;
-    for (int j = 0; j < ntiles; ++j) {
+    int tcur = next_live(0);   // key tile of the j-th live tile
+    for (int j = 0; j < nlive; ++j, tcur = next_live(tcur + 1)) {
       const int sb = j & 1;
       if (!__all_sync(0xffffffffu, wait_or_abort(&s_full[sb], (j >> 1) & 1, abort_flag, p.err))) {
         ok = false;
@@ -350,7 +384,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
       }
       tc_fence_before();
       mbar_arrive(&s_free[sb]);
-      const int key0 = kb + j * BN;
+      const int key0 = kb + tcur * BN;
       // keys [key0, key0 + nvis) pass the causal / split bounds of this row
       const int nvis = row_ok ? min(min(ke, lim) - key0, BN) : 0;
       float mraw = -INFINITY;   // max of the raw scores (the scale is positive)
@@ -401,7 +435,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
       // O rescale needs PV(j-1) finished; the warp shares the TMEM access, so
       // the whole warp takes the path when any of its rows needs it.
       if (__any_sync(0xffffffffu, rescale)) {
-        if (!__all_sync(0xffffffffu, wait_or_abort(o_done, (j - 1) & 1, abort_flag, p.err))) {
+        if (!__all_sync(0xffffffffu, wait_or_abort(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.err))) {
           ok = false;
           break;
         }
@@ -435,15 +469,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
 
     // ---------------- epilogue: the last PV must be complete before O is read
     ok = __all_sync(0xffffffffu, ok);
-    if (ok && ntiles > 0 && !__all_sync(0xffffffffu, wait_or_abort(o_done, (ntiles - 1) & 1, abort_flag, p.err)))
+    if (ok && nlive > 0 && !__all_sync(0xffffffffu, wait_or_abort(o_last, 0, abort_flag, p.err)))
       ok = false;
-    if (ok && ntiles > 0) tc_fence_after();
+    if (ok && nlive > 0) tc_fence_after();
     if (p.num_splits == 1) {
       const float invl = (l_run > 0.f) ? 1.f / l_run : 0.f;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         float o[32];
-        if (ok && ntiles > 0) {
+        if (ok && nlive > 0) {
           tmem_ld32(lane_base + C::TMEM_O + c0, o);
           tmem_wait_ld();
         } else {
@@ -469,9 +503,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   const bool aborted = *abort_flag != 0;
   if (aborted) {
     // let TMA copies in flight land before the shared memory is reused
-    if (tid == 0) {
+    if (tid == 0 && nlive > 0) {   // nothing was issued without live tiles
       mbar_wait(q_full, 0);
-      for (int s = 0; s < STAGES; ++s) mbar_wait(&kv_full[s], 0);
+      for (int s = 0; s < min(STAGES, nlive); ++s) mbar_wait(&kv_full[s], 0);
     }
     __syncthreads();
   }
@@ -479,10 +513,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   float* ost = reinterpret_cast<float*>(smem + C::OFF_OST);   // [BM][D], chunk c of row r at c ^ (r & 7)
   float* mls = reinterpret_cast<float*>(smem + C::OFF_ML);    // [BM][2]
   if (S > 1 && warp < 4) {
-    // Stage this split's rows: every MMA has completed (o_done) and every
+    // Stage this split's rows: every MMA has completed (o_last) and every
     // issued K/V copy has been consumed, so the K ring is free.
     const int row = tid;
-    const bool have = !aborted && ntiles > 0;   // uniform over the CTA
+    const bool have = !aborted && nlive > 0;   // uniform over the CTA
     if (have) tc_fence_after();
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
 #pragma unroll

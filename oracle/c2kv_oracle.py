@@ -297,21 +297,24 @@ def extraction_positions(n_doc: int, n_slot: int, k: int) -> np.ndarray:
     return np.asarray(doc + slots, dtype=np.int64)
 
 
-def masked_extraction_attention(q_pre, k_pre, v, n_doc, n_slot, k, theta):
+def masked_extraction_attention(q_pre, k_pre, v, n_doc, n_slot, k, theta, rows=None):
     """Attention over one document and its slots under the structured mask.
 
     q_pre bits [N][Hq][d], k_pre/v bits [N][Hkv][d] for the N = n_doc+n_slot
     tokens (pre-RoPE).  q and k are rotated at extraction_positions() in fp64
-    (no rounding).  Returns out fp64 [N][Hq][d]."""
+    (no rounding).  Returns out fp64 [N][Hq][d], or [len(rows)][Hq][d] for
+    the query rows listed in `rows` (each row computed exactly as in the full
+    result)."""
     N, hq, d = q_pre.shape
     hkv = k_pre.shape[1]
     g = hq // hkv
+    rows = np.arange(N) if rows is None else np.asarray(rows, dtype=np.int64)
     pos = extraction_positions(n_doc, n_slot, k)
-    q = rope_rotate(bf16_to_f64(q_pre).transpose(1, 0, 2), pos, theta)
+    q = rope_rotate(bf16_to_f64(q_pre[rows]).transpose(1, 0, 2), pos[rows], theta)
     kk = rope_rotate(bf16_to_f64(k_pre).transpose(1, 0, 2), pos, theta)
     vv = bf16_to_f64(v).transpose(1, 0, 2)
-    mask = structured_mask(n_doc, n_slot, k)
-    out = np.empty((N, hq, d), dtype=np.float64)
+    mask = structured_mask(n_doc, n_slot, k)[rows]
+    out = np.empty((len(rows), hq, d), dtype=np.float64)
     for h in range(hq):
         out[:, h, :] = masked_softmax_attention(q[h], kk[h // g], vv[h // g], mask)
     return out

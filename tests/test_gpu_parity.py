@@ -322,6 +322,30 @@ def test_structured_mask_mode(n_doc, n_slot, k):
     check_attention(out, ref, f"structured mask {n_doc}+{n_slot} k={k}")
 
 
+def test_structured_mask_extraction_full_size():
+    """A 4000-token document with its 1000 slots (k=4) under the structured
+    mask, Llama3.1-8B heads: slot tiles skip the document key tiles they
+    cannot see.  The oracle computes sampled rows: document rows, slot rows at
+    tile edges, the last slot and random ones."""
+    g = S.Geometry(1, 32, 8, 128, 5.0e5)
+    n_doc, k = 4000, 4
+    n_slot = O.slot_count(n_doc, k)
+    N = n_doc + n_slot
+    rng = np.random.default_rng(17)
+    q = S.normal_bf16(rng, (N, 32, 128))
+    kk = S.normal_bf16(rng, (N, 8, 128))
+    v = S.normal_bf16(rng, (N, 8, 128))
+    ws = torch.zeros(P.masked_workspace_bytes(g, N), dtype=torch.uint8, device="cuda")
+    out = torch.empty((N, 32, 128), dtype=torch.bfloat16, device="cuda")
+    P.c2kv_attend_masked(g, P.C2KV_MASK_STRUCTURED, n_doc, n_slot, k, to_dev(q), to_dev(kk), to_dev(v), out, ws)
+    torch.cuda.synchronize()
+    assert P.c2kv_device_error() == P.C2KV_OK
+    rows = [0, 1, 63, 64, 1000, 3999, 4000, 4001, 4031, 4032, 4063, 4064, 4500, N - 1]
+    rows += sorted(rng.choice(N, 18, replace=False).tolist())
+    ref = O.masked_extraction_attention(q, kk, v, n_doc, n_slot, k, g.rope_theta, rows=rows)
+    check_attention(out[rows], ref, "structured mask 4000 + 1000, k=4")
+
+
 def test_causal_mask_mode_llama_heads():
     g = S.Geometry(1, 32, 8, 128, 5.0e5)
     N = 300

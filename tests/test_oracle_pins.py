@@ -146,3 +146,18 @@ def test_gqa_mapping_mistake_is_caught(monkeypatch):
     monkeypatch.setattr(O, "attend_new_tokens", modulo_mapping)
     with pytest.raises(AssertionError):
         pins.check_gqa_and_causality(O)
+
+
+def test_masked_attention_row_subset_equals_full_rows():
+    """The sampled-row form of the extraction attention (used at full size)
+    computes each row exactly as the full result does."""
+    rng = np.random.default_rng(2)
+    n_doc, n_slot, k = 37, 10, 4
+    N = n_doc + n_slot
+    q = (rng.standard_normal((N, 4, 16)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    kk = (rng.standard_normal((N, 2, 16)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    v = (rng.standard_normal((N, 2, 16)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    full = O.masked_extraction_attention(q, kk, v, n_doc, n_slot, k, 1e4)
+    rows = [0, 5, 36, 37, 40, 46]
+    sub = O.masked_extraction_attention(q, kk, v, n_doc, n_slot, k, 1e4, rows=rows)
+    assert np.array_equal(sub, full[rows])
