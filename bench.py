@@ -301,7 +301,7 @@ def run_ours(args, rank: int, world: int) -> dict:
     assert P.c2kv_device_error() == P.C2KV_OK
     # per request: one table + one re-rotation per layer sub-group of each
     # compose call; 2 launches per prefill layer; L decode + 1 advance per step
-    rerope_launches = sum(min(l1 - l0, 4) for l0, l1 in groups)
+    rerope_launches = sum(max(1, min(4, (l1 - l0) // 4)) for l0, l1 in groups)
     launches_per_step = (bt.batch * (1 + rerope_launches) + (2 * L if Q else 0) + T * (L + 1))
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]

@@ -625,8 +625,11 @@ c2kv_status c2kv_compose_layers(c2kv_store st, int32_t n_docs, const int32_t* do
 
   // Each layer group's re-rotation runs on the caller's stream once its
   // copies have landed (and after the table, which is earlier on that stream).
+  // Up to kLayerGroups copy/rotate groups per call, of at least 4 layers
+  // each, so that each re-rotation launch has enough rows to stream at the
+  // HBM rate (a layer-group continuation of 4 layers is one group).
   const int nl = layer_end - layer_begin;
-  const int ngroups = std::min(nl, kLayerGroups);
+  const int ngroups = std::max(1, std::min(kLayerGroups, nl / 4));
   uint8_t* kc = static_cast<uint8_t*>(k_cache);
   uint8_t* vc = static_cast<uint8_t*>(v_cache);
   for (int gi = 0; gi < ngroups; ++gi) {

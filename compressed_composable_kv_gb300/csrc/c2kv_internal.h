@@ -86,6 +86,34 @@ __device__ __forceinline__ uint32_t df_to_bf16_bits(float hi, float lo) {
   return r + (up ? 1u : 0u);
 }
 
+// a*(bh + bl) + c*(dh + dl) rounded once to bf16 (nearest even), for bf16-
+// exact a, c and a double-float cos/sin (|bl| <= 2^-24 |bh|, same for d).
+// Fast path: r = fma(a, bh, c*dh) in fp32 is within
+// e = 2^-22 (|a bh| + |c dh|) of the exact value (the dropped lo terms, the
+// product rounding and the fma rounding, each <= 2^-24 of those magnitudes);
+// e is doubled against the rounding of the bound itself.  mid, the bf16
+// midpoint inside r's bf16 interval, is the only midpoint within a quarter
+// bf16 ulp (>= |r| 2^-10) of r, so with e below |r| 2^-10 and |r - mid|
+// (exact) above e, r rounds like the exact value.  Otherwise (near a
+// midpoint, or after heavy cancellation) the double-float evaluation, kept
+// out of line, decides.
+static __device__ __noinline__ uint32_t rot_bf16_bits_slow(float a, float bh, float bl, float c, float dh, float dl) {
+  float hi, lo;
+  dot2_df(a, bh, bl, c, dh, dl, hi, lo);
+  return df_to_bf16_bits(hi, lo);
+}
+
+__device__ __forceinline__ uint32_t rot_bf16_bits(float a, float bh, float bl, float c, float dh, float dl) {
+  const float p = __fmul_rn(c, dh);
+  const float r = fmaf(a, bh, p);
+  const float m = __fadd_rn(fabsf(__fmul_rn(a, bh)), fabsf(p));   // 2^21 e
+  const uint32_t bits = __float_as_uint(r);
+  const float mid = __uint_as_float((bits & 0xFFFF0000u) | 0x8000u);
+  if (__fmul_rn(fabsf(__fsub_rn(r, mid)), 0x1p21f) > m && __fmul_rn(fabsf(r), 0x1p11f) > m)
+    return (bits + 0x7FFFu + ((bits >> 16) & 1u)) >> 16;
+  return rot_bf16_bits_slow(a, bh, bl, c, dh, dl);
+}
+
 // ---------------------------------------------------------------- bf16 helpers
 __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
   f[0] = __uint_as_float(u.x << 16); f[1] = __uint_as_float(u.x & 0xffff0000u);
@@ -107,6 +135,10 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
 // offsets of the second half.  Each output is evaluated in double-float and
 // rounded once to bf16, so it is the correctly rounded rotation of the
 // stored bf16 inputs (to ~2^-44), also when x cos - y sin nearly cancels.
+// t[e * STRIDE] holds the cos/sin of pair e of the 8 (a transposed shared-
+// memory table uses STRIDE > 1 so that neighbouring lanes read neighbouring
+// entries).
+template <int STRIDE = 1>
 __device__ __forceinline__ void rotate8_df(uint4& a, uint4& b, const CosSin2* t) {
   float x[8], y[8];
   unpack8(a, x);
@@ -114,11 +146,9 @@ __device__ __forceinline__ void rotate8_df(uint4& a, uint4& b, const CosSin2* t)
   uint32_t xo[8], yo[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    float hi, lo;
-    dot2_df(x[e], t[e].ch, t[e].cl, -y[e], t[e].sh, t[e].sl, hi, lo);   // x cos - y sin
-    xo[e] = df_to_bf16_bits(hi, lo);
-    dot2_df(y[e], t[e].ch, t[e].cl, x[e], t[e].sh, t[e].sl, hi, lo);    // y cos + x sin
-    yo[e] = df_to_bf16_bits(hi, lo);
+    const CosSin2 te = t[e * STRIDE];
+    xo[e] = rot_bf16_bits(x[e], te.ch, te.cl, -y[e], te.sh, te.sl);   // x cos - y sin
+    yo[e] = rot_bf16_bits(y[e], te.ch, te.cl, x[e], te.sh, te.sl);    // y cos + x sin
   }
   a = make_uint4(xo[0] | (xo[1] << 16), xo[2] | (xo[3] << 16), xo[4] | (xo[5] << 16), xo[6] | (xo[7] << 16));
   b = make_uint4(yo[0] | (yo[1] << 16), yo[2] | (yo[3] << 16), yo[4] | (yo[5] << 16), yo[6] | (yo[7] << 16));

@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
       // keys [key0, key0 + nvis) pass the causal / split bounds of this row
       const int nvis = row_ok ? min(min(ke, lim) - key0, BN) : 0;
       float mraw = -INFINITY;   // max of the raw scores (the scale is positive)
-      if (p.mask_mode == kMaskStructured) {
+      if (p.mask_mode == kMaskStructured && tok >= p.n_doc) {   // slot rows; document rows are causal
 #pragma unroll
         for (int c = 0; c < BN; ++c) {
           const bool vis = c < nvis && tc_structured_visible(p, tok, key0 + c);

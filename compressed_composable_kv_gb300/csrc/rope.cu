@@ -50,7 +50,10 @@ __global__ void rope_table_kernel(const __grid_constant__ TableParams p) {
 // One CTA owns kSlots consecutive composed slots: it stages their rows of
 // the cos/sin table in shared memory once and rotates those slots' rows in
 // every (layer, kv head) of the group with 16-byte loads/stores.  V rows are
-// never touched (they land by DMA).
+// never touched (they land by DMA).  A thread owns the 8 pairs of one 16-byte
+// chunk; the staged rows are transposed (pair 8c + e at e * TPR + c) so that
+// the 8 lanes of a row read 8 neighbouring entries instead of entries 128
+// bytes apart on the same banks.
 // ---------------------------------------------------------------------------
 constexpr int kSlots = 32;
 constexpr int kRopeThreads = 256;
@@ -63,7 +66,10 @@ __global__ void __launch_bounds__(kRopeThreads) rerope_kernel(const __grid_const
 
   const int slot0 = blockIdx.x * kSlots;
   const int n_here = min(kSlots, p.n_total - slot0);
-  for (int i = threadIdx.x; i < n_here * H; i += kRopeThreads) tab[i / H][i % H] = p.tab[(size_t)slot0 * H + i];
+  for (int i = threadIdx.x; i < n_here * H; i += kRopeThreads) {
+    const int f = i % H;
+    tab[i / H][(f % 8) * TPR + f / 8] = p.tab[(size_t)slot0 * H + i];
+  }
   __syncthreads();
 
   const int n_rows = (p.layer1 - p.layer0) * p.n_kv;   // (layer, head) row blocks
@@ -94,7 +100,7 @@ __global__ void __launch_bounds__(kRopeThreads) rerope_kernel(const __grid_const
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       if (ok[u]) {
-        rotate8_df(a[u], b[u], &tab[r_[u]][c_[u] * 8]);
+        rotate8_df<TPR>(a[u], b[u], &tab[r_[u]][c_[u]]);
         base[u][c_[u]] = a[u];
         base[u][c_[u] + TPR] = b[u];
       }
