@@ -177,9 +177,17 @@ def measured_peaks() -> dict:
         return {}
 
 
+def sources_sha(srcs: str) -> str:
+    """sha256[:16] over the comma-separated source files, in order."""
+    h = hashlib.sha256()
+    for src in srcs.split(","):
+        h.update(open(os.path.join(ROOT, src), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def profiled_traffic(kernel: str):
     """dram bytes per key-row of `kernel` from the committed ncu summary, if the
-    kernel source is unchanged since the capture (sha256 of its .cu file)."""
+    kernel's sources are unchanged since the capture (sha256 over them)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
         lines = open(path).read().splitlines()
@@ -188,11 +196,10 @@ def profiled_traffic(kernel: str):
     for ln in lines:
         if ln.startswith("#") or not ln.strip():
             continue
-        name, src, sha, per_unit = ln.split()[:4]
+        name, srcs, sha, per_unit = ln.split()[:4]
         if name != kernel:
             continue
-        cur = hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest()[:16]
-        return float(per_unit) if cur == sha else None
+        return float(per_unit) if sources_sha(srcs) == sha else None
     return None
 
 
