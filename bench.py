@@ -424,20 +424,7 @@ def run_ours(args, rank: int, world: int) -> dict:
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {
-            "workload": w.name,
-            "geometry": f"{L} layers, {g.n_q_heads} q / {g.n_kv_heads} kv heads, head_dim {g.head_dim}, "
-                        f"rope_theta {g.rope_theta:g}",
-            "k": w.k, "batch": Bn, "composed_slots": bt.n_slots, "original_tokens": bt.l_tot,
-            "question_tokens": Q, "decode_steps": T,
-            "l2": "inputs larger than L2 (composed cache per request > 1 GB; 129 MB L2)",
-            "graphs": "prefill and decode replayed from CUDA graphs of this library's kernels",
-            "ttft_pipeline": (f"compose and prefill layer-pipelined in {len(groups)} groups: compose_ms = "
-                              "until the whole cache is composed (prefill of earlier groups overlaps it), "
-                              "prefill_ms = the rest of the prefill"),
-            "parallelism": f"replicas x{world}",
-            "attention_only": "no projection/MLP weights: attention over the composed cache only",
-        },
+        "config": workload_config(w, world),
         "compose_ms": comp * 1e3,
         "prefill_ms": pre * 1e3,
         "decode_ms": dec * 1e3,
@@ -460,6 +447,30 @@ def run_ours(args, rank: int, world: int) -> dict:
     torch.cuda.synchronize()
     P.c2kv_store_destroy(store)
     return out
+
+
+def workload_config(w, world: int) -> dict:
+    """The `config` object of both arms' lines (host-side sizes only)."""
+    from compressed_composable_kv_gb300 import synth as S
+    g = w.geom
+    docs_meta, reqs = S.make_requests(w)
+    n_groups = min(g.n_layers, 8)
+    return {
+        "workload": w.name,
+        "geometry": f"{g.n_layers} layers, {g.n_q_heads} q / {g.n_kv_heads} kv heads, head_dim {g.head_dim}, "
+                    f"rope_theta {g.rope_theta:g}",
+        "k": w.k, "batch": w.batch,
+        "composed_slots": [sum(docs_meta[d][1] for d in r.doc_ids) for r in reqs],
+        "original_tokens": [sum(docs_meta[d][0] for d in r.doc_ids) for r in reqs],
+        "question_tokens": w.q_len, "decode_steps": w.decode_steps,
+        "l2": "inputs larger than L2 (composed cache per request > 1 GB; 129 MB L2)",
+        "graphs": "prefill and decode replayed from CUDA graphs of this library's kernels",
+        "ttft_pipeline": (f"compose and prefill layer-pipelined in {n_groups} groups: compose_ms = "
+                          "until the whole cache is composed (prefill of earlier groups overlaps it), "
+                          "prefill_ms = the rest of the prefill"),
+        "parallelism": f"replicas x{world}",
+        "attention_only": "no projection/MLP weights: attention over the composed cache only",
+    }
 
 
 def run_sweep(args) -> None:
@@ -624,6 +635,7 @@ def main():
         # The reference arm is the CPU oracle; only rank 0 runs it.
         if rank != 0:
             return
+        from compressed_composable_kv_gb300 import synth as S
         samples = []
         for i in range(args.warmup + args.steps):
             r = run_oracle_sample(args.workload, budget_s=0.5)
@@ -635,7 +647,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": statistics.mean(s["request_s"] for s in samples) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": args.workload},
+            "data": "synthetic", "config": workload_config(S.WORKLOADS[args.workload], world),
             "cpu_baseline": {"value": tok_s, "unit": "tok/s", "cores": 1, "kind": "oracle",
                              "sample": samples[0]["sample"] + " (one sample per step)"},
             "e2e": {"value": tok_s, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
