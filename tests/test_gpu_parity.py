@@ -258,6 +258,24 @@ def test_varlen_batch_pool():
     sc.close()
 
 
+@pytest.mark.parametrize("batch", [4, 5])
+def test_decode_cluster_merge_batches(batch):
+    """Batches of 4 and 5 sequences (Llama heads): 32 and 40 (sequence, kv
+    head) units leave 4 and 3 key splits per unit, which merge inside a
+    thread-block cluster through distributed shared memory."""
+    g = S.Geometry(1, 32, 8, 128, 5.0e5)
+    rng = np.random.default_rng(40 + batch)
+    specs = [(i, int(n), -(-int(n) // 4)) for i, n in enumerate(rng.integers(1500, 4000, 10))]
+    requests = [([int(x) for x in rng.choice(10, 3, replace=False)], None) for _ in range(batch)]
+    sc = Scenario(g, 4, specs, requests, q_len=16, decode_steps=3)
+    w = S.Workload("clusters", g, 4, batch, 16, 3, seed=0xC2C6 + batch)
+    inputs = S.make_step_inputs(w)
+    pre, dec = run_all(sc, upload(inputs))
+    for b in range(batch):
+        check_request(sc, inputs, pre, dec, b, layers=[0], steps=[0, 2])
+    sc.close()
+
+
 def test_qwen_group5_k16():
     """Qwen3-14B attention geometry (G=5, theta 1e6) at k=16: 16 x 8000-token
     documents -> 8000 slots, 2 layers, batch 2, 128-token question."""
