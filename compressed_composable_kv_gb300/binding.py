@@ -43,6 +43,7 @@ _pvp = ctypes.POINTER(ctypes.c_void_p)
 _pg = ctypes.POINTER(c2kv_geometry)
 
 _SIGNATURES = {
+    "c2kv_test_expire_next_waits": (_i32, [_i32]),
     "c2kv_last_error": (ctypes.c_char_p, []),
     "c2kv_version": (ctypes.c_char_p, []),
     "c2kv_store_create": (_i32, [_pg, _sz, ctypes.POINTER(_vp)]),
@@ -317,6 +318,11 @@ def masked_workspace_bytes(geom, n_tokens: int) -> int:
     """Scratch bytes c2kv_attend_masked needs for one n_tokens sequence."""
     a = c2kv_attend_workspace_size(geom, 1, n_tokens, n_tokens)
     return ((a + 255) // 256) * 256 + c2kv_masked_extra_bytes(geom, n_tokens)
+
+
+def c2kv_test_expire_next_waits(n_launches: int) -> None:
+    """Test hook: the next n decode launches take their bounded-wait timeout path."""
+    _check(load_library().c2kv_test_expire_next_waits(int(n_launches)))
 
 
 def c2kv_device_error() -> int:

@@ -5,6 +5,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <string>
 #include <unordered_map>
@@ -271,6 +272,16 @@ c2kv_status run_prefill_tc(const c2kv_geometry* g, int batch, const void* const*
   return C2KV_OK;
 }
 
+// Test hook: the next n decode launches take their bounded-wait timeout path.
+std::atomic<int> g_inject_timeouts{0};
+
+bool take_injected_timeout() {
+  int n = g_inject_timeouts.load();
+  while (n > 0 && !g_inject_timeouts.compare_exchange_weak(n, n - 1)) {
+  }
+  return n > 0;
+}
+
 // tabs[b]: per-row cos/sin table of sequence b (token t at row n_cached + t).
 c2kv_status run_attention(const c2kv_geometry* g, int batch, const __nv_bfloat16* const* kb,
                           const __nv_bfloat16* const* vb, const CosSin2* const* tabs, const int32_t* n_cached_h,
@@ -332,6 +343,7 @@ c2kv_status run_attention(const c2kv_geometry* g, int batch, const __nv_bfloat16
       }
     }
   }
+  p.inject_timeout = take_injected_timeout() ? 1 : 0;
   p.fuse_append = fused_k_new != nullptr ? 1 : 0;
   p.k_new = static_cast<const __nv_bfloat16*>(fused_k_new);
   p.v_new = static_cast<const __nv_bfloat16*>(fused_v_new);
@@ -860,6 +872,12 @@ c2kv_status c2kv_attend_masked(const c2kv_geometry* geom, int32_t mask, int32_t 
   const void* v0 = vt;
   return run_prefill_tc(geom, 1, &k0, &v0, &zero, &N, geom->n_kv_heads, N, 0, N, N, mmode, n_doc, kblk, out, w,
                         ws, st);
+}
+
+c2kv_status c2kv_test_expire_next_waits(int32_t n_launches) {
+  if (n_launches < 0) return fail(C2KV_EINVAL, "n_launches < 0");
+  g_inject_timeouts.store(n_launches);
+  return C2KV_OK;
 }
 
 c2kv_status c2kv_device_error(int32_t* code) {

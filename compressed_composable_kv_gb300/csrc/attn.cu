@@ -90,7 +90,7 @@ struct DCfg {
   static constexpr int OFF_SC = OFF_QS + G * D * 4;             // per-group scores [HS][NG][VP]
   static constexpr int OFF_W = OFF_SC + HS * NG * VP * 4;       // merge weights [G][WN] + [G] M, L
   static constexpr int OFF_BAR = (OFF_W + G * WN * 4 + 2 * G * 4 + 15) / 16 * 16;
-  static constexpr int OFF_CS = OFF_BAR + (2 * kStages + 2) * 8;   // merge flag
+  static constexpr int OFF_CS = OFF_BAR + (2 * kStages + 3) * 8;   // merge flag
   static constexpr int SMEM = OFF_CS + 16;
   static_assert(G % GW == 0 && NWK >= 1 && NG % 2 == 0, "decode tiling");
 };
@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, 1) decode_kernel(const __
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + kStages;
   uint64_t* inj = empty + kStages;                                     // new-key row injected
+  uint64_t* never = inj + 1;                                           // test hook: nothing arrives
   int* flag = reinterpret_cast<int*>(smem + C::OFF_CS);
 
   const int tid = threadIdx.x;
@@ -190,6 +191,7 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, 1) decode_kernel(const __
       mbar_init(&empty[s], NW);
     }
     mbar_init(inj, TPR);
+    mbar_init(never, 1);
     fence_barrier_init();
     for (; issued < min(kStages, ntiles); ++issued) issue(issued);
   }
@@ -272,6 +274,7 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, 1) decode_kernel(const __
     const int s = t % kStages;
     const uint32_t ph = (t / kStages) & 1;
     if (!mbar_wait(&full[s], ph)) { aborted = true; break; }
+    if (p.inject_timeout && t == 0 && !mbar_wait(never, 0, kInjectWaitCycles)) { aborted = true; break; }
     if (t == t_new) {
       if (warp == 1 && lane < TPR) {
         const int r = nk - (kb + t * T);

@@ -21,6 +21,7 @@ constexpr unsigned kErrLength = 2u;       // a device-side length exceeded cap /
 
 // Bounded waits give up after this many SM cycles (about 2 s at 2 GHz).
 constexpr long long kWaitCycles = 4000000000LL;
+constexpr long long kInjectWaitCycles = 1000000LL;   // the test hook's wait (~0.5 ms)
 
 // ---------------------------------------------------------------- RoPE angles
 // The angle pos * inv_freq is formed in fp64 and reduced modulo 2*pi with a
@@ -190,11 +191,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit = kWaitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   }
   return true;
 }
@@ -294,6 +295,10 @@ struct AttnParams {
   // The num_splits CTAs of a (sequence, kv head) run as one thread-block
   // cluster and merge their partial results in distributed shared memory.
   int32_t cluster_merge;
+  // Test hook (c2kv_test_expire_next_waits): the CTA's first tile wait also
+  // waits on a barrier nothing arrives on, ~0.5 ms, and so takes the
+  // timeout path.
+  int32_t inject_timeout;
   float scale_log2;
 };
 

@@ -364,6 +364,18 @@ size_t c2kv_masked_extra_bytes(const c2kv_geometry* geom, int32_t n_tokens);
  */
 c2kv_status c2kv_device_error(int32_t* code);
 
+/*
+ * Test hook for the failure path (the pages have no counterpart): the next
+ * n_launches decode launches (c2kv_attend_decode, c2kv_attend_decode_noalloc,
+ * c2kv_attend_prefill with q_len 1) each wait, at their first key tile, on a
+ * barrier nothing arrives on, for ~0.5 ms of GPU clock.  The wait expires and
+ * the kernel takes its timeout path: it records C2KV_ETIMEOUT in the device
+ * error word, lets its copies in flight land and returns; that launch's
+ * outputs are undefined, the cache rows it appends are written, and the
+ * context stays usable.  0 disarms it.  Process-wide; C2KV_EINVAL for n < 0.
+ */
+c2kv_status c2kv_test_expire_next_waits(int32_t n_launches);
+
 #ifdef __cplusplus
 }
 #endif

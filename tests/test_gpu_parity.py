@@ -276,6 +276,45 @@ def test_decode_cluster_merge_batches(batch):
     sc.close()
 
 
+@pytest.mark.parametrize("batch", [1, 4])
+def test_decode_wait_timeout_is_reported_and_context_recovers(batch):
+    """Failure detection without a fault: the test hook makes a decode launch
+    wait ~0.5 ms on a barrier nothing arrives on.  The kernel takes its
+    timeout path (global last-CTA merge at batch 1, cluster merge at batch 4),
+    the host reads C2KV_ETIMEOUT, and the same step decoded again right after
+    matches the oracle."""
+    g = S.Geometry(1, 32, 8, 128, 5.0e5)
+    specs = [(i, 3000 + 400 * i, 750 + 100 * i) for i in range(4)]
+    requests = [([i % 4, (i + 1) % 4], None) for i in range(batch)]
+    sc = Scenario(g, 4, specs, requests, q_len=8, decode_steps=1)
+    w = S.Workload("timeout", g, 4, batch, 8, 1, seed=0xC2C9 + batch)
+    inputs = S.make_step_inputs(w)
+    dev = upload(inputs)
+    bt = sc.batch
+    bt.compose()
+    pre = []
+    for l in range(g.n_layers):
+        o = torch.empty_like(dev["q_pre"][l])
+        bt.prefill(l, dev["q_pre"][l], dev["kq_pre"][l], dev["vq"][l], o)
+        pre.append(o)
+    bt.reset_decode()
+    torch.cuda.synchronize()
+    assert P.c2kv_device_error() == P.C2KV_OK
+    junk = torch.empty_like(dev["qd_pre"][0, 0])
+    P.c2kv_test_expire_next_waits(1)
+    bt.decode(0, dev["qd_pre"][0, 0], dev["kd_pre"][0, 0], dev["vd"][0, 0], junk)
+    torch.cuda.synchronize()
+    assert P.c2kv_device_error() == P.C2KV_ETIMEOUT
+    out = torch.empty_like(junk)
+    bt.decode(0, dev["qd_pre"][0, 0], dev["kd_pre"][0, 0], dev["vd"][0, 0], out)
+    torch.cuda.synchronize()
+    assert P.c2kv_device_error() == P.C2KV_OK
+    for b in range(batch):
+        check_request(sc, inputs, pre, [[out]], b, layers=[0], steps=[0])
+    P.c2kv_test_expire_next_waits(0)
+    sc.close()
+
+
 def test_qwen_group5_k16():
     """Qwen3-14B attention geometry (G=5, theta 1e6) at k=16: 16 x 8000-token
     documents -> 8000 slots, 2 layers, batch 2, 128-token question."""
