@@ -9,24 +9,30 @@
 // extraction-time mode (used here only for one-token sequences).
 //
 // One token per sequence.  A CTA owns one (sequence b, kv head h, key split)
-// and is wide (NW warps, one wave of CTAs over the GPU) so that few splits
+// and is wide (16 warps, one wave of CTAs over the GPU) so that few splits
 // cover a layer and their merge stays short.  The split's keys stream through
-// a 3-stage ring of K/V tiles in shared memory, each tile fetched by two 1-D
-// bulk copies (TMA engine) completing on an mbarrier.  A "key group" of d/8
-// lanes scores one key at a time: each lane holds 8 elements of d for all G
-// q heads of the kv head (as fp32 pairs for the packed fma.rn.f32x2), the
-// partial dots are reduced with xor shuffles, and each group keeps its own
-// online-softmax state (m, l, o), rescaled lazily (only when the running max
-// grows by more than 2^8).  Groups are merged in shared memory; with several
-// splits the CTA writes (m, l, o) partials and the last CTA of its (b, h) to
-// arrive (atomic counter) merges them, one output element per thread, and
-// resets the counter.
+// a 3-stage ring of 128-key K/V tiles in shared memory, each tile fetched by
+// two 1-D bulk copies (TMA engine) completing on an mbarrier; the first tiles
+// are requested before anything else waits on memory.  The G q heads are
+// split over warp slices of GW heads; a "key group" of d/16 lanes takes 4
+// keys of every tile, lane li owning the 16-byte chunks li and li + d/16
+// of each row (for d = 128 a RoPE pair), so partial dots use packed
+// fma.rn.f32x2 and a transposed reduce-scatter over the group leaves one
+// score per lane; scores are exchanged through shared memory.  Each group
+// keeps its own online-softmax state (m, l, o), rescaled lazily (only when
+// the running max grows by more than 2^8).  q is rotated once per CTA from
+// the sequence's RoPE table and pre-scaled.  Groups are merged in shared
+// memory; with several splits the CTA writes (m, l, o) partials, arrives on
+// a per-(b, h) counter with one acq_rel atomic, and the last CTA to arrive
+// merges them and resets the counter.  When a thread-block cluster of all
+// the splits of every unit can be resident at once, the splits merge through
+// distributed shared memory instead.
 //
 // Decode fuses the append: the CTA whose split holds the new key rotates it
-// (double-float, correctly rounded, from the sequence's RoPE table), stores
-// it with its value at row n_cached, and writes it into its last shared-memory
-// tile, which the bulk copy leaves free; an mbarrier orders that write before
-// the other warps read the tile.
+// (correctly rounded to bf16, from the sequence's RoPE table), stores it with
+// its value at row n_cached, and writes it into its last shared-memory tile,
+// which the bulk copy leaves free; an mbarrier orders that write before the
+// other warps read the tile.
 #include <float.h>
 
 #include <cooperative_groups.h>
