@@ -250,9 +250,9 @@ c2kv_status run_prefill_tc(const c2kv_geometry* g, int batch, const void* const*
   if (s != C2KV_OK) return s;
   for (int b = 0; b < batch; ++b) {
     const uint64_t stride2 = (uint64_t)block_rows * D * 2;
-    s = encode_map(&p.tm_k[b], kb0[b], 3, D, valid[b], n_blocks, stride2, 64);
+    s = encode_map(&p.tm_k[b], kb0[b], 3, D, valid[b], n_blocks, stride2, (uint32_t)prefill_tc_key_tile());
     if (s != C2KV_OK) return s;
-    s = encode_map(&p.tm_v[b], vb0[b], 3, D, valid[b], n_blocks, stride2, 64);
+    s = encode_map(&p.tm_v[b], vb0[b], 3, D, valid[b], n_blocks, stride2, (uint32_t)prefill_tc_key_tile());
     if (s != C2KV_OK) return s;
     p.n_cached[b] = n_cached[b];
   }

@@ -39,8 +39,8 @@ namespace c2kv {
 namespace {
 
 constexpr int BM = 128;        // rows per M tile (TMEM lanes)
-constexpr int BN = 64;         // keys per tile
-constexpr int STAGES = 5;
+constexpr int BN = 128;        // keys per tile
+constexpr int STAGES = 2;
 constexpr int kMaxClusterTc = 16;   // key splits merged in one cluster
 constexpr int kSoftmaxThreads = 128;
 constexpr int kThreadsTc = 160;
@@ -68,9 +68,10 @@ struct TcCfg {
   // [rows per CTA][S] m, l and weights; rows per CTA * S <= BM + S
   static_assert((BM + kMaxClusterTc) * 3 * 4 <= Q_BYTES, "merge scratch must fit the Q tile");
   static_assert(SMEM <= 232448, "shared memory per CTA");
-  static constexpr int TMEM_S = 0;                    // two 64-column S buffers
+  static constexpr int TMEM_S = 0;                    // two BN-column S buffers
   static constexpr int TMEM_O = 2 * BN;               // d columns
-  static constexpr int TMEM_COLS = 256;
+  static constexpr int TMEM_COLS = 512;
+  static_assert(TMEM_O + D <= TMEM_COLS, "TMEM columns");
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -315,7 +316,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t a = sw128_desc(smem_addr(sP + pb * C::P_BYTES) + kk * 32, 16, 1024);
+          // P is BN/64 K-major sub-tiles of [BM rows][64 keys]
+          const uint64_t a = sw128_desc(smem_addr(sP + pb * C::P_BYTES + (kk / 4) * BM * 128) + (kk % 4) * 32, 16, 1024);
           const uint64_t bdesc = sw128_desc(smem_addr(sV + s * C::KV_BYTES) + kk * 2048, BN * 128, 1024);
           mma_bf16(tmem + C::TMEM_O, a, bdesc, IDESC_PV, (t > 0 || kk > 0) ? 1u : 0u);
         }
@@ -372,15 +374,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
       tc_fence_after();
       float sv[BN];
       {
-        float t0[32], t1[32];
-        tmem_ld32(lane_base + C::TMEM_S + sb * BN, t0);
-        tmem_ld32(lane_base + C::TMEM_S + sb * BN + 32, t1);
+        float t[BN / 32][32];
+#pragma unroll
+        for (int q4 = 0; q4 < BN / 32; ++q4) tmem_ld32(lane_base + C::TMEM_S + sb * BN + q4 * 32, t[q4]);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          sv[c] = t0[c];
-          sv[32 + c] = t1[c];
-        }
+        for (int q4 = 0; q4 < BN / 32; ++q4)
+#pragma unroll
+          for (int c = 0; c < 32; ++c) sv[q4 * 32 + c] = t[q4][c];
       }
       tc_fence_before();
       mbar_arrive(&s_free[sb]);
@@ -422,7 +423,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
       // are -inf and give 0)
       const float sc = p.scale_log2;
       float lsum0 = 0.f, lsum1 = 0.f;
-      uint32_t pk[BN / 2];
+      uint32_t pk[BN / 2];   // packed in place of sv as it is consumed
 #pragma unroll
       for (int c = 0; c < BN; c += 2) {
         const float p0 = ex2_approx(fmaf(sv[c], sc, -mu)), p1 = ex2_approx(fmaf(sv[c + 1], sc, -mu));
@@ -458,9 +459,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
       }
       uint8_t* prow = sP + pb * C::P_BYTES + row * 128;
 #pragma unroll
-      for (int ch = 0; ch < BN / 8; ++ch) {
+      for (int ch = 0; ch < BN / 8; ++ch) {   // 16-byte chunk ch of sub-tile ch / 8
         const uint4 v = make_uint4(pk[ch * 4 + 0], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
-        *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) = v;
+        *reinterpret_cast<uint4*>(prow + (ch / 8) * BM * 128 + (((ch % 8) ^ (row & 7)) << 4)) = v;
       }
       fence_proxy_async();
       tc_fence_before();
