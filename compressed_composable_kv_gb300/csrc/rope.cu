@@ -47,7 +47,7 @@ __global__ void rope_table_kernel(const __grid_constant__ TableParams p) {
 
 // ---------------------------------------------------------------------------
 // K1: in-place re-rotation of composed K rows for a group of layers.
-// One CTA owns kSlots consecutive composed slots: it stages their rows of
+// One CTA owns kSlots (16) consecutive composed slots: it stages their rows of
 // the cos/sin table in shared memory once and rotates those slots' rows in
 // every (layer, kv head) of the group with 16-byte loads/stores.  V rows are
 // never touched (they land by DMA).  A thread owns the 8 pairs of one 16-byte
@@ -55,7 +55,7 @@ __global__ void rope_table_kernel(const __grid_constant__ TableParams p) {
 // the 8 lanes of a row read 8 neighbouring entries instead of entries 128
 // bytes apart on the same banks.
 // ---------------------------------------------------------------------------
-constexpr int kSlots = 32;
+constexpr int kSlots = 16;
 constexpr int kRopeThreads = 256;
 
 template <int D>
