@@ -17,11 +17,11 @@ import torch
 from .build import LIB
 
 C2KV_OK, C2KV_EINVAL, C2KV_ENOMEM, C2KV_ENOTFOUND = 0, 1, 2, 3
-C2KV_ECAPACITY, C2KV_ECUDA, C2KV_ETIMEOUT, C2KV_EDEVICE = 4, 5, 6, 7
+C2KV_ECAPACITY, C2KV_ECUDA, C2KV_ETIMEOUT, C2KV_EDEVICE, C2KV_EIO = 4, 5, 6, 7, 8
 C2KV_MASK_CAUSAL, C2KV_MASK_STRUCTURED = 0, 1
 
 STATUS_NAMES = {0: "C2KV_OK", 1: "C2KV_EINVAL", 2: "C2KV_ENOMEM", 3: "C2KV_ENOTFOUND",
-                4: "C2KV_ECAPACITY", 5: "C2KV_ECUDA", 6: "C2KV_ETIMEOUT", 7: "C2KV_EDEVICE"}
+                4: "C2KV_ECAPACITY", 5: "C2KV_ECUDA", 6: "C2KV_ETIMEOUT", 7: "C2KV_EDEVICE", 8: "C2KV_EIO"}
 
 
 class C2KVError(RuntimeError):
@@ -43,6 +43,8 @@ _pvp = ctypes.POINTER(ctypes.c_void_p)
 _pg = ctypes.POINTER(c2kv_geometry)
 
 _SIGNATURES = {
+    "c2kv_store_save": (_i32, [_vp, ctypes.c_char_p]),
+    "c2kv_store_load": (_i32, [_vp, ctypes.c_char_p]),
     "c2kv_test_expire_next_waits": (_i32, [_i32]),
     "c2kv_last_error": (ctypes.c_char_p, []),
     "c2kv_version": (ctypes.c_char_p, []),
@@ -318,6 +320,16 @@ def masked_workspace_bytes(geom, n_tokens: int) -> int:
     """Scratch bytes c2kv_attend_masked needs for one n_tokens sequence."""
     a = c2kv_attend_workspace_size(geom, 1, n_tokens, n_tokens)
     return ((a + 255) // 256) * 256 + c2kv_masked_extra_bytes(geom, n_tokens)
+
+
+def c2kv_store_save(store: int, path: str) -> None:
+    """Writes every stored document of `store` to `path`."""
+    _check(load_library().c2kv_store_save(store, os.fsencode(path)))
+
+
+def c2kv_store_load(store: int, path: str) -> None:
+    """Adds the documents of a file written by c2kv_store_save to `store`."""
+    _check(load_library().c2kv_store_load(store, os.fsencode(path)))
 
 
 def c2kv_test_expire_next_waits(n_launches: int) -> None:

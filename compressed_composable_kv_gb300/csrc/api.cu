@@ -4,6 +4,7 @@
 // enqueued.  See include/c2kv.h for the contract of each call.
 #include <algorithm>
 #include <cmath>
+#include <cstdio>
 #include <cstring>
 #include <atomic>
 #include <mutex>
@@ -486,6 +487,98 @@ c2kv_status c2kv_store_segments(c2kv_store st, int32_t n_docs, const int32_t* do
     sg.n_slots = n_slots[i];
     sg.k = k;
     st->docs[doc_ids[i]] = sg;
+  }
+  return C2KV_OK;
+}
+
+namespace {
+// Store file: a header, then per document (ascending ids) its record, its K
+// rows and its V rows exactly as held in the pool ([layer][kv head][slot][d]
+// bf16), all in host byte order.
+constexpr char kStoreMagic[8] = {'C', '2', 'K', 'V', 'S', 'T', 'O', 'R'};
+constexpr uint32_t kStoreVersion = 1;
+struct StoreFileHeader {
+  char magic[8];
+  uint32_t version, reserved;
+  int32_t n_layers, n_q_heads, n_kv_heads, head_dim;
+  double rope_theta;
+  uint64_t n_docs;
+};
+struct StoreFileDoc {
+  int32_t doc_id, n_tokens, n_slots, k;
+};
+}  // namespace
+
+c2kv_status c2kv_store_save(c2kv_store st, const char* path) {
+  if (st == nullptr || path == nullptr) return fail(C2KV_EINVAL, "store or path is null");
+  std::lock_guard<std::mutex> lk(st->mu);
+  const c2kv_geometry& g = st->g;
+  const size_t row = (size_t)g.n_layers * g.n_kv_heads * g.head_dim * 2;
+  std::vector<int32_t> ids;
+  for (const auto& kv : st->docs) ids.push_back(kv.first);
+  std::sort(ids.begin(), ids.end());
+  FILE* f = std::fopen(path, "wb");
+  if (f == nullptr) return fail(C2KV_EIO, std::string("cannot open ") + path + " for writing");
+  StoreFileHeader hd;
+  std::memset(&hd, 0, sizeof(hd));
+  std::memcpy(hd.magic, kStoreMagic, sizeof(kStoreMagic));
+  hd.version = kStoreVersion;
+  hd.n_layers = g.n_layers;
+  hd.n_q_heads = g.n_q_heads;
+  hd.n_kv_heads = g.n_kv_heads;
+  hd.head_dim = g.head_dim;
+  hd.rope_theta = g.rope_theta;
+  hd.n_docs = ids.size();
+  bool ok = std::fwrite(&hd, sizeof(hd), 1, f) == 1;
+  for (size_t i = 0; ok && i < ids.size(); ++i) {
+    const Seg& sg = st->docs.at(ids[i]);
+    const StoreFileDoc rec{ids[i], sg.n_tokens, sg.n_slots, sg.k};
+    const size_t bytes = row * sg.n_slots;
+    ok = std::fwrite(&rec, sizeof(rec), 1, f) == 1 && std::fwrite(st->pool + sg.k_off, 1, bytes, f) == bytes &&
+         std::fwrite(st->pool + sg.v_off, 1, bytes, f) == bytes;
+  }
+  if (std::fclose(f) != 0) ok = false;
+  if (!ok) return fail(C2KV_EIO, std::string("writing ") + path + " failed");
+  return C2KV_OK;
+}
+
+c2kv_status c2kv_store_load(c2kv_store st, const char* path) {
+  if (st == nullptr || path == nullptr) return fail(C2KV_EINVAL, "store or path is null");
+  FILE* f = std::fopen(path, "rb");
+  if (f == nullptr) return fail(C2KV_EIO, std::string("cannot open ") + path);
+  struct Closer {
+    FILE* f;
+    ~Closer() { std::fclose(f); }
+  } closer{f};
+  StoreFileHeader hd;
+  if (std::fread(&hd, sizeof(hd), 1, f) != 1) return fail(C2KV_EIO, std::string(path) + ": truncated header");
+  if (std::memcmp(hd.magic, kStoreMagic, sizeof(kStoreMagic)) != 0 || hd.version != kStoreVersion)
+    return fail(C2KV_EINVAL, std::string(path) + " is not a c2kv store file of version 1");
+  const c2kv_geometry& g = st->g;
+  if (hd.n_layers != g.n_layers || hd.n_q_heads != g.n_q_heads || hd.n_kv_heads != g.n_kv_heads ||
+      hd.head_dim != g.head_dim || hd.rope_theta != g.rope_theta)
+    return fail(C2KV_EINVAL, std::string(path) + " was saved with another geometry");
+  const size_t row = (size_t)g.n_layers * g.n_kv_heads * g.head_dim * 2;
+  std::vector<uint8_t> kb, vb;
+  for (uint64_t i = 0; i < hd.n_docs; ++i) {
+    StoreFileDoc rec;
+    if (std::fread(&rec, sizeof(rec), 1, f) != 1) return fail(C2KV_EIO, std::string(path) + ": truncated");
+    if (rec.n_tokens < 1 || rec.n_slots < 1 || rec.n_slots > rec.n_tokens || rec.k < 1)
+      return fail(C2KV_EINVAL, std::string(path) + ": bad document record");
+    const size_t bytes = row * (size_t)rec.n_slots;
+    {
+      std::lock_guard<std::mutex> lk(st->mu);
+      if (st->used + 2 * align256(bytes) > st->pool_bytes)
+        return fail(C2KV_ENOMEM, "pinned pool full: document " + std::to_string(rec.doc_id) + " does not fit");
+    }
+    kb.resize(bytes);
+    vb.resize(bytes);
+    if (std::fread(kb.data(), 1, bytes, f) != bytes || std::fread(vb.data(), 1, bytes, f) != bytes)
+      return fail(C2KV_EIO, std::string(path) + ": truncated");
+    const void* kp = kb.data();
+    const void* vp = vb.data();
+    const c2kv_status s = c2kv_store_segments(st, 1, &rec.doc_id, &rec.n_tokens, &rec.n_slots, rec.k, &kp, &vp);
+    if (s != C2KV_OK) return s;
   }
   return C2KV_OK;
 }

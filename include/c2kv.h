@@ -67,7 +67,8 @@ typedef enum {
   C2KV_ECAPACITY = 4,  /* composed or appended rows exceed the cache capacity */
   C2KV_ECUDA = 5,      /* a CUDA runtime call failed (message in c2kv_last_error) */
   C2KV_ETIMEOUT = 6,   /* a kernel's bounded wait expired (from c2kv_device_error) */
-  C2KV_EDEVICE = 7     /* a kernel rejected a device-side value (from c2kv_device_error) */
+  C2KV_EDEVICE = 7,    /* a kernel rejected a device-side value (from c2kv_device_error) */
+  C2KV_EIO = 8         /* a store file could not be opened, read or written */
 } c2kv_status;
 
 typedef enum {
@@ -114,6 +115,25 @@ c2kv_status c2kv_store_segments(c2kv_store store, int32_t n_docs,
                                 const int32_t* doc_ids, const int32_t* n_tokens,
                                 const int32_t* n_slots, int32_t k,
                                 const void* const* k_pre, const void* const* v);
+
+/*
+ * Persists the store.  [EXPL] "pipeline: extract, store, concatenate": each
+ * document's compressed cache is extracted once, stored, and reused by any
+ * later request; these two calls keep the stored caches across processes.
+ *
+ * c2kv_store_save writes every stored document (ascending ids: id, original
+ * length, slots, k, then its K and V rows [n_layers][n_kv_heads][slot][d]
+ * bf16) after a header holding the geometry, in host byte order, to `path`
+ * (created or truncated).  Errors: C2KV_EINVAL (null argument), C2KV_EIO.
+ *
+ * c2kv_store_load adds the documents of such a file to `store`, which must
+ * have the geometry the file was saved with.  Documents read before an error
+ * stay in the store.  Errors: C2KV_EIO (cannot open, truncated), C2KV_EINVAL
+ * (not a store file, another geometry, a bad record, an id already stored),
+ * C2KV_ENOMEM (pool full).
+ */
+c2kv_status c2kv_store_save(c2kv_store store, const char* path);
+c2kv_status c2kv_store_load(c2kv_store store, const char* path);
 
 /* Looks up one stored document: its original length, slot count and k. */
 c2kv_status c2kv_store_lookup(c2kv_store store, int32_t doc_id,

@@ -418,6 +418,56 @@ def test_causal_mask_mode_llama_heads():
     check_attention(out, ref, "causal mask mode")
 
 
+def test_store_save_and_load_round_trip(tmp_path):
+    """A saved store, loaded into a new one, composes the same caches bit for
+    bit; documents stored at different k keep theirs.  Files of another
+    geometry, truncated files, missing files and ids already stored are
+    rejected."""
+    g = S.Geometry(2, 8, 2, 128, 5.0e5)
+    docs4 = {i: S.make_document(g, i, n, 4, 0xC2CA) for i, n in ((1, 401), (2, 64), (3, 1000))}
+    docs16 = {7: S.make_document(g, 7, 320, 16, 0xC2CA)}
+    pool = sum(2 * d.k_pre.nbytes + 1024 for d in list(docs4.values()) + list(docs16.values())) + (1 << 20)
+    a = P.c2kv_store_create(g, pool)
+    for k, docs in ((4, docs4), (16, docs16)):
+        ids = list(docs)
+        P.c2kv_store_segments(a, ids, [docs[i].n_tokens for i in ids], [docs[i].n_slots for i in ids], k,
+                              [docs[i].k_pre for i in ids], [docs[i].v for i in ids])
+    path = str(tmp_path / "store.c2kv")
+    P.c2kv_store_save(a, path)
+    b = P.c2kv_store_create(g, pool)
+    P.c2kv_store_load(b, path)
+    for i in (1, 2, 3, 7):
+        assert P.c2kv_store_lookup(a, i) == P.c2kv_store_lookup(b, i)
+    caches = []
+    for st in (a, b):
+        kc = torch.full((2, 2, 2048, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+        vc = torch.full_like(kc, 7.0)
+        tab = torch.empty(P.c2kv_rope_table_bytes(g, 2048) // 4, dtype=torch.float32, device="cuda")
+        P.c2kv_compose(st, [3, 1, 2, 1], [1, 0, 3, 2], 4, kc, vc, 2048, tab)
+        caches.append((kc, vc))
+    torch.cuda.synchronize()
+    assert torch.equal(caches[0][0], caches[1][0]) and torch.equal(caches[0][1], caches[1][1])
+    with pytest.raises(P.C2KVError) as e:
+        P.c2kv_store_load(b, path)                        # ids already stored
+    assert e.value.status == P.C2KV_EINVAL
+    other = P.c2kv_store_create(S.Geometry(2, 8, 2, 64, 5.0e5), 1 << 20)
+    with pytest.raises(P.C2KVError) as e:
+        P.c2kv_store_load(other, path)
+    assert e.value.status == P.C2KV_EINVAL
+    raw = open(path, "rb").read()
+    cut = str(tmp_path / "cut.c2kv")
+    open(cut, "wb").write(raw[:len(raw) // 2])
+    c = P.c2kv_store_create(g, pool)
+    with pytest.raises(P.C2KVError) as e:
+        P.c2kv_store_load(c, cut)
+    assert e.value.status == P.C2KV_EIO
+    with pytest.raises(P.C2KVError) as e:
+        P.c2kv_store_load(c, str(tmp_path / "missing.c2kv"))
+    assert e.value.status == P.C2KV_EIO
+    for st in (a, b, c, other):
+        P.c2kv_store_destroy(st)
+
+
 def test_host_side_errors():
     g = S.Geometry(1, 8, 2, 128, 5.0e5)
     sc = Scenario(g, 4, [(1, 40, 10), (2, 8, 2)], [([1, 2], None)], q_len=4, decode_steps=2)
