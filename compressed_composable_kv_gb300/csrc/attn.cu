@@ -69,13 +69,15 @@ template <int D, int G>
 struct DCfg {
   // The G query heads of a kv head are split over HS warp slices of GW heads
   // each, so a thread holds q and o of GW heads only and 16 warps fit an SM.
-  static constexpr int GW = (G % 2 == 0) ? 2 : 1;     // heads per warp
+  // An odd group (G = 5) would leave G one-head slices of 3 warps and
+  // 48-key tiles; its warps take all G heads instead, 8 warps per CTA.
+  static constexpr int GW = (G % 2 == 0) ? 2 : (G > 1 ? G : 1);   // heads per warp
   static constexpr int HS = G / GW;                   // head slices
   static constexpr int EPL = 16;                      // d elements a lane owns
   static constexpr int LPK = D / EPL;                 // lanes per key (a key group)
   static constexpr int NCH = EPL / 8;                 // 16-byte chunks a lane owns
   static constexpr int GPW = 32 / LPK;                // key groups per warp
-  static constexpr int NWK0 = 16 / HS;
+  static constexpr int NWK0 = (GW > 2 ? 8 : 16) / HS;
   // warps per slice, halved while the 3-stage K/V ring would exceed 192 KB
   static constexpr int NWK1 = (NWK0 * GPW * KPG * D * 2 * 2 * kStages > 196608) ? NWK0 / 2 : NWK0;
   static constexpr int NWK = (NWK1 * GPW * KPG * D * 2 * 2 * kStages > 196608) ? NWK1 / 2 : NWK1;
