@@ -3,9 +3,11 @@
 One step = one full request of the workload: compose the documents'
 compressed pre-RoPE segments from the pinned host store into HBM (host->
 device copies + re-rotation), prefill the question on every layer, then
-decode every answer token on every layer.  Headline value: answer tokens
-per second over the whole request.  Prefill and decode are replayed from
-CUDA graphs captured once (the graphs hold only this library's kernels).
+decode every answer token on every layer.  Consecutive requests overlap as
+in a serving loop: request r+1 is composed on a second stream, into its own
+cache, while request r decodes.  Headline value: answer tokens per second
+over the timed requests.  Prefill and decode are replayed from CUDA graphs
+captured once (the graphs hold only this library's kernels).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W]
                        [--impl ours|reference] [--workload NAME]
@@ -244,7 +246,13 @@ def run_ours(args, rank: int, world: int) -> dict:
                           w.k, [docs[i].k_pre for i in used], [docs[i].v for i in used])
     compose_bytes = sum(2 * docs[d].k_pre.nbytes for r in reqs for d in r.doc_ids)
     del docs
-    bt = P.RequestBatch(store, g, [P.RequestSpec(r.doc_ids, r.order) for r in reqs], w.k, Q, T)
+    # Two request states (caches, tables, scratch, graphs): request r uses
+    # state r % 2, and request r+1 is composed on a second stream while
+    # request r decodes, as a serving loop would.  Every request does all of
+    # its work inside the timed region.
+    specs = [P.RequestSpec(r.doc_ids, r.order) for r in reqs]
+    bts = [P.RequestBatch(store, g, specs, w.k, Q, T) for _ in range(2)]
+    bt = bts[0]
     inp = S.make_step_inputs(w)
     names = ["q_pre", "kq_pre", "vq", "qd_pre", "kd_pre", "vd"]
     host = {}
@@ -262,7 +270,8 @@ def run_ours(args, rank: int, world: int) -> dict:
     res_host = torch.empty((T, Bn, g.n_q_heads, g.head_dim), dtype=torch.bfloat16).pin_memory()
     d2h_bytes = res_host.numel() * 2
 
-    stream = torch.cuda.Stream()
+    stream = torch.cuda.Stream()    # prefill and decode
+    cstream = torch.cuda.Stream()   # compose of the next request
     torch.cuda.synchronize()
 
     # Compose and prefill are layer-pipelined: layer group i is composed
@@ -272,68 +281,98 @@ def run_ours(args, rank: int, world: int) -> dict:
     n_groups = min(L, 8)
     groups = [(i * L // n_groups, (i + 1) * L // n_groups) for i in range(n_groups)]
 
-    def prefill_layers(l0, l1):
+    def prefill_layers(b, l0, l1):
         for l in range(l0, l1):
-            bt.prefill(l, dev_in["q_pre"][l], dev_in["kq_pre"][l], dev_in["vq"][l], pre_out[l], stream)
+            b.prefill(l, dev_in["q_pre"][l], dev_in["kq_pre"][l], dev_in["vq"][l], pre_out[l], stream)
 
-    def prefill_all():
-        prefill_layers(0, L)
-
-    def decode_all(steps=T):
+    def decode_all(b, steps=T):
         for t in range(steps):
             for l in range(L):
-                bt.decode(l, dev_in["qd_pre"][t, l], dev_in["kd_pre"][t, l], dev_in["vd"][t, l],
-                          dec_out[t, l], stream)
-            bt.advance(stream)
+                b.decode(l, dev_in["qd_pre"][t, l], dev_in["kd_pre"][t, l], dev_in["vd"][t, l],
+                         dec_out[t, l], stream)
+            b.advance(stream)
 
-    # Warm the launch paths eagerly once (one decode step is enough to set the
-    # kernels' attributes), then capture.
-    with torch.cuda.stream(stream):
-        bt.compose(stream)
-        if Q:
-            prefill_all()
-        bt.reset_decode(stream)
-        decode_all(1)
-    torch.cuda.synchronize()
-    g_pre = [torch.cuda.CUDAGraph() for _ in groups] if Q else None
-    g_dec = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        if Q:
-            for gr, (l0, l1) in zip(g_pre, groups):
-                with torch.cuda.graph(gr, stream=stream):
-                    prefill_layers(l0, l1)
-        with torch.cuda.graph(g_dec, stream=stream):
-            decode_all()
-    torch.cuda.synchronize()
+    # Warm the launch paths eagerly once per state (one decode step is enough
+    # to set the kernels' attributes), then capture.
+    g_pre = [[torch.cuda.CUDAGraph() for _ in groups] if Q else None for _ in bts]
+    g_dec = [torch.cuda.CUDAGraph() for _ in bts]
+    for i, b in enumerate(bts):
+        with torch.cuda.stream(stream):
+            b.compose(stream)
+            if Q:
+                prefill_layers(b, 0, L)
+            b.reset_decode(stream)
+            decode_all(b, 1)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            if Q:
+                for gr, (l0, l1) in zip(g_pre[i], groups):
+                    with torch.cuda.graph(gr, stream=stream):
+                        prefill_layers(b, l0, l1)
+            with torch.cuda.graph(g_dec[i], stream=stream):
+                decode_all(b)
+        torch.cuda.synchronize()
     assert P.c2kv_device_error() == P.C2KV_OK
     # per request: one table + one re-rotation per layer sub-group of each
     # compose call; 2 launches per prefill layer; L decode + 1 advance per step
     rerope_launches = sum(max(1, min(4, (l1 - l0) // 4)) for l0, l1 in groups)
     launches_per_step = (bt.batch * (1 + rerope_launches) + (2 * L if Q else 0) + T * (L + 1))
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    def isolated_request(e):
+        """One request alone on the stream: compose layer-pipelined with the
+        prefill, then decode (the time-to-first-token measurement)."""
+        with torch.cuda.stream(stream):
+            e[0].record(stream)
+            for gi, (l0, l1) in enumerate(groups):
+                bt.compose_layers(l0, l1, stream)
+                if gi == len(groups) - 1:
+                    e[1].record(stream)   # the whole cache is composed
+                if Q:
+                    g_pre[0][gi].replay()
+            bt.reset_decode(stream)
+            e[2].record(stream)
+            g_dec[0].replay()
+            e[3].record(stream)
 
-    def step(e=None, with_host=False):
+    ev_grp = [[torch.cuda.Event() for _ in groups] for _ in bts]
+    ev_free = [torch.cuda.Event() for _ in bts]
+    ev_go = torch.cuda.Event()
+
+    def enqueue_compose(i):
+        with torch.cuda.stream(cstream):
+            cstream.wait_event(ev_free[i])   # the state's previous request has decoded
+            for gi, (l0, l1) in enumerate(groups):
+                bts[i].compose_layers(l0, l1, cstream)
+                ev_grp[i][gi].record(cstream)
+
+    def run_request(i, e=None, with_host=False):
         with torch.cuda.stream(stream):
             if with_host:
                 for n in dev_in:
                     dev_in[n].copy_(host[n], non_blocking=True)
+            for gi in range(len(groups)):
+                stream.wait_event(ev_grp[i][gi])
+                if Q:
+                    g_pre[i][gi].replay()
+            bts[i].reset_decode(stream)
             if e:
                 e[0].record(stream)
-            for gi, (l0, l1) in enumerate(groups):
-                bt.compose_layers(l0, l1, stream)
-                if gi == len(groups) - 1 and e:
-                    e[1].record(stream)   # the whole cache is composed
-                if Q:
-                    g_pre[gi].replay()
-            bt.reset_decode(stream)
+            g_dec[i].replay()
             if e:
-                e[2].record(stream)
-            g_dec.replay()
-            if e:
-                e[3].record(stream)
+                e[1].record(stream)
+            ev_free[i].record(stream)
             if with_host:
                 res_host.copy_(dec_out[:, L - 1], non_blocking=True)
+
+    def pipeline(n, evs=None, with_host=False):
+        """n requests; request r+1's compose overlaps request r's decode."""
+        ev_go.record(stream)
+        cstream.wait_event(ev_go)
+        enqueue_compose(0)
+        for r in range(n):
+            run_request(r % 2, evs[r] if evs else None, with_host)
+            if r + 1 < n:
+                enqueue_compose((r + 1) % 2)
 
     # pinned host->device copy bandwidth (denominator of the compose copies)
     big = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
@@ -355,17 +394,25 @@ def run_ours(args, rank: int, world: int) -> dict:
             import torch.distributed as dist
             dist.barrier()
 
-    for _ in range(args.warmup):
-        step()
+    # time to first token and the phases of one request alone (untimed region)
+    iso = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(3)]
+    for e in [iso[0]] + iso:
+        isolated_request(e)
+        torch.cuda.synchronize()
+    comp = statistics.mean(e[0].elapsed_time(e[1]) for e in iso) / 1e3
+    pre = statistics.mean(e[1].elapsed_time(e[2]) for e in iso) / 1e3
+    dec_iso = statistics.mean(e[2].elapsed_time(e[3]) for e in iso) / 1e3
+
+    pipeline(args.warmup)
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     t_beg, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     gpu_idx = torch.cuda.current_device()
     with ClockSampler(gpu_idx) as clk:
         t_beg.record(stream)
-        for i in range(args.steps):
-            step(ev[i])
+        pipeline(args.steps, ev)
         t_end.record(stream)
         torch.cuda.synchronize()
     barrier()
@@ -373,19 +420,16 @@ def run_ours(args, rank: int, world: int) -> dict:
     elapsed = t_beg.elapsed_time(t_end) / 1e3
     err = P.c2kv_device_error()
     assert err == P.C2KV_OK, f"device error {err}"
-    comp = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / 1e3
-    pre = statistics.mean(e[1].elapsed_time(e[2]) for e in ev) / 1e3
-    dec = statistics.mean(e[2].elapsed_time(e[3]) for e in ev) / 1e3
+    dec = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / 1e3   # decode phase in the timed region
 
-    # e2e: the same step with inputs copied from pinned host memory and the
-    # answer read back, all inside the timed region
-    step(with_host=True)
+    # e2e: the same requests with inputs copied from pinned host memory and
+    # the answer read back, all inside the timed region
+    pipeline(1, with_host=True)
     torch.cuda.synchronize()
     barrier()
     e_beg, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_beg.record(stream)
-    for i in range(args.steps):
-        step(with_host=True)
+    pipeline(args.steps, with_host=True)
     e_end.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -410,7 +454,7 @@ def run_ours(args, rank: int, world: int) -> dict:
     per_key = profiled_traffic("decode_kernel")
     traffic = None if per_key is None else per_key * (keys / T)
     clocks = clk.summary()
-    ttft = comp + pre + dec / T
+    ttft = comp + pre + dec_iso / T
     out = {
         "metric": METRIC,
         "value": toks / elapsed,
@@ -429,6 +473,9 @@ def run_ours(args, rank: int, world: int) -> dict:
         "prefill_ms": pre * 1e3,
         "decode_ms": dec * 1e3,
         "ttft_ms": ttft * 1e3,
+        "phases": ("compose_ms, prefill_ms and ttft_ms: a request alone on the GPU (compose layer-"
+                   "pipelined with its prefill), mean of 3; decode_ms: mean decode phase of the timed "
+                   "requests"),
         "decode_only_tok_s": Bn * T / dec,
         "attention_hbm_gbs": achieved,
         "h2d": {"compose_bytes": compose_bytes, "achieved_gbs": compose_bytes / comp / 1e9,
@@ -468,6 +515,8 @@ def workload_config(w, world: int) -> dict:
         "ttft_pipeline": (f"compose and prefill layer-pipelined in {n_groups} groups: compose_ms = "
                           "until the whole cache is composed (prefill of earlier groups overlaps it), "
                           "prefill_ms = the rest of the prefill"),
+        "request_pipeline": ("consecutive requests: request r+1 is composed (host->device copies and "
+                             "re-rotation, second stream, its own cache) while request r decodes"),
         "parallelism": f"replicas x{world}",
         "attention_only": "no projection/MLP weights: attention over the composed cache only",
     }
