@@ -256,14 +256,15 @@ def run_ours(args, rank: int, world: int) -> dict:
     inp = S.make_step_inputs(w)
     names = ["q_pre", "kq_pre", "vq", "qd_pre", "kd_pre", "vd"]
     host = {}
-    dev_in = {}
+    dev_ins = [{}, {}]   # per request state, so a request's inputs can land while the other decodes
     for n in names:
         a = getattr(inp, n)
         if a.size == 0:
             continue
         t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
         host[n] = t.pin_memory()
-        dev_in[n] = host[n].to(dev)
+        for d_in in dev_ins:
+            d_in[n] = host[n].to(dev)
     h2d_bytes = sum(t.numel() * 2 for t in host.values())
     pre_out = torch.empty((L, Bn, Q, g.n_q_heads, g.head_dim), dtype=torch.bfloat16, device=dev) if Q else None
     dec_out = torch.empty((T, L, Bn, g.n_q_heads, g.head_dim), dtype=torch.bfloat16, device=dev)
@@ -281,15 +282,16 @@ def run_ours(args, rank: int, world: int) -> dict:
     n_groups = min(L, 8)
     groups = [(i * L // n_groups, (i + 1) * L // n_groups) for i in range(n_groups)]
 
-    def prefill_layers(b, l0, l1):
+    def prefill_layers(i, l0, l1):
+        b, d_in = bts[i], dev_ins[i]
         for l in range(l0, l1):
-            b.prefill(l, dev_in["q_pre"][l], dev_in["kq_pre"][l], dev_in["vq"][l], pre_out[l], stream)
+            b.prefill(l, d_in["q_pre"][l], d_in["kq_pre"][l], d_in["vq"][l], pre_out[l], stream)
 
-    def decode_all(b, steps=T):
+    def decode_all(i, steps=T):
+        b, d_in = bts[i], dev_ins[i]
         for t in range(steps):
             for l in range(L):
-                b.decode(l, dev_in["qd_pre"][t, l], dev_in["kd_pre"][t, l], dev_in["vd"][t, l],
-                         dec_out[t, l], stream)
+                b.decode(l, d_in["qd_pre"][t, l], d_in["kd_pre"][t, l], d_in["vd"][t, l], dec_out[t, l], stream)
             b.advance(stream)
 
     # Warm the launch paths eagerly once per state (one decode step is enough
@@ -300,17 +302,17 @@ def run_ours(args, rank: int, world: int) -> dict:
         with torch.cuda.stream(stream):
             b.compose(stream)
             if Q:
-                prefill_layers(b, 0, L)
+                prefill_layers(i, 0, L)
             b.reset_decode(stream)
-            decode_all(b, 1)
+            decode_all(i, 1)
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             if Q:
                 for gr, (l0, l1) in zip(g_pre[i], groups):
                     with torch.cuda.graph(gr, stream=stream):
-                        prefill_layers(b, l0, l1)
+                        prefill_layers(i, l0, l1)
             with torch.cuda.graph(g_dec[i], stream=stream):
-                decode_all(b)
+                decode_all(i)
         torch.cuda.synchronize()
     assert P.c2kv_device_error() == P.C2KV_OK
     # per request: one table + one re-rotation per layer sub-group of each
@@ -338,18 +340,18 @@ def run_ours(args, rank: int, world: int) -> dict:
     ev_free = [torch.cuda.Event() for _ in bts]
     ev_go = torch.cuda.Event()
 
-    def enqueue_compose(i):
+    def enqueue_compose(i, with_host=False):
         with torch.cuda.stream(cstream):
             cstream.wait_event(ev_free[i])   # the state's previous request has decoded
+            if with_host:                    # this request's inputs, from pinned host memory
+                for n, d in dev_ins[i].items():
+                    d.copy_(host[n], non_blocking=True)
             for gi, (l0, l1) in enumerate(groups):
                 bts[i].compose_layers(l0, l1, cstream)
                 ev_grp[i][gi].record(cstream)
 
     def run_request(i, e=None, with_host=False):
         with torch.cuda.stream(stream):
-            if with_host:
-                for n in dev_in:
-                    dev_in[n].copy_(host[n], non_blocking=True)
             for gi in range(len(groups)):
                 stream.wait_event(ev_grp[i][gi])
                 if Q:
@@ -368,11 +370,11 @@ def run_ours(args, rank: int, world: int) -> dict:
         """n requests; request r+1's compose overlaps request r's decode."""
         ev_go.record(stream)
         cstream.wait_event(ev_go)
-        enqueue_compose(0)
+        enqueue_compose(0, with_host)
         for r in range(n):
             run_request(r % 2, evs[r] if evs else None, with_host)
             if r + 1 < n:
-                enqueue_compose((r + 1) % 2)
+                enqueue_compose((r + 1) % 2, with_host)
 
     # pinned host->device copy bandwidth (denominator of the compose copies)
     big = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
