@@ -111,3 +111,16 @@ def test_geometry_validation(P):
         with pytest.raises(P.C2KVError) as e:
             P.c2kv_store_create(g, 0)
         assert e.value.status == P.C2KV_EINVAL
+
+
+def test_store_file_and_test_hook_arguments_are_checked_on_the_host(P, tmp_path):
+    """Null stores and negative counts are rejected before any CUDA call."""
+    lib = P.load_library()
+    assert lib.c2kv_store_save(None, os.fsencode(str(tmp_path / "x"))) == P.C2KV_EINVAL
+    assert lib.c2kv_store_load(None, os.fsencode(str(tmp_path / "x"))) == P.C2KV_EINVAL
+    with pytest.raises(P.C2KVError) as e:
+        P.c2kv_test_expire_next_waits(-1)
+    assert e.value.status == P.C2KV_EINVAL
+    P.c2kv_test_expire_next_waits(0)
+    assert P.STATUS_NAMES[P.C2KV_EIO] == "C2KV_EIO"
+
