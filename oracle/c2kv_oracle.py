@@ -33,6 +33,11 @@ Readings where the pages are silent (each listed in the design notes):
   S15 the "no position re-alignment" ablation (section "results") keeps
       every document at its extraction positions (no offset off_c); the
       question still starts at L_tot.
+  S16 the "anchor tokens" ablation (section "results") swaps only the mask
+      of the extraction pass: the extra tokens sit where the slots sit and
+      see every document token, and every document token sees every extra
+      token as well as its causal prefix of the document; the extra tokens
+      see each other causally, as the slots do.
 
 Parity pins: every function below is checked by tests/test_oracle_pins.py
 against the pages' worked values, closed forms, invariants or brute force.
@@ -290,6 +295,25 @@ def structured_mask(n_doc: int, n_slot: int, k: int) -> np.ndarray:
     return m
 
 
+def anchor_mask(n_doc: int, n_slot: int) -> np.ndarray:
+    """Mask of the "anchor tokens" ablation (reading S16) over n_doc document
+    tokens followed by n_slot anchor tokens (True = visible).
+
+    Documents and anchors see each other in both directions: document token r
+    sees document tokens 0..r and every anchor; anchor i sees every document
+    token and anchors 0..i."""
+    N = n_doc + n_slot
+    m = np.zeros((N, N), dtype=bool)
+    for r in range(n_doc):
+        m[r, :r + 1] = True
+        m[r, n_doc:] = True
+    for i in range(n_slot):
+        row = n_doc + i
+        m[row, :n_doc] = True
+        m[row, n_doc:n_doc + i + 1] = True
+    return m
+
+
 def extraction_positions(n_doc: int, n_slot: int, k: int) -> np.ndarray:
     """Documents at 0..n_doc-1, slot i at the last token of its block."""
     doc = list(range(n_doc))
@@ -297,8 +321,11 @@ def extraction_positions(n_doc: int, n_slot: int, k: int) -> np.ndarray:
     return np.asarray(doc + slots, dtype=np.int64)
 
 
-def masked_extraction_attention(q_pre, k_pre, v, n_doc, n_slot, k, theta, rows=None):
-    """Attention over one document and its slots under the structured mask.
+def masked_extraction_attention(q_pre, k_pre, v, n_doc, n_slot, k, theta, rows=None,
+                                mask="structured"):
+    """Attention over one document and its slots under the structured mask
+    (mask="structured") or the anchor-token mask of the ablation
+    (mask="anchor", reading S16; the extra tokens take the slots' positions).
 
     q_pre bits [N][Hq][d], k_pre/v bits [N][Hkv][d] for the N = n_doc+n_slot
     tokens (pre-RoPE).  q and k are rotated at extraction_positions() in fp64
@@ -313,10 +340,15 @@ def masked_extraction_attention(q_pre, k_pre, v, n_doc, n_slot, k, theta, rows=N
     q = rope_rotate(bf16_to_f64(q_pre[rows]).transpose(1, 0, 2), pos[rows], theta)
     kk = rope_rotate(bf16_to_f64(k_pre).transpose(1, 0, 2), pos, theta)
     vv = bf16_to_f64(v).transpose(1, 0, 2)
-    mask = structured_mask(n_doc, n_slot, k)[rows]
+    if mask == "structured":
+        vis = structured_mask(n_doc, n_slot, k)[rows]
+    elif mask == "anchor":
+        vis = anchor_mask(n_doc, n_slot)[rows]
+    else:
+        raise ValueError("unknown mask %r" % (mask,))
     out = np.empty((len(rows), hq, d), dtype=np.float64)
     for h in range(hq):
-        out[:, h, :] = masked_softmax_attention(q[h], kk[h // g], vv[h // g], mask)
+        out[:, h, :] = masked_softmax_attention(q[h], kk[h // g], vv[h // g], vis)
     return out
 
 

@@ -288,9 +288,73 @@ def check_llama3_bytes(o):
                                g["head_dim"][0]) == g["bytes_per_token"][0]
 
 
+# ----------------------------------------------------- anchor-token ablation
+
+def check_anchor_mask_uniform_scores(o):
+    """Anchor-token ablation (section "results"): the extra tokens and the
+    document tokens see each other in both directions, so the document
+    tokens' outputs are rewritten by the anchors.  With q = 0 every score is
+    0 and each output row is the plain mean of the values it can see; with
+    value j the unit vector e_j the row shows exactly which keys it saw.
+    Expected: document token r sees documents 0..r (the base causal mask is
+    kept among the documents) and every anchor; anchor i sees every document
+    token and anchors 0..i."""
+    rng = np.random.default_rng(17)
+    n_doc, k, d, theta = 7, 3, 16, 1.0e4
+    n_slot = -(-n_doc // k)
+    N = n_doc + n_slot
+    q = np.zeros((N, 2, d), np.uint16)
+    kk = _bits(rng, (N, 1, d))
+    one = o.f64_to_bf16(np.array([1.0]))[0]
+    v = np.zeros((N, 1, d), np.uint16)
+    for j in range(N):
+        v[j, 0, j] = one
+    out = o.masked_extraction_attention(q, kk, v, n_doc, n_slot, k, theta, mask="anchor")
+    for r in range(N):
+        if r < n_doc:
+            seen = set(range(r + 1)) | set(range(n_doc, N))
+        else:
+            seen = set(range(n_doc)) | set(range(n_doc, r + 1))
+        want = np.zeros(d)
+        want[sorted(seen)] = 1.0 / len(seen)
+        for h in range(2):
+            assert np.allclose(out[r, h], want, atol=1e-12), (r, h)
+    # the structured mask on the same input: documents see no anchor
+    st = o.masked_extraction_attention(q, kk, v, n_doc, n_slot, k, theta, mask="structured")
+    assert np.allclose(st[0, 0, :N], np.eye(N)[0], atol=1e-12)
+
+
+def check_anchor_rows_are_causal_attention(o):
+    """Anchor rows see every earlier token of the sequence, so they are plain
+    causal attention (torch's fp64 scaled_dot_product_attention) over the
+    sequence rotated at its extraction positions; with no anchors the whole
+    result is causal attention at positions 0..n-1."""
+    rng = np.random.default_rng(19)
+    hq, hkv, d, theta = 4, 2, 16, 5.0e5
+    for n_doc, k in ((9, 4), (5, 1), (6, 0)):
+        n_slot = -(-n_doc // k) if k else 0
+        kk_ = max(k, 1)
+        N = n_doc + n_slot
+        q, kk, v = _bits(rng, (N, hq, d)), _bits(rng, (N, hkv, d)), _bits(rng, (N, hkv, d))
+        out = o.masked_extraction_attention(q, kk, v, n_doc, n_slot, kk_, theta, mask="anchor")
+        pos = o.extraction_positions(n_doc, n_slot, kk_)
+        qr = o.rope_rotate(o.bf16_to_f64(q).transpose(1, 0, 2), pos, theta)
+        kr = o.rope_rotate(o.bf16_to_f64(kk).transpose(1, 0, 2), pos, theta)
+        vr = o.bf16_to_f64(v).transpose(1, 0, 2)
+        g = hq // hkv
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(qr), torch.from_numpy(np.repeat(kr, g, axis=0)),
+            torch.from_numpy(np.repeat(vr, g, axis=0)), is_causal=True).numpy().transpose(1, 0, 2)
+        rows = slice(n_doc, N) if n_slot else slice(0, N)
+        assert np.allclose(out[rows], ref[rows], atol=1e-12), (n_doc, k)
+        if n_slot:   # documents that see anchors are not causal rows
+            assert not np.allclose(out[:n_doc - 1], ref[:n_doc - 1], atol=1e-6)
+
+
 ALL_CHECKS = [
     check_blog_positions, check_slot_counts, check_positions_bruteforce, check_no_realign_positions,
     check_blog_mask, check_extraction_positions, check_bf16_conversion,
     check_rope, check_attention_special_cases, check_gqa_and_causality,
     check_k1_equals_uncompressed, check_llama3_bytes,
+    check_anchor_mask_uniform_scores, check_anchor_rows_are_causal_attention,
 ]

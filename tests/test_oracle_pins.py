@@ -90,6 +90,31 @@ def _mask_block_shifted(n_doc, n_slot, k):
     return m
 
 
+def _anchor_docs_causal_over_anchors(n_doc, n_slot):
+    m = np.tril(np.ones((n_doc + n_slot,) * 2, bool))
+    return m
+
+
+def _anchor_docs_see_anchors_only(n_doc, n_slot):
+    m = np.zeros((n_doc + n_slot,) * 2, bool)
+    m[:n_doc, n_doc:] = True
+    for r in range(n_doc):
+        m[r, r] = True
+    for i in range(n_slot):
+        m[n_doc + i, :n_doc + i + 1] = True
+    return m
+
+
+def _anchor_anchors_see_all_anchors(n_doc, n_slot):
+    N = n_doc + n_slot
+    m = np.zeros((N, N), bool)
+    for r in range(n_doc):
+        m[r, :r + 1] = True
+        m[r, n_doc:] = True
+    m[n_doc:, :] = True
+    return m
+
+
 def _softmax_no_scale(q, K, V, mask):
     s = np.where(mask, q @ K.T, -np.inf)
     p = np.exp(s - s.max(1, keepdims=True))
@@ -118,6 +143,11 @@ MUTATIONS = [
     ("structured_mask", _mask_no_sink, pins.check_blog_mask),
     ("structured_mask", _mask_block_shifted, pins.check_blog_mask),
     ("masked_softmax_attention", _softmax_no_scale, pins.check_attention_special_cases),
+    ("anchor_mask", _anchor_docs_causal_over_anchors, pins.check_anchor_mask_uniform_scores),
+    ("anchor_mask", _anchor_docs_causal_over_anchors, pins.check_anchor_rows_are_causal_attention),
+    ("anchor_mask", _anchor_docs_see_anchors_only, pins.check_anchor_mask_uniform_scores),
+    ("anchor_mask", _anchor_anchors_see_all_anchors, pins.check_anchor_mask_uniform_scores),
+    ("anchor_mask", _anchor_anchors_see_all_anchors, pins.check_anchor_rows_are_causal_attention),
     ("f64_to_bf16", _bf16_truncate, pins.check_bf16_conversion),
     ("f64_to_bf16", _bf16_double_round, pins.check_bf16_conversion),
 ]
