@@ -604,9 +604,10 @@ def run_extract(args) -> None:
     """Extraction-side attention at full size (section "structured information
     flow"): one document of 4000 tokens followed by its 1000 slots (k=4),
     Llama3.1-8B attention geometry, one c2kv_attend_masked call per layer for
-    32 layers, under the structured mask and, for comparison, the plain causal
-    mask over the same 5000 tokens (which skips nothing).  achieved TFLOP/s
-    counts 4*d flops per visible (query head, key) pair."""
+    32 layers, under the structured mask, the anchor-token mask of the
+    ablation (section "results") and, for comparison, the plain causal mask
+    over the same 5000 tokens (which skips nothing).  achieved TFLOP/s counts
+    4*d flops per visible (query head, key) pair."""
     import torch
     import compressed_composable_kv_gb300 as P
     from compressed_composable_kv_gb300 import synth as S
@@ -629,7 +630,11 @@ def run_extract(args) -> None:
     doc_pairs = n_doc * (n_doc + 1) // 2
     slot_pairs = sum(len(set(range(min(k, n_doc))) | set(range(i * k, min((i + 1) * k, n_doc)))) + i + 1
                      for i in range(n_slot))
+    # anchor mask: the causal pairs plus every (document, anchor) pair
+    anchor_pairs = N * (N + 1) // 2 + n_doc * n_slot
+    names = {P.C2KV_MASK_STRUCTURED: "structured", P.C2KV_MASK_ANCHOR: "anchor", P.C2KV_MASK_CAUSAL: "causal"}
     for mask, n_d, n_s, pairs in ((P.C2KV_MASK_STRUCTURED, n_doc, n_slot, doc_pairs + slot_pairs),
+                                  (P.C2KV_MASK_ANCHOR, n_doc, n_slot, anchor_pairs),
                                   (P.C2KV_MASK_CAUSAL, N, 0, N * (N + 1) // 2)):
         def run_layers():
             for l in range(L):
@@ -651,7 +656,7 @@ def run_extract(args) -> None:
         assert P.c2kv_device_error() == P.C2KV_OK
         t = statistics.median(times)
         flops = L * g.n_q_heads * pairs * 4 * g.head_dim
-        print(json.dumps({"extract": "structured" if mask == P.C2KV_MASK_STRUCTURED else "causal",
+        print(json.dumps({"extract": names[mask],
                           "doc_tokens": n_doc, "slots": n_s, "k": k, "layers": L,
                           "ms_per_document": t * 1e3, "tokens_per_s": N / t,
                           "visible_pairs_per_head": pairs, "achieved_tflops": flops / t / 1e12,
@@ -671,7 +676,8 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="decode time vs context (16k..128k), compressed k=16/8/4 vs uncompressed")
     ap.add_argument("--extract", action="store_true",
-                    help="extraction-side structured-mask attention, 4000-token document + 1000 slots")
+                    help="extraction-side attention (structured, anchor and causal masks), "
+                         "4000-token document + 1000 slots")
     args = ap.parse_args()
     if args.sweep:
         run_sweep(args)

@@ -18,7 +18,7 @@ from .build import LIB
 
 C2KV_OK, C2KV_EINVAL, C2KV_ENOMEM, C2KV_ENOTFOUND = 0, 1, 2, 3
 C2KV_ECAPACITY, C2KV_ECUDA, C2KV_ETIMEOUT, C2KV_EDEVICE, C2KV_EIO = 4, 5, 6, 7, 8
-C2KV_MASK_CAUSAL, C2KV_MASK_STRUCTURED = 0, 1
+C2KV_MASK_CAUSAL, C2KV_MASK_STRUCTURED, C2KV_MASK_ANCHOR = 0, 1, 2
 
 STATUS_NAMES = {0: "C2KV_OK", 1: "C2KV_EINVAL", 2: "C2KV_ENOMEM", 3: "C2KV_ENOTFOUND",
                 4: "C2KV_ECAPACITY", 5: "C2KV_ECUDA", 6: "C2KV_ETIMEOUT", 7: "C2KV_EDEVICE", 8: "C2KV_EIO"}

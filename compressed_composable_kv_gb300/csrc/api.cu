@@ -910,10 +910,11 @@ c2kv_status c2kv_attend_masked(const c2kv_geometry* geom, int32_t mask, int32_t 
                                size_t workspace_bytes, void* stream) {
   c2kv_status s = check_geom(geom);
   if (s != C2KV_OK) return s;
-  if (mask != C2KV_MASK_CAUSAL && mask != C2KV_MASK_STRUCTURED) return fail(C2KV_EINVAL, "unknown mask");
+  if (mask != C2KV_MASK_CAUSAL && mask != C2KV_MASK_STRUCTURED && mask != C2KV_MASK_ANCHOR)
+    return fail(C2KV_EINVAL, "unknown mask");
   if (n_doc < 1 || n_slot < 0) return fail(C2KV_EINVAL, "need n_doc >= 1 and n_slot >= 0");
   if (mask == C2KV_MASK_CAUSAL && n_slot != 0) return fail(C2KV_EINVAL, "causal mask takes n_slot = 0");
-  if (mask == C2KV_MASK_STRUCTURED && k < 1) return fail(C2KV_EINVAL, "k must be >= 1");
+  if (mask != C2KV_MASK_CAUSAL && k < 1) return fail(C2KV_EINVAL, "k must be >= 1");
   if ((int64_t)n_doc + n_slot > (1 << 24)) return fail(C2KV_EINVAL, "sequence too long");
   if (!q || !kk || !v || !out || !workspace) return fail(C2KV_EINVAL, "null pointer");
   if (!aligned16(q) || !aligned16(kk) || !aligned16(v) || !aligned16(workspace))
@@ -932,28 +933,31 @@ c2kv_status c2kv_attend_masked(const c2kv_geometry* geom, int32_t mask, int32_t 
   s = device_state(nullptr, nullptr);
   if (s != C2KV_OK) return s;
   // Rows are the sequence's tokens: extraction positions (documents at
-  // 0..n_doc-1, slot s at min((s+1)k, n_doc) - 1), or t for the causal mask.
-  const int kblk = mask == C2KV_MASK_STRUCTURED ? k : 1;
+  // 0..n_doc-1, slot or anchor s at min((s+1)k, n_doc) - 1), or t for the
+  // causal mask.
+  const bool causal = mask == C2KV_MASK_CAUSAL;
+  const int kblk = causal ? 1 : k;
   TableParams tp;
   std::memset(&tp, 0, sizeof(tp));
   tp.tab = tab;
   tp.rows = N;
   tp.half = geom->head_dim / 2;
   tp.mode = kTableExtraction;
-  tp.n_doc = mask == C2KV_MASK_STRUCTURED ? n_doc : N;
+  tp.n_doc = causal ? N : n_doc;
   tp.kblk = kblk;
   fill_inv_freq(geom, tp.inv_freq);
   C2KV_CUDA(launch_rope_table(tp, st));
   const int32_t zero = 0;
   const CosSin2* tabs[1] = {tab};
-  const int mmode = mask == C2KV_MASK_STRUCTURED ? kMaskStructured : kMaskCausal;
-  if (N == 1) {
+  const int mmode = mask == C2KV_MASK_STRUCTURED ? kMaskStructured : mask == C2KV_MASK_ANCHOR ? kMaskAnchor
+                                                                                            : kMaskCausal;
+  if (N == 1) {   // one document token and no slot or anchor
     s = run_append(geom, 1, &krot, &vt, tabs, &zero, nullptr, N, N, kk, v, st);
     if (s != C2KV_OK) return s;
     const __nv_bfloat16* kb = krot;
     const __nv_bfloat16* vb = vt;
-    return run_attention(geom, 1, &kb, &vb, tabs, &zero, nullptr, N, N, N, mmode, n_doc, kblk, q, out, workspace,
-                         attn_bytes, st);
+    return run_attention(geom, 1, &kb, &vb, tabs, &zero, nullptr, N, N, N,
+                         mmode == kMaskAnchor ? kMaskCausal : mmode, n_doc, kblk, q, out, workspace, attn_bytes, st);
   }
   int sms = 0;
   s = device_state(nullptr, &sms);

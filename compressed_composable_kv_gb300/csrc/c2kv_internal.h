@@ -241,7 +241,7 @@ struct TableParams {
 enum TableMode : int32_t { kTableComposed = 0, kTableExplicit = 1, kTableExtraction = 2 };
 
 enum PosMode : int32_t { kPosSequential = 0, kPosExtraction = 1 };
-enum MaskMode : int32_t { kMaskCausal = 0, kMaskStructured = 1 };
+enum MaskMode : int32_t { kMaskCausal = 0, kMaskStructured = 1, kMaskAnchor = 2 };
 
 struct AppendParams {
   __nv_bfloat16* k_dst[kMaxBatch];   // layer base [Hkv][cap][d]

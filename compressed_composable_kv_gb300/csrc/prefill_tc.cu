@@ -4,7 +4,8 @@
 // C2KV explainer (paper-daily.com), section "pipeline: extract, store,
 // concatenate" (整体流程): once the composed cache is in place the question is
 // appended and prefilled over it; section "structured information flow"
-// (为什么需要“结构化信息流”？) gives the extraction-time mask.
+// (为什么需要“结构化信息流”？) gives the extraction-time mask; section
+// "results" gives the anchor-token ablation's mask.
 //
 // One CTA owns a 128-row M tile of (question token, q head of the group)
 // rows for one (sequence, kv head, key split), token-major: row r is token
@@ -12,10 +13,12 @@
 // warps (thread t owns row t, i.e. TMEM lane t); warp 4's first lane issues
 // every TMA load and every MMA.
 //   Q   : [128 rows][d] bf16, TMA (2-D map over the rotated-q scratch), SW128
-//   K,V : 64-key tiles, TMA (3-D map over [layer*kv head][keys][d]), 3 stages,
-//         keys at or past the sequence's valid length read as zeros (OOB)
-//   S   : Q K^T, fp32 in TMEM, double-buffered (2 x 64 columns)
-//   P   : bf16 in shared memory (K-major SW128), double-buffered
+//   K,V : 128-key tiles, TMA (3-D map over [layer*kv head][keys][d]), 2
+//         stages, keys at or past the sequence's valid length read as zeros
+//         (OOB); key tiles no row of the M tile can see are skipped
+//   S   : Q K^T, fp32 in TMEM, double-buffered (2 x 128 columns)
+//   P   : bf16 in shared memory (K-major, two SW128 sub-tiles of 64 keys),
+//         double-buffered
 //   O   : P V accumulated in TMEM (d columns), rescaled in place only when a
 //         row's running max grows by more than 2^8 (the final O / l uses the
 //         same stale max, so the result is exact)
@@ -227,15 +230,25 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   const int n_cached = p.n_cached[b];
   const int tok0 = mt * TOK;
   const int ntok = min(TOK, p.t_len - tok0);
-  const int kmax = n_cached + tok0 + ntok;
+  // Anchor-token mask: document rows also see every anchor, so an M tile
+  // holding document rows reads the keys of the whole sequence.
+  const bool anchor_docs = p.mask_mode == kMaskAnchor && tok0 < p.n_doc;
+  const int kmax = n_cached + (anchor_docs ? p.t_len : tok0 + ntok);
   const int kb = split * p.split_keys;
   const int ke = min(kb + p.split_keys, kmax);
   const int ntiles = ke > kb ? (ke - kb + BN - 1) / BN : 0;
   // Structured mask ("structured information flow"): an M tile of slot rows
   // only sees the sink block, its own slots' document blocks and the slots,
   // so the other document key tiles hold no visible key and are skipped.
+  // Anchor mask: document key tiles past the M tile's last row hold no key
+  // its rows see (they see the anchors and their causal prefix).  The masked
+  // modes run with no cached rows, so key index = token index.
   // Every role walks the same list of live tiles.
   auto tile_live = [&](int t) -> bool {
+    if (anchor_docs) {
+      const int key0 = kb + t * BN;
+      return key0 < tok0 + ntok || key0 + BN > p.n_doc;
+    }
     if (p.mask_mode != kMaskStructured || tok0 < p.n_doc) return true;   // document rows: causal
     const int key0 = kb + t * BN;
     if (key0 + BN > p.n_doc || key0 < min(p.kblk, p.n_doc)) return true;  // slot keys, sink block
@@ -386,13 +399,28 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
       tc_fence_before();
       mbar_arrive(&s_free[sb]);
       const int key0 = kb + tcur * BN;
-      // keys [key0, key0 + nvis) pass the causal / split bounds of this row
-      const int nvis = row_ok ? min(min(ke, lim) - key0, BN) : 0;
+      // keys [key0, key0 + nvis) pass the causal / split bounds of this row;
+      // under the anchor mask a document row sees all of an anchor tile
+      const bool doc_anchor = anchor_docs && tok < p.n_doc;
+      const int nvis = row_ok ? min(min(ke, doc_anchor && key0 >= p.n_doc ? ke : lim) - key0, BN) : 0;
       float mraw = -INFINITY;   // max of the raw scores (the scale is positive)
-      if (p.mask_mode == kMaskStructured && tok >= p.n_doc) {   // slot rows; document rows are causal
+      if (p.mask_mode == kMaskStructured && tok >= p.n_doc && key0 < p.n_doc) {
+        // slot rows over document keys (slot keys are a causal prefix, and
+        // document rows are causal)
 #pragma unroll
         for (int c = 0; c < BN; ++c) {
           const bool vis = c < nvis && tc_structured_visible(p, tok, key0 + c);
+          sv[c] = vis ? sv[c] : -INFINITY;
+          mraw = fmaxf(mraw, sv[c]);
+        }
+      } else if (doc_anchor && key0 < p.n_doc && key0 + BN > p.n_doc) {
+        // a document row's view of the tile holding the last document keys
+        // and the first anchors: its causal prefix, then the anchors
+        const int nend = row_ok ? min(ke - key0, BN) : 0;   // keys before the split's end
+#pragma unroll
+        for (int c = 0; c < BN; ++c) {
+          const int key = key0 + c;
+          const bool vis = c < nend && (key <= tok || key >= p.n_doc);
           sv[c] = vis ? sv[c] : -INFINITY;
           mraw = fmaxf(mraw, sv[c]);
         }

@@ -73,7 +73,8 @@ typedef enum {
 
 typedef enum {
   C2KV_MASK_CAUSAL = 0,      /* plain causal mask over the whole sequence */
-  C2KV_MASK_STRUCTURED = 1   /* [EXPL] "structured information flow" rules */
+  C2KV_MASK_STRUCTURED = 1,  /* [EXPL] "structured information flow" rules */
+  C2KV_MASK_ANCHOR = 2       /* [EXPL] "results": the anchor-token ablation */
 } c2kv_mask;
 
 /* Thread-local description of the last failure on this thread ("" if none). */
@@ -360,7 +361,11 @@ c2kv_status c2kv_seq_advance(int32_t batch, int32_t* n_cached_dev, int32_t delta
  * causal mask and see no slot; slot i sees the sink block B(0) (document
  * tokens [0, k)), its own block [i*k, min((i+1)k, n_doc)) and slots 0..i.
  * [EXPL] "positions at concatenation": documents sit at 0..n_doc-1 and slot
- * i at min((i+1)k, n_doc) - 1.  C2KV_MASK_CAUSAL: plain causal attention,
+ * i at min((i+1)k, n_doc) - 1.  C2KV_MASK_ANCHOR: the anchor-token
+ * ablation of [EXPL] "results", read as a change of mask only: the n_slot
+ * extra tokens take the slots' positions; document token r sees document
+ * tokens 0..r and every extra token; extra token i sees every document
+ * token and extra tokens 0..i.  C2KV_MASK_CAUSAL: plain causal attention,
  * token t at position t (n_slot must be 0).
  * q: device [N][n_q_heads][head_dim], kk, v: device [N][n_kv_heads][head_dim]
  * with N = n_doc + n_slot, all before RoPE; out: device [N][n_q_heads][d].

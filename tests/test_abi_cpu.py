@@ -124,3 +124,24 @@ def test_store_file_and_test_hook_arguments_are_checked_on_the_host(P, tmp_path)
     P.c2kv_test_expire_next_waits(0)
     assert P.STATUS_NAMES[P.C2KV_EIO] == "C2KV_EIO"
 
+
+
+def test_masked_attention_arguments_are_checked_on_the_host(P):
+    """Mask kinds and their size rules are checked before any pointer or CUDA
+    call: an unknown mask, slots under the causal mask and k < 1 under the
+    structured or anchor mask are rejected; a valid call then fails only on
+    its null pointers."""
+    lib = P.load_library()
+    g = ctypes.byref(P.as_geometry(S.TINY))
+    null = [None] * 5
+
+    def call(mask, n_doc, n_slot, k):
+        st = lib.c2kv_attend_masked(g, mask, n_doc, n_slot, k, *null[:4], null[4], 0, None)
+        return st, P.c2kv_last_error()
+
+    assert call(3, 8, 2, 4) == (P.C2KV_EINVAL, "unknown mask")
+    assert call(P.C2KV_MASK_CAUSAL, 8, 2, 1)[1] == "causal mask takes n_slot = 0"
+    for m in (P.C2KV_MASK_STRUCTURED, P.C2KV_MASK_ANCHOR):
+        assert call(m, 8, 2, 0) == (P.C2KV_EINVAL, "k must be >= 1")
+        assert call(m, 0, 2, 4)[1] == "need n_doc >= 1 and n_slot >= 0"
+        assert call(m, 8, 2, 4) == (P.C2KV_EINVAL, "null pointer")

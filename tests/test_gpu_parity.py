@@ -403,6 +403,53 @@ def test_structured_mask_extraction_full_size():
     check_attention(out[rows], ref, "structured mask 4000 + 1000, k=4")
 
 
+@pytest.mark.parametrize("n_doc,n_slot,k", [(12, 3, 4), (200, 50, 4), (257, 17, 16), (40, 40, 1),
+                                             (600, 150, 4), (300, 0, 4), (1, 0, 4)])
+def test_anchor_mask_mode(n_doc, n_slot, k):
+    """The anchor-token ablation: document rows see their causal prefix and
+    every anchor (the key tiles in between are skipped), anchors see the
+    document and earlier anchors.  (600, 150) leaves dead key tiles between
+    the first document rows and the anchors; n_slot = 0 is plain causal
+    attention, and a single token takes the one-token path."""
+    g = S.TINY
+    rng = np.random.default_rng(n_doc * 137 + n_slot)
+    N = n_doc + n_slot
+    q = S.normal_bf16(rng, (N, g.n_q_heads, g.head_dim))
+    kk = S.normal_bf16(rng, (N, g.n_kv_heads, g.head_dim))
+    v = S.normal_bf16(rng, (N, g.n_kv_heads, g.head_dim))
+    ws = torch.zeros(P.masked_workspace_bytes(g, N), dtype=torch.uint8, device="cuda")
+    out = torch.empty((N, g.n_q_heads, g.head_dim), dtype=torch.bfloat16, device="cuda")
+    P.c2kv_attend_masked(g, P.C2KV_MASK_ANCHOR, n_doc, n_slot, k, to_dev(q), to_dev(kk), to_dev(v), out, ws)
+    torch.cuda.synchronize()
+    assert P.c2kv_device_error() == P.C2KV_OK
+    ref = O.masked_extraction_attention(q, kk, v, n_doc, n_slot, k, g.rope_theta, mask="anchor")
+    check_attention(out, ref, f"anchor mask {n_doc}+{n_slot} k={k}")
+
+
+def test_anchor_mask_extraction_full_size():
+    """A 4000-token document with 1000 anchor tokens (k=4 positions) under the
+    anchor-token mask, Llama3.1-8B heads, sampled rows: early document rows
+    (most key tiles dead), rows at M-tile edges, the last document row, the
+    first and last anchors and random ones."""
+    g = S.Geometry(1, 32, 8, 128, 5.0e5)
+    n_doc, k = 4000, 4
+    n_slot = O.slot_count(n_doc, k)
+    N = n_doc + n_slot
+    rng = np.random.default_rng(23)
+    q = S.normal_bf16(rng, (N, 32, 128))
+    kk = S.normal_bf16(rng, (N, 8, 128))
+    v = S.normal_bf16(rng, (N, 8, 128))
+    ws = torch.zeros(P.masked_workspace_bytes(g, N), dtype=torch.uint8, device="cuda")
+    out = torch.empty((N, 32, 128), dtype=torch.bfloat16, device="cuda")
+    P.c2kv_attend_masked(g, P.C2KV_MASK_ANCHOR, n_doc, n_slot, k, to_dev(q), to_dev(kk), to_dev(v), out, ws)
+    torch.cuda.synchronize()
+    assert P.c2kv_device_error() == P.C2KV_OK
+    rows = [0, 1, 15, 16, 127, 128, 2047, 3968, 3999, 4000, 4001, 4015, 4016, N - 1]
+    rows += sorted(rng.choice(N, 18, replace=False).tolist())
+    ref = O.masked_extraction_attention(q, kk, v, n_doc, n_slot, k, g.rope_theta, rows=rows, mask="anchor")
+    check_attention(out[rows], ref, "anchor mask 4000 + 1000, k=4")
+
+
 def test_causal_mask_mode_llama_heads():
     g = S.Geometry(1, 32, 8, 128, 5.0e5)
     N = 300
