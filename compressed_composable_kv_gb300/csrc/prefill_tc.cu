@@ -197,7 +197,9 @@ __device__ __forceinline__ bool tc_structured_visible(const PrefillTcParams& p, 
   return key < min(p.kblk, p.n_doc) || (key >= i * p.kblk && key < min((i + 1) * p.kblk, p.n_doc));
 }
 
-template <int D, int G>
+// MASKED: the extraction masks (structured, anchor); the question prefill
+// runs the causal instantiation, which carries no mask code.
+template <int D, int G, bool MASKED>
 __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
   using C = TcCfg<D>;
   constexpr int TOK = BM / G;    // tokens per M tile
@@ -232,7 +234,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   const int ntok = min(TOK, p.t_len - tok0);
   // Anchor-token mask: document rows also see every anchor, so an M tile
   // holding document rows reads the keys of the whole sequence.
-  const bool anchor_docs = p.mask_mode == kMaskAnchor && tok0 < p.n_doc;
+  const int mode = MASKED ? p.mask_mode : (int)kMaskCausal;
+  const bool anchor_docs = mode == kMaskAnchor && tok0 < p.n_doc;
   const int kmax = n_cached + (anchor_docs ? p.t_len : tok0 + ntok);
   const int kb = split * p.split_keys;
   const int ke = min(kb + p.split_keys, kmax);
@@ -249,7 +252,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
       const int key0 = kb + t * BN;
       return key0 < tok0 + ntok || key0 + BN > p.n_doc;
     }
-    if (p.mask_mode != kMaskStructured || tok0 < p.n_doc) return true;   // document rows: causal
+    if (mode != kMaskStructured || tok0 < p.n_doc) return true;   // document rows: causal
     const int key0 = kb + t * BN;
     if (key0 + BN > p.n_doc || key0 < min(p.kblk, p.n_doc)) return true;  // slot keys, sink block
     const int lo = (tok0 - p.n_doc) * p.kblk;
@@ -404,7 +407,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
       const bool doc_anchor = anchor_docs && tok < p.n_doc;
       const int nvis = row_ok ? min(min(ke, doc_anchor && key0 >= p.n_doc ? ke : lim) - key0, BN) : 0;
       float mraw = -INFINITY;   // max of the raw scores (the scale is positive)
-      if (p.mask_mode == kMaskStructured && tok >= p.n_doc && key0 < p.n_doc) {
+      if (mode == kMaskStructured && tok >= p.n_doc && key0 < p.n_doc) {
         // slot rows over document keys (slot keys are a causal prefix, and
         // document rows are causal)
 #pragma unroll
@@ -642,15 +645,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   cl.sync();
 }
 
-template <int D, int G>
+template <int D, int G, bool MASKED>
 bool configure_tc() {
   using C = TcCfg<D>;
   static int state = 0;   // 0 unknown, 1 ready, -1 failed
   if (state == 0) {
     const bool okk =
-        cudaFuncSetAttribute(prefill_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) ==
+        cudaFuncSetAttribute(prefill_tc_kernel<D, G, MASKED>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) ==
             cudaSuccess &&
-        cudaFuncSetAttribute(prefill_tc_kernel<D, G>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+        cudaFuncSetAttribute(prefill_tc_kernel<D, G, MASKED>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
             cudaSuccess;
     if (!okk) cudaGetLastError();
     state = okk ? 1 : -1;
@@ -658,10 +661,10 @@ bool configure_tc() {
   return state == 1;
 }
 
-template <int D, int G>
+template <int D, int G, bool MASKED>
 cudaError_t launch_tc(const PrefillTcParams& p, cudaStream_t st) {
   using C = TcCfg<D>;
-  if (!configure_tc<D, G>()) return cudaErrorInvalidValue;
+  if (!configure_tc<D, G, MASKED>()) return cudaErrorInvalidValue;
   if (p.num_splits < 1 || p.num_splits > kMaxClusterTc) return cudaErrorInvalidValue;
   const int tok = BM / G;
   const int n_mt = (p.t_len + tok - 1) / tok;
@@ -677,16 +680,16 @@ cudaError_t launch_tc(const PrefillTcParams& p, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, G>, p);
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, G, MASKED>, p);
 }
 
 // Number of `cs`-CTA clusters of the kernel that can be resident at once
 // (cached; 0 when unknown).
-template <int D, int G>
+template <int D, int G, bool MASKED>
 int tc_active_clusters(int cs) {
   using C = TcCfg<D>;
   static int cache[kMaxClusterTc + 1] = {};   // -1 = queried, none
-  if (cs < 1 || cs > kMaxClusterTc || !configure_tc<D, G>()) return 0;
+  if (cs < 1 || cs > kMaxClusterTc || !configure_tc<D, G, MASKED>()) return 0;
   if (cache[cs] == 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cs, 1, 1);
@@ -700,7 +703,7 @@ int tc_active_clusters(int cs) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, prefill_tc_kernel<D, G>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, prefill_tc_kernel<D, G, MASKED>, &cfg) != cudaSuccess) {
       cudaGetLastError();
       n = 0;
     }
@@ -709,28 +712,34 @@ int tc_active_clusters(int cs) {
   return cache[cs] > 0 ? cache[cs] : 0;
 }
 
-template <int D>
+template <int D, bool MASKED>
 int active_clusters_d(int cs, int group) {
   switch (group) {
-    case 1: return tc_active_clusters<D, 1>(cs);
-    case 2: return tc_active_clusters<D, 2>(cs);
-    case 4: return tc_active_clusters<D, 4>(cs);
-    case 5: return tc_active_clusters<D, 5>(cs);
-    case 8: return tc_active_clusters<D, 8>(cs);
+    case 1: return tc_active_clusters<D, 1, MASKED>(cs);
+    case 2: return tc_active_clusters<D, 2, MASKED>(cs);
+    case 4: return tc_active_clusters<D, 4, MASKED>(cs);
+    case 5: return tc_active_clusters<D, 5, MASKED>(cs);
+    case 8: return tc_active_clusters<D, 8, MASKED>(cs);
     default: return 0;
   }
 }
 
-template <int D>
+template <int D, bool MASKED>
 cudaError_t launch_tc_d(const PrefillTcParams& p, int group, cudaStream_t st) {
   switch (group) {
-    case 1: return launch_tc<D, 1>(p, st);
-    case 2: return launch_tc<D, 2>(p, st);
-    case 4: return launch_tc<D, 4>(p, st);
-    case 5: return launch_tc<D, 5>(p, st);
-    case 8: return launch_tc<D, 8>(p, st);
+    case 1: return launch_tc<D, 1, MASKED>(p, st);
+    case 2: return launch_tc<D, 2, MASKED>(p, st);
+    case 4: return launch_tc<D, 4, MASKED>(p, st);
+    case 5: return launch_tc<D, 5, MASKED>(p, st);
+    case 8: return launch_tc<D, 8, MASKED>(p, st);
     default: return cudaErrorInvalidValue;
   }
+}
+
+int active_clusters(int cs, int head_dim, int group, bool masked) {
+  if (head_dim == 128) return masked ? active_clusters_d<128, true>(cs, group) : active_clusters_d<128, false>(cs, group);
+  if (head_dim == 64) return masked ? active_clusters_d<64, true>(cs, group) : active_clusters_d<64, false>(cs, group);
+  return 0;
 }
 
 }  // namespace
@@ -749,8 +758,9 @@ void prefill_tc_plan(int units, int max_keys, int num_sms, int head_dim, int gro
   s = std::min(s, (max_keys + BN - 1) / BN);
   s = std::min(s, kMaxClusterTc);
   for (; s >= 2; --s) {
-    const int n = head_dim == 128 ? active_clusters_d<128>(s, group)
-                                  : head_dim == 64 ? active_clusters_d<64>(s, group) : 0;
+    // both instantiations take the same shared memory (one CTA per SM), so
+    // the causal one answers for the masked one too
+    const int n = active_clusters(s, head_dim, group, false);
     if (n >= units) break;
   }
   if (s < 1) s = 1;
@@ -761,8 +771,9 @@ void prefill_tc_plan(int units, int max_keys, int num_sms, int head_dim, int gro
 }
 
 cudaError_t launch_prefill_tc(const PrefillTcParams& p, int head_dim, int group, cudaStream_t st) {
-  if (head_dim == 128) return launch_tc_d<128>(p, group, st);
-  if (head_dim == 64) return launch_tc_d<64>(p, group, st);
+  const bool masked = p.mask_mode != kMaskCausal;
+  if (head_dim == 128) return masked ? launch_tc_d<128, true>(p, group, st) : launch_tc_d<128, false>(p, group, st);
+  if (head_dim == 64) return masked ? launch_tc_d<64, true>(p, group, st) : launch_tc_d<64, false>(p, group, st);
   return cudaErrorInvalidValue;
 }
 
