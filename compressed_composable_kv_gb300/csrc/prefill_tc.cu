@@ -750,7 +750,7 @@ int prefill_tc_key_tile() { return BN; }
 
 // Key splits of each (sequence, M tile, kv head) unit: as many as keep all
 // the units' clusters resident at once (one CTA per SM), at most 16 and at
-// most one per 64-key tile.  Small units counts thereby fill the SMs; with
+// most one per key tile.  Small units counts thereby fill the SMs; with
 // units >= SMs / 2 there is one split and no merge.
 void prefill_tc_plan(int units, int max_keys, int num_sms, int head_dim, int group, int* num_splits,
                      int* split_keys) {
