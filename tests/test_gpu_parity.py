@@ -426,6 +426,29 @@ def test_anchor_mask_mode(n_doc, n_slot, k):
     check_attention(out, ref, f"anchor mask {n_doc}+{n_slot} k={k}")
 
 
+@pytest.mark.parametrize("mask", ["structured", "anchor"])
+@pytest.mark.parametrize("hq,hkv,d", [(40, 8, 128), (8, 8, 128), (16, 2, 64)])
+def test_masked_modes_group_sizes(hq, hkv, d, mask):
+    """Both extraction masks at G = 5 (25 tokens per 125-row M tile), G = 1
+    and G = 8, with the document/slot boundary inside an M tile."""
+    g = S.Geometry(1, hq, hkv, d, 1.0e6)
+    n_doc, k = 310, 4
+    n_slot = O.slot_count(n_doc, k)
+    N = n_doc + n_slot
+    rng = np.random.default_rng(hq * 7 + hkv + d)
+    q = S.normal_bf16(rng, (N, hq, d))
+    kk = S.normal_bf16(rng, (N, hkv, d))
+    v = S.normal_bf16(rng, (N, hkv, d))
+    ws = torch.zeros(P.masked_workspace_bytes(g, N), dtype=torch.uint8, device="cuda")
+    out = torch.empty((N, hq, d), dtype=torch.bfloat16, device="cuda")
+    code = P.C2KV_MASK_STRUCTURED if mask == "structured" else P.C2KV_MASK_ANCHOR
+    P.c2kv_attend_masked(g, code, n_doc, n_slot, k, to_dev(q), to_dev(kk), to_dev(v), out, ws)
+    torch.cuda.synchronize()
+    assert P.c2kv_device_error() == P.C2KV_OK
+    ref = O.masked_extraction_attention(q, kk, v, n_doc, n_slot, k, g.rope_theta, mask=mask)
+    check_attention(out, ref, f"{mask} mask, {hq}/{hkv} heads, d={d}")
+
+
 def test_anchor_mask_extraction_full_size():
     """A 4000-token document with 1000 anchor tokens (k=4 positions) under the
     anchor-token mask, Llama3.1-8B heads, sampled rows: early document rows
