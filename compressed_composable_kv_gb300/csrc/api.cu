@@ -113,18 +113,22 @@ struct c2kv_store_s {
   std::vector<cudaEvent_t> ev;
   std::mutex mu;
   // the last composition into each RoPE table (one per request), which a
-  // C2KV_COMPOSE_CONTINUE call must match
+  // C2KV_COMPOSE_CONTINUE call must match; at most kMaxTrackedTables tables,
+  // the least recently started composition dropped first
   struct Composition {
     std::vector<int32_t> doc_ids, order;
     int32_t k = 0, cap = 0;
     uint32_t flags = 0;
     const void *k_cache = nullptr, *v_cache = nullptr;
+    uint64_t seq = 0;   // order in which the compositions started
   };
   std::unordered_map<const void*, Composition> last;
+  uint64_t next_seq = 0;
 };
 
 namespace {
 constexpr int kLayerGroups = 4;   // copy/rotate pipeline depth of one compose
+constexpr size_t kMaxTrackedTables = 1024;
 
 // Composition plan shared by c2kv_plan and c2kv_compose.
 c2kv_status plan_impl(int32_t n_docs, const int32_t* n_tokens, const int32_t* n_slots,
@@ -705,7 +709,14 @@ c2kv_status c2kv_compose_layers(c2kv_store st, int32_t n_docs, const int32_t* do
       tp.seg[c].n_tokens = ntok[d];
     }
     C2KV_CUDA(launch_rope_table(tp, us));
+    if (st->last.size() >= kMaxTrackedTables) {   // this table's entry was erased above
+      auto oldest = st->last.begin();
+      for (auto it = st->last.begin(); it != st->last.end(); ++it)
+        if (it->second.seq < oldest->second.seq) oldest = it;
+      st->last.erase(oldest);
+    }
     auto& lc = st->last[rope_table_out];
+    lc.seq = st->next_seq++;
     lc.doc_ids.assign(doc_ids, doc_ids + n_docs);
     if (order)
       lc.order.assign(order, order + n_docs);

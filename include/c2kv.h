@@ -220,7 +220,9 @@ c2kv_status c2kv_compose(c2kv_store store, int32_t n_docs, const int32_t* doc_id
  * 0 <= layer_begin < layer_end <= n_layers.  Other arguments, outputs and
  * errors as c2kv_compose; C2KV_EINVAL also for a CONTINUE that does not
  * follow a composition of the same request (documents, k, flags, caches,
- * cap, table) on this store.
+ * cap, table) on this store.  The store remembers the compositions into the
+ * 1024 tables most recently composed into; a CONTINUE into an older one is
+ * refused the same way.
  */
 #define C2KV_COMPOSE_NO_REALIGN 1u
 #define C2KV_COMPOSE_CONTINUE 2u

@@ -488,6 +488,35 @@ def test_causal_mask_mode_llama_heads():
     check_attention(out, ref, "causal mask mode")
 
 
+def test_continue_tracks_the_most_recent_tables():
+    """The store remembers the compositions into the 1024 tables composed into
+    most recently: after 1025 compositions into distinct tables, continuing
+    the first one is refused and continuing the second and the last works."""
+    g = S.Geometry(2, 4, 2, 64, 1.0e4)
+    k = 4
+    doc = S.make_document(g, 1, 8, k, 3)
+    store = P.c2kv_store_create(g, 1 << 20)
+    try:
+        P.c2kv_store_segments(store, [1], [doc.n_tokens], [doc.n_slots], k, [doc.k_pre], [doc.v])
+        cap = doc.n_slots
+        kc = torch.zeros((g.n_layers, g.n_kv_heads, cap, g.head_dim), dtype=torch.bfloat16, device="cuda")
+        vc = torch.zeros_like(kc)
+        tb = P.c2kv_rope_table_bytes(g, cap)
+        n = 1025
+        tabs = torch.zeros((n, tb), dtype=torch.uint8, device="cuda")
+        for i in range(n):
+            P.c2kv_compose_layers(store, [1], None, k, 0, 0, 1, kc, vc, cap, tabs[i])
+        with pytest.raises(P.C2KVError) as e:
+            P.c2kv_compose_layers(store, [1], None, k, P.C2KV_COMPOSE_CONTINUE, 1, 2, kc, vc, cap, tabs[0])
+        assert e.value.status == P.C2KV_EINVAL
+        for i in (1, n - 1):
+            P.c2kv_compose_layers(store, [1], None, k, P.C2KV_COMPOSE_CONTINUE, 1, 2, kc, vc, cap, tabs[i])
+        torch.cuda.synchronize()
+        assert P.c2kv_device_error() == P.C2KV_OK
+    finally:
+        P.c2kv_store_destroy(store)
+
+
 def test_store_save_and_load_round_trip(tmp_path):
     """A saved store, loaded into a new one, composes the same caches bit for
     bit; documents stored at different k keep theirs.  Files of another
