@@ -574,13 +574,34 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, 1) decode_kernel(const __
 }
 
 template <int D, int G>
+KernelSetup& decode_setup() {
+  static KernelSetup s;
+  return s;
+}
+
+// Sets the kernel's attributes on device `dev` once (caller holds s.mu).
+template <int D, int G>
+cudaError_t configure_decode(KernelSetup& s, int dev) {
+  using C = DCfg<D, G>;
+  if (s.state[dev] == 0) {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) cudaGetLastError();
+    s.state[dev] = e == cudaSuccess ? 1 : -(int)e;
+  }
+  return s.state[dev] == 1 ? cudaSuccess : (cudaError_t)(-s.state[dev]);
+}
+
+template <int D, int G>
 cudaError_t launch_one(const AttnParams& p, bool overlap, cudaStream_t st) {
   using C = DCfg<D, G>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  {
+    KernelSetup& s = decode_setup<D, G>();
+    const int dev = setup_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(s.mu);
+    const cudaError_t e = configure_decode<D, G>(s, dev);
     if (e != cudaSuccess) return e;
-    configured = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.num_splits, p.n_kv, p.batch);
@@ -611,17 +632,12 @@ cudaError_t launch_one(const AttnParams& p, bool overlap, cudaStream_t st) {
 template <int D, int G>
 int cluster_splits_for(int units, int want) {
   using C = DCfg<D, G>;
-  static int cache[17] = {};   // max active clusters per size, -1 = unknown error
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
-      cudaGetLastError();
-      return 0;
-    }
-    configured = true;
-  }
+  KernelSetup& s = decode_setup<D, G>();
+  const int dev = setup_device();
+  if (dev < 0) return 0;
+  std::lock_guard<std::mutex> lk(s.mu);
+  if (configure_decode<D, G>(s, dev) != cudaSuccess) return 0;
+  int* cache = s.clusters[dev];
   for (int cs = want < 16 ? want : 16; cs >= 2; --cs) {
     if (cache[cs] == 0) {
       cudaLaunchConfig_t cfg = {};

@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "c2kv.h"
 
 namespace c2kv {
@@ -18,6 +20,27 @@ constexpr int kMaxSplits = 256;           // split-K partitions per (sequence, t
 // Device error word bits (see c2kv_device_error).
 constexpr unsigned kErrTimeout = 1u;      // a bounded mbarrier wait expired
 constexpr unsigned kErrLength = 2u;       // a device-side length exceeded cap / max_keys
+
+// One-time host setup of a kernel (function attributes) and the cluster
+// occupancy answers that depend on it.  Attributes belong to the device that
+// was current when they were set, so every device has its own entry; `mu`
+// makes first use from several host threads safe.
+constexpr int kMaxSetupDevices = 64;
+struct KernelSetup {
+  std::mutex mu;
+  int state[kMaxSetupDevices] = {};          // 0 not yet, 1 ready, else -(cudaError_t)
+  int clusters[kMaxSetupDevices][17] = {};   // active clusters per size: 0 unknown, -1 none
+};
+
+// The current device as an index into KernelSetup (-1 if there is none).
+inline int setup_device() {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  return d >= 0 && d < kMaxSetupDevices ? d : -1;
+}
 
 // Bounded waits give up after this many SM cycles (about 2 s at 2 GHz).
 constexpr long long kWaitCycles = 4000000000LL;

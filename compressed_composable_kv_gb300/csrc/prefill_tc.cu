@@ -646,25 +646,37 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
 }
 
 template <int D, int G, bool MASKED>
-bool configure_tc() {
+KernelSetup& tc_setup() {
+  static KernelSetup s;
+  return s;
+}
+
+// Sets the kernel's attributes on device `dev` once (caller holds s.mu).
+template <int D, int G, bool MASKED>
+cudaError_t configure_tc(KernelSetup& s, int dev) {
   using C = TcCfg<D>;
-  static int state = 0;   // 0 unknown, 1 ready, -1 failed
-  if (state == 0) {
-    const bool okk =
-        cudaFuncSetAttribute(prefill_tc_kernel<D, G, MASKED>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) ==
-            cudaSuccess &&
-        cudaFuncSetAttribute(prefill_tc_kernel<D, G, MASKED>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-            cudaSuccess;
-    if (!okk) cudaGetLastError();
-    state = okk ? 1 : -1;
+  if (s.state[dev] == 0) {
+    cudaError_t e =
+        cudaFuncSetAttribute(prefill_tc_kernel<D, G, MASKED>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(prefill_tc_kernel<D, G, MASKED>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) cudaGetLastError();
+    s.state[dev] = e == cudaSuccess ? 1 : -(int)e;
   }
-  return state == 1;
+  return s.state[dev] == 1 ? cudaSuccess : (cudaError_t)(-s.state[dev]);
 }
 
 template <int D, int G, bool MASKED>
 cudaError_t launch_tc(const PrefillTcParams& p, cudaStream_t st) {
   using C = TcCfg<D>;
-  if (!configure_tc<D, G, MASKED>()) return cudaErrorInvalidValue;
+  {
+    KernelSetup& s = tc_setup<D, G, MASKED>();
+    const int dev = setup_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(s.mu);
+    const cudaError_t e = configure_tc<D, G, MASKED>(s, dev);
+    if (e != cudaSuccess) return e;
+  }
   if (p.num_splits < 1 || p.num_splits > kMaxClusterTc) return cudaErrorInvalidValue;
   const int tok = BM / G;
   const int n_mt = (p.t_len + tok - 1) / tok;
@@ -688,8 +700,14 @@ cudaError_t launch_tc(const PrefillTcParams& p, cudaStream_t st) {
 template <int D, int G, bool MASKED>
 int tc_active_clusters(int cs) {
   using C = TcCfg<D>;
-  static int cache[kMaxClusterTc + 1] = {};   // -1 = queried, none
-  if (cs < 1 || cs > kMaxClusterTc || !configure_tc<D, G, MASKED>()) return 0;
+  static_assert(kMaxClusterTc < 17, "KernelSetup::clusters holds sizes up to 16");
+  if (cs < 1 || cs > kMaxClusterTc) return 0;
+  KernelSetup& s = tc_setup<D, G, MASKED>();
+  const int dev = setup_device();
+  if (dev < 0) return 0;
+  std::lock_guard<std::mutex> lk(s.mu);
+  if (configure_tc<D, G, MASKED>(s, dev) != cudaSuccess) return 0;
+  int* cache = s.clusters[dev];
   if (cache[cs] == 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cs, 1, 1);
