@@ -129,15 +129,26 @@ def _i32arr(vals) -> ctypes.Array:
     return (ctypes.c_int32 * max(1, len(vals)))(*vals)
 
 
-def _host_ptr(a) -> int:
+def _host_ptr(a, nbytes: Optional[int], name: str) -> int:
+    """Address of a host array of 2-byte elements that the caller keeps alive
+    (no conversion: a temporary copy would be freed before the C call reads
+    it).  nbytes, when known, is the exact size the C side will read."""
     if isinstance(a, torch.Tensor):
-        if a.is_cuda or not a.is_contiguous():
-            raise ValueError("host segment must be a contiguous CPU tensor")
-        return a.data_ptr()
-    a = np.asarray(a)
-    if not a.flags.c_contiguous:
-        raise ValueError("host segment must be C-contiguous")
-    return a.ctypes.data
+        if a.is_cuda or not a.is_contiguous() or a.element_size() != 2:
+            raise ValueError(f"{name} must be a contiguous CPU tensor of 2-byte elements")
+        size, ptr = a.numel() * 2, a.data_ptr()
+    elif isinstance(a, np.ndarray):
+        if not a.flags.c_contiguous or a.itemsize != 2:
+            raise ValueError(f"{name} must be a C-contiguous array of 2-byte elements (bf16 bits)")
+        size, ptr = a.nbytes, a.ctypes.data
+    else:
+        raise ValueError(f"{name} must be a numpy array or a CPU tensor, got {type(a).__name__}")
+    if nbytes is not None and size != nbytes:
+        raise ValueError(f"{name} holds {size} bytes, expected {nbytes}")
+    return ptr
+
+
+_STORE_GEOMETRY = {}   # store handle -> geometry, for the binding's size checks
 
 
 # --------------------------------------------------------------------- API
@@ -154,18 +165,27 @@ def c2kv_store_create(geom, pinned_bytes: int) -> int:
     g = as_geometry(geom)
     h = ctypes.c_void_p()
     _check(load_library().c2kv_store_create(ctypes.byref(g), int(pinned_bytes), ctypes.byref(h)))
+    _STORE_GEOMETRY[h.value] = c2kv_geometry(g.n_layers, g.n_q_heads, g.n_kv_heads, g.head_dim, g.rope_theta)
     return h.value
 
 
 def c2kv_store_destroy(store: int) -> None:
+    _STORE_GEOMETRY.pop(store, None)
     load_library().c2kv_store_destroy(store)
 
 
 def c2kv_store_segments(store: int, doc_ids, n_tokens, n_slots, k: int, k_pre, v) -> None:
+    """k_pre[i], v[i]: host bf16 bits [n_layers][n_kv_heads][n_slots[i]][head_dim]
+    (numpy uint16 or a CPU tensor), checked against the store's geometry."""
     n = len(doc_ids)
+    if not (len(n_tokens) == len(n_slots) == len(k_pre) == len(v) == n):
+        raise ValueError("doc_ids, n_tokens, n_slots, k_pre and v must have one entry per document")
+    g = _STORE_GEOMETRY.get(store)
+    row = None if g is None else g.n_layers * g.n_kv_heads * g.head_dim * 2
+    sizes = [None if row is None or int(s) < 1 else row * int(s) for s in n_slots]
     keep = list(k_pre) + list(v)   # keep the arrays alive through the call
-    kp = (ctypes.c_void_p * max(1, n))(*[_host_ptr(a) for a in k_pre])
-    vp = (ctypes.c_void_p * max(1, n))(*[_host_ptr(a) for a in v])
+    kp = (ctypes.c_void_p * max(1, n))(*[_host_ptr(a, b, f"k_pre[{i}]") for i, (a, b) in enumerate(zip(k_pre, sizes))])
+    vp = (ctypes.c_void_p * max(1, n))(*[_host_ptr(a, b, f"v[{i}]") for i, (a, b) in enumerate(zip(v, sizes))])
     _check(load_library().c2kv_store_segments(store, n, _i32arr(doc_ids), _i32arr(n_tokens),
                                               _i32arr(n_slots), int(k), kp, vp))
     del keep

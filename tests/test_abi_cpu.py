@@ -145,3 +145,29 @@ def test_masked_attention_arguments_are_checked_on_the_host(P):
         assert call(m, 8, 2, 0) == (P.C2KV_EINVAL, "k must be >= 1")
         assert call(m, 0, 2, 4)[1] == "need n_doc >= 1 and n_slot >= 0"
         assert call(m, 8, 2, 4) == (P.C2KV_EINVAL, "null pointer")
+
+
+def test_store_segment_arrays_are_checked_by_the_binding(P, monkeypatch):
+    """Host segments must be arrays of 2-byte elements of exactly the size the
+    store's geometry gives (a converted temporary or a short array would be
+    read past its end).  The null handle stands in for a store, so a check
+    that let a bad array through would end in C2KV_EINVAL, not a read."""
+    import compressed_composable_kv_gb300.binding as bnd
+    g = S.TINY
+    monkeypatch.setitem(bnd._STORE_GEOMETRY, 0, bnd.as_geometry(g))
+    good = np.zeros((g.n_layers, g.n_kv_heads, 2, g.head_dim), np.uint16)
+    bad = [
+        [good.tolist()],                              # a list: would be converted into a temporary
+        [good.astype(np.uint8)],                      # 1-byte elements
+        [good[:, :, :1]],                             # one slot short of n_slots = 2
+        [np.asfortranarray(good.transpose(3, 2, 1, 0))],   # not C-contiguous
+        [torch.zeros(good.shape, dtype=torch.float32)],    # 4-byte elements
+    ]
+    for ks in bad:
+        with pytest.raises(ValueError):
+            P.c2kv_store_segments(0, [1], [8], [2], 4, ks, [good])
+    with pytest.raises(ValueError):
+        P.c2kv_store_segments(0, [1, 2], [8], [2], 4, [good], [good])   # lengths disagree
+    with pytest.raises(P.C2KVError) as e:   # well-formed arrays reach the C side
+        P.c2kv_store_segments(0, [1], [8], [2], 4, [good], [torch.from_numpy(good.view(np.int16))])
+    assert e.value.status == P.C2KV_EINVAL
