@@ -124,6 +124,18 @@ def _dev(t: Optional[torch.Tensor], dtype=None, name="tensor") -> int:
     return t.data_ptr()
 
 
+def _nbytes(t: Optional[torch.Tensor]) -> int:
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+def _need(t: Optional[torch.Tensor], nbytes: int, name: str, exact: bool = False) -> None:
+    """The C side reads or writes nbytes of t's memory (it only sees a pointer),
+    so t must hold that many bytes: exactly, for per-token inputs and outputs."""
+    have = _nbytes(t)
+    if have < nbytes or (exact and have != nbytes):
+        raise ValueError(f"{name} holds {have} bytes, expected {'' if exact else 'at least '}{nbytes}")
+
+
 def _i32arr(vals) -> ctypes.Array:
     vals = [int(v) for v in vals]
     return (ctypes.c_int32 * max(1, len(vals)))(*vals)
@@ -209,10 +221,26 @@ def c2kv_plan(n_tokens: Sequence[int], n_slots: Sequence[int], order: Optional[S
     return list(ss)[:n], list(po)[:n], ts.value, tt.value
 
 
+def _check_compose_buffers(store, k_cache, v_cache, cap, rope_table, pos_dev_out) -> None:
+    """Caches [n_layers][n_kv_heads][cap][head_dim] bf16, a RoPE table of cap
+    rows and pos_dev_out of cap entries, for stores made through this module
+    (whose geometry it knows)."""
+    g = _STORE_GEOMETRY.get(store)
+    if g is None or int(cap) <= 0:
+        return
+    cache = 2 * g.n_layers * g.n_kv_heads * int(cap) * g.head_dim
+    _need(k_cache, cache, "k_cache")
+    _need(v_cache, cache, "v_cache")
+    _need(rope_table, c2kv_rope_table_bytes(g, int(cap)), "rope_table")
+    if pos_dev_out is not None:
+        _need(pos_dev_out, 4 * int(cap), "pos_dev_out")
+
+
 def c2kv_compose(store: int, doc_ids, order, k: int, k_cache: torch.Tensor, v_cache: torch.Tensor,
                  cap: int, rope_table: torch.Tensor, pos_dev_out: Optional[torch.Tensor] = None, stream=None):
     """Returns (n_slots, next_pos).  rope_table: device buffer of
     c2kv_rope_table_bytes(geom, cap) bytes (any dtype)."""
+    _check_compose_buffers(store, k_cache, v_cache, cap, rope_table, pos_dev_out)
     ns, nxt = ctypes.c_int32(), ctypes.c_int32()
     _check(load_library().c2kv_compose(
         store, len(doc_ids), _i32arr(doc_ids), None if order is None else _i32arr(order), int(k),
@@ -231,6 +259,7 @@ def c2kv_compose_layers(store: int, doc_ids, order, k: int, flags: int, layer_be
                         pos_dev_out: Optional[torch.Tensor] = None, stream=None):
     """c2kv_compose over layers [layer_begin, layer_end) with C2KV_COMPOSE_* flags.
     Returns (n_slots, next_pos)."""
+    _check_compose_buffers(store, k_cache, v_cache, cap, rope_table, pos_dev_out)
     ns, nxt = ctypes.c_int32(), ctypes.c_int32()
     _check(load_library().c2kv_compose_layers(
         store, len(doc_ids), _i32arr(doc_ids), None if order is None else _i32arr(order), int(k), int(flags),
@@ -247,6 +276,7 @@ def c2kv_rope_table_bytes(geom, rows: int) -> int:
 
 def c2kv_rope_table(geom, pos_dev: torch.Tensor, table_out: torch.Tensor, stream=None) -> None:
     g = as_geometry(geom)
+    _need(table_out, c2kv_rope_table_bytes(g, pos_dev.numel()), "table_out")
     _check(load_library().c2kv_rope_table(ctypes.byref(g), _dev(pos_dev, torch.int32, "pos_dev"),
                                           pos_dev.numel(), _dev(table_out, None, "table_out"),
                                           _stream(stream)))
@@ -276,12 +306,43 @@ def _tabs(ts):
     return (ctypes.c_void_p * len(ts))(*[_dev(t, None, "rope_table") for t in ts])
 
 
+def _check_request_state(g, k_caches, v_caches, rope_tables, cap: int) -> None:
+    """Per-sequence caches [n_layers][n_kv_heads][cap][head_dim] bf16 and RoPE
+    tables of cap rows, one of each per sequence."""
+    B = len(k_caches)
+    if not (len(v_caches) == len(rope_tables) == B):
+        raise ValueError("k_caches, v_caches and rope_tables need one entry per sequence")
+    cache = 2 * g.n_layers * g.n_kv_heads * max(0, int(cap)) * g.head_dim
+    table = c2kv_rope_table_bytes(g, max(0, int(cap)))
+    for b in range(B):
+        _need(k_caches[b], cache, f"k_caches[{b}]")
+        _need(v_caches[b], cache, f"v_caches[{b}]")
+        _need(rope_tables[b], table, f"rope_tables[{b}]")
+
+
+def _check_decode_args(g, k_caches, v_caches, rope_tables, cap, n_cached_dev, q, k_new, v_new, out) -> None:
+    B = len(k_caches)
+    _check_request_state(g, k_caches, v_caches, rope_tables, cap)
+    _need(n_cached_dev, 4 * B, "n_cached_dev")
+    _need(q, 2 * B * g.n_q_heads * g.head_dim, "q", exact=True)
+    _need(k_new, 2 * B * g.n_kv_heads * g.head_dim, "k_new", exact=True)
+    _need(v_new, 2 * B * g.n_kv_heads * g.head_dim, "v_new", exact=True)
+    _need(out, 2 * B * g.n_q_heads * g.head_dim, "out", exact=True)
+
+
 def c2kv_attend_prefill(geom, layer: int, k_caches, v_caches, rope_tables, cap: int, n_cached,
                         q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, out: torch.Tensor,
                         workspace: Optional[torch.Tensor], stream=None) -> None:
     g = as_geometry(geom)
     B = len(k_caches)
     q_len = q.shape[1]
+    _check_request_state(g, k_caches, v_caches, rope_tables, cap)
+    if len(n_cached) != B:
+        raise ValueError("n_cached needs one entry per sequence")
+    _need(q, 2 * B * q_len * g.n_q_heads * g.head_dim, "q", exact=True)
+    _need(k_new, 2 * B * q_len * g.n_kv_heads * g.head_dim, "k_new", exact=True)
+    _need(v_new, 2 * B * q_len * g.n_kv_heads * g.head_dim, "v_new", exact=True)
+    _need(out, 2 * B * q_len * g.n_q_heads * g.head_dim, "out", exact=True)
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load_library().c2kv_attend_prefill(
         ctypes.byref(g), int(layer), B, _ptrs(k_caches, "k_cache"), _ptrs(v_caches, "v_cache"),
@@ -298,6 +359,7 @@ def c2kv_attend_decode(geom, layer: int, k_caches, v_caches, rope_tables, cap: i
                        out: torch.Tensor, workspace: Optional[torch.Tensor], stream=None, flags: int = 0) -> None:
     g = as_geometry(geom)
     B = len(k_caches)
+    _check_decode_args(g, k_caches, v_caches, rope_tables, cap, n_cached_dev, q, k_new, v_new, out)
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load_library().c2kv_attend_decode(
         ctypes.byref(g), int(layer), B, _ptrs(k_caches, "k_cache"), _ptrs(v_caches, "v_cache"),
@@ -314,6 +376,7 @@ def c2kv_attend_decode_noalloc(geom, layer: int, k_caches, v_caches, rope_tables
     all calls, so calls must not overlap on the GPU)."""
     g = as_geometry(geom)
     B = len(k_caches)
+    _check_decode_args(g, k_caches, v_caches, rope_tables, cap, n_cached_dev, q, k_new, v_new, out)
     _check(load_library().c2kv_attend_decode_noalloc(
         ctypes.byref(g), int(layer), B, _ptrs(k_caches, "k_cache"), _ptrs(v_caches, "v_cache"),
         _tabs(rope_tables), int(cap), _dev(n_cached_dev, torch.int32, "n_cached_dev"), int(max_keys),
@@ -330,6 +393,11 @@ def c2kv_attend_masked(geom, mask: int, n_doc: int, n_slot: int, k: int, q: torc
                        kk: torch.Tensor, v: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor,
                        stream=None) -> None:
     g = as_geometry(geom)
+    N = int(n_doc) + int(n_slot)
+    _need(q, 2 * N * g.n_q_heads * g.head_dim, "q", exact=True)
+    _need(kk, 2 * N * g.n_kv_heads * g.head_dim, "kk", exact=True)
+    _need(v, 2 * N * g.n_kv_heads * g.head_dim, "v", exact=True)
+    _need(out, 2 * N * g.n_q_heads * g.head_dim, "out", exact=True)
     _check(load_library().c2kv_attend_masked(
         ctypes.byref(g), int(mask), int(n_doc), int(n_slot), int(k), _dev(q, torch.bfloat16, "q"),
         _dev(kk, torch.bfloat16, "kk"), _dev(v, torch.bfloat16, "v"), _dev(out, torch.bfloat16, "out"),

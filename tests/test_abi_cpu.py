@@ -171,3 +171,44 @@ def test_store_segment_arrays_are_checked_by_the_binding(P, monkeypatch):
     with pytest.raises(P.C2KVError) as e:   # well-formed arrays reach the C side
         P.c2kv_store_segments(0, [1], [8], [2], 4, [good], [torch.from_numpy(good.view(np.int16))])
     assert e.value.status == P.C2KV_EINVAL
+
+
+def test_device_buffer_sizes_are_checked_by_the_binding(P, monkeypatch):
+    """The C side sees only pointers, so the binding checks every buffer
+    against the sizes the call implies before anything is launched: one
+    token short, a cache of too few rows or a table for too few rows raise
+    ValueError (CPU tensors stand in: the size check comes first)."""
+    import compressed_composable_kv_gb300.binding as bnd
+    g = S.TINY
+    Hq, Hkv, d, L = g.n_q_heads, g.n_kv_heads, g.head_dim, g.n_layers
+    bf = torch.bfloat16
+    N = 10
+    short = torch.zeros((N - 1, Hq, d), dtype=bf)
+    kv = torch.zeros((N, Hkv, d), dtype=bf)
+    with pytest.raises(ValueError, match="q holds"):
+        P.c2kv_attend_masked(g, P.C2KV_MASK_ANCHOR, 8, 2, 4, short, kv, kv, short, torch.zeros(16, dtype=torch.uint8))
+    cap = 32
+    cache = torch.zeros((L, Hkv, cap - 1, d), dtype=bf)       # one row short
+    tab = torch.zeros(P.c2kv_rope_table_bytes(g, cap), dtype=torch.uint8)
+    q1, k1 = torch.zeros((1, Hq, d), dtype=bf), torch.zeros((1, Hkv, d), dtype=bf)
+    n_dev = torch.zeros(1, dtype=torch.int32)
+    with pytest.raises(ValueError, match="k_caches"):
+        P.c2kv_attend_decode(g, 0, [cache], [cache], [tab], cap, n_dev, 8, q1, k1, k1, q1, None)
+    with pytest.raises(ValueError, match="k_caches"):
+        P.c2kv_attend_decode_noalloc(g, 0, [cache], [cache], [tab], cap, n_dev, 8, q1, k1, k1, q1)
+    good = torch.zeros((L, Hkv, cap, d), dtype=bf)
+    with pytest.raises(ValueError, match="rope_tables"):
+        P.c2kv_attend_decode(g, 0, [good], [good], [tab[:-16]], cap, n_dev, 8, q1, k1, k1, q1, None)
+    with pytest.raises(ValueError, match="n_cached"):
+        P.c2kv_attend_prefill(g, 0, [good], [good], [tab], cap, [0, 0], q1[None], k1[None], k1[None],
+                              q1[None], None)
+    with pytest.raises(ValueError, match="out holds"):
+        P.c2kv_attend_prefill(g, 0, [good], [good], [tab], cap, [0], q1[None], k1[None], k1[None],
+                              torch.zeros((1, 2, Hq, d), dtype=bf), None)
+    with pytest.raises(ValueError, match="table_out"):
+        P.c2kv_rope_table(g, torch.zeros(cap, dtype=torch.int32), tab[:-16])
+    monkeypatch.setitem(bnd._STORE_GEOMETRY, 0, bnd.as_geometry(g))
+    with pytest.raises(ValueError, match="rope_table"):
+        P.c2kv_compose(0, [1], None, 4, good, good, cap, tab[:-16])
+    with pytest.raises(ValueError, match="pos_dev_out"):
+        P.c2kv_compose_layers(0, [1], None, 4, 0, 0, 1, good, good, cap, tab, torch.zeros(cap - 1, dtype=torch.int32))
