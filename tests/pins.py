@@ -288,6 +288,36 @@ def check_llama3_bytes(o):
                                g["head_dim"][0]) == g["bytes_per_token"][0]
 
 
+def check_structured_attention_on_the_blog_figure(o):
+    """The k=4 figure of section "structured information flow" (12 document
+    tokens, 3 slots), run through the whole extraction attention: with q = 0
+    every score is 0, so each row is the plain mean of the values it sees,
+    and value j = e_j shows exactly which keys.  Slot rows must see the
+    document cells the figure lists and the slots up to themselves; document
+    rows their causal prefix and no slot."""
+    g = read_golden("structured_mask_k4_12tok_3slot.txt")
+    k, n, m = g["k"][0], g["n_doc"][0], g["n_slot"][0]
+    N, d = n + m, 16
+    rng = np.random.default_rng(29)
+    q = np.zeros((N, 2, d), np.uint16)
+    kk = _bits(rng, (N, 1, d))
+    one = o.f64_to_bf16(np.array([1.0]))[0]
+    v = np.zeros((N, 1, d), np.uint16)
+    for j in range(N):
+        v[j, 0, j] = one
+    out = o.masked_extraction_attention(q, kk, v, n, m, k, 1.0e4, mask="structured")
+    for r in range(N):
+        if r < n:
+            seen = set(range(r + 1))
+        else:
+            i = r - n
+            seen = {c - 1 for c in g["slot%d" % (i + 1)]} | set(range(n, r + 1))
+        want = np.zeros(d)
+        want[sorted(seen)] = 1.0 / len(seen)
+        for h in range(2):
+            assert np.allclose(out[r, h], want, atol=1e-12), (r, h)
+
+
 # ----------------------------------------------------- anchor-token ablation
 
 def check_anchor_mask_uniform_scores(o):
@@ -356,5 +386,6 @@ ALL_CHECKS = [
     check_blog_mask, check_extraction_positions, check_bf16_conversion,
     check_rope, check_attention_special_cases, check_gqa_and_causality,
     check_k1_equals_uncompressed, check_llama3_bytes,
+    check_structured_attention_on_the_blog_figure,
     check_anchor_mask_uniform_scores, check_anchor_rows_are_causal_attention,
 ]

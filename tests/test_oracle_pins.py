@@ -90,6 +90,10 @@ def _mask_block_shifted(n_doc, n_slot, k):
     return m
 
 
+def _structured_as_causal(n_doc, n_slot, k):
+    return np.tril(np.ones((n_doc + n_slot,) * 2, bool))
+
+
 def _anchor_docs_causal_over_anchors(n_doc, n_slot):
     m = np.tril(np.ones((n_doc + n_slot,) * 2, bool))
     return m
@@ -143,6 +147,9 @@ MUTATIONS = [
     ("structured_mask", _mask_no_sink, pins.check_blog_mask),
     ("structured_mask", _mask_block_shifted, pins.check_blog_mask),
     ("masked_softmax_attention", _softmax_no_scale, pins.check_attention_special_cases),
+    ("structured_mask", _mask_no_sink, pins.check_structured_attention_on_the_blog_figure),
+    ("structured_mask", _mask_block_shifted, pins.check_structured_attention_on_the_blog_figure),
+    ("structured_mask", _structured_as_causal, pins.check_structured_attention_on_the_blog_figure),
     ("anchor_mask", _anchor_docs_causal_over_anchors, pins.check_anchor_mask_uniform_scores),
     ("anchor_mask", _anchor_docs_causal_over_anchors, pins.check_anchor_rows_are_causal_attention),
     ("anchor_mask", _anchor_docs_see_anchors_only, pins.check_anchor_mask_uniform_scores),
