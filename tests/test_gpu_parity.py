@@ -131,14 +131,16 @@ def test_no_position_realignment_ablation():
     sc.close()
 
 
-def test_layer_pipelined_compose_matches_one_shot():
+@pytest.mark.parametrize("realign", [True, False])
+def test_layer_pipelined_compose_matches_one_shot(realign):
     """Composing layer groups one by one (C2KV_COMPOSE_CONTINUE) with the
     question prefill of each group enqueued in between gives the same caches
-    and outputs, bit for bit, as one compose followed by the prefill."""
+    and outputs, bit for bit, as one compose followed by the prefill; also
+    with the no-re-alignment ablation."""
     g = S.Geometry(8, 16, 4, 128, 5.0e5)
     specs = [(1, 900, 225), (2, 333, 84), (3, 1200, 300)]
     requests = [([3, 1, 2], None), ([2, 3], [1, 0])]
-    sc = Scenario(g, 4, specs, requests, q_len=24, decode_steps=0)
+    sc = Scenario(g, 4, specs, requests, q_len=24, decode_steps=0, realign=realign)
     bt = sc.batch
     rng = np.random.default_rng(5)
     q = to_dev(S.normal_bf16(rng, (g.n_layers, 2, 24, g.n_q_heads, g.head_dim)))
@@ -183,6 +185,50 @@ def test_layer_pipelined_compose_matches_one_shot():
     with pytest.raises(P.C2KVError):
         P.c2kv_compose_layers(sc.store, [3, 1, 2], None, 4, 0, 4, 4, bt.k_caches[0], bt.v_caches[0], bt.cap,
                               bt.rope_tables[0])
+    if not realign:   # a continuation keeps the ablation flag of the composition it continues
+        with pytest.raises(P.C2KVError):
+            P.c2kv_compose_layers(sc.store, [3, 1, 2], None, 4, P.C2KV_COMPOSE_CONTINUE, 2, 4, bt.k_caches[0],
+                                  bt.v_caches[0], bt.cap, bt.rope_tables[0])
+    sc.close()
+
+
+def test_empty_composition_question_only():
+    """A request that composes no document: the table places every row at its
+    own index (L_tot = 0), the question is prefilled over itself alone and
+    the answer decoded after it."""
+    g = S.Geometry(1, 8, 2, 128, 5.0e5)
+    Q, T = 20, 3
+    sc = Scenario(g, 4, [(1, 40, 10)], [([], None)], q_len=Q, decode_steps=T)
+    bt = sc.batch
+    assert bt.n_slots == [0] and bt.l_tot == [0]
+    bt.compose()
+    rng = np.random.default_rng(31)
+    q = S.normal_bf16(rng, (1, Q, 8, 128))
+    kq = S.normal_bf16(rng, (1, Q, 2, 128))
+    vq = S.normal_bf16(rng, (1, Q, 2, 128))
+    qd = S.normal_bf16(rng, (T, 1, 8, 128))
+    kd = S.normal_bf16(rng, (T, 1, 2, 128))
+    vd = S.normal_bf16(rng, (T, 1, 2, 128))
+    pre = torch.empty((1, Q, 8, 128), dtype=torch.bfloat16, device="cuda")
+    bt.prefill(0, to_dev(q), to_dev(kq), to_dev(vq), pre)
+    bt.reset_decode()
+    dec = []
+    for t in range(T):
+        o = torch.empty((1, 8, 128), dtype=torch.bfloat16, device="cuda")
+        bt.decode(0, to_dev(qd[t]), to_dev(kd[t]), to_dev(vd[t]), o)
+        bt.advance()
+        dec.append(o)
+    torch.cuda.synchronize()
+    assert P.c2kv_device_error() == P.C2KV_OK
+    assert np.array_equal(bt.pos[0].cpu().numpy(), np.arange(bt.cap))
+    empty = np.zeros((2, 0, 128), np.uint16)
+    ref_pre, krot = O.attend_new_tokens(q[0], kq[0], vq[0], empty, empty, 0, g.rope_theta)
+    check_attention(pre[0], ref_pre, "question-only prefill")
+    check_keys(to_bits(bt.k_caches[0][0, :, :Q]), krot, "question keys")
+    ref_dec, kc, vc = O.decode_sequence(qd[:, 0], kd[:, 0], vd[:, 0], krot, vq[0].transpose(1, 0, 2), Q,
+                                        g.rope_theta)
+    check_attention(torch.stack(dec)[:, 0], ref_dec, "decode after a question-only prefill")
+    assert np.array_equal(to_bits(bt.v_caches[0][0, :, :Q + T]), vc)
     sc.close()
 
 
@@ -363,7 +409,7 @@ def test_decode_multi_split_long_cache():
     sc.close()
 
 
-@pytest.mark.parametrize("n_doc,n_slot,k", [(12, 3, 4), (200, 50, 4), (257, 17, 16), (40, 40, 1)])
+@pytest.mark.parametrize("n_doc,n_slot,k", [(12, 3, 4), (200, 50, 4), (257, 17, 16), (40, 40, 1), (1, 0, 4)])
 def test_structured_mask_mode(n_doc, n_slot, k):
     g = S.TINY
     rng = np.random.default_rng(n_doc * 131 + n_slot)
