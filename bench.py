@@ -217,6 +217,19 @@ def max_over_ranks(values, world: int, device="cpu"):
     return [float(x) for x in t.tolist()]
 
 
+def init_ranks(backend=None) -> None:
+    """Process group of the replicas (env:// rendezvous), with a bounded
+    timeout (C2KV_RANK_TIMEOUT_S, default 300 s): a rank that dies makes the
+    others' next barrier or timing reduction fail instead of waiting on it."""
+    import datetime
+    import torch
+    import torch.distributed as dist
+    if backend is None:
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+    timeout = datetime.timedelta(seconds=float(os.environ.get("C2KV_RANK_TIMEOUT_S", "300")))
+    dist.init_process_group(backend, timeout=timeout)
+
+
 def replica_tokens(batch: int, decode_steps: int, steps: int, world: int) -> int:
     """Answer tokens all ranks produce in `steps` requests each (weak scaling)."""
     return batch * decode_steps * steps * world
@@ -716,9 +729,7 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = run_oracle_sample(args.workload, args.cpu_budget)
     if world > 1:
-        import torch
-        import torch.distributed as dist
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        init_ranks()
     out = run_ours(args, rank, world)
     if cpu is not None:
         out["cpu_baseline"] = {"value": cpu["tok_s"], "unit": "tok/s", "cores": cpu["cores"],
