@@ -282,6 +282,89 @@ def check_k1_equals_uncompressed(o):
     assert np.array_equal(vcat, raw_v)
 
 
+def check_k1_attention_equals_uncompressed(o):
+    """k=1 (section "C2 tokens": one slot per k tokens, so every token is its
+    own slot): composing the documents, prefilling the question after them and
+    decoding the answer must be exactly the causal attention of the plain,
+    uncompressed token sequence, with token t at position t for every t < L_tot
+    + Q + T (section "positions at concatenation": documents keep their
+    original lengths of positions, the question follows them).  The reference
+    is torch's fp64 scaled_dot_product_attention (a library routine) over
+    keys rotated token by token through complex multiplication at arange
+    positions and rounded to bf16 as the cache stores them; it shares neither
+    the oracle's position bookkeeping nor its attention."""
+    rng = np.random.default_rng(23)
+    hq, hkv, d, theta = 4, 2, 16, 5.0e5
+    lens = [6, 2, 5]
+    ids = [20, 21, 22]
+    order = [1, 2, 0]
+    store = {i: (n, n, _bits(rng, (1, hkv, n, d)), _bits(rng, (1, hkv, n, d))) for i, n in zip(ids, lens)}
+    Q, T = 3, 4
+    q, kn, vn = _bits(rng, (Q + T, hq, d)), _bits(rng, (Q + T, hkv, d)), _bits(rng, (Q + T, hkv, d))
+    # the oracle's path: compose at k=1, the question at L_tot, decode after it
+    _, l_tot, kc, vc = o.compose(store, ids, order, 1, theta)
+    kc, vc = kc[0], vc[0]
+    out_q, kq = o.attend_new_tokens(q[:Q], kn[:Q], vn[:Q], kc, vc, l_tot, theta)
+    kc = np.concatenate([kc, kq], axis=1)
+    vc = np.concatenate([vc, vn[:Q].transpose(1, 0, 2)], axis=1)
+    out_d, _, _ = o.decode_sequence(q[Q:], kn[Q:], vn[Q:], kc, vc, l_tot + Q, theta)
+    got = np.concatenate([out_q, out_d], axis=0)                 # [Q+T][hq][d]
+    # the reference: the token sequence written out, position = index
+    seq = [ids[i] for i in order]
+    k_all = np.concatenate([store[s][2][0] for s in seq] + [kn.transpose(1, 0, 2)], axis=1)
+    v_all = np.concatenate([store[s][3][0] for s in seq] + [vn.transpose(1, 0, 2)], axis=1)
+    n_all = k_all.shape[1]
+    assert n_all == sum(lens) + Q + T
+    inv = np.power(theta, -2.0 * np.arange(d // 2) / d)
+
+    def rot(x, p):   # x [..., n, d] fp64 at positions p[n]
+        z = (x[..., : d // 2] + 1j * x[..., d // 2:]) * np.exp(1j * p[:, None] * inv[None, :])
+        return np.concatenate([z.real, z.imag], axis=-1)
+
+    t_all = np.arange(n_all, dtype=np.float64)
+    kr = o.bf16_to_f64(o.f64_to_bf16(rot(o.bf16_to_f64(k_all), t_all)))   # stored as bf16
+    qr = rot(o.bf16_to_f64(q).transpose(1, 0, 2), t_all[sum(lens):])      # q is not rounded
+    vis = np.arange(n_all)[None, :] <= np.arange(sum(lens), n_all)[:, None]
+    g = hq // hkv
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(qr), torch.from_numpy(np.repeat(kr, g, axis=0)),
+        torch.from_numpy(np.repeat(o.bf16_to_f64(v_all), g, axis=0)),
+        attn_mask=torch.from_numpy(vis)).numpy().transpose(1, 0, 2)
+    assert np.allclose(got, ref, rtol=0, atol=1e-12), np.abs(got - ref).max()
+
+
+def check_ulp_distance(o):
+    """bf16_ulp_distance, the comparator of every re-rotated key, against its
+    definition: the number of steps between two values along the ordered set
+    of distinct finite bf16 values (+0 and -0 are one value).  The ordered set
+    is built here from torch's bf16 -> fp64 widening (a library routine), and
+    hand pairs cover +-0, neighbours, a 2-ulp gap, a binade edge, the sign
+    boundary and the largest finite values."""
+    allbits = np.arange(0x10000, dtype=np.uint32).astype(np.uint16)
+    vals = torch.from_numpy(allbits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    finite = np.isfinite(vals)
+    distinct = np.unique(vals[finite])            # sorted; -0 and +0 compare equal
+    rank = np.full(0x10000, -1, np.int64)
+    rank[finite] = np.searchsorted(distinct, vals[finite])
+    hand = [(0x3F80, 0x3F80, 0), (0x3F80, 0x3F81, 1), (0x3F80, 0x3F82, 2), (0x3F7F, 0x3F80, 1),
+            (0x0000, 0x8000, 0), (0x0001, 0x8001, 2), (0x0001, 0x0000, 1), (0xBF80, 0xBF81, 1),
+            (0x3F80, 0x4000, 128), (0x7F7F, 0x7F7E, 1), (0x7F7F, 0xFF7F, int(rank[0x7F7F] - rank[0xFF7F]))]
+    for a, b, want in hand:
+        assert int(rank[b] - rank[a]) in (want, -want), (hex(a), hex(b))
+        got = o.bf16_ulp_distance(np.array([a], np.uint16), np.array([b], np.uint16))
+        assert int(got[0]) == want, (hex(a), hex(b), int(got[0]), want)
+    rng = np.random.default_rng(31)
+    fin = allbits[finite]
+    a = rng.choice(fin, 20000)
+    near = np.clip(rank[a] + rng.integers(-3, 4, a.size), 0, distinct.size - 1)
+    # b: half random finite values, half within 3 steps of a (a bit pattern of that value)
+    first_of = np.full(distinct.size, 0, np.int64)
+    first_of[rank[fin][::-1]] = fin[::-1]
+    b = np.where(rng.random(a.size) < 0.5, rng.choice(fin, a.size), first_of[near]).astype(np.uint16)
+    want = np.abs(rank[a] - rank[b])
+    assert np.array_equal(o.bf16_ulp_distance(a, b), want)
+
+
 def check_llama3_bytes(o):
     g = read_golden("kv_bytes_llama3.txt")
     assert o.kv_bytes_per_slot(g["n_layers"][0], g["n_kv_heads"][0],
@@ -385,7 +468,8 @@ ALL_CHECKS = [
     check_blog_positions, check_slot_counts, check_positions_bruteforce, check_no_realign_positions,
     check_blog_mask, check_extraction_positions, check_bf16_conversion,
     check_rope, check_attention_special_cases, check_gqa_and_causality,
-    check_k1_equals_uncompressed, check_llama3_bytes,
+    check_k1_equals_uncompressed, check_k1_attention_equals_uncompressed, check_ulp_distance,
+    check_llama3_bytes,
     check_structured_attention_on_the_blog_figure,
     check_anchor_mask_uniform_scores, check_anchor_rows_are_causal_attention,
 ]

@@ -136,6 +136,31 @@ def _bf16_double_round(x):
     return torch.from_numpy(x32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
 
 
+def _attend_question_shifted(q_pre, k_new_pre, v_new, k_cache, v_cache, start_pos, theta):
+    """The new tokens placed one position late (start_pos + 1 + i)."""
+    return _REAL_ATTEND(q_pre, k_new_pre, v_new, k_cache, v_cache, start_pos + 1, theta)
+
+
+_REAL_ATTEND = O.attend_new_tokens
+
+
+def _ulp_always_zero(a_bits, b_bits):
+    return np.zeros(np.broadcast(np.asarray(a_bits), np.asarray(b_bits)).shape, np.int32)
+
+
+def _ulp_sign_magnitude_ignored(a_bits, b_bits):
+    """Bit patterns subtracted as plain integers (wrong across the sign)."""
+    return np.abs(np.asarray(a_bits, np.int32) - np.asarray(b_bits, np.int32))
+
+
+def _ulp_off_by_one_across_zero(a_bits, b_bits):
+    """-0 and +0 treated as two values."""
+    def ordered(bits):
+        v = np.asarray(bits, dtype=np.uint16).astype(np.int32)
+        return np.where(v & 0x8000, 0x7FFF - v, v)
+    return np.abs(ordered(a_bits) - ordered(b_bits))
+
+
 MUTATIONS = [
     ("composed_positions", _positions_no_minus_one, pins.check_blog_positions),
     ("composed_positions", _positions_offset_by_slots, pins.check_blog_positions),
@@ -157,6 +182,10 @@ MUTATIONS = [
     ("anchor_mask", _anchor_anchors_see_all_anchors, pins.check_anchor_rows_are_causal_attention),
     ("f64_to_bf16", _bf16_truncate, pins.check_bf16_conversion),
     ("f64_to_bf16", _bf16_double_round, pins.check_bf16_conversion),
+    ("attend_new_tokens", _attend_question_shifted, pins.check_k1_attention_equals_uncompressed),
+    ("bf16_ulp_distance", _ulp_always_zero, pins.check_ulp_distance),
+    ("bf16_ulp_distance", _ulp_sign_magnitude_ignored, pins.check_ulp_distance),
+    ("bf16_ulp_distance", _ulp_off_by_one_across_zero, pins.check_ulp_distance),
 ]
 
 
