@@ -27,9 +27,10 @@ def test_workload_config_names_the_workload_and_its_sizes(name):
 
 
 def test_default_workload_sizes():
-    """8 documents of 4000 tokens at k = 4: 8000 slots of 32 000 tokens."""
+    """The largest workload that fits one GPU: 4 sequences, each 32 documents
+    of 4096 tokens at k = 4, i.e. 32 768 slots of 131 072 tokens."""
     c = bench.workload_config(S.WORKLOADS[bench.DEFAULT_WORKLOAD], 1)
-    assert c["composed_slots"] == [8000] and c["original_tokens"] == [32000]
+    assert c["composed_slots"] == [32768] * 4 and c["original_tokens"] == [131072] * 4
 
 
 def test_traffic_record_applies_only_to_the_captured_sources(tmp_path, monkeypatch):
@@ -74,5 +75,7 @@ def test_reference_arm_prints_the_contract_line():
     assert d["value"] > 0 and d["steps"] == 1 and d["warmup"] == 1 and d["higher_is_better"] is True
     assert d["config"]["workload"] == "tiny"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
-    assert d["cpu_baseline"]["cores"] >= 1 and d["cpu_baseline"]["sample"]
+    assert d["cpu_baseline"]["cores"] == len(os.sched_getaffinity(0)) and d["cpu_baseline"]["sample"]
+    # the step time is the work the step ran, not the extrapolated request
+    assert 0 < d["ms_per_step"] < 60e3 and d["extrapolated_request_s"] > 0
     assert d["e2e"] == {"value": d["value"], "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
