@@ -16,6 +16,7 @@
 #include <cudaTypedefs.h>
 
 #include "c2kv_internal.h"
+#include "decode_plan.h"
 
 using namespace c2kv;
 
@@ -163,14 +164,40 @@ c2kv_status plan_impl(int32_t n_docs, const int32_t* n_tokens, const int32_t* n_
 
 // Scratch of one attention call: split-K partials and arrival counters, and
 // for multi-token calls the rotated q in the tensor-core tile layout.
+// With tc set (one token per sequence, head_dim 128: the tensor-core decode),
+// the partials are two slots per CTA of the launch (one CTA per SM), not
+// per split.
 struct AttnWs {
   int n_tb, num_splits, split_keys;
-  size_t counters_off, ml_off, o_off, qrot_off, total;
+  bool tc;
+  size_t counters_off, counters_bytes, ml_off, o_off, qrot_off, total;
 };
+
+// The tensor-core decode serves one token per sequence at head_dim 128, with
+// one CTA per SM (at most kDecMaxCtas).
+bool use_decode_tc(const c2kv_geometry* g, int t_len) { return t_len == 1 && g->head_dim == 128; }
+int decode_tc_ctas(int num_sms) { return std::max(1, std::min(num_sms, kDecMaxCtas)); }
 
 AttnWs attn_workspace(const c2kv_geometry* g, int batch, int t_len, int max_keys, int num_sms) {
   AttnWs w{};
   const int grp = g->n_q_heads / g->n_kv_heads;
+  if (use_decode_tc(g, t_len)) {
+    w.tc = true;
+    w.n_tb = 1;
+    w.num_splits = 1;
+    w.split_keys = max_keys;
+    w.counters_off = 0;
+    w.counters_bytes = align256((size_t)kMaxBatch * g->n_kv_heads * sizeof(int32_t));
+    size_t off = w.counters_bytes;
+    const size_t slots = 2 * (size_t)decode_tc_ctas(num_sms);
+    w.ml_off = off;
+    off += align256(slots * grp * 2 * sizeof(float));
+    w.o_off = off;
+    off += align256(slots * grp * g->head_dim * sizeof(float));
+    w.qrot_off = off;
+    w.total = off;
+    return w;
+  }
   if (t_len == 1) {
     w.n_tb = 1;
     attn_plan_splits(batch * g->n_kv_heads, max_keys, num_sms, grp, &w.num_splits, &w.split_keys);
@@ -188,7 +215,8 @@ AttnWs attn_workspace(const c2kv_geometry* g, int batch, int t_len, int max_keys
   // overwrites counters another call relies on being zero.
   size_t off = 0;
   w.counters_off = 0;
-  off += align256((size_t)kMaxBatch * g->n_kv_heads * sizeof(int32_t));
+  w.counters_bytes = align256((size_t)kMaxBatch * g->n_kv_heads * sizeof(int32_t));
+  off += w.counters_bytes;
   if (w.num_splits > 1) {
     w.ml_off = off;
     off += align256(rows * 2 * sizeof(float));
@@ -287,6 +315,58 @@ bool take_injected_timeout() {
   return n > 0;
 }
 
+// One token per sequence at head_dim 128, on the tensor cores: kb/vb are the
+// layer bases [Hkv][cap][d] of each sequence's cache.
+c2kv_status run_decode_tc(const c2kv_geometry* g, int batch, const __nv_bfloat16* const* kb,
+                          const __nv_bfloat16* const* vb, const CosSin2* const* tabs, const int32_t* n_cached_h,
+                          const int32_t* n_cached_d, int cap, int max_keys, const void* q, void* out,
+                          void* workspace, size_t workspace_bytes, cudaStream_t st, const void* k_new,
+                          const void* v_new, bool overlap) {
+  unsigned* err = nullptr;
+  int sms = 0;
+  c2kv_status s = device_state(&err, &sms);
+  if (s != C2KV_OK) return s;
+  const AttnWs w = attn_workspace(g, batch, 1, max_keys, sms);
+  if (workspace == nullptr || workspace_bytes < w.total)
+    return fail(C2KV_EINVAL, "workspace too small: need " + std::to_string(w.total) + " bytes");
+  static DecodeTcParams p;   // large (tensor maps); guarded by the mutex below
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  std::memset(&p, 0, sizeof(p));
+  const int D = g->head_dim;
+  for (int b = 0; b < batch; ++b) {
+    const uint64_t stride2 = (uint64_t)cap * D * 2;
+    s = encode_map(&p.tm_k[b], kb[b], 3, D, (uint64_t)cap, g->n_kv_heads, stride2, 128);
+    if (s != C2KV_OK) return s;
+    s = encode_map(&p.tm_v[b], vb[b], 3, D, (uint64_t)cap, g->n_kv_heads, stride2, 128);
+    if (s != C2KV_OK) return s;
+    p.k_base[b] = const_cast<__nv_bfloat16*>(kb[b]);
+    p.v_base[b] = const_cast<__nv_bfloat16*>(vb[b]);
+    p.tab[b] = tabs[b];
+    p.n_cached_h[b] = n_cached_h ? n_cached_h[b] : 0;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.n_cached_d = n_cached_d;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  p.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  p.part_o = reinterpret_cast<float*>(ws + w.o_off);
+  p.part_ml = reinterpret_cast<float*>(ws + w.ml_off);
+  p.counters = reinterpret_cast<int32_t*>(ws + w.counters_off);
+  p.err = err;
+  p.batch = batch;
+  p.n_q = g->n_q_heads;
+  p.n_kv = g->n_kv_heads;
+  p.cap = cap;
+  p.max_keys = max_keys;
+  p.fuse_append = k_new != nullptr ? 1 : 0;
+  p.inject_timeout = take_injected_timeout() ? 1 : 0;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+  C2KV_CUDA(launch_decode_tc(p, g->n_q_heads / g->n_kv_heads, decode_tc_ctas(sms), overlap, st));
+  return C2KV_OK;
+}
+
 // tabs[b]: per-row cos/sin table of sequence b (token t at row n_cached + t).
 c2kv_status run_attention(const c2kv_geometry* g, int batch, const __nv_bfloat16* const* kb,
                           const __nv_bfloat16* const* vb, const CosSin2* const* tabs, const int32_t* n_cached_h,
@@ -294,6 +374,9 @@ c2kv_status run_attention(const c2kv_geometry* g, int batch, const __nv_bfloat16
                           int kblk, const void* q, void* out, void* workspace, size_t workspace_bytes,
                           cudaStream_t st, const void* fused_k_new = nullptr, const void* fused_v_new = nullptr,
                           bool overlap = false) {
+  if (use_decode_tc(g, t_len))   // any mask is causal for a one-token sequence
+    return run_decode_tc(g, batch, kb, vb, tabs, n_cached_h, n_cached_d, cap, max_keys, q, out, workspace,
+                         workspace_bytes, st, fused_k_new, fused_v_new, overlap);
   unsigned* err = nullptr;
   int sms = 0;
   c2kv_status s = device_state(&err, &sms);
@@ -1072,7 +1155,7 @@ extern "C" c2kv_status c2kv_attend_decode_noalloc(const c2kv_geometry* geom, int
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // The array keeps whatever the previous call left in it; the arrival
   // counters must start at zero, the partial results need no clearing.
-  if (w.num_splits > 1) C2KV_CUDA(cudaMemsetAsync(scratch + w.counters_off, 0, w.ml_off - w.counters_off, st));
+  if (w.tc || w.num_splits > 1) C2KV_CUDA(cudaMemsetAsync(scratch + w.counters_off, 0, w.counters_bytes, st));
   return c2kv_attend_decode(geom, layer, batch, k_caches, v_caches, rope_tables, cap, n_cached_dev, max_keys, q,
                             k_new, v_new, out, scratch, kNoallocScratchBytes, 0, stream);
 }

@@ -325,7 +325,33 @@ struct AttnParams {
   float scale_log2;
 };
 
+// Decode on the tensor cores (head_dim 128): one launch per layer, the key
+// tiles of all (sequence, kv head) units split evenly over one CTA per SM
+// (decode_plan.h).  tm_k / tm_v: per sequence, a 3-D map {d, cap, kv heads}
+// of this layer's cache, 64 x 128 x 1 boxes, 128-byte swizzle.
+struct DecodeTcParams {
+  CUtensorMap tm_k[kMaxBatch];
+  CUtensorMap tm_v[kMaxBatch];
+  __nv_bfloat16* k_base[kMaxBatch];   // layer base [Hkv][cap][d] (the fused append's rows)
+  __nv_bfloat16* v_base[kMaxBatch];
+  const CosSin2* tab[kMaxBatch];      // per-row cos/sin table of each sequence
+  int32_t n_cached_h[kMaxBatch];      // host lengths (when n_cached_d is null)
+  const int32_t* n_cached_d;          // device lengths
+  const __nv_bfloat16* q;             // [B][Hq][d]
+  __nv_bfloat16* out;                 // [B][Hq][d]
+  const __nv_bfloat16* k_new;         // [B][Hkv][d] (fused append) or null
+  const __nv_bfloat16* v_new;
+  float* part_o;                      // [2 * CTAs][G][d] partial O of shared units
+  float* part_ml;                     // [2 * CTAs][G][2] their (m, l)
+  int32_t* counters;                  // [B * Hkv] tiles merged so far per unit
+  unsigned* err;
+  int32_t batch, n_q, n_kv, cap, max_keys;
+  int32_t fuse_append, inject_timeout;
+  float scale_log2;
+};
+
 // Launchers (return cudaGetLastError()).
+cudaError_t launch_decode_tc(const DecodeTcParams& p, int group, int ctas, bool overlap, cudaStream_t st);
 cudaError_t launch_rerope(const RopeParams& p, int head_dim, cudaStream_t st);
 cudaError_t launch_rope_table(const TableParams& p, cudaStream_t st);
 cudaError_t launch_append(const AppendParams& p, int head_dim, int batch, cudaStream_t st);
