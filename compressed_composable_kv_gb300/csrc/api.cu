@@ -363,7 +363,25 @@ c2kv_status run_decode_tc(const c2kv_geometry* g, int batch, const __nv_bfloat16
   p.fuse_append = k_new != nullptr ? 1 : 0;
   p.inject_timeout = take_injected_timeout() ? 1 : 0;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
-  C2KV_CUDA(launch_decode_tc(p, g->n_q_heads / g->n_kv_heads, decode_tc_ctas(sms), overlap, st));
+  // Few tiles per SM (short caches, few sequences): the launch is latency-
+  // bound and the units' partial merges dominate, so launch one thread-block
+  // cluster per unit when that many clusters fit at once; they merge in
+  // distributed shared memory.
+  const int grp = g->n_q_heads / g->n_kv_heads;
+  const int units = batch * g->n_kv_heads;
+  const int ctas_max = decode_tc_ctas(sms);
+  const int64_t tiles = (int64_t)units * ((max_keys + kDecKeyTile - 1) / kDecKeyTile);
+  int ctas = ctas_max;
+  if (tiles < (int64_t)kDecClusterTilesPerSm * ctas_max) {
+    for (int cs = std::min(16, ctas_max / units); cs >= 2; --cs) {
+      if (decode_tc_active_clusters(grp, cs) >= units) {
+        p.cluster = cs;
+        ctas = units * cs;
+        break;
+      }
+    }
+  }
+  C2KV_CUDA(launch_decode_tc(p, grp, ctas, overlap, st));
   return C2KV_OK;
 }
 

@@ -347,11 +347,18 @@ struct DecodeTcParams {
   unsigned* err;
   int32_t batch, n_q, n_kv, cap, max_keys;
   int32_t fuse_append, inject_timeout;
+  // > 0: the launch is batch * n_kv thread-block clusters of `cluster` CTAs;
+  // when every sequence has the same number of tiles (at least `cluster`),
+  // cluster u holds exactly unit u and merges it in distributed shared memory
+  int32_t cluster;
   float scale_log2;
 };
 
 // Launchers (return cudaGetLastError()).
 cudaError_t launch_decode_tc(const DecodeTcParams& p, int group, int ctas, bool overlap, cudaStream_t st);
+// Clusters of `cs` CTAs of the tensor-core decode that fit the device at once
+// (0 if unknown).
+int decode_tc_active_clusters(int group, int cs);
 cudaError_t launch_rerope(const RopeParams& p, int head_dim, cudaStream_t st);
 cudaError_t launch_rope_table(const TableParams& p, cudaStream_t st);
 cudaError_t launch_append(const AppendParams& p, int head_dim, int batch, cudaStream_t st);

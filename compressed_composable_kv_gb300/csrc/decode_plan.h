@@ -17,6 +17,7 @@ namespace c2kv {
 constexpr int kDecKeyTile = 128;       // keys per tile
 constexpr int kDecMaxSeqs = 16;        // sequences per launch
 constexpr int kDecMaxCtas = 256;       // CTAs per launch (one per SM)
+constexpr int kDecClusterTilesPerSm = 8;   // below this many tiles per SM, prefer the cluster merge
 
 struct DecodeMap {
   int32_t nseq, hkv, ctas;

@@ -38,9 +38,13 @@
 // masked in the softmax.
 #include <float.h>
 
+#include <cooperative_groups.h>
+
 #include "c2kv_internal.h"
 #include "decode_plan.h"
 #include "tcgen05.h"
+
+namespace cg = cooperative_groups;
 
 namespace c2kv {
 
@@ -67,7 +71,8 @@ struct DtCfg {
   static constexpr int OFF_MAP = OFF_RED + 2 * 4 * 8 * 4;
   static constexpr int OFF_NC = OFF_MAP + (int)((sizeof(DecodeMap) + 15) / 16 * 16);   // [16] lengths
   static constexpr int OFF_SLOTS = OFF_NC + kDecMaxSeqs * 4;       // merge: slot of each contributor
-  static constexpr int OFF_BAR = OFF_SLOTS + kDecMaxCtas * 4;
+  static constexpr int OFF_STML = OFF_SLOTS + kDecMaxCtas * 4;      // cluster merge: staged m [8], l [8]
+  static constexpr int OFF_BAR = OFF_STML + 16 * 4;
   static constexpr int N_BAR = 2 * DT_STAGES + 2 * 8 + 5;
   static constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;   // + slack for 1024-byte alignment
@@ -156,6 +161,8 @@ __global__ void __launch_bounds__(DT_THREADS, 1) decode_tc_kernel(const __grid_c
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
+  volatile int* aligned_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 24);
+  float* stml = reinterpret_cast<float*>(smem + C::OFF_STML);
   DecodeMap& M = *reinterpret_cast<DecodeMap*>(smem + C::OFF_MAP);
   int32_t* ncs = reinterpret_cast<int32_t*>(smem + C::OFF_NC);
   float* red = reinterpret_cast<float*>(smem + C::OFF_RED);   // [2][4][8]
@@ -184,6 +191,16 @@ __global__ void __launch_bounds__(DT_THREADS, 1) decode_tc_kernel(const __grid_c
     }
     if (bad && cta == 0) atomicOr(p.err, kErrLength);
     decode_map_build(M, keys, p.batch, p.n_kv, (int)gridDim.x);
+    // One cluster per unit (the cluster merge) when every sequence has the
+    // same number of tiles, at least one per CTA of the cluster.
+    bool al = p.cluster > 0 && !bad && M.tb[0] >= p.cluster &&
+              (int)gridDim.x == p.batch * p.n_kv * p.cluster;
+    for (int b = 1; b < p.batch; ++b) al = al && M.tb[b] == M.tb[0];
+    *aligned_flag = al ? 1 : 0;
+    for (int g = 0; g < 8; ++g) {
+      stml[g] = -INFINITY;   // staged (m, l) of a CTA that never finishes its segment
+      stml[8 + g] = 0.f;
+    }
     for (int s = 0; s < DT_STAGES; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
@@ -206,17 +223,11 @@ __global__ void __launch_bounds__(DT_THREADS, 1) decode_tc_kernel(const __grid_c
     *abort_flag = 0;
     fence_barrier_init();
   }
-  __syncthreads();
-  const int64_t x0 = decode_cta_first(M, cta), x1 = decode_cta_first(M, cta + 1);
-  const int ntiles = (int)(x1 - x0);
-  if (ntiles == 0) return;   // uniform over the CTA
-
   uint8_t* sKV = smem + C::OFF_KV;
   uint8_t* sQ = smem + C::OFF_Q;
   uint8_t* sP = smem + C::OFF_P;
   auto stage_k = [&](int s) { return sKV + s * C::STAGE; };
   auto stage_v = [&](int s) { return sKV + s * C::STAGE + C::KV_BYTES; };
-
   if (warp == 4) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr((const void*)tmem_slot)),
@@ -234,6 +245,14 @@ __global__ void __launch_bounds__(DT_THREADS, 1) decode_tc_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int64_t x0 = decode_cta_first(M, cta), x1 = decode_cta_first(M, cta + 1);
+  const int ntiles = (int)(x1 - x0);
+  if (ntiles == 0) {   // uniform over the CTA (never in a cluster-merged launch)
+    if (warp == 4)
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");
+    return;
+  }
+  const bool aligned = *aligned_flag != 0;
   int issued = 0;   // the TMA thread's count of tiles requested
 
   if (warp == 4) {
@@ -310,6 +329,23 @@ __global__ void __launch_bounds__(DT_THREADS, 1) decode_tc_kernel(const __grid_c
   } else if (warp == 6) {
     // ---------------- rotated q of each segment, the new key of each unit the
     // CTA finishes
+    // The first segment's cos/sin (the table is not written by the previous
+    // kernel) are loaded before waiting for it; q and the new key after.
+    constexpr int kItems = (G * 8 + 31) / 32;   // 8-pair items of q per lane
+    DtSeg cur = seg_at(M, x0, x1, 0);
+    float2 cs0[kItems][8];
+    {
+      const CosSin2* trow = p.tab[cur.b] + (size_t)ncs[cur.b] * (DT_D / 2);
+#pragma unroll
+      for (int it = 0; it < kItems; ++it) {
+        const int item = lane + 32 * it;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const CosSin2 t = item < G * 8 ? trow[(item & 7) * 8 + e] : CosSin2{0.f, 0.f, 0.f, 0.f};
+          cs0[it][e] = make_float2(t.ch, t.sh);
+        }
+      }
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     auto prep_q = [&](int i, const DtSeg& sg) -> bool {
@@ -318,7 +354,10 @@ __global__ void __launch_bounds__(DT_THREADS, 1) decode_tc_kernel(const __grid_c
       const int n = ncs[sg.b];
       const CosSin2* trow = p.tab[sg.b] + (size_t)n * (DT_D / 2);
       uint8_t* qb = sQ + (i & 1) * C::QP_BYTES;
-      for (int item = lane; item < G * 8; item += 32) {
+#pragma unroll
+      for (int it = 0; it < kItems; ++it) {
+        const int item = lane + 32 * it;
+        if (item >= G * 8) break;
         const int g = item >> 3, c = item & 7;   // pairs f = 8c .. 8c+7 of head g
         const uint4* row = reinterpret_cast<const uint4*>(p.q + ((size_t)sg.b * p.n_q + sg.h * G + g) * DT_D);
         float x[8], y[8];
@@ -327,9 +366,15 @@ __global__ void __launch_bounds__(DT_THREADS, 1) decode_tc_kernel(const __grid_c
         float h0[8], l0[8], h1[8], l1[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const CosSin2 t = trow[c * 8 + e];
-          const float a = (x[e] * t.ch - y[e] * t.sh) * p.scale_log2;
-          const float b = (y[e] * t.ch + x[e] * t.sh) * p.scale_log2;
+          float2 t;
+          if (i == 0) {
+            t = cs0[it][e];
+          } else {
+            const CosSin2 tt = trow[c * 8 + e];
+            t = make_float2(tt.ch, tt.sh);
+          }
+          const float a = (x[e] * t.x - y[e] * t.y) * p.scale_log2;
+          const float b = (y[e] * t.x + x[e] * t.y) * p.scale_log2;
           h0[e] = __bfloat162float(__float2bfloat16_rn(a));
           l0[e] = a - h0[e];
           h1[e] = __bfloat162float(__float2bfloat16_rn(b));
@@ -392,7 +437,6 @@ __global__ void __launch_bounds__(DT_THREADS, 1) decode_tc_kernel(const __grid_c
       if (lane == 0) mbar_arrive(fix_bar);
       return true;
     };
-    DtSeg cur = seg_at(M, x0, x1, 0);
     bool ok = prep_q(0, cur);
     for (int i = 0; ok; ++i) {
       const bool more = cur.j0 + cur.n < ntiles;
@@ -536,6 +580,19 @@ __global__ void __launch_bounds__(DT_THREADS, 1) decode_tc_kernel(const __grid_c
 #pragma unroll
         for (int g = 0; g < G; ++g)
           p.out[((size_t)sg.b * p.n_q + sg.h * G + g) * DT_D + tid] = __float2bfloat16_rn(o_acc[g] / L[g]);
+      } else if (ok && aligned) {
+        // the cluster merges the unit after the teardown: stage this CTA's
+        // partial in shared memory (the P^T buffers are free: every PV has
+        // completed)
+        float* st_o = reinterpret_cast<float*>(sP);   // [G][d]
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          st_o[g * DT_D + tid] = o_acc[g];
+          if (tid == g) {
+            stml[g] = m_ref[g];
+            stml[8 + g] = L[g];
+          }
+        }
       } else if (ok) {
         const int slot = 2 * cta + (i == 0 ? 0 : 1);
 #pragma unroll
@@ -621,10 +678,10 @@ __global__ void __launch_bounds__(DT_THREADS, 1) decode_tc_kernel(const __grid_c
       if (sg.j0 + sg.n >= ntiles) break;
       sg = seg_at(M, x0, x1, sg.j0 + sg.n);
     }
-    if (!ok && tid == 0) {
+    if (!ok && tid == 0 && !aligned) {
       // The CTA gave up: still add the tiles of its remaining shared units to
       // their counters (their outputs are undefined), so every counter is back
-      // at zero when the launch ends.
+      // at zero when the launch ends.  (A cluster-merged launch uses none.)
       DtSeg q = seg_at(M, x0, x1, 0);
       for (int k = 0;; ++k) {
         const bool whole_q = q.t0 == 0 && q.n == M.tb[q.b];
@@ -651,12 +708,53 @@ __global__ void __launch_bounds__(DT_THREADS, 1) decode_tc_kernel(const __grid_c
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");
   }
+  if (aligned) {
+    // ---------------- cluster merge: the cluster is the unit's CTAs; CTA r
+    // writes its share of the G x d outputs from every CTA's staged partial.
+    // Every CTA reaches both cluster barriers on every path (all waits above
+    // are bounded; a CTA that gave up stages m = -inf and adds nothing), and
+    // none leaves before its peers' reads of its shared memory are done.
+    cg::cluster_group cl = cg::this_cluster();
+    cl.sync();
+    const int CS = p.cluster;
+    const int r = (int)cl.block_rank();
+    const int unit = cta / CS;
+    const int b = unit / p.n_kv, h = unit % p.n_kv;
+    const int per = (G * DT_D + CS - 1) / CS;
+    const float* st_o = reinterpret_cast<const float*>(sP);
+    for (int e = r * per + tid; e < min(G * DT_D, (r + 1) * per); e += DT_THREADS) {
+      const int g = e / DT_D, d = e % DT_D;
+      float mx = -INFINITY;
+      for (int sp = 0; sp < CS; ++sp) mx = fmaxf(mx, cl.map_shared_rank(stml, sp)[g]);
+      float lt = 0.f, ot = 0.f;
+      for (int sp = 0; sp < CS; ++sp) {
+        const float ms = cl.map_shared_rank(stml, sp)[g];
+        const float w = ms == -INFINITY ? 0.f : exp2f(ms - mx);
+        lt = fmaf(w, cl.map_shared_rank(stml, sp)[8 + g], lt);
+        ot = fmaf(w, cl.map_shared_rank(st_o, sp)[g * DT_D + d], ot);
+      }
+      p.out[((size_t)b * p.n_q + h * G + g) * DT_D + d] = __float2bfloat16_rn(ot / lt);
+    }
+    cl.sync();
+  }
 }
 
 template <int G>
 KernelSetup& dtc_setup() {
   static KernelSetup s;
   return s;
+}
+
+// Sets the kernel's attributes on device `dev` once (caller holds s.mu).
+template <int G>
+cudaError_t configure_dtc(KernelSetup& s, int dev) {
+  if (s.state[dev] == 0) {
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, DtCfg::SMEM);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_tc_kernel<G>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) cudaGetLastError();
+    s.state[dev] = e == cudaSuccess ? 1 : -(int)e;
+  }
+  return s.state[dev] == 1 ? cudaSuccess : (cudaError_t)(-s.state[dev]);
 }
 
 template <int G>
@@ -666,24 +764,26 @@ cudaError_t launch_dtc(const DecodeTcParams& p, int ctas, bool overlap, cudaStre
     const int dev = setup_device();
     if (dev < 0) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lk(s.mu);
-    if (s.state[dev] == 0) {
-      const cudaError_t e =
-          cudaFuncSetAttribute(decode_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, DtCfg::SMEM);
-      if (e != cudaSuccess) cudaGetLastError();
-      s.state[dev] = e == cudaSuccess ? 1 : -(int)e;
-    }
-    if (s.state[dev] != 1) return (cudaError_t)(-s.state[dev]);
+    const cudaError_t e = configure_dtc<G>(s, dev);
+    if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);
   cfg.blockDim = dim3(DT_THREADS);
   cfg.dynamicSmemBytes = DtCfg::SMEM;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   int na = 0;
   if (overlap) {
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (p.cluster > 0) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = p.cluster;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
     ++na;
   }
   cfg.attrs = attr;
@@ -691,7 +791,49 @@ cudaError_t launch_dtc(const DecodeTcParams& p, int ctas, bool overlap, cudaStre
   return cudaLaunchKernelEx(&cfg, decode_tc_kernel<G>, p);
 }
 
+template <int G>
+int dtc_active_clusters(int cs) {
+  if (cs < 2 || cs > 16) return 0;
+  KernelSetup& s = dtc_setup<G>();
+  const int dev = setup_device();
+  if (dev < 0) return 0;
+  std::lock_guard<std::mutex> lk(s.mu);
+  if (configure_dtc<G>(s, dev) != cudaSuccess) return 0;
+  int* cache = s.clusters[dev];
+  if (cache[cs] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs);
+    cfg.blockDim = dim3(DT_THREADS);
+    cfg.dynamicSmemBytes = DtCfg::SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel<G>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    cache[cs] = n > 0 ? n : -1;
+  }
+  return cache[cs] > 0 ? cache[cs] : 0;
+}
+
 }  // namespace
+
+int decode_tc_active_clusters(int group, int cs) {
+  switch (group) {
+    case 1: return dtc_active_clusters<1>(cs);
+    case 2: return dtc_active_clusters<2>(cs);
+    case 4: return dtc_active_clusters<4>(cs);
+    case 5: return dtc_active_clusters<5>(cs);
+    case 8: return dtc_active_clusters<8>(cs);
+    default: return 0;
+  }
+}
 
 cudaError_t launch_decode_tc(const DecodeTcParams& p, int group, int ctas, bool overlap, cudaStream_t st) {
   switch (group) {
