@@ -1158,6 +1158,10 @@ extern "C" c2kv_status c2kv_attend_decode_noalloc(const c2kv_geometry* geom, int
   if (!n_cached_dev || !rope_tables) return fail(C2KV_EINVAL, "n_cached_dev / rope_tables is null");
   if (max_keys < 1 || max_keys > cap) return fail(C2KV_EINVAL, "max_keys must be in [1, cap]");
   if (!q || !k_new || !v_new || !out) return fail(C2KV_EINVAL, "null tensor pointer");
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new))
+    return fail(C2KV_EINVAL, "q / k_new / v_new must be 16-byte aligned");
+  for (int b = 0; b < batch; ++b)
+    if (rope_tables[b] == nullptr || !aligned16(rope_tables[b])) return fail(C2KV_EINVAL, "bad rope table pointer");
   int sms = 0;
   s = device_state(nullptr, &sms);
   if (s != C2KV_OK) return s;

@@ -43,11 +43,15 @@ class Scenario:
     """Documents, store and per-request device state of one test workload."""
 
     def __init__(self, geom, k, doc_specs, requests, q_len, decode_steps, seed=0xC2C0, layers=None,
-                 cap_multiple=32, realign=True):
+                 cap_multiple=32, realign=True, mutate=None):
+        """mutate(docs): edits the drawn documents before they are stored
+        (planted keys); the oracle reads the same edited arrays."""
         self.geom, self.k, self.seed, self.realign = geom, k, seed, realign
         self.docs = {}
         for doc_id, n_tok, n_slot in doc_specs:
             self.docs[doc_id] = S.make_document(geom, doc_id, n_tok, k, seed, n_slots=n_slot, layers=layers)
+        if mutate is not None:
+            mutate(self.docs)
         pool = sum(2 * d.k_pre.nbytes + 1024 for d in self.docs.values()) + (1 << 20)
         self.store = P.c2kv_store_create(geom, pool)
         ids = list(self.docs)
@@ -64,3 +68,79 @@ class Scenario:
     def close(self):
         torch.cuda.synchronize()
         P.c2kv_store_destroy(self.store)
+
+
+def upload(inputs: S.StepInputs):
+    return {name: to_dev(getattr(inputs, name)) for name in
+            ("q_pre", "kq_pre", "vq", "qd_pre", "kd_pre", "vd")}
+
+
+def run_all(sc: Scenario, dev):
+    """Compose, prefill every layer, decode every step (the bench's launch
+    configuration, without graphs).  Returns the output tensors."""
+    bt = sc.batch
+    L = sc.geom.n_layers
+    bt.compose()
+    pre = []
+    if bt.q_len:
+        for l in range(L):
+            out = torch.empty_like(dev["q_pre"][l])
+            bt.prefill(l, dev["q_pre"][l], dev["kq_pre"][l], dev["vq"][l], out)
+            pre.append(out)
+    bt.reset_decode()
+    dec = []
+    for t in range(bt.decode_steps):
+        row = []
+        for l in range(L):
+            out = torch.empty_like(dev["qd_pre"][t, l])
+            bt.decode(l, dev["qd_pre"][t, l], dev["kd_pre"][t, l], dev["vd"][t, l], out)
+            row.append(out)
+        bt.advance()
+        dec.append(row)
+    torch.cuda.synchronize()
+    assert P.c2kv_device_error() == P.C2KV_OK
+    return pre, dec
+
+
+def check_request(sc: Scenario, inputs: S.StepInputs, pre, dec, b: int, layers, steps):
+    bt = sc.batch
+    g = sc.geom
+    req = sc.reqs[b]
+    st = sc.oracle_store()
+    N, lt, Q = bt.n_slots[b], bt.l_tot[b], bt.q_len
+    seq = O.composed_order(req.doc_ids, req.order)
+    pos_ref, lt_ref = O.composed_positions([sc.docs[d].n_tokens for d in seq],
+                                           [sc.docs[d].n_slots for d in seq], sc.k, sc.realign)
+    assert lt_ref == lt
+    assert np.array_equal(bt.pos[b][:N].cpu().numpy(), pos_ref)
+    kc = bt.k_caches[b]
+    vc = bt.v_caches[b]
+    for l in layers:
+        _, _, kref, vref = O.compose(st, req.doc_ids, req.order, sc.k, g.rope_theta, layers=[l],
+                                     realign=sc.realign)
+        kg = to_bits(kc[l, :, :N])
+        vg = to_bits(vc[l, :, :N])
+        assert np.array_equal(vg, vref[0]), f"V rows differ (layer {l})"
+        check_keys(kg, kref[0], f"composed K layer {l}")
+        kcache, vcache = kref[0], vref[0]
+        if Q:
+            o_ref, kq_rot = O.attend_new_tokens(inputs.q_pre[l, b], inputs.kq_pre[l, b], inputs.vq[l, b],
+                                                kcache, vcache, lt, g.rope_theta)
+            check_attention(pre[l][b], o_ref, f"prefill layer {l} seq {b}")
+            check_keys(to_bits(kc[l, :, N:N + Q]), kq_rot, f"question keys layer {l}")
+            assert np.array_equal(to_bits(vc[l, :, N:N + Q]), inputs.vq[l, b].transpose(1, 0, 2))
+            kcache = np.concatenate([kcache, kq_rot], axis=1)
+            vcache = np.concatenate([vcache, inputs.vq[l, b].transpose(1, 0, 2)], axis=1)
+        for t in steps:
+            if t > 0:
+                prev_pos = lt + Q + np.arange(t)
+                kd = O.rotate_keys_bf16(inputs.kd_pre[:t, l, b], prev_pos, g.rope_theta)
+                kc_t = np.concatenate([kcache, kd], axis=1)
+                vc_t = np.concatenate([vcache, inputs.vd[:t, l, b].transpose(1, 0, 2)], axis=1)
+            else:
+                kc_t, vc_t = kcache, vcache
+            o_ref, kn = O.attend_new_tokens(inputs.qd_pre[t:t + 1, l, b], inputs.kd_pre[t:t + 1, l, b],
+                                            inputs.vd[t:t + 1, l, b], kc_t, vc_t, lt + Q + t, g.rope_theta)
+            check_attention(dec[t][l][b], o_ref[0], f"decode layer {l} step {t} seq {b}")
+            row = N + Q + t
+            check_keys(to_bits(kc[l, :, row:row + 1]), kn, f"decode key layer {l} step {t}")

@@ -212,3 +212,23 @@ def test_device_buffer_sizes_are_checked_by_the_binding(P, monkeypatch):
         P.c2kv_compose(0, [1], None, 4, good, good, cap, tab[:-16])
     with pytest.raises(ValueError, match="pos_dev_out"):
         P.c2kv_compose_layers(0, [1], None, 4, 0, 0, 1, good, good, cap, tab, torch.zeros(cap - 1, dtype=torch.int32))
+
+
+def test_decode_scratch_fits_the_fixed_noalloc_array(P):
+    """c2kv_attend_decode_noalloc keeps its scratch in a fixed 4 MiB device
+    array and rejects a decode that would need more.  For every supported
+    geometry on a 152-SM GPU (the sizing used without a GPU) the one-token
+    scratch is far below that: two partial slots per SM plus per-unit
+    counters at head_dim 128, at most one split per SM at head_dim 64."""
+    limit = 4 << 20
+    worst = 0
+    for d in (64, 128):
+        for grp in (1, 2, 4, 5, 8):
+            for hkv in (1, 8, 1024 // (d // 16)):
+                g = S.Geometry(1, hkv * grp, hkv, d, 1.0e4)
+                for batch in (1, 4, 16):
+                    for keys in (1, 1000, 131072, 1 << 22):
+                        need = P.c2kv_attend_workspace_size(g, batch, 1, keys)
+                        assert 0 < need
+                        worst = max(worst, need)
+    assert worst <= limit // 2, worst

@@ -11,85 +11,9 @@ import torch
 import oracle.c2kv_oracle as O
 import compressed_composable_kv_gb300 as P
 from compressed_composable_kv_gb300 import synth as S
-from gpu_util import Scenario, check_attention, check_keys, to_bits, to_dev
+from gpu_util import Scenario, check_attention, check_keys, check_request, run_all, to_bits, to_dev, upload
 
 pytestmark = pytest.mark.gpu
-
-
-def upload(inputs: S.StepInputs):
-    return {name: to_dev(getattr(inputs, name)) for name in
-            ("q_pre", "kq_pre", "vq", "qd_pre", "kd_pre", "vd")}
-
-
-def run_all(sc: Scenario, dev):
-    """Compose, prefill every layer, decode every step (the bench's launch
-    configuration, without graphs).  Returns the output tensors."""
-    bt = sc.batch
-    L = sc.geom.n_layers
-    bt.compose()
-    pre = []
-    if bt.q_len:
-        for l in range(L):
-            out = torch.empty_like(dev["q_pre"][l])
-            bt.prefill(l, dev["q_pre"][l], dev["kq_pre"][l], dev["vq"][l], out)
-            pre.append(out)
-    bt.reset_decode()
-    dec = []
-    for t in range(bt.decode_steps):
-        row = []
-        for l in range(L):
-            out = torch.empty_like(dev["qd_pre"][t, l])
-            bt.decode(l, dev["qd_pre"][t, l], dev["kd_pre"][t, l], dev["vd"][t, l], out)
-            row.append(out)
-        bt.advance()
-        dec.append(row)
-    torch.cuda.synchronize()
-    assert P.c2kv_device_error() == P.C2KV_OK
-    return pre, dec
-
-
-def check_request(sc: Scenario, inputs: S.StepInputs, pre, dec, b: int, layers, steps):
-    bt = sc.batch
-    g = sc.geom
-    req = sc.reqs[b]
-    st = sc.oracle_store()
-    N, lt, Q = bt.n_slots[b], bt.l_tot[b], bt.q_len
-    seq = O.composed_order(req.doc_ids, req.order)
-    pos_ref, lt_ref = O.composed_positions([sc.docs[d].n_tokens for d in seq],
-                                           [sc.docs[d].n_slots for d in seq], sc.k, sc.realign)
-    assert lt_ref == lt
-    assert np.array_equal(bt.pos[b][:N].cpu().numpy(), pos_ref)
-    kc = bt.k_caches[b]
-    vc = bt.v_caches[b]
-    for l in layers:
-        _, _, kref, vref = O.compose(st, req.doc_ids, req.order, sc.k, g.rope_theta, layers=[l],
-                                     realign=sc.realign)
-        kg = to_bits(kc[l, :, :N])
-        vg = to_bits(vc[l, :, :N])
-        assert np.array_equal(vg, vref[0]), f"V rows differ (layer {l})"
-        check_keys(kg, kref[0], f"composed K layer {l}")
-        kcache, vcache = kref[0], vref[0]
-        if Q:
-            o_ref, kq_rot = O.attend_new_tokens(inputs.q_pre[l, b], inputs.kq_pre[l, b], inputs.vq[l, b],
-                                                kcache, vcache, lt, g.rope_theta)
-            check_attention(pre[l][b], o_ref, f"prefill layer {l} seq {b}")
-            check_keys(to_bits(kc[l, :, N:N + Q]), kq_rot, f"question keys layer {l}")
-            assert np.array_equal(to_bits(vc[l, :, N:N + Q]), inputs.vq[l, b].transpose(1, 0, 2))
-            kcache = np.concatenate([kcache, kq_rot], axis=1)
-            vcache = np.concatenate([vcache, inputs.vq[l, b].transpose(1, 0, 2)], axis=1)
-        for t in steps:
-            if t > 0:
-                prev_pos = lt + Q + np.arange(t)
-                kd = O.rotate_keys_bf16(inputs.kd_pre[:t, l, b], prev_pos, g.rope_theta)
-                kc_t = np.concatenate([kcache, kd], axis=1)
-                vc_t = np.concatenate([vcache, inputs.vd[:t, l, b].transpose(1, 0, 2)], axis=1)
-            else:
-                kc_t, vc_t = kcache, vcache
-            o_ref, kn = O.attend_new_tokens(inputs.qd_pre[t:t + 1, l, b], inputs.kd_pre[t:t + 1, l, b],
-                                            inputs.vd[t:t + 1, l, b], kc_t, vc_t, lt + Q + t, g.rope_theta)
-            check_attention(dec[t][l][b], o_ref[0], f"decode layer {l} step {t} seq {b}")
-            row = N + Q + t
-            check_keys(to_bits(kc[l, :, row:row + 1]), kn, f"decode key layer {l} step {t}")
 
 
 def test_tiny_end_to_end():
@@ -392,6 +316,50 @@ def test_llama_8x4000_full_size():
     seq = O.composed_order(sc.reqs[0].doc_ids, sc.reqs[0].order)
     vcat = np.concatenate([sc.docs[d].v for d in seq], axis=2)
     assert np.array_equal(to_bits(bt.v_caches[0][:, :, :N]), vcat)
+    check_request(sc, inputs, pre, dec, 0, layers=[0, 31], steps=[0, 1, 127])
+    sc.close()
+
+
+def test_llama_8x4000_full_size_sharp_needles():
+    """The benchmark workload at full size with a sharp softmax: q scaled by 4
+    (so a handful of keys dominate every row instead of a near-uniform spread
+    over 8000 keys) and, in every layer and kv head, 16 planted "needle" keys
+    pointing along the first decode token's q (of the group's first head)
+    once both are rotated to their positions, so at decode step 0 the needles
+    take almost all of the weight.  Checked on layers 0 and 31, decode steps 0,
+    1 and 127 and every question row, at the same tolerances as the flat case."""
+    w = S.WORKLOADS["llama8b_8x4000_k4"]
+    g = w.geom
+    docs, reqs = S.make_requests(w)
+    inputs = S.make_step_inputs(w, q_scale=4.0)
+    req = reqs[0]
+    seq = O.composed_order(req.doc_ids, req.order)
+    pos, l_tot = O.composed_positions([docs[d][0] for d in seq], [docs[d][1] for d in seq], w.k)
+    target = l_tot + w.q_len                      # position of decode step 0
+    starts = np.cumsum([0] + [docs[d][1] for d in seq])
+    needles = np.linspace(5, len(pos) - 9, 16).astype(np.int64)   # composed slot indices
+    G = g.n_q_heads // g.n_kv_heads
+
+    def plant(dd):
+        for i in needles:
+            c = int(np.searchsorted(starts, i, side="right") - 1)
+            doc, j = dd[seq[c]], int(i - starts[c])
+            # pre-RoPE key k = R(target - pos_i) q0, so that R(pos_i) k = R(target) q0
+            q0 = O.bf16_to_f64(inputs.qd_pre[0, :, 0, ::G])           # [L][Hkv][d]
+            k = O.rope_rotate(q0, np.array([target - pos[i]] * g.n_kv_heads), g.rope_theta)
+            k *= 6.0 / np.linalg.norm(k, axis=-1, keepdims=True)
+            doc.k_pre[:, :, j, :] = O.f64_to_bf16(k)
+
+    sc = Scenario(g, w.k, [(i, n, s) for i, (n, s) in docs.items()], [(r.doc_ids, r.order) for r in reqs],
+                  w.q_len, w.decode_steps, seed=w.seed, mutate=plant)
+    # the planted keys do dominate step 0 (layer 0, head 0): each needle's
+    # score exceeds every other composed key's by more than 5 (natural log)
+    _, _, k0, _ = O.compose(sc.oracle_store(), req.doc_ids, req.order, w.k, g.rope_theta, layers=[0])
+    qr = O.rope_rotate(O.bf16_to_f64(inputs.qd_pre[0, 0, 0, :1]), np.array([target]), g.rope_theta)[0]
+    sc0 = O.bf16_to_f64(k0[0, 0]) @ qr / np.sqrt(g.head_dim)
+    others = np.delete(sc0, needles)
+    assert sc0[needles].min() - others.max() > 5.0, (sc0[needles].min(), others.max())
+    pre, dec = run_all(sc, upload(inputs))
     check_request(sc, inputs, pre, dec, 0, layers=[0, 31], steps=[0, 1, 127])
     sc.close()
 
