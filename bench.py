@@ -490,6 +490,9 @@ def run_ours(args, rank: int, world: int) -> dict:
     err = P.c2kv_device_error()
     assert err == P.C2KV_OK, f"device error {err}"
     dec = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / 1e3   # decode phase in the timed region
+    # between one request's decode and the next one's: that request's question
+    # prefill (its compose ran during the decode before)
+    gaps = [ev[r - 1][1].elapsed_time(ev[r][0]) / 1e3 for r in range(1, args.steps)]
 
     # e2e: the same requests with inputs copied from pinned host memory and
     # the answer read back, all inside the timed region
@@ -546,6 +549,7 @@ def run_ours(args, rank: int, world: int) -> dict:
                    "pipelined with its prefill), mean of 3; decode_ms: mean decode phase of the timed "
                    "requests"),
         "decode_only_tok_s": Bn * T / dec,
+        "between_decodes_ms": statistics.mean(gaps) * 1e3 if gaps else None,
         "attention_hbm_gbs": achieved,
         "h2d": {"compose_bytes": compose_bytes, "achieved_gbs": compose_bytes / comp / 1e9,
                 "pinned_copy_gbs": pinned_gbs, "frac": compose_bytes / comp / 1e9 / pinned_gbs,
@@ -667,6 +671,95 @@ def run_sweep(args) -> None:
             torch.cuda.empty_cache()
 
 
+def run_kernel_probe(args) -> None:
+    """The attention launches of --workload alone, on a small device
+    footprint (the case its kernel profiles are taken on): the workload's
+    geometry with --probe-layers layers, its batch and composed lengths, caches
+    and question filled with N(0,1) on the device, every row's RoPE table at
+    its index.  Runs one eager question prefill per layer (if the workload has
+    a question) and one eager decode step over every layer, then replays
+    --steps decode steps over the layers from a CUDA graph and times them.
+    Prints one JSON line."""
+    import torch
+    import compressed_composable_kv_gb300 as P
+    from compressed_composable_kv_gb300 import synth as S
+
+    w = S.WORKLOADS[args.workload]
+    g0 = w.geom
+    g = S.Geometry(args.probe_layers, g0.n_q_heads, g0.n_kv_heads, g0.head_dim, g0.rope_theta)
+    docs, reqs = S.make_requests(w)
+    lens = [sum(docs[d][1] for d in r.doc_ids) for r in reqs]
+    L, H, D, B, Q, T = g.n_layers, g.n_kv_heads, g.head_dim, len(lens), w.q_len, args.steps
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    stream = torch.cuda.Stream()
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    cap = max(lens) + Q + T + 32
+
+    def rnd(*shape):
+        return torch.randn(shape, device="cuda", generator=gen).to(torch.bfloat16)
+
+    kc = [rnd(L, H, cap, D) for _ in range(B)]
+    vc = [rnd(L, H, cap, D) for _ in range(B)]
+    tabs = [torch.empty(P.c2kv_rope_table_bytes(g, cap) // 4, dtype=torch.float32, device="cuda") for _ in range(B)]
+    idx = torch.arange(cap, dtype=torch.int32, device="cuda")
+    for t in tabs:
+        P.c2kv_rope_table(g, idx, t)
+    start = torch.tensor([n + Q for n in lens], dtype=torch.int32, device="cuda")
+    n_dev = start.clone()
+    max_keys = max(lens) + Q + T
+    ws_bytes = P.c2kv_attend_workspace_size(g, B, 1, max_keys)
+    if Q:
+        ws_bytes = max(ws_bytes, P.c2kv_attend_workspace_size(g, B, Q, max(lens) + Q))
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    qd, kd = rnd(T, L, B, g.n_q_heads, D), rnd(T, L, B, H, D)
+    outd = torch.empty_like(qd)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        if Q:
+            qp, kp = rnd(L, B, Q, g.n_q_heads, D), rnd(L, B, Q, H, D)
+            outp = torch.empty_like(qp)
+            for l in range(L):
+                P.c2kv_attend_prefill(g, l, kc, vc, tabs, cap, lens, qp[l], kp[l], kp[l], outp[l], ws, stream)
+        for l in range(L):
+            P.c2kv_attend_decode(g, l, kc, vc, tabs, cap, n_dev, max_keys, qd[0, l], kd[0, l], kd[0, l],
+                                 outd[0, l], ws, stream, 0)
+
+    def decode_all():
+        for t in range(T):
+            for l in range(L):
+                P.c2kv_attend_decode(g, l, kc, vc, tabs, cap, n_dev, max_keys, qd[t, l], kd[t, l], kd[t, l],
+                                     outd[t, l], ws, stream, P.C2KV_DECODE_OVERLAP_PREVIOUS if l else 0)
+            P.c2kv_seq_advance(n_dev, 1, stream)
+
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            decode_all()
+    times = []
+    for _ in range(args.warmup + 3):
+        with torch.cuda.stream(stream):
+            n_dev.copy_(start)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) / 1e3)
+    assert P.c2kv_device_error() == P.C2KV_OK
+    t_launch = statistics.median(times[args.warmup:]) / (T * L)
+    keys = sum(n + Q + t + 1 for n in lens for t in range(T)) / T
+    gbs = keys * H * D * 4 / t_launch / 1e9
+    peak = measured_peaks().get("hbm_gbs") or 6800.0
+    print(json.dumps({"kernel_probe": w.name, "layers": L, "batch": B, "composed_slots": lens, "question_tokens": Q,
+                      "decode_us_per_launch": t_launch * 1e6, "decode_attention_gbs": gbs,
+                      "decode_frac_of_hbm_peak": gbs / peak,
+                      "note": (f"{L} layers of random caches; eager: {L if Q else 0} prefill + {L} decode launches, "
+                               f"then {T} decode steps x {L} layers from a graph (timed)")}))
+
+
 def run_extract(args) -> None:
     """Extraction-side attention at full size (section "structured information
     flow"): one document of 4000 tokens followed by its 1000 slots (k=4),
@@ -745,6 +838,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="decode time vs context (16k..128k), compressed k=16/8/4 vs uncompressed")
+    ap.add_argument("--kernel-probe", action="store_true",
+                    help="the workload's prefill and decode launches alone, on --probe-layers layers of random caches")
+    ap.add_argument("--probe-layers", type=int, default=2)
     ap.add_argument("--extract", action="store_true",
                     help="extraction-side attention (structured, anchor and causal masks), "
                          "4000-token document + 1000 slots")
@@ -754,6 +850,9 @@ def main():
         return
     if args.extract:
         run_extract(args)
+        return
+    if args.kernel_probe:
+        run_kernel_probe(args)
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

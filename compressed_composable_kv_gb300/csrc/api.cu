@@ -173,6 +173,12 @@ struct AttnWs {
   size_t counters_off, counters_bytes, ml_off, o_off, qrot_off, total;
 };
 
+// Bytes of one part (hi or lo) of the rotated-q scratch of the tensor-core
+// prefill, 256-byte aligned.
+size_t qrot_part_bytes(const c2kv_geometry* g, int batch, int t_len) {
+  return align256((size_t)batch * g->n_q_heads * t_len * g->head_dim * 2);
+}
+
 // The tensor-core decode serves one token per sequence at head_dim 128, with
 // one CTA per SM (at most kDecMaxCtas).
 bool use_decode_tc(const c2kv_geometry* g, int t_len) { return t_len == 1 && g->head_dim == 128; }
@@ -223,8 +229,8 @@ AttnWs attn_workspace(const c2kv_geometry* g, int batch, int t_len, int max_keys
     w.o_off = off;
     off += align256(rows * g->head_dim * sizeof(float));
   }
-  w.qrot_off = off;
-  if (t_len > 1) off += align256((size_t)batch * g->n_q_heads * t_len * g->head_dim * 2);
+  w.qrot_off = off;   // rotated q for the tensor-core prefill: bf16 hi part, then lo part
+  if (t_len > 1) off += 2 * align256((size_t)batch * g->n_q_heads * t_len * g->head_dim * 2);
   w.total = off;
   return w;
 }
@@ -279,8 +285,8 @@ c2kv_status run_prefill_tc(const c2kv_geometry* g, int batch, const void* const*
   std::memset(&p, 0, sizeof(p));
   const int D = g->head_dim;
   const int grp = g->n_q_heads / g->n_kv_heads;
-  s = encode_map(&p.tm_q, ws + w.qrot_off, 2, D, (uint64_t)batch * g->n_q_heads * t_len, 0, 0, 128);
-  if (s != C2KV_OK) return s;
+  p.q_hi = reinterpret_cast<const __nv_bfloat16*>(ws + w.qrot_off);
+  p.q_lo = reinterpret_cast<const __nv_bfloat16*>(ws + w.qrot_off + qrot_part_bytes(g, batch, t_len));
   for (int b = 0; b < batch; ++b) {
     const uint64_t stride2 = (uint64_t)block_rows * D * 2;
     s = encode_map(&p.tm_k[b], kb0[b], 3, D, valid[b], n_blocks, stride2, (uint32_t)prefill_tc_key_tile());
@@ -462,6 +468,7 @@ c2kv_status run_append(const c2kv_geometry* g, int batch, __nv_bfloat16* const* 
                        const CosSin2* const* tabs, const int32_t* row_h, const int32_t* row_d, int cap, int t_len,
                        const void* k_src, const void* v_src, cudaStream_t st, const void* q_src = nullptr,
                        void* q_dst = nullptr) {
+  // q_dst: the rotated-q scratch, bf16 hi part then lo part
   unsigned* err = nullptr;
   c2kv_status s = device_state(&err, nullptr);
   if (s != C2KV_OK) return s;
@@ -478,6 +485,8 @@ c2kv_status run_append(const c2kv_geometry* g, int batch, __nv_bfloat16* const* 
   p.v_src = static_cast<const __nv_bfloat16*>(v_src);
   p.q_src = static_cast<const __nv_bfloat16*>(q_src);
   p.q_dst = static_cast<__nv_bfloat16*>(q_dst);
+  p.q_dst_lo = q_dst ? reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(q_dst) + qrot_part_bytes(g, batch, t_len))
+                     : nullptr;
   p.err = err;
   p.t_len = t_len;
   p.n_kv = g->n_kv_heads;

@@ -155,6 +155,17 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
   return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
 }
 
+// fp32 -> bf16 bits, round to nearest even (finite inputs)
+__device__ __forceinline__ uint32_t bf16_bits_rn(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+}
+
+// 8 bf16 bit patterns (low 16 bits of each word) -> 16 bytes, element 0 first
+__device__ __forceinline__ uint4 pack_bits8(const uint32_t (&h)[8]) {
+  return make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+}
+
 // Rotates 8 pairs: a holds elements [8c, 8c+8) of the first half, b the same
 // offsets of the second half.  Each output is evaluated in double-float and
 // rounded once to bf16, so it is the correctly rounded rotation of the
@@ -275,15 +286,18 @@ struct AppendParams {
   const __nv_bfloat16* k_src;        // [B][t_len][Hkv][d]
   const __nv_bfloat16* v_src;
   const __nv_bfloat16* q_src;        // optional [B][t_len][Hq][d], rotated into ...
-  __nv_bfloat16* q_dst;              // ... [B][Hkv][t_len][G][d]
+  __nv_bfloat16* q_dst;              // ... [B][Hkv][t_len][G][d] (bf16 hi part)
+  __nv_bfloat16* q_dst_lo;           // and the same layout (bf16 lo part)
   unsigned* err;
   int32_t t_len, n_kv, n_q, cap;
 };
 
-// Tensor-core prefill: Q from the rotated-q scratch, K/V from 3-D maps
-// {d, valid keys, layer * kv head} of each sequence's cache.
+// Tensor-core prefill: Q (hi and lo bf16 parts) from the rotated-q scratch
+// [B][Hkv][t_len][G][d], K/V from 3-D maps {d, valid keys, layer * kv head}
+// of each sequence's cache.
 struct PrefillTcParams {
-  CUtensorMap tm_q;
+  const __nv_bfloat16* q_hi;
+  const __nv_bfloat16* q_lo;
   CUtensorMap tm_k[kMaxBatch];
   CUtensorMap tm_v[kMaxBatch];
   int32_t n_cached[kMaxBatch];

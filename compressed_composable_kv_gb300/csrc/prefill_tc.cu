@@ -12,7 +12,11 @@
 // tok0 + r / G, head r % G (G = 5 uses 125 rows).  Warps 0-3 are the softmax
 // warps (thread t owns row t, i.e. TMEM lane t); warp 4's first lane issues
 // every TMA load and every MMA.
-//   Q   : [128 rows][d] bf16, TMA (2-D map over the rotated-q scratch), SW128
+//   Q   : [128 rows][d] as bf16 hi + lo parts (hi + lo within ~2^-16 of the
+//         rotated q), loaded by the softmax threads (thread = row) into TMEM;
+//         S = Q_hi K^T + Q_lo K^T takes A from TMEM, so the logits keep
+//         fp32-level accuracy (a bf16 q alone errs by ~2^-9 of |q||k|, which a
+//         sharp softmax turns into output errors near the tolerance)
 //   K,V : 128-key tiles, TMA (3-D map over [layer*kv head][keys][d]), 2
 //         stages, keys at or past the sequence's valid length read as zeros
 //         (OOB); key tiles no row of the M tile can see are skipped
@@ -53,15 +57,15 @@ constexpr float kRescaleLog2 = 8.f;
 template <int D>
 struct TcCfg {
   static constexpr int NSUB = D / 64;           // 128-byte column blocks of d
-  static constexpr int Q_BYTES = NSUB * BM * 128;
   static constexpr int KV_BYTES = NSUB * BN * 128;
   static constexpr int P_BYTES = BM * BN * 2;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int MRG_BYTES = (BM + kMaxClusterTc) * 3 * 4;   // split merge: m, l, weights
+  static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
   static constexpr int OFF_ML = OFF_P + 2 * P_BYTES;   // split merge: (m, l) of every row
-  static constexpr int OFF_BAR = OFF_ML + BM * 2 * 4;
+  static constexpr int OFF_MRG = OFF_ML + BM * 2 * 4;
+  static constexpr int OFF_BAR = OFF_MRG + MRG_BYTES;
   static constexpr int N_BAR = 1 + 2 * STAGES + 2 + 2 + 2 + 2 + 2 + 1;
   static constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;   // + slack for 1024-byte alignment
@@ -69,13 +73,13 @@ struct TcCfg {
   // by row & 7) over the K ring, merge weights over the Q tile
   static constexpr int OFF_OST = OFF_K;
   static_assert(BM * D * 4 <= STAGES * KV_BYTES, "O staging must fit the K ring");
-  // [rows per CTA][S] m, l and weights; rows per CTA * S <= BM + S
-  static_assert((BM + kMaxClusterTc) * 3 * 4 <= Q_BYTES, "merge scratch must fit the Q tile");
   static_assert(SMEM <= 232448, "shared memory per CTA");
   static constexpr int TMEM_S = 0;                    // two BN-column S buffers
   static constexpr int TMEM_O = 2 * BN;               // d columns
+  static constexpr int TMEM_QH = 3 * BN;              // Q_hi: d / 2 columns (two bf16 per column)
+  static constexpr int TMEM_QL = TMEM_QH + D / 2;     // Q_lo
   static constexpr int TMEM_COLS = 512;
-  static_assert(TMEM_O + D <= TMEM_COLS, "TMEM columns");
+  static_assert(TMEM_O + D <= TMEM_QH && TMEM_QL + D / 2 <= TMEM_COLS, "TMEM columns");
 };
 
 __device__ __forceinline__ bool tc_structured_visible(const PrefillTcParams& p, int tok, int key) {
@@ -154,7 +158,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   for (int t = 0; t < ntiles; ++t) nlive += tile_live(t) ? 1 : 0;
 
   if (tid == 0) {
-    mbar_init(q_full, 1);
+    mbar_init(q_full, kSoftmaxThreads);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
@@ -183,7 +187,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  uint8_t* sQ = smem + C::OFF_Q;
   uint8_t* sK = smem + C::OFF_K;
   uint8_t* sV = smem + C::OFF_V;
   uint8_t* sP = smem + C::OFF_P;
@@ -193,9 +196,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   if (warp == 4) {
     if (lane == 0 && nlive > 0) {
       // ---------------- producer + MMA issuer (one thread)
-      const int q_row0 = ((b * p.n_kv + h) * p.t_len + tok0) * G;
-      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
-      for (int sub = 0; sub < C::NSUB; ++sub) tma_load_2d(sQ + sub * BM * 128, &p.tm_q, sub * 64, q_row0, q_full);
       // the jj-th live tile (key tile t) goes to stage jj % STAGES
       auto issue_kv = [&](int jj, int t) {
         const int s = jj % STAGES;
@@ -237,11 +237,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const int sub = kk / 4, ko = (kk % 4) * 32;
-          const uint64_t a = sw128_desc(smem_addr(sQ + sub * BM * 128) + ko, 16, 1024);
-          const uint64_t bdesc = sw128_desc(smem_addr(sK + s * C::KV_BYTES + sub * BN * 128) + ko, 16, 1024);
-          mma_bf16(tmem + C::TMEM_S + sb * BN, a, bdesc, IDESC_QK, kk > 0 ? 1u : 0u);
+        for (int half = 0; half < 2; ++half) {   // Q_hi K^T, then + Q_lo K^T
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const int sub = kk / 4, ko = (kk % 4) * 32;
+            const uint64_t bdesc = sw128_desc(smem_addr(sK + s * C::KV_BYTES + sub * BN * 128) + ko, 16, 1024);
+            mma_bf16_tmem_a(tmem + C::TMEM_S + sb * BN, tmem + (half ? C::TMEM_QL : C::TMEM_QH) + kk * 8, bdesc,
+                            IDESC_QK, (half | kk) ? 1u : 0u);
+          }
         }
         mma_commit(&s_full[sb]);
         if (j >= 1) {
@@ -266,6 +269,33 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
     const bool row_ok = row < ROWS && tl < ntok;
     const int lim = n_cached + tok + 1;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    {
+      // this row's q (hi and lo parts) into TMEM: rows past the tile's tokens
+      // and heads are zero
+      const size_t qrow = (((size_t)b * p.n_kv + h) * p.t_len + tok0) * G + row;
+      const uint4* qh = reinterpret_cast<const uint4*>(p.q_hi + qrow * D);
+      const uint4* ql = reinterpret_cast<const uint4*>(p.q_lo + qrow * D);
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        const uint4* src = part ? ql : qh;
+#pragma unroll
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {   // 32 columns = 64 bf16 = 8 x 16 bytes
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint4 u = row_ok ? src[c0 / 4 + j] : make_uint4(0, 0, 0, 0);
+            v[4 * j + 0] = __uint_as_float(u.x);
+            v[4 * j + 1] = __uint_as_float(u.y);
+            v[4 * j + 2] = __uint_as_float(u.z);
+            v[4 * j + 3] = __uint_as_float(u.w);
+          }
+          tmem_st32(lane_base + (part ? C::TMEM_QL : C::TMEM_QH) + c0, v);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(q_full);
+    }
     bool ok = true;
     int tcur = next_live(0);   // key tile of the j-th live tile
     for (int j = 0; j < nlive; ++j, tcur = next_live(tcur + 1)) {
@@ -423,7 +453,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   if (aborted) {
     // let TMA copies in flight land before the shared memory is reused
     if (tid == 0 && nlive > 0) {   // nothing was issued without live tiles
-      mbar_wait(q_full, 0);
       for (int s = 0; s < min(STAGES, nlive); ++s) mbar_wait(&kv_full[s], 0);
     }
     __syncthreads();
@@ -476,7 +505,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   const int rows_per = (BM + S - 1) / S;
   const int r0 = rank * rows_per;
   const int nr = max(0, min(BM, r0 + rows_per) - r0);
-  float* sm_m = reinterpret_cast<float*>(smem + C::OFF_Q);   // [nr][S]
+  float* sm_m = reinterpret_cast<float*>(smem + C::OFF_MRG);   // [nr][S]
   float* sm_l = sm_m + nr * S;
   float* sm_w = sm_l + nr * S;
   for (int i = tid; i < nr * S; i += kThreadsTc) {

@@ -135,12 +135,30 @@ __global__ void append_kernel(const __grid_constant__ AppendParams p) {
     if (p.q_src == nullptr || hq >= p.n_q) return;
     const int grp = p.n_q / p.n_kv;
     const uint4* qs = reinterpret_cast<const uint4*>(p.q_src + (((size_t)b * p.t_len + i) * p.n_q + hq) * D);
-    uint4 a = qs[c], bb = qs[c + TPR];
-    rotate8_df(a, bb, &tab[c * 8]);
-    uint4* qd = reinterpret_cast<uint4*>(
-        p.q_dst + ((((size_t)b * p.n_kv + hq / grp) * p.t_len + i) * grp + hq % grp) * D);
-    qd[c] = a;
-    qd[c + TPR] = bb;
+    // q as two bf16 parts: hi, the correctly rounded rotation, and lo, the
+    // rounded rest (hi + lo is within ~2^-16 of the exact rotation)
+    float x[8], y[8];
+    unpack8(qs[c], x);
+    unpack8(qs[c + TPR], y);
+    uint32_t h0[8], l0[8], h1[8], l1[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const CosSin2 t = tab[c * 8 + e];
+      float hi, lo;
+      dot2_df(x[e], t.ch, t.cl, -y[e], t.sh, t.sl, hi, lo);   // x cos - y sin
+      h0[e] = df_to_bf16_bits(hi, lo);
+      l0[e] = bf16_bits_rn(__fadd_rn(__fsub_rn(hi, __uint_as_float(h0[e] << 16)), lo));
+      dot2_df(y[e], t.ch, t.cl, x[e], t.sh, t.sl, hi, lo);    // y cos + x sin
+      h1[e] = df_to_bf16_bits(hi, lo);
+      l1[e] = bf16_bits_rn(__fadd_rn(__fsub_rn(hi, __uint_as_float(h1[e] << 16)), lo));
+    }
+    const size_t qoff = ((((size_t)b * p.n_kv + hq / grp) * p.t_len + i) * grp + hq % grp) * D;
+    uint4* qd = reinterpret_cast<uint4*>(p.q_dst + qoff);
+    uint4* ql = reinterpret_cast<uint4*>(p.q_dst_lo + qoff);
+    qd[c] = pack_bits8(h0);
+    qd[c + TPR] = pack_bits8(h1);
+    ql[c] = pack_bits8(l0);
+    ql[c + TPR] = pack_bits8(l1);
     return;
   }
   const size_t src = (((size_t)b * p.t_len + i) * p.n_kv + h) * D;
