@@ -54,7 +54,7 @@ def test_traffic_record_applies_only_to_the_captured_sources(tmp_path, monkeypat
 def test_committed_traffic_record_parses():
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     rows = [ln.split() for ln in open(path) if ln.strip() and not ln.startswith("#")]
-    assert any(r[0] == "decode_kernel" for r in rows)
+    assert any(r[0] == "decode_tc_kernel" for r in rows)
     for r in rows:
         for src in r[1].split(","):
             assert os.path.exists(os.path.join(ROOT, src)), src
