@@ -12,4 +12,4 @@ raises ImportError on first use.
 """
 from .binding import *  # noqa: F401,F403
 from .binding import C2KVError, load_library  # noqa: F401
-from .pipeline import RequestBatch, RequestSpec  # noqa: F401
+from .pipeline import DecoderModel, RequestBatch, RequestSpec  # noqa: F401

@@ -70,6 +70,10 @@ _SIGNATURES = {
     "c2kv_seq_advance": (_i32, [_i32, _vp, _i32, _vp]),
     "c2kv_attend_masked": (_i32, [_pg, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "c2kv_device_error": (_i32, [_pi32]),
+    "c2kv_linear_workspace_size": (_sz, [_i32, _i32]),
+    "c2kv_linear": (_i32, [_vp, _i32, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _sz,
+                           ctypes.c_uint32, _vp]),
+    "c2kv_rmsnorm": (_i32, [_vp, _i32, _i32, _vp, ctypes.c_float, _vp, ctypes.c_uint32, _vp]),
 }
 
 _lib = None
@@ -429,3 +433,50 @@ def c2kv_device_error() -> int:
     code = ctypes.c_int32()
     _check(load_library().c2kv_device_error(ctypes.byref(code)))
     return code.value
+
+
+# ---------------------------------------------------------------- decoder step
+C2KV_LINEAR_STORE = 0
+C2KV_LINEAR_ADD = 1
+C2KV_LINEAR_SPLIT3 = 2
+C2KV_LINEAR_SWIGLU = 3
+C2KV_LINEAR_OVERLAP_PREVIOUS = 1
+
+
+def c2kv_linear_workspace_size(tokens: int, n_out: int) -> int:
+    return int(load_library().c2kv_linear_workspace_size(int(tokens), int(n_out)))
+
+
+def c2kv_linear(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor, workspace: torch.Tensor,
+                epilogue: int = C2KV_LINEAR_STORE, residual: Optional[torch.Tensor] = None,
+                y2: Optional[torch.Tensor] = None, y3: Optional[torch.Tensor] = None, split1: int = 0,
+                split2: int = 0, stream=None, flags: int = 0) -> None:
+    """y = x @ w.T on the tensor cores with an epilogue (see include/c2kv.h):
+    x [tokens][k_in], w [n_out][k_in] bf16; y per the epilogue."""
+    tokens, k_in = x.shape
+    n_out = w.shape[0]
+    if w.shape[1] != k_in:
+        raise ValueError("w must be [n_out][k_in] with the k_in of x")
+    width = {C2KV_LINEAR_SPLIT3: split1, C2KV_LINEAR_SWIGLU: n_out // 2}.get(epilogue, n_out)
+    _need(y, 2 * tokens * width, "y", exact=True)
+    if epilogue == C2KV_LINEAR_ADD:
+        _need(residual, 2 * tokens * n_out, "residual", exact=True)
+    if epilogue == C2KV_LINEAR_SPLIT3:
+        _need(y2, 2 * tokens * (split2 - split1), "y2", exact=True)
+        _need(y3, 2 * tokens * (n_out - split2), "y3", exact=True)
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().c2kv_linear(
+        _dev(x, torch.bfloat16, "x"), int(tokens), int(k_in), _dev(w, torch.bfloat16, "w"), int(n_out),
+        int(epilogue), _dev(residual, torch.bfloat16, "residual"), _dev(y, torch.bfloat16, "y"),
+        _dev(y2, torch.bfloat16, "y2"), _dev(y3, torch.bfloat16, "y3"), int(split1), int(split2),
+        _dev(workspace, None, "workspace"), ws, int(flags), _stream(stream)))
+
+
+def c2kv_rmsnorm(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor, eps: float = 1e-5, stream=None,
+                 flags: int = 0) -> None:
+    tokens, dim = x.shape
+    _need(w, 2 * dim, "w", exact=True)
+    _need(y, 2 * tokens * dim, "y", exact=True)
+    _check(load_library().c2kv_rmsnorm(_dev(x, torch.bfloat16, "x"), int(tokens), int(dim),
+                                       _dev(w, torch.bfloat16, "w"), float(eps), _dev(y, torch.bfloat16, "y"),
+                                       int(flags), _stream(stream)))

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libc2kv.so")
 
-SOURCES = ["api.cu", "rope.cu", "attn.cu", "prefill_tc.cu", "decode_tc.cu"]
+SOURCES = ["api.cu", "rope.cu", "attn.cu", "prefill_tc.cu", "decode_tc.cu", "linear_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

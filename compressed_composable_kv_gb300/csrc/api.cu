@@ -1092,6 +1092,85 @@ c2kv_status c2kv_attend_masked(const c2kv_geometry* geom, int32_t mask, int32_t 
                         ws, st);
 }
 
+// Linear workspace: the per-tile arrival counters in a fixed region at offset
+// 0 (sized for the largest tile count, so that calls with other shapes that
+// share the workspace never write their partials over counters another call
+// relies on being zero), then two partial tiles per CTA.
+constexpr int kLinearMaxTiles = 8192;
+constexpr size_t kLinearCountersBytes = (size_t)kLinearMaxTiles * sizeof(int32_t);
+
+size_t c2kv_linear_workspace_size(int32_t tokens, int32_t n_out) {
+  if (tokens < 1 || tokens > 256 || n_out < 128 || n_out % 128 != 0 || n_out / 128 > kLinearMaxTiles) return 0;
+  const int n_pad = (tokens + 15) / 16 * 16;
+  const size_t ctas = (size_t)decode_tc_ctas(sm_count_for_sizing());
+  return kLinearCountersBytes + 2 * ctas * n_pad * 128 * sizeof(float);
+}
+
+c2kv_status c2kv_linear(const void* x, int32_t tokens, int32_t k_in, const void* w, int32_t n_out, int32_t epilogue,
+                        const void* residual, void* y, void* y2, void* y3, int32_t split1, int32_t split2,
+                        void* workspace, size_t workspace_bytes, uint32_t flags, void* stream) {
+  if (flags & ~uint32_t(C2KV_LINEAR_OVERLAP_PREVIOUS)) return fail(C2KV_EINVAL, "unknown linear flags");
+  if (tokens < 1 || tokens > 256) return fail(C2KV_EINVAL, "tokens must be in [1, 256]");
+  if (k_in < 64 || k_in % 64 != 0) return fail(C2KV_EINVAL, "k_in must be a positive multiple of 64");
+  if (n_out < 128 || n_out % 128 != 0 || n_out / 128 > kLinearMaxTiles)
+    return fail(C2KV_EINVAL, "n_out must be a positive multiple of 128, at most 1048576");
+  if (epilogue < C2KV_LINEAR_STORE || epilogue > C2KV_LINEAR_SWIGLU) return fail(C2KV_EINVAL, "unknown epilogue");
+  if (!x || !w || !y || !workspace) return fail(C2KV_EINVAL, "null pointer");
+  if (epilogue == C2KV_LINEAR_ADD && !residual) return fail(C2KV_EINVAL, "residual is null");
+  if (epilogue == C2KV_LINEAR_SPLIT3) {
+    if (!y2 || !y3) return fail(C2KV_EINVAL, "y2 / y3 is null");
+    if (!(0 < split1 && split1 < split2 && split2 < n_out)) return fail(C2KV_EINVAL, "need 0 < split1 < split2 < n_out");
+  }
+  if (!aligned16(x) || !aligned16(w)) return fail(C2KV_EINVAL, "x and w must be 16-byte aligned");
+  const size_t need = c2kv_linear_workspace_size(tokens, n_out);
+  if (workspace_bytes < need) return fail(C2KV_EINVAL, "workspace too small: need " + std::to_string(need) + " bytes");
+  unsigned* err = nullptr;
+  int sms = 0;
+  c2kv_status s = device_state(&err, &sms);
+  if (s != C2KV_OK) return s;
+  const int n_pad = (tokens + 15) / 16 * 16;
+  LinearParams p;
+  std::memset(&p, 0, sizeof(p));
+  s = encode_map(&p.tm_w, w, 2, (uint64_t)k_in, (uint64_t)n_out, 0, 0, 128);
+  if (s != C2KV_OK) return s;
+  s = encode_map(&p.tm_x, x, 2, (uint64_t)k_in, (uint64_t)tokens, 0, 0, (uint32_t)n_pad);
+  if (s != C2KV_OK) return s;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.residual = static_cast<const __nv_bfloat16*>(residual);
+  p.y = static_cast<__nv_bfloat16*>(y);
+  p.y2 = static_cast<__nv_bfloat16*>(y2);
+  p.y3 = static_cast<__nv_bfloat16*>(y3);
+  p.counters = reinterpret_cast<int32_t*>(ws);
+  p.part = reinterpret_cast<float*>(ws + kLinearCountersBytes);
+  p.err = err;
+  p.tokens = tokens;
+  p.n_pad = n_pad;
+  p.k_in = k_in;
+  p.n_out = n_out;
+  p.split1 = split1;
+  p.split2 = split2;
+  p.stages = linear_stages(n_pad);
+  p.epi = epilogue;
+  C2KV_CUDA(launch_linear(p, decode_tc_ctas(sms), (flags & C2KV_LINEAR_OVERLAP_PREVIOUS) != 0,
+                          static_cast<cudaStream_t>(stream)));
+  return C2KV_OK;
+}
+
+c2kv_status c2kv_rmsnorm(const void* x, int32_t tokens, int32_t dim, const void* w, float eps, void* y,
+                         uint32_t flags, void* stream) {
+  if (flags & ~uint32_t(C2KV_LINEAR_OVERLAP_PREVIOUS)) return fail(C2KV_EINVAL, "unknown rmsnorm flags");
+  if (tokens < 1 || dim < 8 || dim % 8 != 0) return fail(C2KV_EINVAL, "need tokens >= 1 and dim a multiple of 8");
+  if (!(eps > 0.f)) return fail(C2KV_EINVAL, "eps must be > 0");
+  if (!x || !w || !y) return fail(C2KV_EINVAL, "null pointer");
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return fail(C2KV_EINVAL, "pointers must be 16-byte aligned");
+  c2kv_status s = device_state(nullptr, nullptr);
+  if (s != C2KV_OK) return s;
+  C2KV_CUDA(launch_rmsnorm(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w),
+                           static_cast<__nv_bfloat16*>(y), tokens, dim, eps, (flags & C2KV_LINEAR_OVERLAP_PREVIOUS) != 0,
+                           static_cast<cudaStream_t>(stream)));
+  return C2KV_OK;
+}
+
 c2kv_status c2kv_test_expire_next_waits(int32_t n_launches) {
   if (n_launches < 0) return fail(C2KV_EINVAL, "n_launches < 0");
   g_inject_timeouts.store(n_launches);

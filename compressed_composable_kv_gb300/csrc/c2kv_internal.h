@@ -368,7 +368,30 @@ struct DecodeTcParams {
   float scale_log2;
 };
 
+// Linear layer on the tensor cores (linear_tc.cu): Y[t][n] = sum_k X[t][k] W[n][k]
+// for t < tokens <= 256, with an epilogue.  tm_w: 2-D map {k_in, n_out} of W
+// (box 64 x 128), tm_x: 2-D map {k_in, tokens} of X (box 64 x n_pad; rows past
+// `tokens` read as zero), both with 128-byte swizzle.
+enum LinearEpilogue : int32_t { kLinearStore = 0, kLinearAdd = 1, kLinearSplit3 = 2, kLinearSwiglu = 3 };
+constexpr int kLinearSmemMax = 232448;
+struct LinearParams {
+  CUtensorMap tm_w;
+  CUtensorMap tm_x;
+  const __nv_bfloat16* residual;   // kLinearAdd: [tokens][n_out] (may be y)
+  __nv_bfloat16* y;                // [tokens][n_out]; kLinearSplit3: [tokens][split1];
+  __nv_bfloat16* y2;               // kLinearSwiglu: [tokens][n_out / 2]
+  __nv_bfloat16* y3;
+  float* part;                     // [2 * CTAs][n_pad][128] partial tiles
+  int32_t* counters;               // [n_out / 128] chunks summed so far per tile
+  unsigned* err;
+  int32_t tokens, n_pad, k_in, n_out, split1, split2, stages, epi;
+};
+
 // Launchers (return cudaGetLastError()).
+cudaError_t launch_linear(const LinearParams& p, int ctas, bool overlap, cudaStream_t st);
+int linear_stages(int n_pad);
+cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* w, __nv_bfloat16* y, int tokens, int dim,
+                           float eps, bool overlap, cudaStream_t st);
 cudaError_t launch_decode_tc(const DecodeTcParams& p, int group, int ctas, bool overlap, cudaStream_t st);
 // Clusters of `cs` CTAs of the tensor-core decode that fit the device at once
 // (0 if unknown).

@@ -183,4 +183,29 @@ __device__ __forceinline__ void tmem_ld_cols<16>(uint32_t taddr, float (&r)[16])
   for (int i = 0; i < 16; ++i) r[i] = __uint_as_float(u[i]);
 }
 
+// Max over the warp (ordered-integer form of the floats, one redux).
+__device__ __forceinline__ float warp_max(float v) {
+  int i = __float_as_int(v);
+  i = i >= 0 ? i : i ^ 0x7FFFFFFF;
+  i = __reduce_max_sync(0xffffffffu, i);
+  i = i >= 0 ? i : i ^ 0x7FFFFFFF;
+  return __int_as_float(i);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// Barrier of the 4 softmax warps (an mbarrier of count 4, phase k at the
+// k-th use, bounded and abort-aware; false if the CTA aborts).
+__device__ __forceinline__ bool group_sync(uint64_t* bar, int& k, volatile int* abort_flag, unsigned* err) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+  const bool ok = wait_or_abort(bar, (uint32_t)(k & 1), abort_flag, err);
+  ++k;
+  return __all_sync(0xffffffffu, ok);
+}
+
 }  // namespace c2kv

@@ -104,3 +104,94 @@ class RequestBatch:
 
     def advance(self, stream=None) -> None:
         B.c2kv_seq_advance(self.n_cached_dev, 1, stream)
+
+
+class DecoderModel:
+    """A synthetic-weight decoder stack around a RequestBatch's attention, on
+    the device (C2KV explainer, section "the problem", Fig. 1: the decode rate
+    of the whole model).  The layer is the Llama-3 one (no biases):
+        h = rmsnorm(x) * w_attn; q | k | v = h W_qkv^T (split by the epilogue)
+        x += attention(q, k, v) W_o^T          (the batch's composed caches)
+        h = rmsnorm(x) * w_mlp;  x += (silu(h W_g^T) * h W_u^T) W_d^T
+    then rmsnorm and the LM head.  Every step is a C-ABI call; launches after
+    the first may overlap the tail of the one before (programmatic dependent
+    launch): each kernel touches its activations only after the previous one
+    has finished.
+
+    weights: dict as synth.make_decoder_weights, values device bf16 tensors.
+    """
+
+    def __init__(self, geom, shape, weights: dict, batch: int, device: str = "cuda"):
+        self.geom, self.shape, self.w = geom, shape, weights
+        self.batch = batch
+        d = geom.head_dim
+        self.nq, self.nkv = geom.n_q_heads * d, geom.n_kv_heads * d
+        nb, dim, F = batch, shape.dim, shape.ffn
+        bf = torch.bfloat16
+
+        def buf(*sz):
+            return torch.zeros(sz, dtype=bf, device=device)
+
+        self.x, self.h = buf(nb, dim), buf(nb, dim)
+        self.q, self.k, self.v = buf(nb, self.nq), buf(nb, self.nkv), buf(nb, self.nkv)
+        self.att, self.m = buf(nb, self.nq), buf(nb, F)
+        has_head = "lm_head" in weights
+        self.logits = buf(nb, shape.vocab) if has_head else None
+        widest = max(self.nq + 2 * self.nkv, 2 * F, dim, shape.vocab if has_head else 0)
+        self.workspace = torch.zeros(B.c2kv_linear_workspace_size(nb, widest), dtype=torch.uint8, device=device)
+        B.c2kv_workspace_init(self.workspace)
+
+    def layer(self, l: int, rb: "RequestBatch", stream=None) -> None:
+        w = self.w["layers"][l]
+        ov = B.C2KV_LINEAR_OVERLAP_PREVIOUS
+        eps = self.shape.eps
+        B.c2kv_rmsnorm(self.x, w["attn_norm"], self.h, eps, stream, ov)
+        B.c2kv_linear(self.h, w["qkv"], self.q, self.workspace, B.C2KV_LINEAR_SPLIT3, y2=self.k, y3=self.v,
+                       split1=self.nq, split2=self.nq + self.nkv, stream=stream, flags=ov)
+        rb.decode(l, self.q, self.k, self.v, self.att, stream, overlap_previous=True)
+        B.c2kv_linear(self.att, w["o"], self.x, self.workspace, B.C2KV_LINEAR_ADD, residual=self.x,
+                       stream=stream, flags=ov)
+        B.c2kv_rmsnorm(self.x, w["mlp_norm"], self.h, eps, stream, ov)
+        B.c2kv_linear(self.h, w["gate_up"], self.m, self.workspace, B.C2KV_LINEAR_SWIGLU, stream=stream,
+                       flags=ov)
+        B.c2kv_linear(self.m, w["down"], self.x, self.workspace, B.C2KV_LINEAR_ADD, residual=self.x,
+                       stream=stream, flags=ov)
+
+    def decode_step(self, rb: "RequestBatch", stream=None) -> None:
+        """One answer token per sequence: every layer, the LM head (if the
+        weights have one), then the batch's lengths advance.  x holds the
+        step's input embeddings and is updated in place."""
+        for l in range(len(self.w["layers"])):
+            self.layer(l, rb, stream)
+        if self.logits is not None:
+            B.c2kv_rmsnorm(self.x, self.w["final_norm"], self.h, self.shape.eps, stream,
+                            B.C2KV_LINEAR_OVERLAP_PREVIOUS)
+            B.c2kv_linear(self.h, self.w["lm_head"], self.logits, self.workspace, stream=stream,
+                           flags=B.C2KV_LINEAR_OVERLAP_PREVIOUS)
+        rb.advance(stream)
+
+    def linears_only(self, stream=None) -> None:
+        """The step's linear layers and norms without the attention (their
+        own weight-streaming rate, for the roofline)."""
+        ov = B.C2KV_LINEAR_OVERLAP_PREVIOUS
+        eps = self.shape.eps
+        for w in self.w["layers"]:
+            B.c2kv_rmsnorm(self.x, w["attn_norm"], self.h, eps, stream, ov)
+            B.c2kv_linear(self.h, w["qkv"], self.q, self.workspace, B.C2KV_LINEAR_SPLIT3, y2=self.k,
+                           y3=self.v, split1=self.nq, split2=self.nq + self.nkv, stream=stream, flags=ov)
+            B.c2kv_linear(self.att, w["o"], self.x, self.workspace, B.C2KV_LINEAR_ADD, residual=self.x,
+                           stream=stream, flags=ov)
+            B.c2kv_rmsnorm(self.x, w["mlp_norm"], self.h, eps, stream, ov)
+            B.c2kv_linear(self.h, w["gate_up"], self.m, self.workspace, B.C2KV_LINEAR_SWIGLU, stream=stream,
+                           flags=ov)
+            B.c2kv_linear(self.m, w["down"], self.x, self.workspace, B.C2KV_LINEAR_ADD, residual=self.x,
+                           stream=stream, flags=ov)
+        if self.logits is not None:
+            B.c2kv_rmsnorm(self.x, self.w["final_norm"], self.h, self.shape.eps, stream, ov)
+            B.c2kv_linear(self.h, self.w["lm_head"], self.logits, self.workspace, stream=stream, flags=ov)
+
+    def weight_bytes(self) -> int:
+        n = sum(t.numel() for w in self.w["layers"] for t in w.values())
+        if self.logits is not None:
+            n += self.w["lm_head"].numel() + self.w["final_norm"].numel()
+        return 2 * n

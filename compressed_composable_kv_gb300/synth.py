@@ -191,3 +191,45 @@ def make_step_inputs(w: Workload, layers: Optional[int] = None,
         normal_bf16(rng, (T, L, B, g.n_kv_heads, d)),
         normal_bf16(rng, (T, L, B, g.n_kv_heads, d)),
     )
+
+
+# ---------------------------------------------------------------- decoder step
+@dataclass(frozen=True)
+class ModelShape:
+    """Sizes of a decoder stack around the attention geometry: hidden size,
+    MLP width, vocabulary, RMSNorm epsilon (Llama-3.1-8B's published sizes)."""
+    dim: int
+    ffn: int
+    vocab: int
+    eps: float
+
+
+LLAMA31_8B_MODEL = ModelShape(4096, 14336, 128256, 1e-5)
+
+
+def make_decoder_weights(geom: Geometry, shape: ModelShape, layers: int, seed: int,
+                         lm_head: bool = False) -> dict:
+    """Seeded bf16 weights (uint16 bit patterns) of `layers` decoder layers:
+    norms 1 + 0.1 N(0,1), projections N(0, 1/fan_in) so activations stay O(1).
+    Per layer: attn_norm [dim], qkv [(Hq + 2 Hkv) d][dim], o [dim][Hq d],
+    mlp_norm [dim], gate_up [2 ffn][dim] (gate and up rows in 64-row blocks),
+    down [dim][ffn]; with lm_head also final_norm [dim] and lm_head
+    [vocab][dim]."""
+    d, dim, F = geom.head_dim, shape.dim, shape.ffn
+    nq, nkv = geom.n_q_heads * d, geom.n_kv_heads * d
+    out = {"layers": []}
+    for l in range(layers):
+        rng = _rng(seed, 0xDEC, l)
+        out["layers"].append({
+            "attn_norm": bf16_bits(1.0 + 0.1 * rng.standard_normal(dim, dtype=np.float32)),
+            "qkv": normal_bf16(rng, (nq + 2 * nkv, dim), dim ** -0.5),
+            "o": normal_bf16(rng, (dim, nq), nq ** -0.5),
+            "mlp_norm": bf16_bits(1.0 + 0.1 * rng.standard_normal(dim, dtype=np.float32)),
+            "gate_up": normal_bf16(rng, (2 * F, dim), dim ** -0.5),
+            "down": normal_bf16(rng, (dim, F), F ** -0.5),
+        })
+    if lm_head:
+        rng = _rng(seed, 0xDEC, 0xFFFF)
+        out["final_norm"] = bf16_bits(1.0 + 0.1 * rng.standard_normal(dim, dtype=np.float32))
+        out["lm_head"] = normal_bf16(rng, (shape.vocab, dim), dim ** -0.5)
+    return out

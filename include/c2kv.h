@@ -385,6 +385,55 @@ c2kv_status c2kv_attend_masked(const c2kv_geometry* geom, int32_t mask,
 size_t c2kv_masked_extra_bytes(const c2kv_geometry* geom, int32_t n_tokens);
 
 /*
+ * The synthetic-weight decoder step around the attention calls: its linear
+ * layers and RMSNorm.  [EXPL] "the problem" (Fig. 1): the time to first token
+ * and the decode rate of the whole model are what the cache reuse buys, and
+ * a decoder layer runs these projections and its MLP around the attention
+ * over the composed cache.
+ *
+ * c2kv_linear: y[t][n] = sum_k x[t][k] * w[n][k] on the tensor cores (fp32
+ * accumulation, bf16 result) for t < tokens, then an epilogue:
+ *   C2KV_LINEAR_STORE   y [tokens][n_out] = the product;
+ *   C2KV_LINEAR_ADD     y [tokens][n_out] = product + residual [tokens][n_out]
+ *                       (residual may be y: an in-place residual update);
+ *   C2KV_LINEAR_SPLIT3  output columns [0, split1) to y [tokens][split1],
+ *                       [split1, split2) to y2, [split2, n_out) to y3 (the
+ *                       q, k and v of a fused QKV projection);
+ *   C2KV_LINEAR_SWIGLU  rows 128i .. 128i+63 of w are the gate rows of
+ *                       features 64i .. 64i+63 and rows 128i+64 .. 128i+127
+ *                       their up rows; y [tokens][n_out / 2] =
+ *                       silu(gate) * up, silu(g) = g / (1 + e^-g).
+ * x: device bf16 [tokens][k_in], w: device bf16 [n_out][k_in] (row-major,
+ * as a linear layer's weight), both 16-byte aligned.  1 <= tokens <= 256,
+ * k_in a positive multiple of 64, n_out a positive multiple of 128 up to
+ * 1048576.  workspace: c2kv_linear_workspace_size(tokens, n_out) bytes of
+ * device memory, zeroed once (c2kv_workspace_init); calls of any shapes that
+ * fit it may share it as long as their GPU work does not overlap (a launch
+ * with C2KV_LINEAR_OVERLAP_PREVIOUS touches it only after the kernel before
+ * it has completed).  flags: C2KV_LINEAR_OVERLAP_PREVIOUS lets the launch
+ * begin, and request its first weight tiles, while the kernel before it on
+ * `stream` finishes (the caller promises that kernel does not write w); x,
+ * the residual and the outputs are touched only after it completes.
+ * Errors: C2KV_EINVAL, C2KV_ECUDA.
+ *
+ * c2kv_rmsnorm: y[t] = x[t] / sqrt(mean_i x[t][i]^2 + eps) * w for t < tokens,
+ * x and y device bf16 [tokens][dim], w bf16 [dim] (dim a multiple of 8,
+ * 16-byte aligned pointers), sums in fp32.  flags as c2kv_linear.
+ */
+#define C2KV_LINEAR_STORE 0
+#define C2KV_LINEAR_ADD 1
+#define C2KV_LINEAR_SPLIT3 2
+#define C2KV_LINEAR_SWIGLU 3
+#define C2KV_LINEAR_OVERLAP_PREVIOUS 1u
+size_t c2kv_linear_workspace_size(int32_t tokens, int32_t n_out);
+c2kv_status c2kv_linear(const void* x, int32_t tokens, int32_t k_in, const void* w, int32_t n_out,
+                        int32_t epilogue, const void* residual, void* y, void* y2, void* y3,
+                        int32_t split1, int32_t split2, void* workspace, size_t workspace_bytes,
+                        uint32_t flags, void* stream);
+c2kv_status c2kv_rmsnorm(const void* x, int32_t tokens, int32_t dim, const void* w, float eps, void* y,
+                         uint32_t flags, void* stream);
+
+/*
  * Reads and clears the device error word of the current device (waits for
  * the device).  *code receives C2KV_OK, C2KV_ETIMEOUT or C2KV_EDEVICE; the
  * return value is C2KV_ECUDA only if the read itself failed.

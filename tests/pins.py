@@ -473,3 +473,104 @@ ALL_CHECKS = [
     check_structured_attention_on_the_blog_figure,
     check_anchor_mask_uniform_scores, check_anchor_rows_are_causal_attention,
 ]
+
+
+# ------------------------------------------------- decoder step (D17 reading)
+
+def check_rms_norm(d):
+    """RMSNorm against its definition written as a loop, and a closed form:
+    a constant row c gives c / sqrt(c^2 + eps) times the weights."""
+    rng = np.random.default_rng(41)
+    eps = 1e-5
+    x = _bits(rng, (3, 24))
+    w = _bits(rng, (24,))
+    got = d.rms_norm(x, w, eps)
+    xf, wf = d.O.bf16_to_f64(x), d.O.bf16_to_f64(w)
+    for t in range(3):
+        ss = 0.0
+        for i in range(24):
+            ss += xf[t, i] * xf[t, i]
+        r = math.sqrt(ss / 24 + eps)
+        for i in range(24):
+            assert abs(got[t, i] - xf[t, i] / r * wf[i]) <= 1e-12 * (1 + abs(got[t, i]))
+    c = 0.375
+    xc = np.full((1, 16), d.O.f64_to_bf16(np.array([c]))[0], np.uint16)
+    assert np.allclose(d.rms_norm(xc, w[:16], eps)[0], c / math.sqrt(c * c + eps) * wf[:16], rtol=1e-12)
+
+
+def check_linear(d):
+    """x W^T against the triple loop."""
+    rng = np.random.default_rng(43)
+    x, w = _bits(rng, (3, 20)), _bits(rng, (7, 20))
+    got = d.linear(x, w)
+    xf, wf = d.O.bf16_to_f64(x), d.O.bf16_to_f64(w)
+    for t in range(3):
+        for n in range(7):
+            acc = 0.0
+            for k in range(20):
+                acc += xf[t, k] * wf[n, k]
+            assert abs(got[t, n] - acc) <= 1e-12 * (1 + abs(acc))
+
+
+def check_silu_and_gate_up_layout(d):
+    """silu(g) = g * sigmoid(g) (scipy's expit, a library routine), 0 at 0;
+    and the fused gate/up weight in the library's layout (64-row gate and up
+    blocks per 128-row tile) gives silu(h W_g^T) * (h W_u^T) of the separate
+    weights."""
+    g = np.linspace(-30, 30, 601)
+    assert np.allclose(d.silu(g), g * expit(g), rtol=1e-13, atol=1e-300)
+    assert d.silu(np.array([0.0]))[0] == 0.0
+    rng = np.random.default_rng(47)
+    F, k = 192, 32
+    wg, wu = _bits(rng, (F, k)), _bits(rng, (F, k))
+    fused = np.empty((2 * F, k), np.uint16)
+    for i in range(F // 64):
+        fused[128 * i:128 * i + 64] = wg[64 * i:64 * i + 64]
+        fused[128 * i + 64:128 * i + 128] = wu[64 * i:64 * i + 64]
+    h = _bits(rng, (2, k))
+    hf = d.O.bf16_to_f64(h)
+    gate = hf @ d.O.bf16_to_f64(wg).T
+    up = hf @ d.O.bf16_to_f64(wu).T
+    assert np.allclose(d.swiglu(h, fused), gate * expit(gate) * up, rtol=1e-12)
+
+
+def _decoder_case(d, rng, zero=()):
+    B, Hq, Hkv, hd, n, F = 2, 4, 2, 16, 9, 128
+    dim = Hq * hd
+    w = {"attn_norm": _bits(rng, (dim,)), "mlp_norm": _bits(rng, (dim,)),
+         "qkv": _bits(rng, ((Hq + 2 * Hkv) * hd, dim), 0.2), "o": _bits(rng, (dim, Hq * hd), 0.2),
+         "gate_up": _bits(rng, (2 * F, dim), 0.2), "down": _bits(rng, (dim, F), 0.2)}
+    for name in zero:
+        w[name] = np.zeros_like(w[name])
+    x = _bits(rng, (B, dim))
+    kc = [_bits(rng, (Hkv, n, hd)) for _ in range(B)]
+    vc = [_bits(rng, (Hkv, n, hd)) for _ in range(B)]
+    return x, w, kc, vc, (Hq, Hkv, hd)
+
+
+def check_decoder_layer_residuals_and_attention(d):
+    """A layer whose output projections are zero is the identity on the
+    residual stream; with q = 0 (zero q rows of the QKV weight) every key
+    scores the same, so each head's attention output is the plain mean of
+    its kv head's cached values and the new token's value."""
+    rng = np.random.default_rng(53)
+    x, w, kc, vc, (Hq, Hkv, hd) = _decoder_case(d, rng, zero=("o", "down"))
+    x2, st = d.decoder_layer_decode(x, w, kc, vc, [20, 31], 1.0e4, Hq, Hkv, 1e-5)
+    assert np.array_equal(x2, x) and np.array_equal(st["x1"], x)
+    x, w, kc, vc, (Hq, Hkv, hd) = _decoder_case(d, rng)
+    w["qkv"][:Hq * hd] = 0
+    x2, st = d.decoder_layer_decode(x, w, kc, vc, [20, 31], 1.0e4, Hq, Hkv, 1e-5)
+    G = Hq // Hkv
+    for b in range(2):
+        vnew = d.O.bf16_to_f64(st["v"][b].reshape(Hkv, hd))
+        for h in range(Hq):
+            vals = np.concatenate([d.O.bf16_to_f64(vc[b][h // G]), vnew[h // G][None]], axis=0)
+            want = d.O.f64_to_bf16(vals.mean(axis=0))
+            assert np.array_equal(st["att"][b].reshape(Hq, hd)[h], want), (b, h)
+    # the layer's output differs from its input once the projections are live
+    assert not np.array_equal(x2, x)
+
+
+# checks of the decoder-step oracle (they take oracle.decoder_oracle)
+DECODER_CHECKS = [check_rms_norm, check_linear, check_silu_and_gate_up_layout,
+                  check_decoder_layer_residuals_and_attention]

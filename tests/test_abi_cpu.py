@@ -232,3 +232,27 @@ def test_decode_scratch_fits_the_fixed_noalloc_array(P):
                         assert 0 < need
                         worst = max(worst, need)
     assert worst <= limit // 2, worst
+
+
+def test_linear_and_rmsnorm_host_checks(P):
+    """c2kv_linear / c2kv_rmsnorm reject bad shapes before touching the GPU;
+    the linear workspace holds the fixed counter region plus two partial
+    tiles per SM."""
+    import compressed_composable_kv_gb300.binding as bnd
+    lib = bnd.load_library()
+    ws = ctypes.c_void_p(16)
+    bad = [(0, 4096, 6144), (257, 4096, 6144), (4, 100, 6144), (4, 4096, 100), (4, 4096, 128 * 8193)]
+    for tokens, k_in, n_out in bad:
+        st = lib.c2kv_linear(ctypes.c_void_p(16), tokens, k_in, ctypes.c_void_p(16), n_out, 0, None,
+                             ctypes.c_void_p(16), None, None, 0, 0, ws, 1 << 30, 0, None)
+        assert st == P.C2KV_EINVAL, (tokens, k_in, n_out)
+    st = lib.c2kv_linear(ctypes.c_void_p(16), 4, 4096, ctypes.c_void_p(16), 6144, P.C2KV_LINEAR_SPLIT3, None,
+                         ctypes.c_void_p(16), None, None, 4096, 5120, ws, 1 << 30, 0, None)
+    assert st == P.C2KV_EINVAL      # y2 / y3 missing
+    st = lib.c2kv_linear(ctypes.c_void_p(16), 4, 4096, ctypes.c_void_p(16), 6144, 0, None,
+                         ctypes.c_void_p(16), None, None, 0, 0, ws, 100, 0, None)
+    assert st == P.C2KV_EINVAL and b"workspace" in lib.c2kv_last_error()
+    assert lib.c2kv_rmsnorm(ctypes.c_void_p(16), 4, 100, ctypes.c_void_p(16), ctypes.c_float(1e-5),
+                            ctypes.c_void_p(16), 0, None) == P.C2KV_EINVAL
+    assert P.c2kv_linear_workspace_size(4, 6144) == 8192 * 4 + 2 * 152 * 16 * 128 * 4
+    assert P.c2kv_linear_workspace_size(0, 6144) == 0

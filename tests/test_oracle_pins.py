@@ -7,12 +7,86 @@ import numpy as np
 import pytest
 
 import oracle.c2kv_oracle as O
+import oracle.decoder_oracle as DO
 import pins
 
 
 @pytest.mark.parametrize("check", pins.ALL_CHECKS, ids=lambda c: c.__name__)
 def test_pin(check):
     check(O)
+
+
+@pytest.mark.parametrize("check", pins.DECODER_CHECKS, ids=lambda c: c.__name__)
+def test_decoder_pin(check):
+    check(DO)
+
+
+def _rms_no_eps(x_bits, w_bits, eps):
+    x = O.bf16_to_f64(x_bits)
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True)) * O.bf16_to_f64(w_bits)[None, :]
+
+
+def _rms_sum_not_mean(x_bits, w_bits, eps):
+    x = O.bf16_to_f64(x_bits)
+    return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps) * O.bf16_to_f64(w_bits)[None, :]
+
+
+def _linear_last_column_dropped(x_bits, w_bits):
+    return O.bf16_to_f64(x_bits)[:, :-1] @ O.bf16_to_f64(w_bits)[:, :-1].T
+
+
+def _silu_as_sigmoid(g):
+    return 1.0 / (1.0 + np.exp(-g))
+
+
+def _gate_up_swapped(w_gu_bits):
+    n2, k = w_gu_bits.shape
+    blocks = w_gu_bits.reshape(n2 // 128, 2, 64, k)
+    return blocks[:, 1].reshape(-1, k), blocks[:, 0].reshape(-1, k)
+
+
+_REAL_LAYER = DO.decoder_layer_decode
+
+
+def _layer_without_mlp_residual(x_bits, w, k_caches, v_caches, start_pos, theta, hq, hkv, eps):
+    x2, st = _REAL_LAYER(x_bits, w, k_caches, v_caches, start_pos, theta, hq, hkv, eps)
+    m_out = DO.linear(st["m"], w["down"])
+    return DO.bf16(m_out), st
+
+
+DECODER_MUTATIONS = [
+    ("rms_norm", _rms_no_eps, pins.check_rms_norm),
+    ("rms_norm", _rms_sum_not_mean, pins.check_rms_norm),
+    ("linear", _linear_last_column_dropped, pins.check_linear),
+    ("silu", _silu_as_sigmoid, pins.check_silu_and_gate_up_layout),
+    ("split_gate_up", _gate_up_swapped, pins.check_silu_and_gate_up_layout),
+    ("decoder_layer_decode", _layer_without_mlp_residual, pins.check_decoder_layer_residuals_and_attention),
+]
+
+
+@pytest.mark.parametrize("name,bad,check", DECODER_MUTATIONS,
+                         ids=[f"{m[0]}:{m[1].__name__}" for m in DECODER_MUTATIONS])
+def test_decoder_planted_mistake_is_caught(monkeypatch, name, bad, check):
+    monkeypatch.setattr(DO, name, bad)
+    with pytest.raises(AssertionError):
+        check(DO)
+
+
+def test_decoder_attention_position_mistake_is_caught(monkeypatch):
+    """The decoder step's attention goes through attend_new_tokens: a GQA
+    mapping mistake there (h % G) breaks the q = 0 mean check of the layer."""
+    real = O.attend_new_tokens
+
+    def modulo_mapping(q_pre, k_new_pre, v_new, k_cache, v_cache, start_pos, theta):
+        t, hq, dd = q_pre.shape
+        hkv = k_new_pre.shape[1]
+        out, kr = real(q_pre, k_new_pre, v_new, k_cache, v_cache, start_pos, theta)
+        perm = [h % hkv * (hq // hkv) + h // hkv for h in range(hq)]
+        return out[:, perm], kr
+
+    monkeypatch.setattr(O, "attend_new_tokens", modulo_mapping)
+    with pytest.raises(AssertionError):
+        pins.check_decoder_layer_residuals_and_attention(DO)
 
 
 def _positions_no_minus_one(n_tokens, n_slots, k, realign=True):
