@@ -1099,10 +1099,15 @@ c2kv_status c2kv_attend_masked(const c2kv_geometry* geom, int32_t mask, int32_t 
 constexpr int kLinearMaxTiles = 8192;
 constexpr size_t kLinearCountersBytes = (size_t)kLinearMaxTiles * sizeof(int32_t);
 
+// The linear kernel runs two CTAs per SM: each keeps ~100 KB of weight tiles
+// in flight, and streaming an SM's share of HBM at the loaded latency takes
+// about twice that.
+int linear_ctas(int num_sms) { return std::min(2 * std::max(1, num_sms), 512); }
+
 size_t c2kv_linear_workspace_size(int32_t tokens, int32_t n_out) {
   if (tokens < 1 || tokens > 256 || n_out < 128 || n_out % 128 != 0 || n_out / 128 > kLinearMaxTiles) return 0;
   const int n_pad = (tokens + 15) / 16 * 16;
-  const size_t ctas = (size_t)decode_tc_ctas(sm_count_for_sizing());
+  const size_t ctas = (size_t)linear_ctas(sm_count_for_sizing());
   return kLinearCountersBytes + 2 * ctas * n_pad * 128 * sizeof(float);
 }
 
@@ -1151,7 +1156,7 @@ c2kv_status c2kv_linear(const void* x, int32_t tokens, int32_t k_in, const void*
   p.split2 = split2;
   p.stages = linear_stages(n_pad);
   p.epi = epilogue;
-  C2KV_CUDA(launch_linear(p, decode_tc_ctas(sms), (flags & C2KV_LINEAR_OVERLAP_PREVIOUS) != 0,
+  C2KV_CUDA(launch_linear(p, linear_ctas(sms), (flags & C2KV_LINEAR_OVERLAP_PREVIOUS) != 0,
                           static_cast<cudaStream_t>(stream)));
   return C2KV_OK;
 }

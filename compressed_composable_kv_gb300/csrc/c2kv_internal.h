@@ -374,6 +374,7 @@ struct DecodeTcParams {
 // `tokens` read as zero), both with 128-byte swizzle.
 enum LinearEpilogue : int32_t { kLinearStore = 0, kLinearAdd = 1, kLinearSplit3 = 2, kLinearSwiglu = 3 };
 constexpr int kLinearSmemMax = 232448;
+constexpr int kLinearSmemPerCta = 113 * 1024;   // two CTAs per SM (228 KB, 1 KB reserved per CTA)
 struct LinearParams {
   CUtensorMap tm_w;
   CUtensorMap tm_x;

@@ -41,11 +41,14 @@ constexpr int LT_W_BYTES = LT_BM * LT_BK * 2;   // 16 KB
 constexpr int LT_MAX_STAGES = 16;
 constexpr int LT_MISC = 2 * LT_MAX_STAGES + 8;  // barriers
 constexpr int LT_XCH_COLS = 16;                  // SwiGLU exchange: columns per round
+constexpr int kMergeChunk = 16;                  // partial tiles whose loads are in flight together
 
 __host__ __device__ constexpr int lt_stage_bytes(int n_pad) { return LT_W_BYTES + n_pad * LT_BK * 2; }
 
+constexpr int kLinearMaxCtas = 512;              // CTAs of one launch (2 per SM)
+
 struct LtLayout {
-  int stage, off_xch, off_map, off_bar, off_misc, total;
+  int stage, off_xch, off_map, off_slots, off_bar, off_misc, total;
 };
 
 __host__ __device__ inline LtLayout lt_layout(int n_pad, int stages) {
@@ -53,7 +56,8 @@ __host__ __device__ inline LtLayout lt_layout(int n_pad, int stages) {
   l.stage = lt_stage_bytes(n_pad);
   l.off_xch = stages * l.stage;                                   // SwiGLU exchange [64][16] fp32
   l.off_map = l.off_xch + 64 * LT_XCH_COLS * 4;
-  l.off_bar = l.off_map + (int)((sizeof(DecodeMap) + 15) / 16 * 16);
+  l.off_slots = l.off_map + (int)((sizeof(DecodeMap) + 15) / 16 * 16);   // merge: contributors' slots
+  l.off_bar = l.off_slots + kLinearMaxCtas * 4;
   l.off_misc = l.off_bar + LT_MISC * 8;
   l.total = l.off_misc + 64 + 1024;                               // + slack for 1024-byte alignment
   return l;
@@ -62,7 +66,7 @@ __host__ __device__ inline LtLayout lt_layout(int n_pad, int stages) {
 __device__ __forceinline__ float silu(float g) { return g / (1.f + __expf(-g)); }
 
 template <int EPI>
-__global__ void __launch_bounds__(LT_THREADS, 1) linear_tc_kernel(const __grid_constant__ LinearParams p) {
+__global__ void __launch_bounds__(LT_THREADS, 2) linear_tc_kernel(const __grid_constant__ LinearParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const LtLayout lay = lt_layout(p.n_pad, p.stages);
@@ -78,6 +82,7 @@ __global__ void __launch_bounds__(LT_THREADS, 1) linear_tc_kernel(const __grid_c
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem + lay.off_misc + 16);
   float* xch = reinterpret_cast<float*>(smem + lay.off_xch);
   DecodeMap& M = *reinterpret_cast<DecodeMap*>(smem + lay.off_map);
+  int32_t* mslots = reinterpret_cast<int32_t*>(smem + lay.off_slots);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -198,18 +203,24 @@ __global__ void __launch_bounds__(LT_THREADS, 1) linear_tc_kernel(const __grid_c
     int k_sync = 0, seg = 0, arrived = -1;
     bool ok = true;
     // Stores one output column chunk: v[c] is token c0 + c of weight row n.
-    auto emit = [&](int tile, int c0, const float* v, int nc) {
+    // (loops over the 16 columns are unrolled with a guard so that v stays in
+    // registers)
+    auto emit = [&](int tile, int c0, const float (&v)[16], int nc) {
       const int n = tile * LT_BM + tid;
       if (EPI == kLinearSwiglu) {
         // rows 0..63 of the tile are gate rows of features 64*tile + r, rows
         // 64..127 the up rows of the same features
-        if (tid >= 64)
-          for (int c = 0; c < nc; ++c) xch[(tid - 64) * LT_XCH_COLS + c] = v[c];
+        if (tid >= 64) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            if (c < nc) xch[(tid - 64) * LT_XCH_COLS + c] = v[c];
+        }
         return;
       }
-      for (int c = 0; c < nc; ++c) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
         const int t = c0 + c;
-        if (t >= T) break;
+        if (c >= nc) break;
         float val = v[c];
         if (EPI == kLinearAdd) val += __bfloat162float(p.residual[(size_t)t * p.n_out + n]);
         if (EPI == kLinearSplit3) {
@@ -225,13 +236,14 @@ __global__ void __launch_bounds__(LT_THREADS, 1) linear_tc_kernel(const __grid_c
       }
     };
     // SwiGLU: after the up rows staged their values, the gate rows finish.
-    auto emit_swiglu = [&](int tile, int c0, const float* v, int nc) -> bool {
+    auto emit_swiglu = [&](int tile, int c0, const float (&v)[16], int nc) -> bool {
       if (!group_sync(grp_bar, k_sync, abort_flag, p.err)) return false;
       if (tid < 64) {
         const int f = tile * 64 + tid;
-        for (int c = 0; c < nc; ++c) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
           const int t = c0 + c;
-          if (t >= T) break;
+          if (c >= nc) break;
           p.y[(size_t)t * (p.n_out / 2) + f] = __float2bfloat16_rn(silu(v[c]) * xch[tid * LT_XCH_COLS + c]);
         }
       }
@@ -260,7 +272,9 @@ __global__ void __launch_bounds__(LT_THREADS, 1) linear_tc_kernel(const __grid_c
           emit(tile, c0, v, nc);
           if (EPI == kLinearSwiglu) ok = emit_swiglu(tile, c0, v, nc);
         } else {
-          for (int c = 0; c < nc; ++c) p.part[((size_t)slot * p.n_pad + c0 + c) * LT_BM + tid] = v[c];
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            if (c < nc) p.part[((size_t)slot * p.n_pad + c0 + c) * LT_BM + tid] = v[c];
         }
       }
       tc_fence_before();
@@ -284,17 +298,34 @@ __global__ void __launch_bounds__(LT_THREADS, 1) linear_tc_kernel(const __grid_c
           // ---- sum the tile's partials in CTA order, then the epilogue
           const int64_t uf = (int64_t)tile * kc;
           const int cf = decode_cta_of(M, uf), cl = decode_cta_of(M, uf + kc - 1);
+          const int nctr = cl - cf + 1;
+          // the contributors' slots, one per thread (each takes a few 64-bit
+          // divisions), then kMergeChunk contributors' loads in flight at a
+          // time, summed in CTA order
+          for (int kk = tid; kk < nctr; kk += LT_EPI_THREADS)
+            mslots[kk] = decode_cta_empty(M, cf + kk) ? -1 : decode_slot_of(M, cf + kk, uf);
+          ok = group_sync(grp_bar, k_sync, abort_flag, p.err);
           for (int c0 = 0; ok && c0 < T; c0 += 16) {
             const int nc = min(16, T - c0);
             float v[16];
 #pragma unroll
             for (int c = 0; c < 16; ++c) v[c] = 0.f;
-            for (int c = cf; c <= cl; ++c) {
-              if (decode_cta_empty(M, c)) continue;
-              const float* src = p.part + ((size_t)decode_slot_of(M, c, uf) * p.n_pad + c0) * LT_BM + tid;
+            for (int q0 = 0; q0 < nc; q0 += 4) {   // 4 columns at a time
+              for (int k0 = 0; k0 < nctr; k0 += kMergeChunk) {
+                float got[kMergeChunk][4];
 #pragma unroll
-              for (int cc = 0; cc < 16; ++cc)
-                if (cc < nc) v[cc] += __ldcg(src + (size_t)cc * LT_BM);
+                for (int k = 0; k < kMergeChunk; ++k) {
+                  const int sl = k0 + k < nctr ? mslots[k0 + k] : -1;   // -1: an empty CTA
+                  const float* src = p.part + ((size_t)(sl < 0 ? 0 : sl) * p.n_pad + c0 + q0) * LT_BM + tid;
+#pragma unroll
+                  for (int cc = 0; cc < 4; ++cc)
+                    got[k][cc] = (sl >= 0 && q0 + cc < nc) ? __ldcg(src + (size_t)cc * LT_BM) : 0.f;
+                }
+#pragma unroll
+                for (int k = 0; k < kMergeChunk; ++k)
+#pragma unroll
+                  for (int cc = 0; cc < 4; ++cc) v[q0 + cc] += got[k][cc];
+              }
             }
             emit(tile, c0, v, nc);
             if (EPI == kLinearSwiglu) ok = emit_swiglu(tile, c0, v, nc);
@@ -412,10 +443,14 @@ cudaError_t launch_lt(const LinearParams& p, int ctas, bool overlap, cudaStream_
 
 }  // namespace
 
-// Pipeline depth for `n_pad` token columns within the shared-memory budget.
+// Pipeline depth for `n_pad` token columns: as deep as half an SM's shared
+// memory allows, so that two CTAs fit on an SM and a launch's CTAs become
+// resident, and stream their first weight tiles, while the kernel before it
+// on the stream finishes.  (A decode-time product moves ~44 GB/s per SM;
+// ~100 KB in flight covers the ~2 us memory latency.)
 int linear_stages(int n_pad) {
   int s = LT_MAX_STAGES;
-  while (s > 2 && lt_layout(n_pad, s).total > kLinearSmemMax) --s;
+  while (s > 2 && lt_layout(n_pad, s).total > kLinearSmemPerCta) --s;
   return s;
 }
 

@@ -254,5 +254,5 @@ def test_linear_and_rmsnorm_host_checks(P):
     assert st == P.C2KV_EINVAL and b"workspace" in lib.c2kv_last_error()
     assert lib.c2kv_rmsnorm(ctypes.c_void_p(16), 4, 100, ctypes.c_void_p(16), ctypes.c_float(1e-5),
                             ctypes.c_void_p(16), 0, None) == P.C2KV_EINVAL
-    assert P.c2kv_linear_workspace_size(4, 6144) == 8192 * 4 + 2 * 152 * 16 * 128 * 4
+    assert P.c2kv_linear_workspace_size(4, 6144) == 8192 * 4 + 2 * 304 * 16 * 128 * 4
     assert P.c2kv_linear_workspace_size(0, 6144) == 0
