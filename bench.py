@@ -853,11 +853,76 @@ def run_kernel_probe(args) -> None:
     keys = sum(n + Q + t + 1 for n in lens for t in range(T)) / T
     gbs = keys * H * D * 4 / t_launch / 1e9
     peak = measured_peaks().get("hbm_gbs") or 6800.0
-    print(json.dumps({"kernel_probe": w.name, "layers": L, "batch": B, "composed_slots": lens, "question_tokens": Q,
-                      "decode_us_per_launch": t_launch * 1e6, "decode_attention_gbs": gbs,
-                      "decode_frac_of_hbm_peak": gbs / peak,
-                      "note": (f"{L} layers of random caches; eager: {L if Q else 0} prefill + {L} decode launches, "
-                               f"then {T} decode steps x {L} layers from a graph (timed)")}))
+    line = {"kernel_probe": w.name, "layers": L, "batch": B, "composed_slots": lens, "question_tokens": Q,
+            "decode_us_per_launch": t_launch * 1e6, "decode_attention_gbs": gbs,
+            "decode_frac_of_hbm_peak": gbs / peak,
+            "note": (f"{L} layers of random caches; eager: {L if Q else 0} prefill + {L} decode launches, "
+                     f"then {T} decode steps x {L} layers from a graph (timed)")}
+    del kc, vc, tabs, graph
+    torch.cuda.empty_cache()
+    if is_llama(g0):
+        line["linear"] = probe_linears(P, S, B, stream, peak)
+    print(json.dumps(line))
+
+
+def probe_linears(P, S, tokens: int, stream, peak: float, sets: int = 4) -> dict:
+    """Each projection of the Llama-3.1-8B layer (and the LM head) for `tokens`
+    tokens: `sets` distinct seeded weights of each (so every call reads its
+    weights from HBM), called back to back from a CUDA graph; per call time and
+    weight bytes / time against the HBM peak.  The first eager calls are the
+    launches the linear kernel's profile is taken on."""
+    import torch
+    shape = S.LLAMA31_8B_MODEL
+    dim, F = shape.dim, shape.ffn
+    kinds = {"qkv": (6144, dim, P.C2KV_LINEAR_SPLIT3), "o": (dim, dim, P.C2KV_LINEAR_ADD),
+             "gate_up": (2 * F, dim, P.C2KV_LINEAR_SWIGLU), "down": (dim, F, P.C2KV_LINEAR_ADD),
+             "lm_head": (shape.vocab, dim, P.C2KV_LINEAR_STORE)}
+    gen = torch.Generator(device="cuda").manual_seed(11)
+    ws = torch.zeros(P.c2kv_linear_workspace_size(tokens, shape.vocab), dtype=torch.uint8, device="cuda")
+    P.c2kv_workspace_init(ws)
+    out = {}
+    for name, (n, k, epi) in kinds.items():
+        wts = [(torch.randn((n, k), device="cuda", generator=gen) * k ** -0.5).to(torch.bfloat16)
+               for _ in range(sets)]
+        x = torch.randn((tokens, k), device="cuda", generator=gen).to(torch.bfloat16)
+        width = {P.C2KV_LINEAR_SPLIT3: 4096, P.C2KV_LINEAR_SWIGLU: n // 2}.get(epi, n)
+        y = torch.zeros((tokens, width), device="cuda", dtype=torch.bfloat16)
+        y2 = torch.zeros((tokens, 1024), device="cuda", dtype=torch.bfloat16)
+        y3 = torch.zeros((tokens, 1024), device="cuda", dtype=torch.bfloat16)
+
+        def run():
+            for wt in wts:
+                kw = {}
+                if epi == P.C2KV_LINEAR_SPLIT3:
+                    kw = dict(y2=y2, y3=y3, split1=4096, split2=5120)
+                elif epi == P.C2KV_LINEAR_ADD:
+                    kw = dict(residual=y)
+                P.c2kv_linear(x, wt, y, ws, epi, stream=stream, flags=P.C2KV_LINEAR_OVERLAP_PREVIOUS, **kw)
+
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            run()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                run()
+        ts = []
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                graph.replay()
+                b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b) / 1e3 / sets)
+        t = statistics.median(ts[1:])
+        out[name] = {"us": t * 1e6, "weight_bytes": n * k * 2, "gbs": n * k * 2 / t / 1e9,
+                     "frac_of_hbm_peak": n * k * 2 / t / 1e9 / peak}
+        del wts, graph
+        torch.cuda.empty_cache()
+    assert P.c2kv_device_error() == P.C2KV_OK
+    return out
 
 
 def run_extract(args) -> None:
