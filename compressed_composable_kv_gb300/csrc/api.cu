@@ -106,12 +106,17 @@ struct Seg {
 struct c2kv_store_s {
   c2kv_geometry g{};
   int device = 0;
-  uint8_t* pool = nullptr;
+  uint8_t* pool = nullptr;       // pinned host pool
+  uint8_t* pool_dev = nullptr;   // the same pool's address on the device (read by the composition kernel)
   size_t pool_bytes = 0, used = 0;
   std::unordered_map<int32_t, Seg> docs;
   cudaStream_t side = nullptr;
-  cudaEvent_t fork = nullptr;
+  // Events that order the copy stream and the callers' streams, used in
+  // turn: an event is recorded again only after kEventRing later records, so
+  // that no record waits on an earlier record of the same event still in
+  // flight (which held the host thread back to the copies' pace).
   std::vector<cudaEvent_t> ev;
+  size_t ev_next = 0;
   std::mutex mu;
   // the last composition into each RoPE table (one per request), which a
   // C2KV_COMPOSE_CONTINUE call must match; at most kMaxTrackedTables tables,
@@ -128,7 +133,7 @@ struct c2kv_store_s {
 };
 
 namespace {
-constexpr int kLayerGroups = 4;   // copy/rotate pipeline depth of one compose
+constexpr int kEventRing = 64;    // events of a store, recorded in turn
 constexpr size_t kMaxTrackedTables = 1024;
 
 // Composition plan shared by c2kv_plan and c2kv_compose.
@@ -530,7 +535,14 @@ c2kv_status c2kv_store_create(const c2kv_geometry* geom, size_t pinned_bytes, c2
   st->g = *geom;
   cudaError_t e = cudaGetDevice(&st->device);
   if (e == cudaSuccess && pinned_bytes > 0) {
-    e = cudaHostAlloc(reinterpret_cast<void**>(&st->pool), pinned_bytes, cudaHostAllocDefault);
+    e = cudaHostAlloc(reinterpret_cast<void**>(&st->pool), pinned_bytes, cudaHostAllocMapped);
+    if (e == cudaSuccess) {
+      e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&st->pool_dev), st->pool, 0);
+      if (e != cudaSuccess) {
+        cudaFreeHost(st->pool);
+        st->pool = nullptr;
+      }
+    }
     if (e != cudaSuccess) {
       cudaGetLastError();
       delete st;
@@ -539,8 +551,7 @@ c2kv_status c2kv_store_create(const c2kv_geometry* geom, size_t pinned_bytes, c2
     st->pool_bytes = pinned_bytes;
   }
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&st->side, cudaStreamNonBlocking);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st->fork, cudaEventDisableTiming);
-  for (int i = 0; e == cudaSuccess && i < kLayerGroups; ++i) {
+  for (int i = 0; e == cudaSuccess && i < kEventRing; ++i) {
     cudaEvent_t ev;
     e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
     if (e == cudaSuccess) st->ev.push_back(ev);
@@ -559,7 +570,6 @@ void c2kv_store_destroy(c2kv_store st) {
     cudaStreamSynchronize(st->side);
     cudaStreamDestroy(st->side);
   }
-  if (st->fork) cudaEventDestroy(st->fork);
   for (cudaEvent_t ev : st->ev) cudaEventDestroy(ev);
   if (st->pool) cudaFreeHost(st->pool);
   delete st;
@@ -777,28 +787,19 @@ c2kv_status c2kv_compose_layers(c2kv_store st, int32_t n_docs, const int32_t* do
   int dev = -1;
   C2KV_CUDA(cudaGetDevice(&dev));
   if (dev != st->device) return fail(C2KV_EINVAL, "current device differs from the store's device");
-  unsigned* err = nullptr;
-  s = device_state(&err, nullptr);
+  s = device_state(nullptr, nullptr);
   if (s != C2KV_OK) return s;
 
   cudaStream_t us = static_cast<cudaStream_t>(stream);
   const int D = g.head_dim, H = g.n_kv_heads;
-  const size_t elem = 2;
   CosSin2* tab = static_cast<CosSin2*>(rope_table_out);
 
-  // Copies run on the store's stream after the caller's earlier work (a
-  // continuation: after the copies of the composition it continues).
-  if (!cont) {
-    C2KV_CUDA(cudaEventRecord(st->fork, us));
-    C2KV_CUDA(cudaStreamWaitEvent(st->side, st->fork, 0));
-    st->last.erase(rope_table_out);
-  }
-
-  // The cos/sin table of every cache row is built on the caller's stream
-  // while the first copies are in flight.
+  // The cos/sin table of every cache row is built on the caller's stream by
+  // the first call of a composition.
   static TableParams tp;   // large (segment table); guarded by the store mutex and g_tab_mu
   static std::mutex g_tab_mu;
   if (!cont) {
+    st->last.erase(rope_table_out);
     std::lock_guard<std::mutex> tl(g_tab_mu);
     std::memset(&tp, 0, sizeof(tp));
     tp.tab = tab;
@@ -840,45 +841,42 @@ c2kv_status c2kv_compose_layers(c2kv_store st, int32_t n_docs, const int32_t* do
   }
   if (total == 0) return C2KV_OK;
 
-  RopeParams rp;
-  std::memset(&rp, 0, sizeof(rp));
-  rp.k_cache = static_cast<__nv_bfloat16*>(k_cache);
-  rp.tab = tab;
-  rp.err = err;
-  rp.cap = cap;
-  rp.n_kv = H;
-  rp.n_total = total;
-
-  // Each layer group's re-rotation runs on the caller's stream once its
-  // copies have landed (and after the table, which is earlier on that stream).
-  // Up to kLayerGroups copy/rotate groups per call, of at least 4 layers
-  // each, so that each re-rotation launch has enough rows to stream at the
-  // HBM rate (a layer-group continuation of 4 layers is one group).
-  const int nl = layer_end - layer_begin;
-  const int ngroups = std::max(1, std::min(kLayerGroups, nl / 4));
-  uint8_t* kc = static_cast<uint8_t*>(k_cache);
-  uint8_t* vc = static_cast<uint8_t*>(v_cache);
-  for (int gi = 0; gi < ngroups; ++gi) {
-    const int l0 = layer_begin + gi * nl / ngroups, l1 = layer_begin + (gi + 1) * nl / ngroups;
-    for (int c = 0; c < n_docs; ++c) {
-      const int d = order ? order[c] : c;
-      const Seg& sg = segs[d];
-      const size_t spitch = (size_t)sg.n_slots * D * elem;          // one (layer, head) run in the store
-      const size_t dpitch = (size_t)cap * D * elem;                  // one (layer, head) run in the cache
-      const size_t src_off = (size_t)l0 * H * spitch;
-      const size_t dst_off = ((size_t)l0 * H * cap + slot0[c]) * D * elem;
-      const size_t height = (size_t)(l1 - l0) * H;
-      C2KV_CUDA(cudaMemcpy2DAsync(kc + dst_off, dpitch, st->pool + sg.k_off + src_off, spitch, spitch, height,
-                                  cudaMemcpyHostToDevice, st->side));
-      C2KV_CUDA(cudaMemcpy2DAsync(vc + dst_off, dpitch, st->pool + sg.v_off + src_off, spitch, spitch, height,
-                                  cudaMemcpyHostToDevice, st->side));
-    }
-    C2KV_CUDA(cudaEventRecord(st->ev[gi], st->side));
-    C2KV_CUDA(cudaStreamWaitEvent(us, st->ev[gi], 0));
-    rp.layer0 = l0;
-    rp.layer1 = l1;
-    C2KV_CUDA(launch_rerope(rp, D, us));
+  // The composition kernel runs on the store's stream, after the caller's
+  // earlier work and the table (a continuation: after the kernel of the call
+  // it continues), so that work the caller enqueues between calls (the
+  // question prefill of the layers already composed) overlaps it; the
+  // caller's stream waits for it.
+  if (!cont) {
+    const cudaEvent_t fork = st->ev[st->ev_next++ % st->ev.size()];
+    C2KV_CUDA(cudaEventRecord(fork, us));
+    C2KV_CUDA(cudaStreamWaitEvent(st->side, fork, 0));
   }
+  static ComposeParams cp;   // large (segment table); guarded by the store mutex and g_cmp_mu
+  static std::mutex g_cmp_mu;
+  {
+    std::lock_guard<std::mutex> cl(g_cmp_mu);
+    std::memset(&cp, 0, sizeof(cp));
+    cp.k_cache = static_cast<__nv_bfloat16*>(k_cache);
+    cp.v_cache = static_cast<__nv_bfloat16*>(v_cache);
+    cp.tab = tab;
+    cp.cap = cap;
+    cp.n_kv = H;
+    cp.layer0 = layer_begin;
+    cp.layer1 = layer_end;
+    cp.n_total = total;
+    cp.n_docs = n_docs;
+    for (int c = 0; c < n_docs; ++c) {
+      const Seg& sg = segs[order ? order[c] : c];
+      cp.seg[c].k = reinterpret_cast<const __nv_bfloat16*>(st->pool_dev + sg.k_off);
+      cp.seg[c].v = reinterpret_cast<const __nv_bfloat16*>(st->pool_dev + sg.v_off);
+      cp.seg[c].slot0 = slot0[c];
+      cp.seg[c].n_slots = sg.n_slots;
+    }
+    C2KV_CUDA(launch_compose(cp, D, st->side));
+  }
+  const cudaEvent_t landed = st->ev[st->ev_next++ % st->ev.size()];
+  C2KV_CUDA(cudaEventRecord(landed, st->side));
+  C2KV_CUDA(cudaStreamWaitEvent(us, landed, 0));
   return C2KV_OK;
 }
 

@@ -253,11 +253,22 @@ struct SegDesc {
   int32_t n_tokens;
 };
 
-struct RopeParams {
+// One document of a composition, in composed order.
+struct ComposeSeg {
+  const __nv_bfloat16* k;   // the document's pre-RoPE K [L][Hkv][n_slots][d] (pinned host pool, device address)
+  const __nv_bfloat16* v;   // its V, same layout
+  int32_t slot0;            // first composed row
+  int32_t n_slots;
+};
+
+constexpr int kComposeCtas = 48;   // CTAs of one composition launch (~1.5 MB of host reads in flight)
+
+struct ComposeParams {
   __nv_bfloat16* k_cache;   // [L][Hkv][cap][d]
+  __nv_bfloat16* v_cache;
   const CosSin2* tab;       // [cap][d/2]: cos/sin of every cache row's position
-  unsigned* err;
-  int32_t cap, n_kv, layer0, layer1, n_total;
+  int32_t cap, n_kv, layer0, layer1, n_total, n_docs;
+  ComposeSeg seg[kMaxDocsPerCompose];
 };
 
 // Builds the per-row cos/sin table (the only kernel that calls fp64 sincos).
@@ -397,7 +408,7 @@ cudaError_t launch_decode_tc(const DecodeTcParams& p, int group, int ctas, bool 
 // Clusters of `cs` CTAs of the tensor-core decode that fit the device at once
 // (0 if unknown).
 int decode_tc_active_clusters(int group, int cs);
-cudaError_t launch_rerope(const RopeParams& p, int head_dim, cudaStream_t st);
+cudaError_t launch_compose(const ComposeParams& p, int head_dim, cudaStream_t st);
 cudaError_t launch_rope_table(const TableParams& p, cudaStream_t st);
 cudaError_t launch_append(const AppendParams& p, int head_dim, int batch, cudaStream_t st);
 cudaError_t launch_attention(const AttnParams& p, int head_dim, int group, bool overlap, cudaStream_t st);

@@ -1,4 +1,5 @@
-// Re-rotation of composed segments, and rotate-and-append of new tokens.
+// Composition of stored segments into the cache (host-link gather with
+// re-rotation), and rotate-and-append of new tokens.
 //
 // C2KV explainer (paper-daily.com), section "positions at concatenation"
 // (拼接时位置怎么处理？): segments are stored before RoPE and rotated at
@@ -6,6 +7,8 @@
 // off_c + min((j+1)k, n_c) - 1, where off_c is the summed original length of
 // the documents before it.  Rotation is the rotate-half form: pair
 // (i, i + d/2) turns by pos * theta^(-2i/d).
+#include <algorithm>
+
 #include "c2kv_internal.h"
 
 namespace c2kv {
@@ -46,63 +49,102 @@ __global__ void rope_table_kernel(const __grid_constant__ TableParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// K1: in-place re-rotation of composed K rows for a group of layers.
-// One CTA owns kSlots (16) consecutive composed slots: it stages their rows of
-// the cos/sin table in shared memory once and rotates those slots' rows in
-// every (layer, kv head) of the group with 16-byte loads/stores.  V rows are
-// never touched (they land by DMA).  A thread owns the 8 pairs of one 16-byte
-// chunk; the staged rows are transposed (pair 8c + e at e * TPR + c) so that
-// the 8 lanes of a row read 8 neighbouring entries instead of entries 128
-// bytes apart on the same banks.
+// K0 + K1: the composition of one request over a range of layers, in one
+// pass from the pinned host pool to the cache.  The SMs read each
+// document's pre-RoPE K and V rows straight from the pinned pool (mapped
+// into the device's address space) over the host link, rotate K at the
+// slot's composed position and write K and V at their composed rows.  (A
+// copy-engine transfer followed by an in-place rotation reads and writes K
+// in HBM once more, and needs one 2-D copy per document and layer group;
+// the 16-byte loads of a few CTAs saturate the link on their own.)
+//
+// A few persistent CTAs (kComposeCtas): enough loads in flight to cover the
+// link's latency, and a footprint small enough to sit beside the decode
+// kernel of another request on the same SMs (its registers and shared
+// memory fit beside the decode kernel's for up to 5 q heads per kv head).
+// A CTA takes tiles of kSlots (8) consecutive composed slots in turn: it
+// stages their rows of the cos/sin table in shared memory once (transposed,
+// pair 8c + e at e * TPR + c, so that the 8 lanes of a row read 8
+// neighbouring entries), looks up each slot's document and index in it,
+// then moves the slots' rows of every (layer, kv head) of the range.  A
+// thread owns the 8 pairs of one 16-byte chunk of K (and the same chunks of
+// V).
 // ---------------------------------------------------------------------------
-constexpr int kSlots = 16;
-constexpr int kRopeThreads = 256;
+constexpr int kSlots = 8;
+constexpr int kComposeThreads = 128;
 
 template <int D>
-__global__ void __launch_bounds__(kRopeThreads) rerope_kernel(const __grid_constant__ RopeParams p) {
+__global__ void __launch_bounds__(kComposeThreads) compose_kernel(const __grid_constant__ ComposeParams p) {
   constexpr int H = D / 2;
   constexpr int TPR = H / 8;   // threads per row, each owns 8 pairs
   __shared__ CosSin2 tab[kSlots][H];
+  __shared__ const __nv_bfloat16* src_k[kSlots];   // the slot's row in layer 0, kv head 0 of its document
+  __shared__ const __nv_bfloat16* src_v[kSlots];
+  __shared__ int64_t src_lh[kSlots];               // elements between (layer, head) runs of its document
 
-  const int slot0 = blockIdx.x * kSlots;
-  const int n_here = min(kSlots, p.n_total - slot0);
-  for (int i = threadIdx.x; i < n_here * H; i += kRopeThreads) {
-    const int f = i % H;
-    tab[i / H][(f % 8) * TPR + f / 8] = p.tab[(size_t)slot0 * H + i];
-  }
-  __syncthreads();
-
+  const int n_tiles = (p.n_total + kSlots - 1) / kSlots;
   const int n_rows = (p.layer1 - p.layer0) * p.n_kv;   // (layer, head) row blocks
   const int work = n_rows * kSlots * TPR;
-  constexpr int U = 4;
-  for (int w0 = threadIdx.x; w0 < work; w0 += kRopeThreads * U) {
-    uint4 a[U], b[U];
-    uint4* base[U];
-    int r_[U], c_[U];
-    bool ok[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int w = w0 + u * kRopeThreads;
-      const int c = w % TPR;
-      const int r = (w / TPR) % kSlots;
-      const int lh = w / (TPR * kSlots);
-      ok[u] = (w < work) && (r < n_here);
-      r_[u] = r;
-      c_[u] = c;
-      base[u] = nullptr;
-      if (ok[u]) {
-        const size_t row = ((size_t)(p.layer0 * p.n_kv + lh) * p.cap + slot0 + r) * D;
-        base[u] = reinterpret_cast<uint4*>(p.k_cache + row);
-        a[u] = base[u][c];
-        b[u] = base[u][c + TPR];
-      }
+  for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const int slot0 = tile * kSlots;
+    const int n_here = min(kSlots, p.n_total - slot0);
+    __syncthreads();   // the previous tile's staged rows are no longer read
+    for (int i = threadIdx.x; i < n_here * H; i += kComposeThreads) {
+      const int f = i % H;
+      tab[i / H][(f % 8) * TPR + f / 8] = p.tab[(size_t)slot0 * H + i];
     }
+    if (threadIdx.x < n_here) {
+      const int s = slot0 + threadIdx.x;
+      int lo = 0, hi = p.n_docs - 1;   // last document with seg.slot0 <= s
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.seg[mid].slot0 <= s) lo = mid; else hi = mid - 1;
+      }
+      const ComposeSeg sg = p.seg[lo];
+      const int64_t lh = (int64_t)sg.n_slots * D;
+      const int64_t off = (int64_t)p.layer0 * p.n_kv * lh + (int64_t)(s - sg.slot0) * D;
+      src_k[threadIdx.x] = sg.k + off;
+      src_v[threadIdx.x] = sg.v + off;
+      src_lh[threadIdx.x] = lh;
+    }
+    __syncthreads();
+
+    constexpr int U = 4;
+    for (int w0 = threadIdx.x; w0 < work; w0 += kComposeThreads * U) {
+      uint4 ka[U], kb[U], va[U], vb[U];
+      int r_[U], c_[U];
+      size_t dst[U];
+      bool ok[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if (ok[u]) {
-        rotate8_df<TPR>(a[u], b[u], &tab[r_[u]][c_[u]]);
-        base[u][c_[u]] = a[u];
-        base[u][c_[u] + TPR] = b[u];
+      for (int u = 0; u < U; ++u) {
+        const int w = w0 + u * kComposeThreads;
+        const int c = w % TPR;
+        const int r = (w / TPR) % kSlots;
+        const int lh = w / (TPR * kSlots);
+        ok[u] = (w < work) && (r < n_here);
+        r_[u] = r;
+        c_[u] = c;
+        dst[u] = ((size_t)(p.layer0 * p.n_kv + lh) * p.cap + slot0 + r) * D;
+        if (ok[u]) {
+          const uint4* ks = reinterpret_cast<const uint4*>(src_k[r] + lh * src_lh[r]);
+          const uint4* vs = reinterpret_cast<const uint4*>(src_v[r] + lh * src_lh[r]);
+          ka[u] = ks[c];
+          kb[u] = ks[c + TPR];
+          va[u] = vs[c];
+          vb[u] = vs[c + TPR];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (ok[u]) {
+          rotate8_df<TPR>(ka[u], kb[u], &tab[r_[u]][c_[u]]);
+          uint4* kd = reinterpret_cast<uint4*>(p.k_cache + dst[u]);
+          uint4* vd = reinterpret_cast<uint4*>(p.v_cache + dst[u]);
+          kd[c_[u]] = ka[u];
+          kd[c_[u] + TPR] = kb[u];
+          vd[c_[u]] = va[u];
+          vd[c_[u] + TPR] = vb[u];
+        }
       }
     }
   }
@@ -182,11 +224,11 @@ __global__ void advance_kernel(int batch, int32_t* n_cached, int delta) {
 
 }  // namespace
 
-cudaError_t launch_rerope(const RopeParams& p, int head_dim, cudaStream_t st) {
-  const int blocks = (p.n_total + kSlots - 1) / kSlots;
+cudaError_t launch_compose(const ComposeParams& p, int head_dim, cudaStream_t st) {
+  const int blocks = std::min(kComposeCtas, (p.n_total + kSlots - 1) / kSlots);
   if (blocks == 0) return cudaSuccess;
-  if (head_dim == 128) rerope_kernel<128><<<blocks, kRopeThreads, 0, st>>>(p);
-  else rerope_kernel<64><<<blocks, kRopeThreads, 0, st>>>(p);
+  if (head_dim == 128) compose_kernel<128><<<blocks, kComposeThreads, 0, st>>>(p);
+  else compose_kernel<64><<<blocks, kComposeThreads, 0, st>>>(p);
   return cudaGetLastError();
 }
 

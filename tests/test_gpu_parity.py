@@ -209,8 +209,11 @@ def test_k1_composition_equals_uncompressed():
 
 def test_varlen_batch_pool():
     """Batch of 16 requests drawn from a document pool in random order
-    (lengths 500..4000 tokens, one not a multiple of k), 2 layers."""
-    g = S.Geometry(2, 32, 8, 128, 5.0e5)
+    (lengths 500..4000 tokens, one not a multiple of k) through the full
+    32-layer Llama stack (the pool workload's launch configuration: per
+    sequence decode splits over 16 composed lengths of ~18 000 slots);
+    checked on the first and last layer of three requests."""
+    g = S.LLAMA31_8B
     rng = np.random.default_rng(0xC2C2)
     lens = [int(x) for x in rng.choice(np.arange(500, 4001, 4), 40)]
     lens[5] = 1003
@@ -224,7 +227,7 @@ def test_varlen_batch_pool():
     inputs = S.make_step_inputs(w)
     pre, dec = run_all(sc, upload(inputs))
     for b in (0, 5, 15):
-        check_request(sc, inputs, pre, dec, b, layers=[1], steps=[0, 3])
+        check_request(sc, inputs, pre, dec, b, layers=[0, 31], steps=[0, 3])
     sc.close()
 
 
