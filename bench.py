@@ -307,10 +307,8 @@ def run_ours(args, rank: int, world: int) -> dict:
     docs_meta, reqs = S.make_requests(w)
     used = sorted({d for r in reqs for d in r.doc_ids})
     seg_bytes = {i: 2 * g.n_layers * g.n_kv_heads * docs_meta[i][1] * g.head_dim * 2 for i in used}
-    # The pinned pool is allocated before the documents are drawn, each
-    # document is drawn, stored and dropped in turn: the pool then takes its
-    # pages from an unfragmented host memory (and the host holds each document
-    # once), which the copy engine's reads of it profit from.
+    # Each document is drawn, stored in the pinned pool and dropped in turn,
+    # so the host holds one document's arrays at a time besides the pool.
     store = P.c2kv_store_create(g, sum(seg_bytes[i] + 512 for i in used) + (1 << 20))
     for i in used:
         d = S.make_document(g, i, docs_meta[i][0], w.k, w.seed, n_slots=docs_meta[i][1])
