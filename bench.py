@@ -818,12 +818,43 @@ def run_kernel_probe(args) -> None:
     qd, kd = rnd(T, L, B, g.n_q_heads, D), rnd(T, L, B, H, D)
     outd = torch.empty_like(qd)
     torch.cuda.synchronize()
+    prefill = None
     with torch.cuda.stream(stream):
         if Q:
             qp, kp = rnd(L, B, Q, g.n_q_heads, D), rnd(L, B, Q, H, D)
             outp = torch.empty_like(qp)
             for l in range(L):
                 P.c2kv_attend_prefill(g, l, kc, vc, tabs, cap, lens, qp[l], kp[l], kp[l], outp[l], ws, stream)
+    if Q:
+        # the question prefill of every layer from a graph, timed: each call
+        # appends the question at rows [n, n + Q) again, so replays are alike
+        gp = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(gp, stream=stream):
+                for l in range(L):
+                    P.c2kv_attend_prefill(g, l, kc, vc, tabs, cap, lens, qp[l], kp[l], kp[l], outp[l], ws, stream)
+        pts = []
+        for _ in range(args.warmup + 3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                gp.replay()
+                e1.record(stream)
+            e1.synchronize()
+            pts.append(e0.elapsed_time(e1) / 1e3)
+        t_pre = statistics.median(pts[args.warmup:]) / L
+        # 4 d flops per visible (q row, key) pair: QK^T and PV, each 2 d
+        pairs = sum(g.n_q_heads * (n + i + 1) for n in lens for i in range(Q))
+        flops = 4 * D * pairs
+        peaks = measured_peaks()
+        tf_peak = peaks.get("bf16_tflops") or 1900.0
+        byts = sum((n + Q) for n in lens) * H * D * 4
+        prefill = {"us_per_layer": t_pre * 1e6, "tflops": flops / t_pre / 1e12,
+                   "frac_of_bf16_peak": flops / t_pre / 1e12 / tf_peak,
+                   "roofline_us": max(byts / ((peaks.get("hbm_gbs") or 6800.0) * 1e9), flops / (tf_peak * 1e12)) * 1e6,
+                   "note": "per layer: append + prefill launches from a graph; flops = 4 d per visible (q row, key) "
+                           "pair (the hi/lo q split runs QK^T twice on the tensor cores: 1.5x these flops)"}
         for l in range(L):
             P.c2kv_attend_decode(g, l, kc, vc, tabs, cap, n_dev, max_keys, qd[0, l], kd[0, l], kd[0, l],
                                  outd[0, l], ws, stream, 0)
@@ -864,6 +895,8 @@ def run_kernel_probe(args) -> None:
                      f"then {T} decode steps x {L} layers from a graph (timed)")}
     del kc, vc, tabs, graph
     torch.cuda.empty_cache()
+    if prefill is not None:
+        line["prefill"] = prefill
     if is_llama(g0):
         line["linear"] = probe_linears(P, S, B, stream, peak)
     print(json.dumps(line))

@@ -51,7 +51,7 @@ constexpr int BN = 128;        // keys per tile
 constexpr int STAGES = 2;
 constexpr int kMaxClusterTc = 16;   // key splits merged in one cluster
 constexpr int kSoftmaxThreads = 128;
-constexpr int kThreadsTc = 160;
+constexpr int kThreadsTc = 224;   // warps 0-3 softmax, 4 MMA, 5 K loads, 6 V loads
 constexpr float kRescaleLog2 = 8.f;
 
 template <int D>
@@ -66,7 +66,7 @@ struct TcCfg {
   static constexpr int OFF_ML = OFF_P + 2 * P_BYTES;   // split merge: (m, l) of every row
   static constexpr int OFF_MRG = OFF_ML + BM * 2 * 4;
   static constexpr int OFF_BAR = OFF_MRG + MRG_BYTES;
-  static constexpr int N_BAR = 1 + 2 * STAGES + 2 + 2 + 2 + 2 + 2 + 1;
+  static constexpr int N_BAR = 1 + 4 * STAGES + 2 + 2 + 2 + 2 + 2 + 1;
   static constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;   // + slack for 1024-byte alignment
   // split merge: unnormalised O of every row (fp32, 16-byte chunks swizzled
@@ -99,9 +99,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = kv_full + STAGES;
-  uint64_t* s_full = kv_empty + STAGES;
+  // K and V stages are filled and freed separately: a K stage is free once
+  // its QK^T has run, a V stage once its PV has.
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + STAGES;
+  uint64_t* v_full = k_empty + STAGES;
+  uint64_t* v_empty = v_full + STAGES;
+  uint64_t* s_full = v_empty + STAGES;
   uint64_t* s_free = s_full + 2;
   uint64_t* p_full = s_free + 2;
   uint64_t* p_free = p_full + 2;
@@ -113,6 +117,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
+  volatile int* k_issued = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 24);   // K loads issued
+  volatile int* v_issued = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 28);   // V loads issued
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -160,8 +166,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   if (tid == 0) {
     mbar_init(q_full, kSoftmaxThreads);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -173,6 +181,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
     mbar_init(&o_done[1], 1);
     mbar_init(o_last, 1);
     *abort_flag = 0;
+    *k_issued = 0;
+    *v_issued = 0;
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -193,29 +203,36 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   const int kv_z = p.layer * p.n_kv + h;
 
   float m_run = -INFINITY, l_run = 0.f;   // softmax threads: running max / sum of their row
-  if (warp == 4) {
+  if (warp >= 5) {
     if (lane == 0 && nlive > 0) {
-      // ---------------- producer + MMA issuer (one thread)
-      // the jj-th live tile (key tile t) goes to stage jj % STAGES
-      auto issue_kv = [&](int jj, int t) {
+      // ---------------- producers: warp 5 loads the live K tiles, warp 6 the
+      // V tiles; the jj-th live tile goes to stage jj % STAGES of its ring
+      const bool is_k = warp == 5;
+      uint64_t* full = is_k ? k_full : v_full;
+      uint64_t* empty = is_k ? k_empty : v_empty;
+      uint8_t* ring = is_k ? sK : sV;
+      const CUtensorMap* map = is_k ? &p.tm_k[b] : &p.tm_v[b];
+      volatile int* issued = is_k ? k_issued : v_issued;
+      int t = next_live(0);
+      for (int jj = 0; jj < nlive; ++jj, t = next_live(t + 1)) {
         const int s = jj % STAGES;
-        mbar_arrive_expect_tx(&kv_full[s], 2 * C::KV_BYTES);
-        for (int sub = 0; sub < C::NSUB; ++sub) {
-          tma_load_3d(sK + s * C::KV_BYTES + sub * BN * 128, &p.tm_k[b], sub * 64, kb + t * BN, kv_z, &kv_full[s]);
-          tma_load_3d(sV + s * C::KV_BYTES + sub * BN * 128, &p.tm_v[b], sub * 64, kb + t * BN, kv_z, &kv_full[s]);
-        }
-      };
-      int next = 0;                  // live tiles issued
-      int tnext = next_live(0);      // key tile of the next one
-      for (; next < min(STAGES, nlive); ++next) {
-        issue_kv(next, tnext);
-        tnext = next_live(tnext + 1);
+        if (jj >= STAGES && !wait_or_abort(&empty[s], ((jj - STAGES) / STAGES) & 1, abort_flag, p.err)) break;
+        mbar_arrive_expect_tx(&full[s], C::KV_BYTES);
+        for (int sub = 0; sub < C::NSUB; ++sub)
+          tma_load_3d(ring + s * C::KV_BYTES + sub * BN * 128, map, sub * 64, kb + t * BN, kv_z, &full[s]);
+        *issued = jj + 1;
       }
+    }
+  } else if (warp == 4) {
+    if (lane == 0 && nlive > 0) {
+      // ---------------- MMA issuer (one thread): QK(j), then PV(j - 1), so
+      // the tensor pipe runs QK(j) while the softmax warps work on tile j - 1
       constexpr uint32_t IDESC_QK = idesc_bf16_m128(BN, false, false);
       constexpr uint32_t IDESC_PV = idesc_bf16_m128(D, false, true);
       auto issue_pv = [&](int t) -> bool {
         const int pb = t & 1, s = t % STAGES;
         if (!wait_or_abort(&p_full[pb], (t >> 1) & 1, abort_flag, p.err)) return false;
+        if (!wait_or_abort(&v_full[s], (t / STAGES) & 1, abort_flag, p.err)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
@@ -224,7 +241,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
           const uint64_t bdesc = sw128_desc(smem_addr(sV + s * C::KV_BYTES) + kk * 2048, BN * 128, 1024);
           mma_bf16(tmem + C::TMEM_O, a, bdesc, IDESC_PV, (t > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&kv_empty[s]);
+        mma_commit(&v_empty[s]);
         mma_commit(&p_free[pb]);
         mma_commit(&o_done[t & 1]);
         return true;
@@ -232,7 +249,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
       bool ok = wait_or_abort(q_full, 0, abort_flag, p.err);
       for (int j = 0; ok && j < nlive; ++j) {
         const int s = j % STAGES, sb = j & 1;
-        ok = wait_or_abort(&kv_full[s], (j / STAGES) & 1, abort_flag, p.err);
+        ok = wait_or_abort(&k_full[s], (j / STAGES) & 1, abort_flag, p.err);
         if (ok && j >= 2) ok = wait_or_abort(&s_free[sb], ((j - 2) >> 1) & 1, abort_flag, p.err);
         if (!ok) break;
         tc_fence_after();
@@ -246,23 +263,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
                             IDESC_QK, (half | kk) ? 1u : 0u);
           }
         }
+        mma_commit(&k_empty[s]);
         mma_commit(&s_full[sb]);
-        if (j >= 1) {
-          ok = issue_pv(j - 1);
-          if (ok && next < nlive) {
-            ok = wait_or_abort(&kv_empty[(j - 1) % STAGES], ((j - 1) / STAGES) & 1, abort_flag, p.err);
-            if (ok) {
-              issue_kv(next++, tnext);
-              tnext = next_live(tnext + 1);
-            }
-          }
-        }
+        if (j >= 1) ok = issue_pv(j - 1);
       }
       if (ok) ok = issue_pv(nlive - 1);
       if (ok) mma_commit(o_last);   // every MMA of the CTA has completed
     }
   } else {
-    // ---------------- softmax warps: thread tid owns row tid (TMEM lane tid)
+    // ---------------- softmax warps (0-3): thread tid owns row tid (TMEM lane tid)
     const int row = tid;
     const int tl = row / G, g = row % G;
     const int tok = tok0 + tl;
@@ -452,8 +461,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   const bool aborted = *abort_flag != 0;
   if (aborted) {
     // let TMA copies in flight land before the shared memory is reused
-    if (tid == 0 && nlive > 0) {   // nothing was issued without live tiles
-      for (int s = 0; s < min(STAGES, nlive); ++s) mbar_wait(&kv_full[s], 0);
+    if (tid == 0) {   // the last STAGES loads of each ring (nothing is issued without live tiles)
+      for (int r = 0; r < 2; ++r) {
+        const int n = r ? *v_issued : *k_issued;
+        uint64_t* full = r ? v_full : k_full;
+        for (int jj = max(0, n - STAGES); jj < n; ++jj) mbar_wait(&full[jj % STAGES], (jj / STAGES) & 1);
+      }
     }
     __syncthreads();
   }
