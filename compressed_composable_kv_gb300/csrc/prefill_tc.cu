@@ -11,18 +11,23 @@
 // rows for one (sequence, kv head, key split), token-major: row r is token
 // tok0 + r / G, head r % G (G = 5 uses 125 rows).  Warps 0-3 are the softmax
 // warps (thread t owns row t, i.e. TMEM lane t); warp 4's first lane issues
-// every TMA load and every MMA.
+// every MMA, warps 5 and 6 the K and the V loads.  Everything the tensor
+// cores read besides K and V sits in TMEM, so shared memory holds only the
+// two load rings.
 //   Q   : [128 rows][d] as bf16 hi + lo parts (hi + lo within ~2^-16 of the
 //         rotated q), loaded by the softmax threads (thread = row) into TMEM;
 //         S = Q_hi K^T + Q_lo K^T takes A from TMEM, so the logits keep
 //         fp32-level accuracy (a bf16 q alone errs by ~2^-9 of |q||k|, which a
 //         sharp softmax turns into output errors near the tolerance)
-//   K,V : 128-key tiles, TMA (3-D map over [layer*kv head][keys][d]), 2
-//         stages, keys at or past the sequence's valid length read as zeros
-//         (OOB); key tiles no row of the M tile can see are skipped
-//   S   : Q K^T, fp32 in TMEM, double-buffered (2 x 128 columns)
-//   P   : bf16 in shared memory (K-major, two SW128 sub-tiles of 64 keys),
-//         double-buffered
+//   K,V : 128-key tiles, TMA (3-D map over [layer*kv head][keys][d]), a ring
+//         of 3 stages each (a tile load takes ~2 us from L2, so 2 stages left
+//         the tensor pipe waiting); keys at or past the sequence's valid
+//         length read as zeros (OOB); key tiles no row of the M tile can see
+//         are skipped
+//   S   : Q K^T, fp32 in TMEM (128 columns); QK(j + 1) runs once the
+//         softmax has read S(j) into registers
+//   P   : bf16 in TMEM, two buffers of 64 columns (two keys per column);
+//         PV takes A = P from TMEM
 //   O   : P V accumulated in TMEM (d columns), rescaled in place only when a
 //         row's running max grows by more than 2^8 (the final O / l uses the
 //         same stale max, so the result is exact)
@@ -48,7 +53,7 @@ namespace {
 
 constexpr int BM = 128;        // rows per M tile (TMEM lanes)
 constexpr int BN = 128;        // keys per tile
-constexpr int STAGES = 2;
+constexpr int STAGES = 3;      // K ring and V ring depth (each its own barriers)
 constexpr int kMaxClusterTc = 16;   // key splits merged in one cluster
 constexpr int kSoftmaxThreads = 128;
 constexpr int kThreadsTc = 224;   // warps 0-3 softmax, 4 MMA, 5 K loads, 6 V loads
@@ -58,14 +63,15 @@ template <int D>
 struct TcCfg {
   static constexpr int NSUB = D / 64;           // 128-byte column blocks of d
   static constexpr int KV_BYTES = NSUB * BN * 128;
-  static constexpr int P_BYTES = BM * BN * 2;
   static constexpr int MRG_BYTES = (BM + kMaxClusterTc) * 3 * 4;   // split merge: m, l, weights
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
-  static constexpr int OFF_ML = OFF_P + 2 * P_BYTES;   // split merge: (m, l) of every row
+  // split merge (after the last PV, when the V ring is free): (m, l) of
+  // every row and the merge's m, l and weights, over the V ring
+  static constexpr int OFF_ML = OFF_V;
   static constexpr int OFF_MRG = OFF_ML + BM * 2 * 4;
-  static constexpr int OFF_BAR = OFF_MRG + MRG_BYTES;
+  static_assert(OFF_MRG + MRG_BYTES <= OFF_V + STAGES * KV_BYTES, "merge scratch must fit the V ring");
+  static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
   static constexpr int N_BAR = 1 + 4 * STAGES + 2 + 2 + 2 + 2 + 2 + 1;
   static constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;   // + slack for 1024-byte alignment
@@ -74,7 +80,8 @@ struct TcCfg {
   static constexpr int OFF_OST = OFF_K;
   static_assert(BM * D * 4 <= STAGES * KV_BYTES, "O staging must fit the K ring");
   static_assert(SMEM <= 232448, "shared memory per CTA");
-  static constexpr int TMEM_S = 0;                    // two BN-column S buffers
+  static constexpr int TMEM_S = 0;                    // S: BN columns
+  static constexpr int TMEM_P = BN;                   // P: two buffers of BN / 2 columns (two bf16 per column)
   static constexpr int TMEM_O = 2 * BN;               // d columns
   static constexpr int TMEM_QH = 3 * BN;              // Q_hi: d / 2 columns (two bf16 per column)
   static constexpr int TMEM_QL = TMEM_QH + D / 2;     // Q_lo
@@ -199,7 +206,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
 
   uint8_t* sK = smem + C::OFF_K;
   uint8_t* sV = smem + C::OFF_V;
-  uint8_t* sP = smem + C::OFF_P;
   const int kv_z = p.layer * p.n_kv + h;
 
   float m_run = -INFINITY, l_run = 0.f;   // softmax threads: running max / sum of their row
@@ -236,10 +242,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          // P is BN/64 K-major sub-tiles of [BM rows][64 keys]
-          const uint64_t a = sw128_desc(smem_addr(sP + pb * C::P_BYTES + (kk / 4) * BM * 128) + (kk % 4) * 32, 16, 1024);
+          // A = P from TMEM (row r in lane r, 16 keys = 8 columns per step)
           const uint64_t bdesc = sw128_desc(smem_addr(sV + s * C::KV_BYTES) + kk * 2048, BN * 128, 1024);
-          mma_bf16(tmem + C::TMEM_O, a, bdesc, IDESC_PV, (t > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_tmem_a(tmem + C::TMEM_O, tmem + C::TMEM_P + pb * (BN / 2) + kk * 8, bdesc, IDESC_PV,
+                          (t > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&v_empty[s]);
         mma_commit(&p_free[pb]);
@@ -248,9 +254,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
       };
       bool ok = wait_or_abort(q_full, 0, abort_flag, p.err);
       for (int j = 0; ok && j < nlive; ++j) {
-        const int s = j % STAGES, sb = j & 1;
+        const int s = j % STAGES;
         ok = wait_or_abort(&k_full[s], (j / STAGES) & 1, abort_flag, p.err);
-        if (ok && j >= 2) ok = wait_or_abort(&s_free[sb], ((j - 2) >> 1) & 1, abort_flag, p.err);
+        // one S buffer: QK(j) once the softmax has read S(j - 1)
+        if (ok && j >= 1) ok = wait_or_abort(&s_free[0], (j - 1) & 1, abort_flag, p.err);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -259,12 +266,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
           for (int kk = 0; kk < D / 16; ++kk) {
             const int sub = kk / 4, ko = (kk % 4) * 32;
             const uint64_t bdesc = sw128_desc(smem_addr(sK + s * C::KV_BYTES + sub * BN * 128) + ko, 16, 1024);
-            mma_bf16_tmem_a(tmem + C::TMEM_S + sb * BN, tmem + (half ? C::TMEM_QL : C::TMEM_QH) + kk * 8, bdesc,
+            mma_bf16_tmem_a(tmem + C::TMEM_S, tmem + (half ? C::TMEM_QL : C::TMEM_QH) + kk * 8, bdesc,
                             IDESC_QK, (half | kk) ? 1u : 0u);
           }
         }
         mma_commit(&k_empty[s]);
-        mma_commit(&s_full[sb]);
+        mma_commit(&s_full[0]);
         if (j >= 1) ok = issue_pv(j - 1);
       }
       if (ok) ok = issue_pv(nlive - 1);
@@ -308,8 +315,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
     bool ok = true;
     int tcur = next_live(0);   // key tile of the j-th live tile
     for (int j = 0; j < nlive; ++j, tcur = next_live(tcur + 1)) {
-      const int sb = j & 1;
-      if (!__all_sync(0xffffffffu, wait_or_abort(&s_full[sb], (j >> 1) & 1, abort_flag, p.err))) {
+      if (!__all_sync(0xffffffffu, wait_or_abort(&s_full[0], j & 1, abort_flag, p.err))) {
         ok = false;
         break;
       }
@@ -318,7 +324,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
       {
         float t[BN / 32][32];
 #pragma unroll
-        for (int q4 = 0; q4 < BN / 32; ++q4) tmem_ld32(lane_base + C::TMEM_S + sb * BN + q4 * 32, t[q4]);
+        for (int q4 = 0; q4 < BN / 32; ++q4) tmem_ld32(lane_base + C::TMEM_S + q4 * 32, t[q4]);
         tmem_wait_ld();
 #pragma unroll
         for (int q4 = 0; q4 < BN / 32; ++q4)
@@ -326,7 +332,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
           for (int c = 0; c < 32; ++c) sv[q4 * 32 + c] = t[q4][c];
       }
       tc_fence_before();
-      mbar_arrive(&s_free[sb]);
+      mbar_arrive(&s_free[0]);
       const int key0 = kb + tcur * BN;
       // keys [key0, key0 + nvis) pass the causal / split bounds of this row;
       // under the anchor mask a document row sees all of an anchor tile
@@ -414,13 +420,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
         ok = false;
         break;
       }
-      uint8_t* prow = sP + pb * C::P_BYTES + row * 128;
+      // P(j) into its TMEM buffer, row = lane, keys 2c and 2c + 1 in column c
 #pragma unroll
-      for (int ch = 0; ch < BN / 8; ++ch) {   // 16-byte chunk ch of sub-tile ch / 8
-        const uint4 v = make_uint4(pk[ch * 4 + 0], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
-        *reinterpret_cast<uint4*>(prow + (ch / 8) * BM * 128 + (((ch % 8) ^ (row & 7)) << 4)) = v;
+      for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+        float v[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(pk[c0 + c]);
+        tmem_st32(lane_base + C::TMEM_P + pb * (BN / 2) + c0, v);
       }
-      fence_proxy_async();
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&p_full[pb]);
     }
