@@ -215,8 +215,7 @@ AttnWs attn_workspace(const c2kv_geometry* g, int batch, int t_len, int max_keys
   } else {
     // tensor-core prefill: splits are merged inside a cluster (no partials
     // here); the scratch holds only the rotated q
-    const int tok = prefill_tc_tokens_per_tile(grp);
-    w.n_tb = (t_len + tok - 1) / tok;
+    w.n_tb = prefill_tc_m_tiles(t_len, grp);
     w.num_splits = 1;
     w.split_keys = max_keys;
   }

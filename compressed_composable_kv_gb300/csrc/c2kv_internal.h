@@ -415,7 +415,7 @@ cudaError_t launch_attention(const AttnParams& p, int head_dim, int group, bool 
 cudaError_t launch_advance(int batch, int32_t* n_cached, int delta, cudaStream_t st);
 
 cudaError_t launch_prefill_tc(const PrefillTcParams& p, int head_dim, int group, cudaStream_t st);
-int prefill_tc_tokens_per_tile(int group);
+int prefill_tc_m_tiles(int t_len, int group);   // M tiles of 128 (token, head) rows
 int prefill_tc_key_tile();
 // Key splits (one thread-block cluster per unit) and keys per split of the
 // tensor-core prefill for `units` (sequence, M tile, kv head) units.

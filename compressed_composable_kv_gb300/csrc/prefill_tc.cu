@@ -8,9 +8,10 @@
 // "results" gives the anchor-token ablation's mask.
 //
 // One CTA owns a 128-row M tile of (question token, q head of the group)
-// rows for one (sequence, kv head, key split), token-major: row r is token
-// tok0 + r / G, head r % G (G = 5 uses 125 rows).  Warps 0-3 are the softmax
-// warps (thread t owns row t, i.e. TMEM lane t); warp 4's first lane issues
+// rows for one (sequence, kv head, key split), token-major and packed across
+// tokens: row r of tile mt is token (128 mt + r) / G, head (128 mt + r) % G.
+// Warps 0-3 are the softmax warps (thread t owns row t, i.e. TMEM lane t);
+// warp 4's first lane issues
 // every MMA, warps 5 and 6 the K and the V loads.  Everything the tensor
 // cores read besides K and V sits in TMEM, so shared memory holds only the
 // two load rings.
@@ -100,8 +101,6 @@ __device__ __forceinline__ bool tc_structured_visible(const PrefillTcParams& p, 
 template <int D, int G, bool MASKED>
 __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
   using C = TcCfg<D>;
-  constexpr int TOK = BM / G;    // tokens per M tile
-  constexpr int ROWS = TOK * G;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -134,8 +133,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   const int mt = blockIdx.y / p.n_kv;
   const int b = blockIdx.z;
   const int n_cached = p.n_cached[b];
-  const int tok0 = mt * TOK;
-  const int ntok = min(TOK, p.t_len - tok0);
+  // The (token, head) rows of the question are packed 128 to an M tile,
+  // token-major: tile mt holds rows [128 mt, 128 mt + 128) of the t_len * G,
+  // so a token's heads may straddle two tiles (G = 5: 5 tiles for 128 tokens
+  // instead of 6 of 25 tokens each).
+  const int r_tile = mt * BM;
+  const int n_rows = p.t_len * G;
+  const int tok0 = r_tile / G;                                  // first token with a row here
+  const int ntok = min((r_tile + BM - 1) / G + 1, p.t_len) - tok0;
   // Anchor-token mask: document rows also see every anchor, so an M tile
   // holding document rows reads the keys of the whole sequence.
   const int mode = MASKED ? p.mask_mode : (int)kMaskCausal;
@@ -280,15 +285,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   } else {
     // ---------------- softmax warps (0-3): thread tid owns row tid (TMEM lane tid)
     const int row = tid;
-    const int tl = row / G, g = row % G;
-    const int tok = tok0 + tl;
-    const bool row_ok = row < ROWS && tl < ntok;
+    const int rq = r_tile + row;   // row of the question
+    const int tok = rq / G, g = rq % G;
+    const bool row_ok = rq < n_rows;
     const int lim = n_cached + tok + 1;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     {
       // this row's q (hi and lo parts) into TMEM: rows past the tile's tokens
       // and heads are zero
-      const size_t qrow = (((size_t)b * p.n_kv + h) * p.t_len + tok0) * G + row;
+      const size_t qrow = ((size_t)b * p.n_kv + h) * p.t_len * G + rq;
       const uint4* qh = reinterpret_cast<const uint4*>(p.q_hi + qrow * D);
       const uint4* ql = reinterpret_cast<const uint4*>(p.q_lo + qrow * D);
 #pragma unroll
@@ -554,8 +559,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   for (int it = tid; it < nr * CH; it += kThreadsTc) {
     const int rr = it / CH, c = it % CH;
     const int row = r0 + rr;
-    const int tl = row / G, g = row % G;
-    if (row >= ROWS || tl >= ntok) continue;
+    const int rq = r_tile + row;
+    const int tok = rq / G, g = rq % G;
+    if (rq >= n_rows) continue;
     const int off = row * D + ((c ^ (row & 7)) << 2);
     float4 v[kMaxClusterTc];
 #pragma unroll
@@ -577,7 +583,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
     uint2 pk;
     pk.x = *reinterpret_cast<uint32_t*>(&lo);
     pk.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(p.out + (((size_t)b * p.t_len + tok0 + tl) * p.n_q + h * G + g) * D + c * 4) = pk;
+    *reinterpret_cast<uint2*>(p.out + (((size_t)b * p.t_len + tok) * p.n_q + h * G + g) * D + c * 4) = pk;
   }
   cl.sync();
 }
@@ -699,14 +705,17 @@ int active_clusters(int cs, int head_dim, int group, bool masked) {
 
 }  // namespace
 
-int prefill_tc_tokens_per_tile(int group) { return BM / group; }
+int prefill_tc_m_tiles(int t_len, int group) { return (t_len * group + BM - 1) / BM; }
 
 int prefill_tc_key_tile() { return BN; }
 
 // Key splits of each (sequence, M tile, kv head) unit: as many as keep all
 // the units' clusters resident at once (one CTA per SM), at most 16 and at
 // most one per key tile.  Small units counts thereby fill the SMs; with
-// units >= SMs / 2 there is one split and no merge.
+// units >= SMs / 2 there is one split and no merge.  (Splitting units that
+// run in several waves anyway, to even out the last wave, was slower: 8 x 8
+// x 5 units of a 128-token G = 5 question took 336 us per layer in clusters
+// of 2 against 294 us unsplit.)
 void prefill_tc_plan(int units, int max_keys, int num_sms, int head_dim, int group, int* num_splits,
                      int* split_keys) {
   int s = units > 0 ? num_sms / units : 1;
