@@ -1153,8 +1153,9 @@ c2kv_status c2kv_linear(const void* x, int32_t tokens, int32_t k_in, const void*
   p.split2 = split2;
   p.stages = linear_stages(n_pad);
   p.epi = epilogue;
-  C2KV_CUDA(launch_linear(p, linear_ctas(sms), (flags & C2KV_LINEAR_OVERLAP_PREVIOUS) != 0,
-                          static_cast<cudaStream_t>(stream)));
+  p.cs = linear_plan_cs(n_out, k_in, n_pad, linear_ctas(sms));
+  const int ctas = p.cs > 0 ? (n_out / 128) * p.cs : linear_ctas(sms);
+  C2KV_CUDA(launch_linear(p, ctas, (flags & C2KV_LINEAR_OVERLAP_PREVIOUS) != 0, static_cast<cudaStream_t>(stream)));
   return C2KV_OK;
 }
 

@@ -397,11 +397,18 @@ struct LinearParams {
   int32_t* counters;               // [n_out / 128] chunks summed so far per tile
   unsigned* err;
   int32_t tokens, n_pad, k_in, n_out, split1, split2, stages, epi;
+  // 0: the (tile, chunk) items split evenly over the CTAs, partial tiles
+  // merged through global memory by the last CTA of each tile.  cs >= 1: one
+  // thread-block cluster of cs CTAs per tile, each CTA an equal share of the
+  // tile's chunks, the cs partials summed through distributed shared memory
+  // (cs = 1: every CTA one whole tile, nothing to merge).
+  int32_t cs;
 };
 
 // Launchers (return cudaGetLastError()).
 cudaError_t launch_linear(const LinearParams& p, int ctas, bool overlap, cudaStream_t st);
 int linear_stages(int n_pad);
+int linear_plan_cs(int n_out, int k_in, int n_pad, int ctas_max);   // LinearParams::cs
 cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* w, __nv_bfloat16* y, int tokens, int dim,
                            float eps, bool overlap, cudaStream_t st);
 cudaError_t launch_decode_tc(const DecodeTcParams& p, int group, int ctas, bool overlap, cudaStream_t st);

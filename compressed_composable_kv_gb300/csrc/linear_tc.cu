@@ -25,9 +25,15 @@
 // stream (weights do not depend on it); the activations after.
 #include <float.h>
 
+#include <algorithm>
+
+#include <cooperative_groups.h>
+
 #include "c2kv_internal.h"
 #include "decode_plan.h"
 #include "tcgen05.h"
+
+namespace cg = cooperative_groups;
 
 namespace c2kv {
 
@@ -123,7 +129,17 @@ __global__ void __launch_bounds__(LT_THREADS, 2) linear_tc_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int64_t x0 = decode_cta_first(M, cta), x1 = decode_cta_first(M, cta + 1);
+  int64_t x0, x1;
+  if (p.cs > 0) {
+    // one cluster of cs CTAs per tile; CTA r of it takes an equal share of the
+    // tile's chunks (the host keeps cs <= chunks, so every CTA has one)
+    const int tile = cta / p.cs, r = cta % p.cs;
+    x0 = (int64_t)tile * kc + (int64_t)r * kc / p.cs;
+    x1 = (int64_t)tile * kc + (int64_t)(r + 1) * kc / p.cs;
+  } else {
+    x0 = decode_cta_first(M, cta);
+    x1 = decode_cta_first(M, cta + 1);
+  }
   const int nitems = (int)(x1 - x0);
   if (nitems == 0) {
     if (warp == 4)
@@ -272,14 +288,24 @@ __global__ void __launch_bounds__(LT_THREADS, 2) linear_tc_kernel(const __grid_c
           emit(tile, c0, v, nc);
           if (EPI == kLinearSwiglu) ok = emit_swiglu(tile, c0, v, nc);
         } else {
+          if (p.cs > 1) {
+            // this CTA's share of a cluster-split tile, staged in its own
+            // shared memory ([n_pad][128] fp32 over the ring: every MMA has
+            // completed) for the cluster's reduction after the teardown
+            float* cpart = reinterpret_cast<float*>(smem);
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
-            if (c < nc) p.part[((size_t)slot * p.n_pad + c0 + c) * LT_BM + tid] = v[c];
+            for (int c = 0; c < 16; ++c)
+              if (c < nc) cpart[(c0 + c) * LT_BM + tid] = v[c];
+          } else {
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+              if (c < nc) p.part[((size_t)slot * p.n_pad + c0 + c) * LT_BM + tid] = v[c];
+          }
         }
       }
       tc_fence_before();
       mbar_arrive(&acc_free[buf]);
-      if (ok && !whole) {
+      if (ok && !whole && p.cs == 0) {
         // every partial store of the CTA is ordered before tid 0's arrival
         ok = group_sync(grp_bar, k_sync, abort_flag, p.err);
         if (ok && tid == 0) {
@@ -335,7 +361,7 @@ __global__ void __launch_bounds__(LT_THREADS, 2) linear_tc_kernel(const __grid_c
       j0 += n;
       if (j0 < nitems) d = decode_locate(M, x0 + j0);
     }
-    if (!ok && tid == 0) {
+    if (!ok && tid == 0 && p.cs == 0) {
       // gave up: add the remaining partial tiles' chunks to their counters
       // (their outputs are undefined) so every counter ends at zero
       DecodeTile e = decode_locate(M, x0);
@@ -362,6 +388,54 @@ __global__ void __launch_bounds__(LT_THREADS, 2) linear_tc_kernel(const __grid_c
   if (warp == 4) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(cols) : "memory");
+  }
+  if (p.cs > 1) {
+    // ---------------- the cluster's reduction: CTA r sums its share of the
+    // tile's rows (SwiGLU: its share of the gate/up row pairs) over the cs
+    // staged partials, in rank order, and applies the epilogue.  Every CTA
+    // reaches both cluster barriers on every path (all waits above are
+    // bounded), and none leaves before its peers' reads are done.
+    cg::cluster_group clu = cg::this_cluster();
+    clu.sync();
+    const int cs = p.cs, r = (int)clu.block_rank(), tile = cta / cs;
+    const int T = p.tokens;
+    const float* cpart = reinterpret_cast<const float*>(smem);
+    const float* peer[8];
+#pragma unroll
+    for (int sp = 0; sp < 8; ++sp) peer[sp] = sp < cs ? clu.map_shared_rank(cpart, sp) : cpart;
+    auto tile_sum = [&](int t, int row) {
+      float v = 0.f;
+#pragma unroll
+      for (int sp = 0; sp < 8; ++sp)
+        if (sp < cs) v += peer[sp][t * LT_BM + row];
+      return v;
+    };
+    if (EPI == kLinearSwiglu) {
+      const int fp = (LT_BM / 2 + cs - 1) / cs, f0 = r * fp, nf = max(0, min(LT_BM / 2, f0 + fp) - f0);
+      for (int it = tid; it < nf * T; it += LT_THREADS) {
+        const int t = it / nf, f = f0 + it % nf;
+        const float gt = tile_sum(t, f), up = tile_sum(t, f + LT_BM / 2);
+        p.y[(size_t)t * (p.n_out / 2) + tile * (LT_BM / 2) + f] = __float2bfloat16_rn(silu(gt) * up);
+      }
+    } else {
+      const int rp = (LT_BM + cs - 1) / cs, r0 = r * rp, nr = max(0, min(LT_BM, r0 + rp) - r0);
+      for (int it = tid; it < nr * T; it += LT_THREADS) {
+        const int t = it / nr, row = r0 + it % nr, n = tile * LT_BM + row;
+        float val = tile_sum(t, row);
+        if (EPI == kLinearAdd) val += __bfloat162float(p.residual[(size_t)t * p.n_out + n]);
+        if (EPI == kLinearSplit3) {
+          if (n < p.split1)
+            p.y[(size_t)t * p.split1 + n] = __float2bfloat16_rn(val);
+          else if (n < p.split2)
+            p.y2[(size_t)t * (p.split2 - p.split1) + (n - p.split1)] = __float2bfloat16_rn(val);
+          else
+            p.y3[(size_t)t * (p.n_out - p.split2) + (n - p.split2)] = __float2bfloat16_rn(val);
+        } else {
+          p.y[(size_t)t * p.n_out + n] = __float2bfloat16_rn(val);
+        }
+      }
+    }
+    clu.sync();
   }
 }
 
@@ -433,11 +507,22 @@ cudaError_t launch_lt(const LinearParams& p, int ctas, bool overlap, cudaStream_
   cfg.blockDim = dim3(LT_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (overlap) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (p.cs > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = p.cs;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = overlap ? 1 : 0;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, linear_tc_kernel<EPI>, p);
 }
 
@@ -454,8 +539,30 @@ int linear_stages(int n_pad) {
   return s;
 }
 
+// The split of a product: with at most as many tiles as the launch has CTAs
+// (two per SM), one cluster of cs CTAs per tile, cs the largest power of two
+// up to 8 with cs * tiles CTAs and at most one CTA per chunk, so that a
+// tile's partials are summed in distributed shared memory instead of through
+// global memory; cs = 1 when every CTA can own a whole tile.  (Clusters of 6
+// for the 48 tiles of the fused QKV projection took 20.5 us against 14.0 us
+// in clusters of 4.)  With more tiles, or a staged partial larger than the
+// shared-memory ring, 0: the even split over all CTAs.
+int linear_plan_cs(int n_out, int k_in, int n_pad, int ctas_max) {
+  const int tiles = n_out / LT_BM, kc = k_in / LT_BK;
+  if (tiles < 1 || tiles > ctas_max) return 0;
+  int cs = 1;
+  while (cs < 8 && 2 * cs * tiles <= ctas_max && 2 * cs <= kc) cs *= 2;
+  const int stages = linear_stages(n_pad);
+  if (cs > 1 && n_pad * LT_BM * 4 > stages * lt_stage_bytes(n_pad)) return 0;
+  return cs;
+}
+
 cudaError_t launch_linear(const LinearParams& p, int ctas, bool overlap, cudaStream_t st) {
   if (p.stages < 2 || p.stages > LT_MAX_STAGES || lt_layout(p.n_pad, p.stages).total > kLinearSmemMax)
+    return cudaErrorInvalidValue;
+  if (p.cs < 0 || p.cs > 8) return cudaErrorInvalidValue;
+  if (p.cs > 0 && (ctas != (p.n_out / LT_BM) * p.cs || p.cs > p.k_in / LT_BK ||
+                   (p.cs > 1 && p.n_pad * LT_BM * 4 > p.stages * lt_stage_bytes(p.n_pad))))
     return cudaErrorInvalidValue;
   switch (p.epi) {
     case kLinearStore: return launch_lt<kLinearStore>(p, ctas, overlap, st);

@@ -191,6 +191,36 @@ def test_compose_orders_repeats_and_ragged_docs():
     sc.close()
 
 
+def test_compose_many_tiny_documents():
+    """500 documents of 1..9 tokens (1..3 slots at k=4) in a shuffled order, so
+    that the composition kernel's 8-slot tiles span several documents each and
+    its document lookup runs over a long segment table; the head_dim 64
+    instantiation as well as 128."""
+    for d in (128, 64):
+        g = S.Geometry(2, 8, 2, d, 1.0e4)
+        rng = np.random.default_rng(0xC0 + d)
+        specs = []
+        for i in range(500):
+            n = int(rng.integers(1, 10))
+            specs.append((i, n, -(-n // 4)))
+        order = [int(x) for x in rng.permutation(500)]
+        requests = [(list(range(500)), order), (list(range(0, 500, 7)), None)]
+        sc = Scenario(g, 4, specs, requests, q_len=0, decode_steps=0)
+        bt = sc.batch
+        bt.compose()
+        torch.cuda.synchronize()
+        st = sc.oracle_store()
+        for b, (ids, order_b) in enumerate(requests):
+            N = bt.n_slots[b]
+            _, _, kref, vref = O.compose(st, ids, order_b, 4, g.rope_theta)
+            seq = O.composed_order(ids, order_b)
+            pos_ref, _ = O.composed_positions([sc.docs[x].n_tokens for x in seq], [sc.docs[x].n_slots for x in seq], 4)
+            assert np.array_equal(bt.pos[b][:N].cpu().numpy(), pos_ref)
+            assert np.array_equal(to_bits(bt.v_caches[b][:, :, :N]), vref), f"V, request {b}, d {d}"
+            check_keys(to_bits(bt.k_caches[b][:, :, :N]), kref, f"request {b}, d {d}")
+        sc.close()
+
+
 def test_k1_composition_equals_uncompressed():
     """k=1 keeps every token: the composed cache and the attention over it must
     equal the plain RoPE cache of the concatenated documents."""
