@@ -907,7 +907,9 @@ def probe_linears(P, S, tokens: int, stream, peak: float, sets: int = 4) -> dict
     tokens: `sets` distinct seeded weights of each (so every call reads its
     weights from HBM), called back to back from a CUDA graph; per call time and
     weight bytes / time against the HBM peak.  The first eager calls are the
-    launches the linear kernel's profile is taken on."""
+    launches the linear kernel's profile is taken on.  Then the layer's four
+    projections in layer order (`layer_chain`), `sets` layers of them from a
+    graph: per layer time and weight bytes / time."""
     import torch
     shape = S.LLAMA31_8B_MODEL
     dim, F = shape.dim, shape.ffn
@@ -918,6 +920,31 @@ def probe_linears(P, S, tokens: int, stream, peak: float, sets: int = 4) -> dict
     ws = torch.zeros(P.c2kv_linear_workspace_size(tokens, shape.vocab), dtype=torch.uint8, device="cuda")
     P.c2kv_workspace_init(ws)
     out = {}
+    layer = {}
+
+    def timed_graph(fn) -> float:
+        """One eager run, then a CUDA graph of `fn` replayed 5 times; the median
+        of the last 4 replays, in seconds."""
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                fn()
+        ts = []
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                graph.replay()
+                b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b) / 1e3)
+        del graph
+        return statistics.median(ts[1:])
+
     for name, (n, k, epi) in kinds.items():
         wts = [(torch.randn((n, k), device="cuda", generator=gen) * k ** -0.5).to(torch.bfloat16)
                for _ in range(sets)]
@@ -927,37 +954,39 @@ def probe_linears(P, S, tokens: int, stream, peak: float, sets: int = 4) -> dict
         y2 = torch.zeros((tokens, 1024), device="cuda", dtype=torch.bfloat16)
         y3 = torch.zeros((tokens, 1024), device="cuda", dtype=torch.bfloat16)
 
+        def call(wt, x=x, y=y, y2=y2, y3=y3, epi=epi):
+            kw = {}
+            if epi == P.C2KV_LINEAR_SPLIT3:
+                kw = dict(y2=y2, y3=y3, split1=4096, split2=5120)
+            elif epi == P.C2KV_LINEAR_ADD:
+                kw = dict(residual=y)
+            P.c2kv_linear(x, wt, y, ws, epi, stream=stream, flags=P.C2KV_LINEAR_OVERLAP_PREVIOUS, **kw)
+
         def run():
             for wt in wts:
-                kw = {}
-                if epi == P.C2KV_LINEAR_SPLIT3:
-                    kw = dict(y2=y2, y3=y3, split1=4096, split2=5120)
-                elif epi == P.C2KV_LINEAR_ADD:
-                    kw = dict(residual=y)
-                P.c2kv_linear(x, wt, y, ws, epi, stream=stream, flags=P.C2KV_LINEAR_OVERLAP_PREVIOUS, **kw)
+                call(wt)
 
-        torch.cuda.synchronize()
-        with torch.cuda.stream(stream):
-            run()
-        torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(graph, stream=stream):
-                run()
-        ts = []
-        for _ in range(5):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                a.record(stream)
-                graph.replay()
-                b.record(stream)
-            b.synchronize()
-            ts.append(a.elapsed_time(b) / 1e3 / sets)
-        t = statistics.median(ts[1:])
+        t = timed_graph(run) / sets
         out[name] = {"us": t * 1e6, "weight_bytes": n * k * 2, "gbs": n * k * 2 / t / 1e9,
                      "frac_of_hbm_peak": n * k * 2 / t / 1e9 / peak}
-        del wts, graph
+        if name != "lm_head":
+            layer[name] = (call, wts)
+        else:
+            del wts
         torch.cuda.empty_cache()
+
+    def run_chain():
+        for s_ in range(sets):
+            for name in ("qkv", "o", "gate_up", "down"):
+                call_, wts_ = layer[name]
+                call_(wts_[s_])
+
+    t = timed_graph(run_chain) / sets
+    byts = sum(kinds[n][0] * kinds[n][1] * 2 for n in ("qkv", "o", "gate_up", "down"))
+    out["layer_chain"] = {"us": t * 1e6, "weight_bytes": byts, "gbs": byts / t / 1e9,
+                          "frac_of_hbm_peak": byts / t / 1e9 / peak}
+    layer.clear()
+    torch.cuda.empty_cache()
     assert P.c2kv_device_error() == P.C2KV_OK
     return out
 
