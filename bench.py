@@ -1,8 +1,9 @@
 """Benchmark of the C2KV composed-cache hot path on one GB300 (or N replicas).
 
 One step = one full request of the workload: compose the documents'
-compressed pre-RoPE segments from the pinned host store into HBM (host->
-device copies + re-rotation), prefill the question on every layer, then
+compressed pre-RoPE segments from the pinned host store into HBM (a kernel
+reads them over the host link and re-rotates K), prefill the question on
+every layer, then
 decode every answer token on every layer.  Consecutive requests overlap as
 in a serving loop: request r+1 is composed on a second stream, into its own
 cache, while request r decodes.  Headline value: answer tokens per second
@@ -567,7 +568,7 @@ def run_ours(args, rank: int, world: int) -> dict:
         "h2d": {"compose_bytes": compose_bytes, "achieved_gbs": compose_bytes / comp / 1e9,
                 "pinned_copy_gbs": pinned_gbs, "frac": compose_bytes / comp / 1e9 / pinned_gbs,
                 "compose_ms_runs": [e[0].elapsed_time(e[1]) for e in iso],
-                "note": ("compose = host->device copies + re-rotation, wall time on the stream; "
+                "note": ("compose = reading the segments over the host link + re-rotation, wall time on the stream; "
                          "pinned_copy_gbs = the best of 1 GiB pinned copies timed right before each of the 3 "
                          "timed composes and 3 after them")},
         "roofline": {"kernel": "decode_tc_kernel" if g.head_dim == 128 else "decode_kernel", "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
@@ -690,8 +691,9 @@ def workload_config(w, world: int) -> dict:
         "ttft_pipeline": (f"compose and prefill layer-pipelined in {n_groups} groups: compose_ms = "
                           "until the whole cache is composed (prefill of earlier groups overlaps it), "
                           "prefill_ms = the rest of the prefill"),
-        "request_pipeline": ("consecutive requests: request r+1 is composed (host->device copies and "
-                             "re-rotation, second stream, its own cache) while request r decodes"),
+        "request_pipeline": ("consecutive requests: request r+1 is composed (host->device reads and "
+                             "re-rotation by the composition kernel, second stream, its own cache) while "
+                             "request r decodes"),
         "parallelism": f"replicas x{world}",
         "attention_only": ("value: attention over the composed cache only (no projection/MLP weights)"
                            + ("; model_tok_s: the whole Llama-3.1-8B decoder step with synthetic weights"
