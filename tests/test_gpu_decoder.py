@@ -94,6 +94,43 @@ def test_linear_split3_and_swiglu():
     check_rounded(m, DO.swiglu(x, wgu), "swiglu")
 
 
+@pytest.mark.parametrize("n_feat", [512, 20480])
+def test_swiglu_cluster_and_global_merge(n_feat):
+    """SwiGLU on the two other splits: 8 tiles (clusters of 8 CTAs summing the
+    gate/up partials in distributed shared memory) and 320 tiles (more than
+    the CTAs: the even split with the global merge)."""
+    rng = np.random.default_rng(n_feat)
+    T, dim = 4, 4096
+    x = S.normal_bf16(rng, (T, dim))
+    wgu = S.normal_bf16(rng, (2 * n_feat, dim), dim ** -0.5)
+    ws = _ws(T, 2 * n_feat)
+    m = torch.empty((T, n_feat), dtype=torch.bfloat16, device="cuda")
+    P.c2kv_linear(to_dev(x), to_dev(wgu), m, ws, P.C2KV_LINEAR_SWIGLU)
+    torch.cuda.synchronize()
+    assert P.c2kv_device_error() == P.C2KV_OK
+    check_rounded(m, DO.swiglu(x, wgu), f"swiglu F={n_feat}")
+
+
+def test_split3_in_clusters():
+    """A 3-tile q/k/v projection (clusters of 8 CTAs per tile) with split
+    points inside the tiles' rows."""
+    rng = np.random.default_rng(83)
+    T, dim = 3, 4096
+    x = S.normal_bf16(rng, (T, dim))
+    w = S.normal_bf16(rng, (384, dim), dim ** -0.5)
+    ws = _ws(T, 384)
+    q = torch.empty((T, 200), dtype=torch.bfloat16, device="cuda")
+    k = torch.empty((T, 100), dtype=torch.bfloat16, device="cuda")
+    v = torch.empty((T, 84), dtype=torch.bfloat16, device="cuda")
+    P.c2kv_linear(to_dev(x), to_dev(w), q, ws, P.C2KV_LINEAR_SPLIT3, y2=k, y3=v, split1=200, split2=300)
+    torch.cuda.synchronize()
+    assert P.c2kv_device_error() == P.C2KV_OK
+    ref = DO.linear(x, w)
+    check_rounded(q, ref[:, :200], "q")
+    check_rounded(k, ref[:, 200:300], "k")
+    check_rounded(v, ref[:, 300:], "v")
+
+
 def test_rmsnorm():
     rng = np.random.default_rng(67)
     for T, dim in ((4, 4096), (3, 5120), (1, 64)):
