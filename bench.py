@@ -376,18 +376,19 @@ def run_ours(args, rank: int, world: int) -> dict:
             b.reset_decode(stream)
             decode_all(i, 1)
         torch.cuda.synchronize()
+        # the library's launch counter around the captures: launches per replay
+        n0 = P.c2kv_kernel_launches()
         with torch.cuda.stream(stream):
             if Q:
                 for gr, (l0, l1) in zip(g_pre[i], groups):
                     with torch.cuda.graph(gr, stream=stream):
                         prefill_layers(i, l0, l1)
+            n1 = P.c2kv_kernel_launches()
             with torch.cuda.graph(g_dec[i], stream=stream):
                 decode_all(i)
         torch.cuda.synchronize()
+        graph_launches = (n1 - n0, P.c2kv_kernel_launches() - n1)   # (prefill, decode) per request
     assert P.c2kv_device_error() == P.C2KV_OK
-    # per request: one table + one composition launch per compose call; 2
-    # launches per prefill layer; L decode + 1 advance per step
-    launches_per_step = (bt.batch * (1 + len(groups)) + (2 * L if Q else 0) + T * (L + 1))
 
     def isolated_request(e):
         """One request alone on the stream: compose layer-pipelined with the
@@ -492,10 +493,14 @@ def run_ours(args, rank: int, world: int) -> dict:
     t_beg, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     gpu_idx = torch.cuda.current_device()
     with ClockSampler(gpu_idx) as clk:
+        n_eager = P.c2kv_kernel_launches()
         t_beg.record(stream)
         pipeline(args.steps, ev)
         t_end.record(stream)
+        n_eager = P.c2kv_kernel_launches() - n_eager   # the composition launches
         torch.cuda.synchronize()
+    # kernels of this library launched in the timed region, per request
+    launches_per_step = n_eager / args.steps + sum(graph_launches)
     barrier()
     torch.cuda.synchronize()
     elapsed = t_beg.elapsed_time(t_end) / 1e3
@@ -579,7 +584,7 @@ def run_ours(args, rank: int, world: int) -> dict:
         "e2e": {"value": toks / e2e_elapsed, "unit": "tok/s", "h2d_bytes_per_step": h2d_bytes + compose_bytes,
                 "d2h_bytes_per_step": d2h_bytes},
         "clocks": clocks,
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": int(round(launches_per_step * args.steps)),
     }
     if model is not None:
         out["model_tok_s"] = model["tok_s"]

@@ -70,6 +70,7 @@ _SIGNATURES = {
     "c2kv_seq_advance": (_i32, [_i32, _vp, _i32, _vp]),
     "c2kv_attend_masked": (_i32, [_pg, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "c2kv_device_error": (_i32, [_pi32]),
+    "c2kv_kernel_launches": (_i32, [ctypes.POINTER(ctypes.c_uint64)]),
     "c2kv_linear_workspace_size": (_sz, [_i32, _i32]),
     "c2kv_linear": (_i32, [_vp, _i32, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _sz,
                            ctypes.c_uint32, _vp]),
@@ -433,6 +434,14 @@ def c2kv_device_error() -> int:
     code = ctypes.c_int32()
     _check(load_library().c2kv_device_error(ctypes.byref(code)))
     return code.value
+
+
+def c2kv_kernel_launches() -> int:
+    """Kernel launches the library has enqueued in this process (a launch
+    captured into a CUDA graph counts once, at capture)."""
+    n = ctypes.c_uint64()
+    _check(load_library().c2kv_kernel_launches(ctypes.byref(n)))
+    return n.value
 
 
 # ---------------------------------------------------------------- decoder step

@@ -36,6 +36,15 @@ c2kv_status fail(c2kv_status st, const std::string& msg) {
       return fail(C2KV_ECUDA, std::string(#call) + ": " + cudaGetErrorString(e_));        \
   } while (0)
 
+// Kernel launches enqueued by this library (c2kv_kernel_launches).
+std::atomic<uint64_t> g_kernel_launches{0};
+
+#define C2KV_LAUNCH(call)                                             \
+  do {                                                                \
+    C2KV_CUDA(call);                                                  \
+    g_kernel_launches.fetch_add(1, std::memory_order_relaxed);        \
+  } while (0)
+
 // Device error word, one per device that loads the library.
 __device__ unsigned int g_error_word = 0;
 
@@ -306,12 +315,29 @@ c2kv_status run_prefill_tc(const c2kv_geometry* g, int batch, const void* const*
   p.n_q = g->n_q_heads;
   p.n_kv = g->n_kv_heads;
   p.layer = layer;
-  prefill_tc_plan(batch * w.n_tb * g->n_kv_heads, max_keys, sms, D, grp, &p.num_splits, &p.split_keys);
+  const int units = batch * w.n_tb * g->n_kv_heads;
+  // every unit's keys are within 2x of each other when each sequence's
+  // cached keys are at least its question's
+  bool even = mask_mode == kMaskCausal;
+  for (int b = 0; b < batch; ++b) even = even && n_cached[b] >= t_len;
+  const PrefillTcSchedule sc = prefill_tc_schedule(units, max_keys, sms, D, grp, even);
+  p.n_mt = w.n_tb;
   p.mask_mode = mask_mode;
   p.n_doc = n_doc;
   p.kblk = kblk;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
-  C2KV_CUDA(launch_prefill_tc(p, D, grp, st));
+  p.unit0 = 0;
+  p.n_units = sc.bulk;
+  p.num_splits = sc.splits0;
+  p.split_keys = sc.keys0;
+  C2KV_LAUNCH(launch_prefill_tc(p, D, grp, st));
+  if (sc.bulk < units) {
+    p.unit0 = sc.bulk;
+    p.n_units = units - sc.bulk;
+    p.num_splits = sc.splits1;
+    p.split_keys = sc.keys1;
+    C2KV_LAUNCH(launch_prefill_tc(p, D, grp, st));
+  }
   return C2KV_OK;
 }
 
@@ -391,7 +417,7 @@ c2kv_status run_decode_tc(const c2kv_geometry* g, int batch, const __nv_bfloat16
       }
     }
   }
-  C2KV_CUDA(launch_decode_tc(p, grp, ctas, overlap, st));
+  C2KV_LAUNCH(launch_decode_tc(p, grp, ctas, overlap, st));
   return C2KV_OK;
 }
 
@@ -464,7 +490,7 @@ c2kv_status run_attention(const c2kv_geometry* g, int batch, const __nv_bfloat16
   p.k_new = static_cast<const __nv_bfloat16*>(fused_k_new);
   p.v_new = static_cast<const __nv_bfloat16*>(fused_v_new);
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)g->head_dim));
-  C2KV_CUDA(launch_attention(p, g->head_dim, g->n_q_heads / g->n_kv_heads, overlap, st));
+  C2KV_LAUNCH(launch_attention(p, g->head_dim, g->n_q_heads / g->n_kv_heads, overlap, st));
   return C2KV_OK;
 }
 
@@ -496,7 +522,7 @@ c2kv_status run_append(const c2kv_geometry* g, int batch, __nv_bfloat16* const* 
   p.n_kv = g->n_kv_heads;
   p.n_q = g->n_q_heads;
   p.cap = cap;
-  C2KV_CUDA(launch_append(p, g->head_dim, batch, st));
+  C2KV_LAUNCH(launch_append(p, g->head_dim, batch, st));
   return C2KV_OK;
 }
 
@@ -818,7 +844,7 @@ c2kv_status c2kv_compose_layers(c2kv_store st, int32_t n_docs, const int32_t* do
       tp.seg[c].off = realign ? off[c] : 0;   // no re-alignment: extraction positions
       tp.seg[c].n_tokens = ntok[d];
     }
-    C2KV_CUDA(launch_rope_table(tp, us));
+    C2KV_LAUNCH(launch_rope_table(tp, us));
     if (st->last.size() >= kMaxTrackedTables) {   // this table's entry was erased above
       auto oldest = st->last.begin();
       for (auto it = st->last.begin(); it != st->last.end(); ++it)
@@ -871,7 +897,7 @@ c2kv_status c2kv_compose_layers(c2kv_store st, int32_t n_docs, const int32_t* do
       cp.seg[c].slot0 = slot0[c];
       cp.seg[c].n_slots = sg.n_slots;
     }
-    C2KV_CUDA(launch_compose(cp, D, st->side));
+    C2KV_LAUNCH(launch_compose(cp, D, st->side));
   }
   const cudaEvent_t landed = st->ev[st->ev_next++ % st->ev.size()];
   C2KV_CUDA(cudaEventRecord(landed, st->side));
@@ -902,7 +928,7 @@ c2kv_status c2kv_rope_table(const c2kv_geometry* geom, const int32_t* pos_dev, i
   p.half = geom->head_dim / 2;
   p.mode = kTableExplicit;
   fill_inv_freq(geom, p.inv_freq);
-  C2KV_CUDA(launch_rope_table(p, static_cast<cudaStream_t>(stream)));
+  C2KV_LAUNCH(launch_rope_table(p, static_cast<cudaStream_t>(stream)));
   return C2KV_OK;
 }
 
@@ -1019,7 +1045,7 @@ c2kv_status c2kv_attend_decode(const c2kv_geometry* geom, int32_t layer, int32_t
 c2kv_status c2kv_seq_advance(int32_t batch, int32_t* n_cached_dev, int32_t delta, void* stream) {
   if (batch < 1 || batch > 32) return fail(C2KV_EINVAL, "batch must be in [1, 32]");
   if (!n_cached_dev) return fail(C2KV_EINVAL, "null device array");
-  C2KV_CUDA(launch_advance(batch, n_cached_dev, delta, static_cast<cudaStream_t>(stream)));
+  C2KV_LAUNCH(launch_advance(batch, n_cached_dev, delta, static_cast<cudaStream_t>(stream)));
   return C2KV_OK;
 }
 
@@ -1064,7 +1090,7 @@ c2kv_status c2kv_attend_masked(const c2kv_geometry* geom, int32_t mask, int32_t 
   tp.n_doc = causal ? N : n_doc;
   tp.kblk = kblk;
   fill_inv_freq(geom, tp.inv_freq);
-  C2KV_CUDA(launch_rope_table(tp, st));
+  C2KV_LAUNCH(launch_rope_table(tp, st));
   const int32_t zero = 0;
   const CosSin2* tabs[1] = {tab};
   const int mmode = mask == C2KV_MASK_STRUCTURED ? kMaskStructured : mask == C2KV_MASK_ANCHOR ? kMaskAnchor
@@ -1155,7 +1181,7 @@ c2kv_status c2kv_linear(const void* x, int32_t tokens, int32_t k_in, const void*
   p.epi = epilogue;
   p.cs = linear_plan_cs(n_out, k_in, n_pad, linear_ctas(sms));
   const int ctas = p.cs > 0 ? (n_out / 128) * p.cs : linear_ctas(sms);
-  C2KV_CUDA(launch_linear(p, ctas, (flags & C2KV_LINEAR_OVERLAP_PREVIOUS) != 0, static_cast<cudaStream_t>(stream)));
+  C2KV_LAUNCH(launch_linear(p, ctas, (flags & C2KV_LINEAR_OVERLAP_PREVIOUS) != 0, static_cast<cudaStream_t>(stream)));
   return C2KV_OK;
 }
 
@@ -1168,7 +1194,7 @@ c2kv_status c2kv_rmsnorm(const void* x, int32_t tokens, int32_t dim, const void*
   if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return fail(C2KV_EINVAL, "pointers must be 16-byte aligned");
   c2kv_status s = device_state(nullptr, nullptr);
   if (s != C2KV_OK) return s;
-  C2KV_CUDA(launch_rmsnorm(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w),
+  C2KV_LAUNCH(launch_rmsnorm(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w),
                            static_cast<__nv_bfloat16*>(y), tokens, dim, eps, (flags & C2KV_LINEAR_OVERLAP_PREVIOUS) != 0,
                            static_cast<cudaStream_t>(stream)));
   return C2KV_OK;
@@ -1177,6 +1203,12 @@ c2kv_status c2kv_rmsnorm(const void* x, int32_t tokens, int32_t dim, const void*
 c2kv_status c2kv_test_expire_next_waits(int32_t n_launches) {
   if (n_launches < 0) return fail(C2KV_EINVAL, "n_launches < 0");
   g_inject_timeouts.store(n_launches);
+  return C2KV_OK;
+}
+
+c2kv_status c2kv_kernel_launches(uint64_t* count) {
+  if (count == nullptr) return fail(C2KV_EINVAL, "count is null");
+  *count = g_kernel_launches.load(std::memory_order_relaxed);
   return C2KV_OK;
 }
 

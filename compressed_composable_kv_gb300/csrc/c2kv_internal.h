@@ -314,8 +314,11 @@ struct PrefillTcParams {
   int32_t n_cached[kMaxBatch];
   __nv_bfloat16* out;          // [B][t_len][Hq][d]
   unsigned* err;
-  // num_splits key splits per unit, merged in a cluster of num_splits CTAs
+  // num_splits key splits per unit, merged in a cluster of num_splits CTAs.
+  // A unit is one (sequence, M tile, kv head), numbered (b * n_mt + mt) *
+  // n_kv + h; a launch covers units [unit0, unit0 + n_units).
   int32_t batch, t_len, n_q, n_kv, layer, num_splits, split_keys, mask_mode, n_doc, kblk;
+  int32_t n_mt, unit0, n_units;
   float scale_log2;
 };
 
@@ -423,6 +426,12 @@ cudaError_t launch_advance(int batch, int32_t* n_cached, int delta, cudaStream_t
 
 cudaError_t launch_prefill_tc(const PrefillTcParams& p, int head_dim, int group, cudaStream_t st);
 int prefill_tc_m_tiles(int t_len, int group);   // M tiles of 128 (token, head) rows
+// Launches of one tensor-core prefill: units [0, bulk) in splits0 key splits
+// of keys0 keys, then, if bulk < units, the rest in splits1 splits of keys1.
+struct PrefillTcSchedule {
+  int bulk, splits0, keys0, splits1, keys1;
+};
+PrefillTcSchedule prefill_tc_schedule(int units, int max_keys, int num_sms, int head_dim, int group, bool even);
 int prefill_tc_key_tile();
 // Key splits (one thread-block cluster per unit) and keys per split of the
 // tensor-core prefill for `units` (sequence, M tile, kv head) units.

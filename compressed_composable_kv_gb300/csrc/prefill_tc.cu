@@ -128,10 +128,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x;
-  const int h = blockIdx.y % p.n_kv;
-  const int mt = blockIdx.y / p.n_kv;
-  const int b = blockIdx.z;
+  // the num_splits CTAs of a unit are consecutive in x and form its cluster
+  const int split = (int)blockIdx.x % p.num_splits;
+  const int unit = p.unit0 + (int)blockIdx.x / p.num_splits;
+  const int h = unit % p.n_kv;
+  const int mt = unit / p.n_kv % p.n_mt;
+  const int b = unit / (p.n_kv * p.n_mt);
   const int n_cached = p.n_cached[b];
   // The (token, head) rows of the question are packed 128 to an M tile,
   // token-major: tile mt holds rows [128 mt, 128 mt + 128) of the t_len * G,
@@ -208,6 +210,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The launch of the rest of the last wave (prefill_tc_schedule) reads
+  // nothing this one writes: its CTAs may take the SMs this launch frees.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   uint8_t* sK = smem + C::OFF_K;
   uint8_t* sV = smem + C::OFF_V;
@@ -519,6 +524,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");
   }
+  // That launch still completes only after this one, so the work after it
+  // on the stream sees both.  (A no-op in a launch without the dependency.)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (S == 1) return;
 
   // ---------------- merge the S splits of the cluster; CTA r owns a row range.
@@ -621,20 +629,26 @@ cudaError_t launch_tc(const PrefillTcParams& p, cudaStream_t st) {
     if (e != cudaSuccess) return e;
   }
   if (p.num_splits < 1 || p.num_splits > kMaxClusterTc) return cudaErrorInvalidValue;
-  const int tok = BM / G;
-  const int n_mt = (p.t_len + tok - 1) / tok;
+  if (p.n_mt != (p.t_len * G + BM - 1) / BM || p.unit0 < 0 || p.n_units < 1 ||
+      p.unit0 + p.n_units > p.batch * p.n_kv * p.n_mt || (int64_t)p.n_units * p.num_splits > INT32_MAX)
+    return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.num_splits, p.n_kv * n_mt, p.batch);
+  cfg.gridDim = dim3(p.num_splits * p.n_units, 1, 1);
   cfg.blockDim = dim3(kThreadsTc);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = p.num_splits;   // the key splits of one unit form a cluster
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (p.unit0 > 0) {   // the rest of the last wave, behind the launch of the units before it
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
+  }
   return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, G, MASKED>, p);
 }
 
@@ -732,6 +746,37 @@ void prefill_tc_plan(int units, int max_keys, int num_sms, int head_dim, int gro
   sk = std::max(BN, (sk + BN - 1) / BN * BN);
   *split_keys = sk;
   *num_splits = std::max(1, (max_keys + sk - 1) / sk);
+}
+
+// Units of about equal work (`even`: a question over a longer cache) that
+// fill whole waves of resident CTAs run unsplit.  The remainder of the last
+// wave, when it splits (its units' clusters all resident at once), goes to
+// a second launch: its keys spread over the SMs instead of a few SMs
+// streaming whole units alone after the others have finished (8 x 8 x 5
+// units of a 128-token G = 5 question on 152 SMs: 304 unsplit, then 16 in
+// clusters of 6; 296 -> 230 us per layer).  Units of unequal work (causal
+// rows over the question's own keys) stay in one launch, where the CTA
+// scheduler already fills the SMs that finish early (a second launch made
+// the 4000 + 1000-token extraction 2-6 % slower).
+PrefillTcSchedule prefill_tc_schedule(int units, int max_keys, int num_sms, int head_dim, int group, bool even) {
+  PrefillTcSchedule sc{};
+  sc.bulk = units;
+  prefill_tc_plan(units, max_keys, num_sms, head_dim, group, &sc.splits0, &sc.keys0);
+  sc.splits1 = 1;
+  sc.keys1 = sc.keys0;
+  int wave = active_clusters(1, head_dim, group, false);   // resident CTAs
+  if (wave <= 0) wave = num_sms;
+  if (even && sc.splits0 == 1 && units > wave && units % wave != 0) {
+    const int rest = units % wave;
+    int s1 = 1, k1 = 0;
+    prefill_tc_plan(rest, max_keys, num_sms, head_dim, group, &s1, &k1);
+    if (s1 > 1) {
+      sc.bulk = units - rest;
+      sc.splits1 = s1;
+      sc.keys1 = k1;
+    }
+  }
+  return sc;
 }
 
 cudaError_t launch_prefill_tc(const PrefillTcParams& p, int head_dim, int group, cudaStream_t st) {

@@ -441,6 +441,14 @@ c2kv_status c2kv_rmsnorm(const void* x, int32_t tokens, int32_t dim, const void*
 c2kv_status c2kv_device_error(int32_t* code);
 
 /*
+ * Kernel launches this library has enqueued in the process so far, counted
+ * once each when the launch call succeeds (a launch enqueued while a stream
+ * is being captured into a CUDA graph counts once, at capture, and not at
+ * each replay).  Host-only; never fails except for a null count (C2KV_EINVAL).
+ */
+c2kv_status c2kv_kernel_launches(uint64_t* count);
+
+/*
  * Test hook for the failure path (the pages have no counterpart): the next
  * n_launches decode launches (c2kv_attend_decode, c2kv_attend_decode_noalloc,
  * c2kv_attend_prefill with q_len 1) each wait, at their first key tile, on a

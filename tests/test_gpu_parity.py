@@ -237,6 +237,25 @@ def test_k1_composition_equals_uncompressed():
     sc.close()
 
 
+def test_k1_uncompressed_128k_tokens():
+    """The 128k-token request uncompressed: 32 documents x 4096 tokens at k=1
+    (131 072 slots, one layer).  The position table is 0..131071, and the
+    composed cache, a 16-token question and two decode steps over 131 088+
+    keys match the oracle: attention over the plain RoPE cache of the
+    concatenated documents."""
+    g = S.Geometry(1, 32, 8, 128, 5.0e5)
+    n = 4096
+    specs = [(i, n, n) for i in range(32)]
+    sc = Scenario(g, 1, specs, [(list(range(32)), None)], q_len=16, decode_steps=2, seed=0xC2C4)
+    w = S.Workload("k1_128k", g, 1, 1, 16, 2, seed=0xC2C4)
+    inputs = S.make_step_inputs(w)
+    pre, dec = run_all(sc, upload(inputs))
+    assert sc.batch.n_slots[0] == 32 * n
+    assert np.array_equal(sc.batch.pos[0][:32 * n].cpu().numpy(), np.arange(32 * n))
+    check_request(sc, inputs, pre, dec, 0, layers=[0], steps=[0, 1])
+    sc.close()
+
+
 def test_varlen_batch_pool():
     """Batch of 16 requests drawn from a document pool in random order
     (lengths 500..4000 tokens, one not a multiple of k) through the full
@@ -666,6 +685,36 @@ def test_device_length_beyond_capacity_is_reported():
     assert P.c2kv_device_error() == P.C2KV_EDEVICE
     assert torch.all(out == 3.0)
     assert P.c2kv_device_error() == P.C2KV_OK   # reading clears the word
+    sc.close()
+
+
+def test_prefill_units_beyond_one_wave():
+    """A question whose (sequence, M tile, kv head) units outnumber the SMs:
+    Qwen3-14B heads (G = 5), 8 requests x 128 tokens = 320 units.  Whole
+    waves run unsplit and the rest of the last wave runs as key-split
+    clusters in a second launch (on 152 SMs: 304 units, then 16); every
+    request's question rows and a decode step against the oracle."""
+    g = S.Geometry(1, 40, 8, 128, 1.0e6)
+    specs = [(i, 1200 + 48 * i, 300 + 12 * i) for i in range(8)]
+    sc = Scenario(g, 4, specs, [([i], None) for i in range(8)], q_len=128, decode_steps=1)
+    w = S.Workload("qwen_waves", g, 4, 8, 128, 1, seed=0xC2C5)
+    inputs = S.make_step_inputs(w)
+    dev = upload(inputs)
+    bt = sc.batch
+    bt.compose()
+    out = torch.empty_like(dev["q_pre"][0])
+    n0 = P.c2kv_kernel_launches()
+    bt.prefill(0, dev["q_pre"][0], dev["kq_pre"][0], dev["vq"][0], out)
+    launches = P.c2kv_kernel_launches() - n0
+    bt.reset_decode()
+    dec = torch.empty_like(dev["qd_pre"][0, 0])
+    bt.decode(0, dev["qd_pre"][0, 0], dev["kd_pre"][0, 0], dev["vd"][0, 0], dec)
+    torch.cuda.synchronize()
+    assert P.c2kv_device_error() == P.C2KV_OK
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert launches == 3, launches   # the question's append, then the two prefill launches
+    for b in range(8):
+        check_request(sc, inputs, [out], [[dec]], b, layers=[0], steps=[0])
     sc.close()
 
 
