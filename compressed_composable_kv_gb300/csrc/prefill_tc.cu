@@ -25,10 +25,12 @@
 //         the tensor pipe waiting); keys at or past the sequence's valid
 //         length read as zeros (OOB); key tiles no row of the M tile can see
 //         are skipped
-//   S   : Q K^T, fp32 in TMEM (128 columns); QK(j + 1) runs once the
-//         softmax has read S(j) into registers
-//   P   : bf16 in TMEM, two buffers of 64 columns (two keys per column);
-//         PV takes A = P from TMEM
+//   S   : Q K^T, fp32 in TMEM, two buffers of 128 columns: QK(j + 1) runs
+//         while the softmax works on S(j)
+//   P   : bf16 in TMEM over the first 64 columns of its own S buffer (two
+//         keys per column); PV takes A = P from TMEM.  QK(j + 2), the next
+//         write of that buffer, is issued after PV(j), and tcgen05.mma
+//         operations of one thread run in issue order
 //   O   : P V accumulated in TMEM (d columns), rescaled in place only when a
 //         row's running max grows by more than 2^8 (the final O / l uses the
 //         same stale max, so the result is exact)
@@ -73,7 +75,7 @@ struct TcCfg {
   static constexpr int OFF_MRG = OFF_ML + BM * 2 * 4;
   static_assert(OFF_MRG + MRG_BYTES <= OFF_V + STAGES * KV_BYTES, "merge scratch must fit the V ring");
   static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
-  static constexpr int N_BAR = 1 + 4 * STAGES + 2 + 2 + 2 + 2 + 2 + 1;
+  static constexpr int N_BAR = 1 + 4 * STAGES + 2 + 2 + 2 + 1;   // q, K/V rings, S, P, PV, last PV
   static constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;   // + slack for 1024-byte alignment
   // split merge: unnormalised O of every row (fp32, 16-byte chunks swizzled
@@ -81,8 +83,9 @@ struct TcCfg {
   static constexpr int OFF_OST = OFF_K;
   static_assert(BM * D * 4 <= STAGES * KV_BYTES, "O staging must fit the K ring");
   static_assert(SMEM <= 232448, "shared memory per CTA");
-  static constexpr int TMEM_S = 0;                    // S: BN columns
-  static constexpr int TMEM_P = BN;                   // P: two buffers of BN / 2 columns (two bf16 per column)
+  // S: two buffers of BN columns; P(j) (bf16, two keys per column) is
+  // written over the first BN / 2 columns of S(j)'s buffer once S(j) is read
+  static constexpr int TMEM_S = 0;
   static constexpr int TMEM_O = 2 * BN;               // d columns
   static constexpr int TMEM_QH = 3 * BN;              // Q_hi: d / 2 columns (two bf16 per column)
   static constexpr int TMEM_QL = TMEM_QH + D / 2;     // Q_lo
@@ -112,13 +115,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   uint64_t* v_full = k_empty + STAGES;
   uint64_t* v_empty = v_full + STAGES;
   uint64_t* s_full = v_empty + STAGES;
-  uint64_t* s_free = s_full + 2;
-  uint64_t* p_full = s_free + 2;
-  uint64_t* p_free = p_full + 2;
+  uint64_t* p_full = s_full + 2;
   // PV(t) completes phase t >> 1 of o_done[t & 1], so a wait for PV(j-1)
   // can never mistake an older phase of the same parity for it; o_last
   // (single use) completes with the last PV of the CTA.
-  uint64_t* o_done = p_free + 2;
+  uint64_t* o_done = p_full + 2;
   uint64_t* o_last = o_done + 2;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
@@ -187,9 +188,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], kSoftmaxThreads);
       mbar_init(&p_full[i], kSoftmaxThreads);
-      mbar_init(&p_free[i], 1);
     }
     mbar_init(&o_done[0], 1);
     mbar_init(&o_done[1], 1);
@@ -241,50 +240,54 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
     }
   } else if (warp == 4) {
     if (lane == 0 && nlive > 0) {
-      // ---------------- MMA issuer (one thread): QK(j), then PV(j - 1), so
-      // the tensor pipe runs QK(j) while the softmax warps work on tile j - 1
+      // ---------------- MMA issuer (one thread): QK(0), QK(1), then PV(j)
+      // and QK(j + 2) for each j, so the tensor pipe runs QK(j + 1) and PV(j)
+      // while the softmax warps work on tiles j + 1 and j + 2
       constexpr uint32_t IDESC_QK = idesc_bf16_m128(BN, false, false);
       constexpr uint32_t IDESC_PV = idesc_bf16_m128(D, false, true);
-      auto issue_pv = [&](int t) -> bool {
-        const int pb = t & 1, s = t % STAGES;
-        if (!wait_or_abort(&p_full[pb], (t >> 1) & 1, abort_flag, p.err)) return false;
-        if (!wait_or_abort(&v_full[s], (t / STAGES) & 1, abort_flag, p.err)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          // A = P from TMEM (row r in lane r, 16 keys = 8 columns per step)
-          const uint64_t bdesc = sw128_desc(smem_addr(sV + s * C::KV_BYTES) + kk * 2048, BN * 128, 1024);
-          mma_bf16_tmem_a(tmem + C::TMEM_O, tmem + C::TMEM_P + pb * (BN / 2) + kk * 8, bdesc, IDESC_PV,
-                          (t > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&v_empty[s]);
-        mma_commit(&p_free[pb]);
-        mma_commit(&o_done[t & 1]);
-        return true;
-      };
-      bool ok = wait_or_abort(q_full, 0, abort_flag, p.err);
-      for (int j = 0; ok && j < nlive; ++j) {
+      auto issue_qk = [&](int j) -> bool {
         const int s = j % STAGES;
-        ok = wait_or_abort(&k_full[s], (j / STAGES) & 1, abort_flag, p.err);
-        // one S buffer: QK(j) once the softmax has read S(j - 1)
-        if (ok && j >= 1) ok = wait_or_abort(&s_free[0], (j - 1) & 1, abort_flag, p.err);
-        if (!ok) break;
+        if (!wait_or_abort(&k_full[s], (j / STAGES) & 1, abort_flag, p.err)) return false;
         tc_fence_after();
+        const uint32_t d = tmem + C::TMEM_S + (j & 1) * BN;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {   // Q_hi K^T, then + Q_lo K^T
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const int sub = kk / 4, ko = (kk % 4) * 32;
             const uint64_t bdesc = sw128_desc(smem_addr(sK + s * C::KV_BYTES + sub * BN * 128) + ko, 16, 1024);
-            mma_bf16_tmem_a(tmem + C::TMEM_S, tmem + (half ? C::TMEM_QL : C::TMEM_QH) + kk * 8, bdesc,
-                            IDESC_QK, (half | kk) ? 1u : 0u);
+            mma_bf16_tmem_a(d, tmem + (half ? C::TMEM_QL : C::TMEM_QH) + kk * 8, bdesc, IDESC_QK,
+                            (half | kk) ? 1u : 0u);
           }
         }
         mma_commit(&k_empty[s]);
-        mma_commit(&s_full[0]);
-        if (j >= 1) ok = issue_pv(j - 1);
+        mma_commit(&s_full[j & 1]);
+        return true;
+      };
+      auto issue_pv = [&](int t) -> bool {
+        const int s = t % STAGES;
+        if (!wait_or_abort(&p_full[t & 1], (t >> 1) & 1, abort_flag, p.err)) return false;
+        if (!wait_or_abort(&v_full[s], (t / STAGES) & 1, abort_flag, p.err)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          // A = P from TMEM (row r in lane r, 16 keys = 8 columns per step)
+          const uint64_t bdesc = sw128_desc(smem_addr(sV + s * C::KV_BYTES) + kk * 2048, BN * 128, 1024);
+          mma_bf16_tmem_a(tmem + C::TMEM_O, tmem + C::TMEM_S + (t & 1) * BN + kk * 8, bdesc, IDESC_PV,
+                          (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&v_empty[s]);
+        mma_commit(&o_done[t & 1]);
+        return true;
+      };
+      bool ok = wait_or_abort(q_full, 0, abort_flag, p.err);
+      for (int j = 0; ok && j < min(2, nlive); ++j) ok = issue_qk(j);
+      for (int j = 0; ok && j < nlive; ++j) {
+        ok = issue_pv(j);
+        // S(j)'s buffer is free for QK(j + 2): the softmax has read S(j) and
+        // written P(j) (p_full), and PV(j), issued above, reads P(j) first
+        if (ok && j + 2 < nlive) ok = issue_qk(j + 2);
       }
-      if (ok) ok = issue_pv(nlive - 1);
       if (ok) mma_commit(o_last);   // every MMA of the CTA has completed
     }
   } else {
@@ -325,7 +328,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
     bool ok = true;
     int tcur = next_live(0);   // key tile of the j-th live tile
     for (int j = 0; j < nlive; ++j, tcur = next_live(tcur + 1)) {
-      if (!__all_sync(0xffffffffu, wait_or_abort(&s_full[0], j & 1, abort_flag, p.err))) {
+      const uint32_t sbuf = lane_base + C::TMEM_S + (j & 1) * BN;   // S(j), then P(j)
+      if (!__all_sync(0xffffffffu, wait_or_abort(&s_full[j & 1], (j >> 1) & 1, abort_flag, p.err))) {
         ok = false;
         break;
       }
@@ -334,15 +338,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
       {
         float t[BN / 32][32];
 #pragma unroll
-        for (int q4 = 0; q4 < BN / 32; ++q4) tmem_ld32(lane_base + C::TMEM_S + q4 * 32, t[q4]);
+        for (int q4 = 0; q4 < BN / 32; ++q4) tmem_ld32(sbuf + q4 * 32, t[q4]);
         tmem_wait_ld();
 #pragma unroll
         for (int q4 = 0; q4 < BN / 32; ++q4)
 #pragma unroll
           for (int c = 0; c < 32; ++c) sv[q4 * 32 + c] = t[q4][c];
       }
-      tc_fence_before();
-      mbar_arrive(&s_free[0]);
       const int key0 = kb + tcur * BN;
       // keys [key0, key0 + nvis) pass the causal / split bounds of this row;
       // under the anchor mask a document row sees all of an anchor tile
@@ -425,22 +427,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
         }
         tmem_wait_st();
       }
-      const int pb = j & 1;
-      if (j >= 2 && !__all_sync(0xffffffffu, wait_or_abort(&p_free[pb], ((j - 2) >> 1) & 1, abort_flag, p.err))) {
-        ok = false;
-        break;
-      }
-      // P(j) into its TMEM buffer, row = lane, keys 2c and 2c + 1 in column c
+      // P(j) over S(j) (read above), row = lane, keys 2c and 2c + 1 in column c
 #pragma unroll
       for (int c0 = 0; c0 < BN / 2; c0 += 32) {
         float v[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(pk[c0 + c]);
-        tmem_st32(lane_base + C::TMEM_P + pb * (BN / 2) + c0, v);
+        tmem_st32(sbuf + c0, v);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[pb]);
+      mbar_arrive(&p_full[j & 1]);
     }
 
     // ---------------- epilogue: the last PV must be complete before O is read
