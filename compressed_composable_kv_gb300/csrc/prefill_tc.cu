@@ -11,8 +11,9 @@
 // rows for one (sequence, kv head, key split), token-major and packed across
 // tokens: row r of tile mt is token (128 mt + r) / G, head (128 mt + r) % G.
 // Warps 0-3 are the softmax warps (thread t owns row t, i.e. TMEM lane t);
-// warp 4's first lane issues
-// every MMA, warps 5 and 6 the K and the V loads.  Everything the tensor
+// one lane of warp 4 issues the QK MMAs and one of warp 7 the PV MMAs, so
+// neither kind waits behind the other's issue; warps 5 and 6 issue the K and
+// the V loads.  Everything the tensor
 // cores read besides K and V sits in TMEM, so shared memory holds only the
 // two load rings.
 //   Q   : [128 rows][d] as bf16 hi + lo parts (hi + lo within ~2^-16 of the
@@ -59,7 +60,7 @@ constexpr int BN = 128;        // keys per tile
 constexpr int STAGES = 3;      // K ring and V ring depth (each its own barriers)
 constexpr int kMaxClusterTc = 16;   // key splits merged in one cluster
 constexpr int kSoftmaxThreads = 128;
-constexpr int kThreadsTc = 224;   // warps 0-3 softmax, 4 MMA, 5 K loads, 6 V loads
+constexpr int kThreadsTc = 256;   // warps 0-3 softmax, 4 QK MMAs, 5 K loads, 6 V loads, 7 PV MMAs
 constexpr float kRescaleLog2 = 8.f;
 
 template <int D>
@@ -218,7 +219,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
   const int kv_z = p.layer * p.n_kv + h;
 
   float m_run = -INFINITY, l_run = 0.f;   // softmax threads: running max / sum of their row
-  if (warp >= 5) {
+  if (warp == 5 || warp == 6) {
     if (lane == 0 && nlive > 0) {
       // ---------------- producers: warp 5 loads the live K tiles, warp 6 the
       // V tiles; the jj-th live tile goes to stage jj % STAGES of its ring
@@ -240,14 +241,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
     }
   } else if (warp == 4) {
     if (lane == 0 && nlive > 0) {
-      // ---------------- MMA issuer (one thread): QK(0), QK(1), then PV(j)
-      // and QK(j + 2) for each j, so the tensor pipe runs QK(j + 1) and PV(j)
-      // while the softmax warps work on tiles j + 1 and j + 2
+      // ---------------- QK issuer (one thread): QK(j) into S buffer j & 1
+      // once PV(j - 2), which read P(j - 2) from that buffer, has completed
       constexpr uint32_t IDESC_QK = idesc_bf16_m128(BN, false, false);
-      constexpr uint32_t IDESC_PV = idesc_bf16_m128(D, false, true);
       auto issue_qk = [&](int j) -> bool {
         const int s = j % STAGES;
         if (!wait_or_abort(&k_full[s], (j / STAGES) & 1, abort_flag, p.err)) return false;
+        if (j >= 2 && !wait_or_abort(&o_done[j & 1], ((j - 2) >> 1) & 1, abort_flag, p.err)) return false;
         tc_fence_after();
         const uint32_t d = tmem + C::TMEM_S + (j & 1) * BN;
 #pragma unroll
@@ -264,6 +264,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
         mma_commit(&s_full[j & 1]);
         return true;
       };
+      bool ok = wait_or_abort(q_full, 0, abort_flag, p.err);
+      for (int j = 0; ok && j < nlive; ++j) ok = issue_qk(j);
+    }
+  } else if (warp == 7) {
+    if (lane == 0 && nlive > 0) {
+      // ---------------- PV issuer (one thread): PV(t) once the softmax has
+      // written P(t), so the QK issuer never waits behind it
+      constexpr uint32_t IDESC_PV = idesc_bf16_m128(D, false, true);
       auto issue_pv = [&](int t) -> bool {
         const int s = t % STAGES;
         if (!wait_or_abort(&p_full[t & 1], (t >> 1) & 1, abort_flag, p.err)) return false;
@@ -280,15 +288,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) prefill_tc_kernel(const __grid_
         mma_commit(&o_done[t & 1]);
         return true;
       };
-      bool ok = wait_or_abort(q_full, 0, abort_flag, p.err);
-      for (int j = 0; ok && j < min(2, nlive); ++j) ok = issue_qk(j);
-      for (int j = 0; ok && j < nlive; ++j) {
-        ok = issue_pv(j);
-        // S(j)'s buffer is free for QK(j + 2): the softmax has read S(j) and
-        // written P(j) (p_full), and PV(j), issued above, reads P(j) first
-        if (ok && j + 2 < nlive) ok = issue_qk(j + 2);
-      }
-      if (ok) mma_commit(o_last);   // every MMA of the CTA has completed
+      bool ok = true;
+      for (int t = 0; ok && t < nlive; ++t) ok = issue_pv(t);
+      // every PV has completed, and with it every QK (PV(t) follows P(t),
+      // which follows S(t))
+      if (ok) mma_commit(o_last);
     }
   } else {
     // ---------------- softmax warps (0-3): thread tid owns row tid (TMEM lane tid)
