@@ -117,9 +117,21 @@ class OraclePool:
                     os.environ.pop(k, None)
                 else:
                     os.environ[k] = v
-        for _ in range(self.cores):
-            msg = self.out_q.get(timeout=900)
+        # every worker reports ready; one that died on start ends the wait
+        # instead of the timeout
+        import queue
+        ready, t_end = 0, time.monotonic() + 900
+        while ready < self.cores:
+            try:
+                msg = self.out_q.get(timeout=2)
+            except queue.Empty:
+                dead = [p.exitcode for p in self.procs if p.exitcode is not None]
+                if dead or time.monotonic() > t_end:
+                    self.close()
+                    raise RuntimeError(f"oracle workers did not start (exit codes {dead})")
+                continue
             assert msg[0] == "ready", msg
+            ready += 1
 
     def sample(self, budget_s: float) -> dict:
         from compressed_composable_kv_gb300 import synth as S
