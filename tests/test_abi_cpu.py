@@ -126,6 +126,13 @@ def test_store_file_and_test_hook_arguments_are_checked_on_the_host(P, tmp_path)
 
 
 
+def test_kernel_launch_counter_is_host_only(P):
+    """The launch counter reads without a GPU, counts nothing when nothing was
+    launched, and rejects a null pointer."""
+    assert P.c2kv_kernel_launches() == P.c2kv_kernel_launches() >= 0
+    assert P.load_library().c2kv_kernel_launches(None) == P.C2KV_EINVAL
+
+
 def test_masked_attention_arguments_are_checked_on_the_host(P):
     """Mask kinds and their size rules are checked before any pointer or CUDA
     call: an unknown mask, slots under the causal mask and k < 1 under the
