@@ -280,6 +280,25 @@ def test_varlen_batch_pool():
     sc.close()
 
 
+def test_decode_four_128k_token_requests():
+    """The largest workload's decode launch: 4 requests of 32 x 4096-token
+    documents at k=4 (32 768 slots each, each request in its own order), so
+    the key tiles of 4 sequences x 8 kv heads are split over the CTAs and
+    merged across CTAs as in the benchmark; every request against the oracle
+    on one layer, two decode steps."""
+    g = S.Geometry(1, 32, 8, 128, 5.0e5)
+    specs = [(i, 4096, 1024) for i in range(32)]
+    rng = np.random.default_rng(0xC2C6)
+    requests = [(list(range(32)), [int(x) for x in rng.permutation(32)]) for _ in range(4)]
+    sc = Scenario(g, 4, specs, requests, q_len=0, decode_steps=2, seed=0xC2C6)
+    w = S.Workload("long_b4", g, 4, 4, 0, 2, seed=0xC2C6)
+    inputs = S.make_step_inputs(w)
+    pre, dec = run_all(sc, upload(inputs))
+    for b in range(4):
+        check_request(sc, inputs, pre, dec, b, layers=[0], steps=[0, 1])
+    sc.close()
+
+
 @pytest.mark.parametrize("batch", [4, 5])
 def test_decode_cluster_merge_batches(batch):
     """Batches of 4 and 5 sequences (Llama heads): 32 and 40 (sequence, kv
