@@ -371,6 +371,25 @@ def test_qwen_group5_k16():
     sc.close()
 
 
+def test_qwen_batch8_full_size():
+    """The Qwen3-14B workload's launches at full size on one layer: 8
+    requests of 16 x 8000-token documents at k=16 (8000 slots each, own
+    orders), a 128-token question (320 prefill units: two launches) and two
+    decode steps (64 units split over the CTAs); four requests against the
+    oracle."""
+    g = S.Geometry(1, 40, 8, 128, 1.0e6)
+    specs = [(i, 8000, 500) for i in range(16)]
+    rng = np.random.default_rng(0xC2C7)
+    requests = [(list(range(16)), [int(x) for x in rng.permutation(16)]) for _ in range(8)]
+    sc = Scenario(g, 16, specs, requests, q_len=128, decode_steps=2, seed=0xC2C7)
+    w = S.Workload("qwen_b8", g, 16, 8, 128, 2, seed=0xC2C7)
+    inputs = S.make_step_inputs(w)
+    pre, dec = run_all(sc, upload(inputs))
+    for b in (0, 3, 6, 7):
+        check_request(sc, inputs, pre, dec, b, layers=[0], steps=[0, 1])
+    sc.close()
+
+
 def test_llama_8x4000_full_size():
     """The benchmark workload at full size (32 layers, 8000 slots, 64-token
     question, 128 decode steps), checked on sampled layers and steps."""
