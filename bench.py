@@ -580,6 +580,7 @@ def run_ours(args, rank: int, world: int) -> dict:
                    "pipelined with its prefill), mean of 3; decode_ms: mean decode phase of the timed "
                    "requests"),
         "decode_only_tok_s": Bn * T / dec,
+        "decode_ms_range": [min(e[0].elapsed_time(e[1]) for e in ev), max(e[0].elapsed_time(e[1]) for e in ev)],
         "between_decodes_ms": statistics.mean(gaps) * 1e3 if gaps else None,
         "attention_hbm_gbs": achieved,
         "h2d": {"compose_bytes": compose_bytes, "achieved_gbs": compose_bytes / comp / 1e9,
