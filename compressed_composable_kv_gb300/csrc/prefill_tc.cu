@@ -737,9 +737,11 @@ void prefill_tc_plan(int units, int max_keys, int num_sms, int head_dim, int gro
   s = std::min(s, (max_keys + BN - 1) / BN);
   s = std::min(s, kMaxClusterTc);
   for (; s >= 2; --s) {
-    // both instantiations take the same shared memory (one CTA per SM), so
-    // the causal one answers for the masked one too
-    const int n = active_clusters(s, head_dim, group, false);
+    // both instantiations take the same shared memory, so the causal one
+    // answers for the masked one too; every CTA allocates all 512 TMEM
+    // columns, so at most one per SM runs at a time whatever the shared
+    // memory would allow (head_dim 64)
+    const int n = std::min(active_clusters(s, head_dim, group, false), num_sms / s);
     if (n >= units) break;
   }
   if (s < 1) s = 1;
@@ -765,7 +767,7 @@ PrefillTcSchedule prefill_tc_schedule(int units, int max_keys, int num_sms, int 
   prefill_tc_plan(units, max_keys, num_sms, head_dim, group, &sc.splits0, &sc.keys0);
   sc.splits1 = 1;
   sc.keys1 = sc.keys0;
-  int wave = active_clusters(1, head_dim, group, false);   // resident CTAs
+  int wave = std::min(active_clusters(1, head_dim, group, false), num_sms);   // CTAs at a time (TMEM: one per SM)
   if (wave <= 0) wave = num_sms;
   if (even && sc.splits0 == 1 && units > wave && units % wave != 0) {
     const int rest = units % wave;
