@@ -185,10 +185,15 @@ def compose(store: Dict[int, StoreDoc], doc_ids: Sequence[int],
     n_tok = [store[d][0] for d in seq]
     n_sl = [store[d][1] for d in seq]
     pos, l_tot = composed_positions(n_tok, n_sl, k, realign)
-    L = store[seq[0]][2].shape[0]
+    if not store:
+        raise ValueError("empty store")
+    L, hkv, _, d = next(iter(store.values()))[2].shape   # every stored segment has this geometry
     layers = list(range(L)) if layers is None else list(layers)
-    k_cat = np.concatenate([store[d][2][layers] for d in seq], axis=2)
-    v_cat = np.concatenate([store[d][3][layers] for d in seq], axis=2)
+    # no documents: the concatenation of no segments, a cache of 0 rows
+    k_cat = np.concatenate([np.zeros((len(layers), hkv, 0, d), np.uint16)] +
+                           [store[d_][2][layers] for d_ in seq], axis=2)
+    v_cat = np.concatenate([np.zeros((len(layers), hkv, 0, d), np.uint16)] +
+                           [store[d_][3][layers] for d_ in seq], axis=2)
     k_rot = f64_to_bf16(rope_rotate(bf16_to_f64(k_cat), pos, theta))
     return pos, l_tot, k_rot, v_cat.copy()
 

@@ -35,6 +35,9 @@ def check_attention(gpu_bf16: torch.Tensor, ref: np.ndarray, what: str, max_abs=
 
 
 def check_keys(gpu_bits: np.ndarray, ref_bits: np.ndarray, what: str):
+    assert gpu_bits.shape == ref_bits.shape, f"{what}: shapes {gpu_bits.shape} vs {ref_bits.shape}"
+    if gpu_bits.size == 0:   # a composition of no documents
+        return
     d = O.bf16_ulp_distance(gpu_bits, ref_bits)
     assert d.max() <= MAX_ULP, f"{what}: {int((d > MAX_ULP).sum())} keys off by > {MAX_ULP} ulp (max {d.max()})"
 

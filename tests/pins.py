@@ -282,6 +282,21 @@ def check_k1_equals_uncompressed(o):
     assert np.array_equal(vcat, raw_v)
 
 
+def check_empty_composition(o):
+    """A request of no documents composes the concatenation of no segments: no
+    positions, L_tot = 0, K and V of 0 rows with the store's geometry; and a
+    request of one document is that document alone at positions from 0."""
+    rng = np.random.default_rng(17)
+    L, hkv, d, theta = 2, 3, 8, 1.0e4
+    store = {7: (12, 3, _bits(rng, (L, hkv, 3, d)), _bits(rng, (L, hkv, 3, d)))}
+    pos, l_tot, krot, vcat = o.compose(store, [], None, 4, theta)
+    assert pos.shape == (0,) and l_tot == 0
+    assert krot.shape == (L, hkv, 0, d) and vcat.shape == (L, hkv, 0, d)
+    pos, l_tot, krot, vcat = o.compose(store, [7], None, 4, theta, layers=[1])
+    assert pos.tolist() == [3, 7, 11] and l_tot == 12
+    assert krot.shape == (1, hkv, 3, d) and np.array_equal(vcat[0], store[7][3][1])
+
+
 def check_k1_attention_equals_uncompressed(o):
     """k=1 (section "C2 tokens": one slot per k tokens, so every token is its
     own slot): composing the documents, prefilling the question after them and
@@ -468,7 +483,8 @@ ALL_CHECKS = [
     check_blog_positions, check_slot_counts, check_positions_bruteforce, check_no_realign_positions,
     check_blog_mask, check_extraction_positions, check_bf16_conversion,
     check_rope, check_attention_special_cases, check_gqa_and_causality,
-    check_k1_equals_uncompressed, check_k1_attention_equals_uncompressed, check_ulp_distance,
+    check_k1_equals_uncompressed, check_empty_composition, check_k1_attention_equals_uncompressed,
+    check_ulp_distance,
     check_llama3_bytes,
     check_structured_attention_on_the_blog_figure,
     check_anchor_mask_uniform_scores, check_anchor_rows_are_causal_attention,
